@@ -1,0 +1,558 @@
+/*
+ * DSpark per-step hot path: CPU ORACLE.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously-correct CPU
+ * statement of what the three hot-path operations compute.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it; the
+ * product path never does.  It shares no code, header, table or constant
+ * generator with the CUDA library.  Floating point is fp64 unless a step is an
+ * explicit rounding to the storage dtype.  Build with -ffp-contract=off so that
+ * x86 and Arm hosts give the same results.
+ *
+ * Sources (page title; section / equation / algorithm):
+ *   [DSP]  "DSpark: Confidence-Scheduled Speculative Decoding with
+ *          Semi-Autoregressive Generation" (arXiv 2607.05147):
+ *          S2.1 acceptance rule; S3.1 semi-autoregressive block distribution
+ *          and Markov head B = W1 W2; S3.2.2 Algorithm 1 (hardware-aware prefix
+ *          scheduler); Appendix A (non-anticipation counterexample).
+ *   [ZTD]  "Speculative decoding, from zero to DSpark": S2 accept rule and
+ *          residual norm(max(0, p_t - p_d)); S6 p_k = softmax(U_k + B_k);
+ *          S8 objective Theta = tau * SPS(B) and a_k = prod c_i; Appendix A1.
+ *   [PRX]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *          1, 2, 3" (SC'11), S4 Philox: the Philox4x32 round function, its
+ *          multipliers and Weyl key increments, 10 rounds.
+ *
+ * Parity pins (tests/test_oracle_*.py): every function below is pinned by at
+ * least one check that does not restate its own formula (printed worked
+ * examples, exact enumeration, closed forms, exhaustive search, published
+ * known-answer vectors, statistical laws).  See the per-function notes.
+ *
+ * Random stream specification (the pages fix none; both implementations
+ * reproduce it from this text):
+ *   key     = (seed & 0xffffffff, seed >> 32)
+ *   counter = (c0, c1 = position, c2 = request id, c3 = tag)
+ *   tag     DRAFT = 0 (draft sampling, position k = 1..K_r),
+ *           ACCEPT = 1 (accept uniform, position j = 1..ell_r, c0 = 0, word 0),
+ *           RESID = 2 (residual at the rejecting position j, or bonus at
+ *                      position ell_r + 1)
+ *   element v uses word (v & 3) of the block with c0 = v >> 2
+ *   gumbel uniform  u = ((w >> 9) + 0.5) * 2^-23  in (0, 1), exact in fp32
+ *   accept uniform  u = (w >> 8) * 2^-24          in [0, 1), exact in fp32
+ *   gumbel noise    g = -log(-log(u))
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- status codes (oracle's own numbering; tests map them by name) ---- */
+enum {
+  ORC_OK = 0,
+  ORC_ERR_NULL = 1,
+  ORC_ERR_DIMS = 2,
+  ORC_ERR_DTYPE = 3,
+  ORC_ERR_TEMPERATURE = 4,
+  ORC_ERR_SPS_TOO_SHORT = 5,
+  ORC_ERR_OFFSETS = 6,
+  ORC_ERR_TOKEN_RANGE = 7,
+  ORC_ERR_LENGTHS = 8,
+  ORC_ERR_CONFIDENCE = 9
+};
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { TAG_DRAFT = 0, TAG_ACCEPT = 1, TAG_RESID = 2 };
+
+#define ORC_MAX_K 16
+#define ORC_MIN_POS_T 1e-3
+#define ORC_SAMPLE_TIE 1e-4 /* sampling near-tie margin (score units) */
+#define ORC_ACCEPT_TIE 1e-5 /* |u - min(1, p/q)| near-tie margin        */
+
+/* ---------------------------------------------------------------------- */
+/* Philox4x32-10 [PRX S4].                                                 */
+/* One round: the two multipliers act on counter words 0 and 2; the high    */
+/* halves are xored with the odd words and the two key words; the low halves */
+/* move to the odd positions.  The key is bumped by the Weyl constants       */
+/* between rounds.  Pinned by the published known-answer vectors.           */
+/* ---------------------------------------------------------------------- */
+void dso_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    uint64_t p0 = (uint64_t)M0 * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)M1 * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    k0 += W0;
+    k1 += W1;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Word for vocabulary element v of the stream (seed, position, request, tag). */
+uint32_t dso_stream_word(uint64_t seed, uint64_t v, uint32_t position, uint32_t request, uint32_t tag) {
+  uint32_t ctr[4] = {(uint32_t)(v >> 2), position, request, tag};
+  uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  dso_philox4x32_10(ctr, key, out);
+  return out[v & 3u];
+}
+
+double dso_uniform_open(uint32_t w) { return ((double)(w >> 9) + 0.5) * 0x1p-23; }
+double dso_uniform_accept(uint32_t w) { return (double)(w >> 8) * 0x1p-24; }
+double dso_gumbel(uint32_t w) { return -log(-log(dso_uniform_open(w))); }
+
+/* ---------------------------------------------------------------------- */
+/* bf16 <-> fp64.  bf16 is the top half of an IEEE binary32.               */
+/* ---------------------------------------------------------------------- */
+static double bf16_to_double(uint16_t h) {
+  uint32_t bits = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &bits, 4);
+  return (double)f;
+}
+
+/* Quantum (spacing) of bf16 values around finite non-zero x. */
+static double bf16_quantum(double x) {
+  int e;
+  (void)frexp(x, &e);            /* |x| in [2^(e-1), 2^e) */
+  if (e - 1 < -126) e = -125;    /* subnormal range: fixed spacing 2^-133 */
+  return ldexp(1.0, e - 8);
+}
+
+/* Round x to the nearest bf16 value, ties to even; returns the value. */
+static double round_bf16(double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  double q = bf16_quantum(x);
+  double r = nearbyint(x / q) * q;         /* default mode: to nearest, ties even */
+  if (fabs(r) > 0x1.FEp127) r = copysign(INFINITY, x);
+  return r;
+}
+
+static uint16_t double_to_bf16_bits(double x) {
+  float f = (float)round_bf16(x);          /* exact: value is a bf16 value */
+  uint32_t bits;
+  memcpy(&bits, &f, 4);
+  return (uint16_t)(bits >> 16);
+}
+
+/* Is x so close to a bf16 rounding midpoint that an fp32 evaluation of it   */
+/* (a few fp32 ulps of error) could round the other way?  Returns the other  */
+/* candidate bf16 value in *alt when it is.                                  */
+static int bf16_ambiguous(double x, double *alt) {
+  if (x == 0.0 || !isfinite(x)) return 0;
+  double q = bf16_quantum(x);
+  double t = x / q;
+  double fl = floor(t);
+  double frac = t - fl;
+  if (fabs(frac - 0.5) < 0x1p-14) {
+    double r = round_bf16(x);
+    double lo = fl * q, hi = (fl + 1.0) * q;
+    *alt = (r == lo) ? hi : lo;
+    return 1;
+  }
+  return 0;
+}
+
+static double load_elem(const void *p, int dtype, int64_t i) {
+  if (dtype == ORC_F32) return (double)((const float *)p)[i];
+  return bf16_to_double(((const uint16_t *)p)[i]);
+}
+
+static void store_elem(void *p, int dtype, int64_t i, double x) {
+  if (dtype == ORC_F32) ((float *)p)[i] = (float)x;
+  else ((uint16_t *)p)[i] = double_to_bf16_bits(x);
+}
+
+static int temperature_ok(float t) {
+  if (!(t == t) || isinf(t) || t < 0.0f) return 0;
+  return t == 0.0f || (double)t >= ORC_MIN_POS_T;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+}
+
+/* ---------------------------------------------------------------------- */
+/* Draft: Markov-head semi-autoregressive sampling.                        */
+/* [DSP S3.1], [ZTD S6]:                                                   */
+/*   p_k(v | x_0, x_<k) = softmax(U_k(v) + B(x_{k-1}, v)),                  */
+/*   B(x_{k-1}, .) = W1[x_{k-1}] . W2   (W1: V x rank lookup, W2: rank x V),  */
+/*   x_0 = the anchor (the previous round's bonus/correction token),        */
+/*   sampled left to right, k = 1..K_r.                                     */
+/* Readings (the pages fix none of these):                                  */
+/*   - the biased logits are materialised in the storage dtype (rounded to  */
+/*     nearest-even from the exact value) and the draft samples from those  */
+/*     stored logits, so verification sees exactly the sampled distribution;*/
+/*   - temperature T divides the biased logit; T = 0 means argmax;          */
+/*   - sampling is Gumbel-max on the stream (seed, k, request, DRAFT);      */
+/*   - ties go to the smallest vocabulary index.                            */
+/* Outputs per (request, position): token, log-sum-exp of z/T (the draft    */
+/* distribution's normaliser; for T = 0 the largest logit), top-2 margin,   */
+/* near-tie flags: bit0 sampling margin < 1e-4 (fp32 storage or T > 0),      */
+/* bit1 a bf16 rounding ambiguity could change the token, bit2 a bf16        */
+/* rounding ambiguity moves the log-sum-exp by more than 1e-6 relative.      */
+/* Pins: exact joint law by enumeration vs Monte Carlo; zero bias equals    */
+/* independent sampling; one-hot rank-1 transition; hand-computed logits;   */
+/* normalisation of the log-sum-exp.                                        */
+/* ---------------------------------------------------------------------- */
+int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dtype,
+                            const int32_t *anchor, const int32_t *K_r, const float *temperature,
+                            const int64_t *req_id, uint64_t seed,
+                            int64_t B, int64_t K_max, int64_t V, int64_t rank,
+                            int32_t *draft_tok, void *draft_logits, double *lse,
+                            double *margin, uint8_t *flags, int nthreads) {
+  if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok) return ORC_ERR_NULL;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2 || rank < 1) return ORC_ERR_DIMS;
+  for (int64_t b = 0; b < B; ++b) {
+    if (K_r[b] < 1 || K_r[b] > K_max) return ORC_ERR_LENGTHS;
+    if (anchor[b] < 0 || anchor[b] >= V) return ORC_ERR_TOKEN_RANGE;
+    if (!temperature_ok(temperature[b])) return ORC_ERR_TEMPERATURE;
+  }
+  set_threads(nthreads);
+  int64_t b;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    double *bias = (double *)malloc(sizeof(double) * (size_t)V);
+    double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    uint32_t rid = (uint32_t)(req_id ? req_id[b] : b);
+    int32_t x_prev = anchor[b];
+    double T = (double)temperature[b];
+    for (int64_t k = 1; k <= K_max; ++k) {
+      int64_t slot = b * K_max + (k - 1);
+      if (k > K_r[b]) { draft_tok[slot] = -1; continue; }
+      /* transition bias: one row of the lookup table times the projection */
+      for (int64_t v = 0; v < V; ++v) bias[v] = 0.0;
+      for (int64_t i = 0; i < rank; ++i) {
+        double e = load_elem(E, dtype, (int64_t)x_prev * rank + i);
+        for (int64_t v = 0; v < V; ++v) bias[v] += e * load_elem(W, dtype, i * V + v);
+      }
+      const int64_t ubase = slot * V;
+      for (int64_t v = 0; v < V; ++v) {
+        double exact = load_elem(U, dtype, ubase + v) + bias[v];
+        z[v] = (dtype == ORC_F32) ? (double)(float)exact : round_bf16(exact);
+      }
+      if (draft_logits) for (int64_t v = 0; v < V; ++v) store_elem(draft_logits, dtype, ubase + v, z[v]);
+      /* scores */
+      int64_t best = -1, second = -1;
+      double sb = -INFINITY, ss = -INFINITY;
+      double m = -INFINITY;
+      for (int64_t v = 0; v < V; ++v) {
+        double s = (T > 0.0) ? z[v] / T + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)k, rid, TAG_DRAFT))
+                             : z[v];
+        if (best < 0 || s > sb) { ss = sb; second = best; sb = s; best = v; }
+        else if (second < 0 || s > ss) { ss = s; second = v; }
+        double zt = (T > 0.0) ? z[v] / T : z[v];
+        if (zt > m) m = zt;
+      }
+      double l;
+      if (T > 0.0) {
+        double S = 0.0;
+        for (int64_t v = 0; v < V; ++v) S += exp(z[v] / T - m);
+        l = m + log(S);
+      } else {
+        l = z[best];
+      }
+      uint8_t f = 0;
+      double mg = sb - ss;
+      if ((T > 0.0 || dtype == ORC_F32) && mg < ORC_SAMPLE_TIE) f |= 1;
+      if (dtype == ORC_BF16) {
+        double lse_shift = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+          double exact = load_elem(U, dtype, ubase + v) + bias[v];
+          double alt;
+          if (!bf16_ambiguous(exact, &alt)) continue;
+          double noise = (T > 0.0) ? dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)k, rid, TAG_DRAFT)) : 0.0;
+          double s_alt = (T > 0.0) ? alt / T + noise : alt;
+          if (v == best) { if (s_alt <= ss + ORC_SAMPLE_TIE) f |= 2; }
+          else if (s_alt >= sb - ORC_SAMPLE_TIE) f |= 2;
+          if (T > 0.0) lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
+        }
+        if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
+      }
+      draft_tok[slot] = (int32_t)best;
+      if (lse) lse[slot] = l;
+      if (margin) margin[slot] = mg;
+      if (flags) flags[slot] = f;
+      x_prev = (int32_t)best;
+    }
+    free(bias);
+    free(z);
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Schedule: confidence-scheduled verification lengths.                     */
+/* [DSP S3.2.2 Algorithm 1], [ZTD S8]:                                      */
+/*   a_{r,j} = prod_{i<=j} c_{r,i};  candidates {(r,j) : a_{r,j} > 0} sorted */
+/*   by a descending; B <- R, tau <- R, Theta_best <- R * SPS(R); for each   */
+/*   candidate in order: B <- B + 1, tau <- tau + a, Theta <- tau * SPS(B);   */
+/*   admit if Theta > Theta_best, else stop.  ell_r = admitted count of r.   */
+/* Readings: a is the sequential fp32 product; ties in a go to the smaller  */
+/* position j, then the smaller request r (earlier positions must win ties  */
+/* for the prefix property); tau is accumulated exactly in 2^-40 fixed point */
+/* (each a rounded half-to-even to a multiple of 2^-40), Theta evaluated in  */
+/* fp64 as ((double)R + T * 2^-40) * SPS[B]; the SPS table must cover every  */
+/* B up to R + #candidates; confidences outside [0, 1] are rejected.        */
+/* Pins: Appendix A worked numbers; the two-request worked example; exhaustive */
+/* search over admissible length tuples; empty-system limit; marginal test.  */
+/* ---------------------------------------------------------------------- */
+typedef struct { float a; int32_t j; int32_t r; } cand_t;
+
+static int cand_cmp(const void *pa, const void *pb) {
+  const cand_t *x = (const cand_t *)pa, *y = (const cand_t *)pb;
+  if (x->a > y->a) return -1;
+  if (x->a < y->a) return 1;
+  if (x->j != y->j) return x->j < y->j ? -1 : 1;
+  if (x->r != y->r) return x->r < y->r ? -1 : 1;
+  return 0;
+}
+
+int dso_schedule_survival(const float *conf, const int32_t *K_r, const double *sps, int64_t sps_len,
+                          int64_t B, int64_t K_max,
+                          int32_t *ell, int32_t *tgt_off, double *theta_best, int64_t *B_star,
+                          double *tau_star, float *survival, int32_t *order, int64_t *n_cand,
+                          int64_t *n_admitted, int64_t *n_theta_ties) {
+  if (!conf || !K_r || !sps || !ell || !tgt_off) return ORC_ERR_NULL;
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K) return ORC_ERR_DIMS;
+  for (int64_t r = 0; r < B; ++r)
+    if (K_r[r] < 1 || K_r[r] > K_max) return ORC_ERR_LENGTHS;
+  for (int64_t r = 0; r < B; ++r)
+    for (int64_t j = 0; j < K_r[r]; ++j) {
+      float c = conf[r * K_max + j];
+      if (!(c >= 0.0f && c <= 1.0f)) return ORC_ERR_CONFIDENCE;
+    }
+  cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(B * K_max));
+  int64_t N = 0;
+  for (int64_t r = 0; r < B; ++r) {
+    float a = 1.0f;
+    for (int64_t j = 1; j <= K_max; ++j) {
+      if (j > K_r[r]) { if (survival) survival[r * K_max + j - 1] = 0.0f; continue; }
+      a = a * conf[r * K_max + j - 1];
+      if (survival) survival[r * K_max + j - 1] = a;
+      if (a > 0.0f) { cand[N].a = a; cand[N].j = (int32_t)j; cand[N].r = (int32_t)r; ++N; }
+    }
+  }
+  qsort(cand, (size_t)N, sizeof(cand_t), cand_cmp);
+  const int64_t R = B;
+  if (sps_len < R + N + 1) { free(cand); return ORC_ERR_SPS_TOO_SHORT; }
+  uint64_t T = 0, T_keep = 0;
+  double th_best = (double)R * sps[R];
+  int64_t admitted = 0, ties = 0;
+  for (int64_t i = 1; i <= N; ++i) {
+    uint64_t t = (uint64_t)nearbyint((double)cand[i - 1].a * 0x1p40);
+    T += t;
+    double th = ((double)R + (double)T * 0x1p-40) * sps[R + i];
+    if (th == th_best) ++ties;
+    if (th > th_best) { th_best = th; admitted = i; T_keep = T; }
+    else break;
+  }
+  for (int64_t r = 0; r < B; ++r) ell[r] = 0;
+  for (int64_t i = 0; i < admitted; ++i) ell[cand[i].r] += 1;
+  tgt_off[0] = 0;
+  for (int64_t r = 0; r < B; ++r) tgt_off[r + 1] = tgt_off[r] + ell[r] + 1;
+  if (theta_best) *theta_best = th_best;
+  if (B_star) *B_star = R + admitted;
+  if (tau_star) *tau_star = (double)R + (double)T_keep * 0x1p-40;
+  if (order) for (int64_t i = 0; i < N; ++i) order[i] = (int32_t)((cand[i].j - 1) * B + cand[i].r);
+  if (n_cand) *n_cand = N;
+  if (n_admitted) *n_admitted = admitted;
+  if (n_theta_ties) *n_theta_ties = ties;
+  free(cand);
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Verify: ragged rejection-sampling verification.                          */
+/* [DSP S2.1], [ZTD S2, A1]:                                                */
+/*   for j = 1..ell_r, left to right: accept x_j iff u < min(1, p_j(x_j) /   */
+/*   q_j(x_j)); at the first rejection sample the correction from            */
+/*   norm(max(0, p_j - q_j)); if every position is accepted, sample a bonus  */
+/*   token from the next target row.                                        */
+/* Layout: draft logits [B, K_max, V] (row j-1 is q_j); flattened target    */
+/* logits with row tgt_off[r] + j - 1 for p_j and row tgt_off[r] + ell_r for */
+/* the bonus; tgt_off[r+1] - tgt_off[r] = ell_r + 1.                         */
+/* Readings: q and p both use the request's temperature; T = 0 means greedy */
+/* (accept iff x_j is the argmax of p_j, correction/bonus = argmax of p);    */
+/* the residual is sampled by Gumbel-max of log(p_v - q_v) over p_v > q_v    */
+/* on stream (seed, j, request, RESID); if no element has p_v > q_v in       */
+/* floating point the correction is sampled from p instead (rounding guard);  */
+/* the bonus is Gumbel-max of z/T on stream (seed, ell+1, request, RESID).    */
+/* Flags per request: bit0 an accept decision with |u - min(1, p/q)| < 1e-5,  */
+/* bit1 the correction/bonus sample has top-2 margin < 1e-4, bit2 the        */
+/* residual mass was below 1e-5 (rounding guard region).  flag_pos is the   */
+/* first position whose decision is flagged (ell + 1 for the final sample),  */
+/* 0 when unflagged.                                                         */
+/* Pins: the two-token worked numbers (output law (0.7, 0.3), acceptance    */
+/* 0.8, every rejection yields A, which rules out the 0.64 full-resample     */
+/* variant); Monte-Carlo output law against the target rows on enumerated     */
+/* tiny cases with Markov-biased drafts; acceptance = sum min(p, q).          */
+/* ---------------------------------------------------------------------- */
+static void row_scaled(const void *base, int dtype, int64_t row, int64_t V, double T, double *out) {
+  for (int64_t v = 0; v < V; ++v) {
+    double z = load_elem(base, dtype, row * V + v);
+    out[v] = (T > 0.0) ? z / T : z;
+  }
+}
+
+static double row_lse(const double *s, int64_t V) {
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) if (s[v] > m) m = s[v];
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v) S += exp(s[v] - m);
+  return m + log(S);
+}
+
+static int64_t row_argmax(const double *s, int64_t V, double *mg) {
+  int64_t best = 0, second = -1;
+  for (int64_t v = 1; v < V; ++v) {
+    if (s[v] > s[best]) { second = best; best = v; }
+    else if (second < 0 || s[v] > s[second]) second = v;
+  }
+  if (mg) *mg = (second >= 0) ? s[best] - s[second] : INFINITY;
+  return best;
+}
+
+int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtype,
+                      const int32_t *tgt_off, const int32_t *ell, const int32_t *draft_tok,
+                      const float *temperature, const int64_t *req_id, uint64_t seed,
+                      int64_t B, int64_t K_max, int64_t V,
+                      int32_t *n_acc, int32_t *out_tok, uint8_t *flags, int32_t *flag_pos,
+                      double *sample_margin, int nthreads) {
+  if (!draft_logits || !tgt_logits || !tgt_off || !ell || !draft_tok || !temperature || !n_acc || !out_tok)
+    return ORC_ERR_NULL;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2) return ORC_ERR_DIMS;
+  if (tgt_off[0] != 0) return ORC_ERR_OFFSETS;
+  for (int64_t r = 0; r < B; ++r) {
+    if (ell[r] < 0 || ell[r] > K_max) return ORC_ERR_LENGTHS;
+    if (tgt_off[r + 1] - tgt_off[r] != ell[r] + 1) return ORC_ERR_OFFSETS;
+    if (!temperature_ok(temperature[r])) return ORC_ERR_TEMPERATURE;
+    for (int64_t j = 0; j < ell[r]; ++j)
+      if (draft_tok[r * K_max + j] < 0 || draft_tok[r * K_max + j] >= V) return ORC_ERR_TOKEN_RANGE;
+  }
+  set_threads(nthreads);
+  int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (r = 0; r < B; ++r) {
+    double *st = (double *)malloc(sizeof(double) * (size_t)V);
+    double *sd = (double *)malloc(sizeof(double) * (size_t)V);
+    double *sc = (double *)malloc(sizeof(double) * (size_t)V);
+    uint32_t rid = (uint32_t)(req_id ? req_id[r] : r);
+    const double T = (double)temperature[r];
+    const int64_t l = ell[r];
+    uint8_t f = 0;
+    int32_t fpos = 0;
+    int64_t n = 0;
+    int rejected = 0;
+    int32_t token = -1;
+    double mg = INFINITY;
+    for (int64_t j = 1; j <= l; ++j) {
+      int32_t x = draft_tok[r * K_max + j - 1];
+      row_scaled(tgt_logits, dtype, (int64_t)tgt_off[r] + j - 1, V, T, st);
+      int accept;
+      if (T > 0.0) {
+        row_scaled(draft_logits, dtype, r * K_max + j - 1, V, T, sd);
+        double lp = st[x] - row_lse(st, V);
+        double lq = sd[x] - row_lse(sd, V);
+        double rho = exp(lp - lq);
+        double thr = rho < 1.0 ? rho : 1.0;
+        double u = dso_uniform_accept(dso_stream_word(seed, 0, (uint32_t)j, rid, TAG_ACCEPT));
+        if (fabs(u - thr) < ORC_ACCEPT_TIE && !fpos) { f |= 1; fpos = (int32_t)j; }
+        accept = u < thr;
+      } else {
+        double amg;
+        int64_t a = row_argmax(st, V, &amg);
+        if (dtype == ORC_F32 && amg < ORC_SAMPLE_TIE && !fpos) { f |= 1; fpos = (int32_t)j; }
+        accept = (x == a);
+      }
+      if (!accept) {
+        rejected = 1;
+        if (T > 0.0) {
+          double lt = row_lse(st, V), ld = row_lse(sd, V);
+          double mass = 0.0;
+          int any = 0;
+          for (int64_t v = 0; v < V; ++v) {
+            double res = exp(st[v] - lt) - exp(sd[v] - ld);
+            if (res > 0.0) {
+              mass += res;
+              any = 1;
+              sc[v] = log(res) + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)j, rid, TAG_RESID));
+            } else {
+              sc[v] = -INFINITY;
+            }
+          }
+          if (mass < 1e-5 && !fpos) { f |= 4; fpos = (int32_t)j; }
+          if (!any)
+            for (int64_t v = 0; v < V; ++v)
+              sc[v] = st[v] + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)j, rid, TAG_RESID));
+          token = (int32_t)row_argmax(sc, V, &mg);
+          if (mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)j; }
+        } else {
+          token = (int32_t)row_argmax(st, V, &mg);
+          if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)j; }
+        }
+        break;
+      }
+      out_tok[r * (K_max + 1) + n] = x;
+      ++n;
+    }
+    if (!rejected) {
+      row_scaled(tgt_logits, dtype, (int64_t)tgt_off[r] + l, V, T, st);
+      if (T > 0.0) {
+        for (int64_t v = 0; v < V; ++v)
+          sc[v] = st[v] + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)(l + 1), rid, TAG_RESID));
+        token = (int32_t)row_argmax(sc, V, &mg);
+        if (mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)(l + 1); }
+      } else {
+        token = (int32_t)row_argmax(st, V, &mg);
+        if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)(l + 1); }
+      }
+    }
+    out_tok[r * (K_max + 1) + n] = token;
+    for (int64_t j = n + 1; j <= K_max; ++j) out_tok[r * (K_max + 1) + j] = -1;
+    n_acc[r] = (int32_t)n;
+    if (flags) flags[r] = f;
+    if (flag_pos) flag_pos[r] = fpos;
+    if (sample_margin) sample_margin[r] = mg;
+    free(st);
+    free(sd);
+    free(sc);
+  }
+  return ORC_OK;
+}
+
+/* Log-sum-exp of rows of logits at per-row temperature (fp64); for T = 0 the */
+/* row maximum.  Used to hand the CUDA verify a precomputed draft normaliser. */
+int dso_row_lse(const void *rows, int dtype, int64_t n_rows, int64_t V, const float *row_temperature,
+                double *out) {
+  if (!rows || !row_temperature || !out) return ORC_ERR_NULL;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
+  double *s = (double *)malloc(sizeof(double) * (size_t)V);
+  for (int64_t i = 0; i < n_rows; ++i) {
+    double T = (double)row_temperature[i];
+    row_scaled(rows, dtype, i, V, T, s);
+    if (T > 0.0) out[i] = row_lse(s, V);
+    else { double m = s[0]; for (int64_t v = 1; v < V; ++v) if (s[v] > m) m = s[v]; out[i] = m; }
+  }
+  free(s);
+  return ORC_OK;
+}
+
+/* bf16 rounding exposed for tests (value in, rounded value out). */
+double dso_round_bf16(double x) { return round_bf16(x); }
