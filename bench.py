@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark per-step hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  draft    dspark_draft_markov_sample  (Markov-head bias GEMM + Gumbel-max sampling,
+                                        writes tokens, draft logits and normalisers)
+  schedule dspark_schedule_survival    (survival products, global rank, greedy
+                                        admission with early stop)
+  verify   dspark_verify_ragged        (rejection sampling over the flattened rows)
+Metric: draft + verify positions per second (sum K_r + sum (ell_r + 1) per step).
+
+Default workload: the Qwen3-4B-shaped step (B=64, K=7, V=151936, rank 256, bf16).
+The L2 is flushed (256 MB write, untimed) between timed steps.  Under torchrun
+each rank runs an independent replica of the step on its own GPU (weak scaling);
+the reported value is all ranks' positions over the slowest rank's time.
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify positions/sec at 1 GB300; % of HBM roofline (GB/s vs ~8 TB/s)"
+UNIT = "positions/s"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="qwen")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sps", choices=["literal", "step"], default="literal")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(positions_per_rank: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput: every rank's positions over the slowest rank's time."""
+    return positions_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def make_workload(cfg, dev, sps_variant):
+    import torch
+
+    import speculative_decoding_draft_gb300 as ds
+    from speculative_decoding_draft_gb300 import workloads as wl
+
+    inp = wl.draft_inputs(cfg, dev)
+    conf = wl.confidences(cfg, dev)
+    sps = wl.sps_table(cfg, sps_variant).to(dev)
+    # the schedule is deterministic: run it once to lay out the target model's rows
+    s = ds.schedule_survival(conf, inp["K_r"], sps)
+    assert ds.check(s["status"]) == "DSPARK_OK"
+    ell = s["ell"].clone()
+    tgt_dense = wl.target_dense(cfg, inp["U"], inp["K_r"])
+    tgt, off = wl.flatten_targets(tgt_dense, ell)
+    del tgt_dense
+    torch.cuda.empty_cache()
+    return dict(inp=inp, conf=conf, sps=sps, ell=ell, tgt=tgt.contiguous(), off=off.to(dev))
+
+
+class Step:
+    """Preallocated buffers and the three C-ABI calls of one step."""
+
+    def __init__(self, cfg, w, dev):
+        import torch
+
+        import speculative_decoding_draft_gb300 as ds
+        self.ds = ds
+        self.cfg = cfg
+        self.w = w
+        B, K, V = cfg.B, cfg.K_max, cfg.V
+        inp = w["inp"]
+        self.status = ds.new_status(dev)
+        self.draft_out = dict(draft_tok=torch.empty(B, K, dtype=torch.int32, device=dev),
+                              draft_logits=torch.empty_like(inp["U"]),
+                              draft_lse=torch.empty(B, K, dtype=torch.float32, device=dev))
+        self.sched_out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
+                              tgt_off=torch.empty(B + 1, dtype=torch.int32, device=dev),
+                              theta_best=torch.empty(1, dtype=torch.float64, device=dev),
+                              b_star=torch.empty(1, dtype=torch.int64, device=dev),
+                              survival=torch.empty(B, K, dtype=torch.float32, device=dev))
+        self.ver_out = dict(n_acc=torch.empty(B, dtype=torch.int32, device=dev),
+                            out_tok=torch.empty(B, K + 1, dtype=torch.int32, device=dev))
+        self.ws_d = torch.empty(ds.draft_workspace_bytes(B, K, V), dtype=torch.uint8, device=dev)
+        self.ws_s = torch.empty(ds.schedule_workspace_bytes(B, K), dtype=torch.uint8, device=dev)
+        self.ws_v = torch.empty(ds.verify_workspace_bytes(B, V), dtype=torch.uint8, device=dev)
+        self.launches_per_step = (1 + K) + 1 + 2
+
+    def draft(self, inp=None):
+        inp = self.w["inp"] if inp is None else inp
+        self.ds.draft_markov_sample(inp["U"], inp["E"], inp["W"], inp["anchor"], inp["K_r"], inp["temperature"],
+                                    self.cfg.philox_seed, out=self.draft_out, workspace=self.ws_d,
+                                    status=self.status)
+
+    def schedule(self, conf=None, K_r=None):
+        conf = self.w["conf"] if conf is None else conf
+        K_r = self.w["inp"]["K_r"] if K_r is None else K_r
+        self.ds.schedule_survival(conf, K_r, self.w["sps"], out=self.sched_out, workspace=self.ws_s,
+                                  status=self.status)
+
+    def verify(self, tgt=None, temperature=None):
+        tgt = self.w["tgt"] if tgt is None else tgt
+        temperature = self.w["inp"]["temperature"] if temperature is None else temperature
+        self.ds.verify_ragged(self.draft_out["draft_logits"], tgt, self.sched_out["tgt_off"],
+                              self.sched_out["ell"], self.draft_out["draft_tok"], temperature,
+                              self.cfg.philox_seed + 7919, draft_lse=self.draft_out["draft_lse"],
+                              out=self.ver_out, workspace=self.ws_v, status=self.status)
+
+
+def algorithmic(cfg, K_r, ell, n_acc, temperature):
+    """Algorithmic bytes / flops of each operation for one step (bf16 = 2 bytes)."""
+    esz = 2 if cfg.dtype == "bf16" else 4
+    V, r = cfg.V, cfg.rank
+    sumK = int(K_r.sum())
+    draft_bytes = sumK * V * esz + r * V * esz + sumK * r * esz
+    draft_flops = 2.0 * sumK * r * V
+    # verify, with the draft normalisers known: target rows up to the deciding row, plus the
+    # draft row at a rejection (T > 0) for the residual
+    ver_rows = 0
+    ver_rows_dense = 0
+    for b in range(cfg.B):
+        l, n = int(ell[b]), int(n_acc[b])
+        ver_rows += n + 1
+        if n < l and float(temperature[b]) > 0:
+            ver_rows += 1
+        ver_rows_dense += 2 * l + 1
+    return dict(draft_bytes=draft_bytes, draft_flops=draft_flops, verify_bytes=ver_rows * V * esz,
+                verify_bytes_dense=ver_rows_dense * V * esz, positions=sumK + int((ell + 1).sum()),
+                draft_positions=sumK, verify_positions=int((ell + 1).sum()))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded by ncu in profiles/, if the kernel source is unchanged."""
+    src = {"draft": "draft_tc.cu", "verify": "verify.cu"}.get(kernel)
+    summ = os.path.join(ROOT, "profiles", f"traffic_{kernel}.md")
+    if not src or not os.path.exists(summ):
+        return None
+    text = open(summ).read()
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"dram_bytes_per_launch_scaled:\s*([0-9.eE+]+)", text)
+    if not m or not t:
+        return None
+    h = hashlib.sha256(open(os.path.join(ROOT, "speculative_decoding_draft_gb300", "csrc", src), "rb").read())
+    return float(t.group(1)) if h.hexdigest() == m.group(1) else None
+
+
+def cpu_baseline(cfg, w, sample_requests):
+    """The oracle, as it stands, on the host cores, on `sample_requests` requests of the step."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_draft_gb300 import workloads as wl
+
+    inp = w["inp"]
+    rows = np.arange(sample_requests)
+    U = wl.bf16_bits(inp["U"][:sample_requests])
+    E = wl.bf16_bits(inp["E"])
+    W = wl.bf16_bits(inp["W"])
+    anchor = inp["anchor"][:sample_requests].cpu().numpy()
+    K_r = inp["K_r"][:sample_requests].cpu().numpy()
+    T = inp["temperature"][:sample_requests].cpu().numpy()
+    conf = w["conf"].cpu().numpy()
+    K_all = inp["K_r"].cpu().numpy()
+    sps = w["sps"].cpu().numpy()
+    ell_all = w["ell"].cpu().numpy()
+    off_all = w["off"].cpu().numpy()
+    tgt_rows = wl.bf16_bits(w["tgt"][: int(off_all[sample_requests])])
+    nthreads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    d = oracle.draft_markov_sample(U, E, W, anchor, K_r, T, cfg.philox_seed, req_id=rows.astype(np.int64),
+                                   nthreads=nthreads)
+    s = oracle.schedule_survival(conf, K_all, sps)
+    ell = s["ell"][:sample_requests]
+    off = s["tgt_off"][: sample_requests + 1]
+    v = oracle.verify_ragged(d["draft_logits"], tgt_rows, off, ell, d["draft_tok"], T, cfg.philox_seed + 7919,
+                             req_id=rows.astype(np.int64), nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    positions = int(K_r.sum()) + int((ell + 1).sum())
+    return positions / dt, dt, nthreads, positions
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on a bounded sample of the workload, on the host cores."""
+    import torch
+
+    from speculative_decoding_draft_gb300 import workloads as wl
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    cfg = wl.CONFIGS[args.config]
+    if not torch.cuda.is_available():          # no GPU machine: a reduced copy keeps the run short
+        cfg = wl.small_config(args.config, B=8, V=4096)
+    import oracle
+    oracle.build()
+    w = make_workload_cpu(cfg, args.sps)       # inputs and layout from the oracle only
+    sample = min(cfg.B, 4)
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, w, sample)
+    times, pos = [], 0
+    for _ in range(args.steps):
+        _, dt, cores, pos = cpu_baseline(cfg, w, sample)
+        times.append(dt)
+    value = pos * len(times) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config),
+                                             "sample": f"{sample} of {cfg.B} requests per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"draft + verify of {sample} requests, full schedule, per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def make_workload_cpu(cfg, sps_variant="literal"):
+    from speculative_decoding_draft_gb300 import workloads as wl
+    import oracle
+    inp = wl.draft_inputs(cfg, "cpu")
+    conf = wl.confidences(cfg, "cpu")
+    sps = wl.sps_table(cfg, sps_variant)
+    s = oracle.schedule_survival(conf.numpy(), inp["K_r"].numpy(), sps.numpy())
+    import torch
+    ell = torch.from_numpy(s["ell"])
+    tgt, off = wl.flatten_targets(wl.target_dense(cfg, inp["U"], inp["K_r"]), ell)
+    return dict(inp=inp, conf=conf, sps=sps, ell=ell, tgt=tgt, off=off)
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import speculative_decoding_draft_gb300 as ds
+    from speculative_decoding_draft_gb300 import workloads as wl
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    ds.lib()          # fails loudly when the CUDA library is missing
+    cfg = wl.CONFIGS[args.config]
+    w = make_workload(cfg, dev, args.sps)
+    step = Step(cfg, w, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def one_step():
+        step.draft()
+        step.schedule()
+        step.verify()
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    st = ds.check(step.status)
+    if st != "DSPARK_OK":
+        raise SystemExit(f"device status {st}")
+    n_acc = step.ver_out["n_acc"].cpu()
+    alg = algorithmic(cfg, w["inp"]["K_r"].cpu(), step.sched_out["ell"].cpu(), n_acc,
+                      w["inp"]["temperature"].cpu())
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            e = ev[i]
+            e[0].record(stream)
+            step.draft()
+            e[1].record(stream)
+            step.schedule()
+            e[2].record(stream)
+            step.verify()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    st = ds.check(step.status)
+    if st != "DSPARK_OK":
+        raise SystemExit(f"device status {st}")
+    t_draft = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    t_sched = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    t_ver = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    ms_step = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    max_s = max_over_ranks(ms_step * 1e-3 * args.steps, world, dev)
+    value = aggregate(alg["positions"] * args.steps, max_s, world)
+
+    hbm, tf, peak_kind = measured_peaks()
+    draft_gbs = alg["draft_bytes"] / (t_draft * 1e-3) / 1e9
+    ver_gbs = alg["verify_bytes"] / (t_ver * 1e-3) / 1e9
+    draft_tflops = alg["draft_flops"] / (t_draft * 1e-3) / 1e12
+    kernels = {
+        "draft": {"ms": t_draft, "alg_bytes": alg["draft_bytes"], "GB/s": draft_gbs, "hbm_frac": draft_gbs / hbm,
+                  "TFLOP/s": draft_tflops, "tensor_frac": draft_tflops / tf, "launches": 1 + cfg.K_max},
+        "schedule": {"ms": t_sched, "launches": 1},
+        "verify": {"ms": t_ver, "alg_bytes": alg["verify_bytes"], "dense_bytes": alg["verify_bytes_dense"],
+                   "GB/s": ver_gbs, "hbm_frac": ver_gbs / hbm,
+                   "hbm_frac_dense": alg["verify_bytes_dense"] / (t_ver * 1e-3) / 1e9 / hbm, "launches": 2},
+    }
+    dom = "draft" if t_draft >= t_ver else "verify"
+    traffic = profiled_traffic(dom)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": hbm, "unit": "GB/s",
+                "frac": kernels[dom]["hbm_frac"], "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "per": "one call (all positions of the step)"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config), "B": cfg.B, "K": cfg.K_max,
+                       "V": cfg.V, "rank": cfg.rank, "sps": args.sps,
+                       "positions_per_step": alg["positions"], "draft_positions": alg["draft_positions"],
+                       "verify_positions": alg["verify_positions"],
+                       "l2": "flushed between timed steps (256 MB write, untimed)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "kernels": kernels, "gpu_launches": step.launches_per_step * args.steps,
+            "clocks": clocks.summary()}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(cfg, w, step, dev, args, alg)
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, dt, cores, pos = cpu_baseline(cfg, w, min(cfg.B, 8))
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"draft + verify of {min(cfg.B, 8)} of {cfg.B} requests "
+                                          f"({pos} positions) and the full schedule, {dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(cfg, w, step, dev, args, alg):
+    """Same metric through the public API with host buffers: pinned H2D of the step's
+    inputs (base logits, target rows, anchors, lengths, temperatures, confidences),
+    the three calls, D2H of the emitted tokens; weights and the SPS table stay resident."""
+    import torch
+    inp = w["inp"]
+    h = {k: inp[k].cpu().pin_memory() for k in ("U", "anchor", "K_r", "temperature")}
+    h["conf"] = w["conf"].cpu().pin_memory()
+    h["tgt"] = w["tgt"].cpu().pin_memory()
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    out_tok = torch.empty(cfg.B, cfg.K_max + 1, dtype=torch.int32).pin_memory()
+    n_acc = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
+    drafts = torch.empty(cfg.B, cfg.K_max, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = out_tok.numel() * 4 + n_acc.numel() * 4 + drafts.numel() * 4
+    stream = torch.cuda.current_stream()
+
+    def run():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        dinp = dict(inp)
+        dinp.update(U=d["U"], anchor=d["anchor"], K_r=d["K_r"], temperature=d["temperature"])
+        step.draft(dinp)
+        step.schedule(d["conf"], d["K_r"])
+        step.verify(d["tgt"], d["temperature"])
+        out_tok.copy_(step.ver_out["out_tok"], non_blocking=True)
+        n_acc.copy_(step.ver_out["n_acc"], non_blocking=True)
+        drafts.copy_(step.draft_out["draft_tok"], non_blocking=True)
+
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": alg["positions"] / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

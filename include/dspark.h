@@ -1,0 +1,207 @@
+/*
+ * dspark.h -- C ABI of the DSpark per-step speculative-decoding hot path on one
+ * GB300 GPU (sm_103a).
+ *
+ * The method is described in "DSpark: Confidence-Scheduled Speculative
+ * Decoding with Semi-Autoregressive Generation" (arXiv 2607.05147) and in the
+ * tutorial "Speculative decoding, from zero to DSpark".  Section references
+ * below are to those pages.
+ *
+ * Conventions for every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *     never allocates or frees device memory; scratch space is passed in as a
+ *     caller-owned workspace whose size is given by the matching *_workspace_bytes
+ *     query.  Tensors are dense, row-major, with the layouts stated per argument.
+ *   - `stream` is a cudaStream_t passed as void*.  All work is enqueued
+ *     asynchronously on that stream; the host never synchronises, except in
+ *     dspark_check().
+ *   - The return value reports HOST-side validation of sizes, pointers and
+ *     dtypes, done before anything is launched.  On a non-zero return nothing was
+ *     enqueued.
+ *   - Errors that depend on device data (a token id out of range, lengths out of
+ *     range, an inconsistent offset table, a too-short SPS table, a temperature
+ *     out of range) are written to the caller's int32 `dev_status` word (the
+ *     first error wins).  While *dev_status is non-zero every kernel of the
+ *     library returns without doing work, so a failed step leaves its outputs
+ *     unspecified and skips the rest.  dspark_check() synchronises the stream,
+ *     returns the device status and resets the word to zero.
+ *   - Logits and transition factors of one call share one dtype (DSPARK_F32 or
+ *     DSPARK_BF16, dims.dtype).  Token ids are int32 in [0, V).
+ *   - All randomness comes from one counter-based stream, Philox4x32-10
+ *     (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11):
+ *       key = (seed low 32 bits, seed high 32 bits),
+ *       counter = (v >> 2 | 0, position, request, tag), word (v & 3) for element v,
+ *       tag 0 = draft sampling (position k), 1 = accept uniform (position j,
+ *       counter word 0 = 0, word 0), 2 = residual / bonus sample (the rejecting
+ *       position j, or ell_r + 1 for the bonus);
+ *       Gumbel uniform u = ((w >> 9) + 0.5) * 2^-23, g = -log(-log u);
+ *       accept uniform u = (w >> 8) * 2^-24.
+ *     Requests are identified by their index r in the call.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_NULL = 1,            /* a required pointer is NULL                          */
+  DSPARK_ERR_DIMS = 2,            /* B < 1, K_max not in 1..16, V < 2, rank < 1, sizes   */
+  DSPARK_ERR_DTYPE = 3,           /* dtype not DSPARK_F32 / DSPARK_BF16                  */
+  DSPARK_ERR_TEMPERATURE = 4,     /* device: temperature NaN, inf, < 0 or in (0, 1e-3)   */
+  DSPARK_ERR_SPS_TOO_SHORT = 5,   /* device: sps_len < B + #candidates + 1               */
+  DSPARK_ERR_OFFSETS = 6,         /* device: tgt_off[0] != 0 or a gap != ell_r + 1        */
+  DSPARK_ERR_TOKEN_RANGE = 7,     /* device: an anchor / draft token outside [0, V)      */
+  DSPARK_ERR_LENGTHS = 8,         /* device: K_r not in 1..K_max or ell_r not in 0..K_max */
+  DSPARK_ERR_CONFIDENCE = 9,      /* device: a confidence outside [0, 1] or NaN          */
+  DSPARK_ERR_WORKSPACE = 10,      /* workspace NULL, too small or not 256-byte aligned   */
+  DSPARK_ERR_DEVICE_TIMEOUT = 11, /* device: a bounded wait inside a kernel gave up      */
+  DSPARK_ERR_CUDA = 12,           /* a CUDA runtime call failed (launch, query, copy)    */
+  DSPARK_ERR_UNSUPPORTED = 13     /* the current device is not sm_103 / shape unsupported */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+/* dims.flags bits */
+#define DSPARK_FLAG_FORCE_SIMT 1u /* draft: use the CUDA-core bias path even when the tensor-core path applies */
+
+typedef struct {
+  int64_t B;      /* requests in the call                                  */
+  int64_t K_max;  /* block size: draft positions per request, 1..16        */
+  int64_t V;      /* vocabulary size                                       */
+  int64_t rank;   /* Markov-head rank r (draft only; ignored by verify)     */
+  int32_t dtype;  /* dspark_dtype of every logits / factor tensor           */
+  uint32_t flags; /* DSPARK_FLAG_* bits                                    */
+} dspark_dims;
+
+/* ------------------------------------------------------------------------
+ * Draft: Markov-head semi-autoregressive sampling ("DSpark" S3.1, Markov head;
+ * "Speculative decoding, from zero to DSpark" S6).
+ *
+ * For each request r and position k = 1..K_r[r], left to right:
+ *   z_k(v) = U[r, k-1, v] + sum_i E[x_{k-1}, i] * W[i, v]     (x_0 = anchor[r])
+ *   stored in the call dtype (bf16 values are rounded to nearest even), then
+ *   x_k = argmax_v ( z_k(v) / T_r + g(seed, k, r, v) )         (T_r > 0)
+ *   x_k = argmax_v z_k(v)                                      (T_r = 0)
+ * ties to the smallest v.  This samples x_k ~ softmax(z_k / T_r).
+ *
+ *   U            [B, K_max, V]  base logits of the parallel backbone.
+ *   E            [V, rank]      W1, the Markov embedding table (row per previous token).
+ *   W            [rank, V]      W2, the logit projection.
+ *   anchor       [B] int32      x_0, the previous round's bonus/correction token.
+ *   K_r          [B] int32      draft length per request, 1..K_max.
+ *   temperature  [B] float      T_r: 0 (greedy) or >= 1e-3.
+ *   draft_tok    [B, K_max] int32 out: x_1..x_{K_r}; entries k > K_r are set to -1.
+ *   draft_logits [B, K_max, V]  out, optional (NULL = not written): z_k, the logits
+ *                actually sampled from; rows k > K_r are not written.
+ *   draft_lse    [B, K_max] float out, optional: log sum_v exp(z_k(v) / T_r), the
+ *                draft distribution's normaliser (for T_r = 0: max_v z_k(v));
+ *                entries k > K_r are not written.
+ *   workspace    >= dspark_draft_workspace_bytes(B, K_max, V) bytes, 256-byte aligned.
+ * The tensor-core path is used when dtype = DSPARK_BF16, rank is a multiple of
+ * 64 and <= 256, V is a multiple of 8 and the device is sm_103; otherwise (or
+ * with DSPARK_FLAG_FORCE_SIMT) the CUDA-core path runs.  Both give the same
+ * tokens except where two perturbed scores are within fp32 rounding.
+ * ------------------------------------------------------------------------ */
+size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V);
+
+dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W,
+                                         const int32_t *anchor, const int32_t *K_r,
+                                         const float *temperature, uint64_t seed, dspark_dims dims,
+                                         int32_t *draft_tok, void *draft_logits, float *draft_lse,
+                                         void *workspace, size_t workspace_bytes,
+                                         int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Schedule: hardware-aware prefix scheduler ("DSpark" S3.2.2, Algorithm 1;
+ * "Speculative decoding, from zero to DSpark" S8).
+ *
+ *   a[r, j] = prod_{i <= j} conf[r, i]     (sequential fp32 product, j = 1..K_r[r])
+ *   candidates {(r, j) : a[r, j] > 0}, ranked by a descending, ties to the smaller
+ *   position j, then the smaller request r;
+ *   walking that order with B <- R + i and tau_i = R + sum of the first i values of
+ *   a (exact 2^-40 fixed point), Theta_i = tau_i * SPS[R + i] (fp64, Theta_0 =
+ *   R * SPS[R]); admit while Theta_i > Theta_{i-1}; stop at the first decline.
+ *   ell[r] = number of admitted candidates of request r.
+ *
+ *   conf        [B, K_max] float  per-position acceptance confidences in [0, 1].
+ *   K_r         [B] int32         draft lengths, 1..K_max.
+ *   sps         [sps_len] double  SPS table indexed by verify batch tokens (entry 0
+ *               unused); must hold every index up to B + #candidates.
+ *   ell         [B] int32 out     scheduled verification lengths.
+ *   tgt_off     [B+1] int32 out   exclusive scan of (ell + 1): row offsets of the
+ *               flattened target logits consumed by dspark_verify_ragged.
+ *   theta_best  [1] double out, optional: the objective at the stop.
+ *   b_star      [1] int64 out, optional: the verify batch size R + sum(ell).
+ *   survival    [B, K_max] float out, optional: a (0 for j > K_r).
+ *   workspace   >= dspark_schedule_workspace_bytes(B, K_max) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dspark_schedule_workspace_bytes(int64_t B, int64_t K_max);
+
+dspark_status dspark_schedule_survival(const float *conf, const int32_t *K_r, const double *sps,
+                                       int64_t sps_len, int64_t B, int64_t K_max, int32_t *ell,
+                                       int32_t *tgt_off, double *theta_best, int64_t *b_star,
+                                       float *survival, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Verify: ragged rejection-sampling verification ("DSpark" S2.1;
+ * "Speculative decoding, from zero to DSpark" S2 and Appendix A1).
+ *
+ * For request r with temperature T and length ell_r, with
+ *   q_j = softmax(draft_logits[r, j-1] / T),  p_j = softmax(tgt_logits[tgt_off[r]+j-1] / T):
+ *   for j = 1..ell_r: accept x_j = draft_tok[r, j-1] iff u_j < min(1, p_j(x_j) / q_j(x_j)),
+ *   u_j the accept uniform of (seed, j, r); stop at the first rejection and sample the
+ *   correction by Gumbel-max of log(p_j - q_j) over {v : p_j(v) > q_j(v)} on stream
+ *   (seed, j, r, tag 2) (from p_j if that set is empty in floating point); if every
+ *   position is accepted, sample the bonus from row tgt_off[r] + ell_r by Gumbel-max
+ *   of z / T on stream (seed, ell_r + 1, r, tag 2).
+ *   T = 0: accept iff x_j is the argmax of p_j; correction and bonus are argmaxes.
+ *
+ *   draft_logits [B, K_max, V]   the logits the drafts were sampled from.
+ *   draft_lse    [B, K_max] float, optional: log-sum-exp of draft_logits / T per row
+ *                (as written by dspark_draft_markov_sample).  When given, draft rows
+ *                are read only at the rejecting position; when NULL they are
+ *                streamed at every verified position.
+ *   tgt_logits   [tgt_off[B], V]  flattened target logits, ell_r + 1 rows per request.
+ *   tgt_off      [B+1] int32      row offsets; tgt_off[r+1] - tgt_off[r] = ell_r + 1.
+ *   ell          [B] int32        verification lengths, 0..K_max.
+ *   draft_tok    [B, K_max] int32 draft tokens (entries j <= ell_r must lie in [0, V)).
+ *   temperature  [B] float        as for the draft.
+ *   n_acc        [B] int32 out    accepted draft tokens.
+ *   out_tok      [B, K_max+1] int32 out: the n_acc accepted tokens, then the
+ *                correction or bonus token, then -1.
+ *   workspace    >= dspark_verify_workspace_bytes(B, V) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dspark_verify_workspace_bytes(int64_t B, int64_t V);
+
+dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_lse,
+                                   const void *tgt_logits, const int32_t *tgt_off, const int32_t *ell,
+                                   const int32_t *draft_tok, const float *temperature, uint64_t seed,
+                                   dspark_dims dims, int32_t *n_acc, int32_t *out_tok,
+                                   void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Status helpers.
+ * ------------------------------------------------------------------------ */
+/* Static, human-readable name of a status code ("DSPARK_OK", ...). */
+const char *dspark_status_string(dspark_status s);
+
+/* Synchronise `stream`, read *dev_status (a device int32), reset it to 0 and
+ * return it.  Returns DSPARK_ERR_CUDA when the copy or the synchronisation fails. */
+dspark_status dspark_check(int32_t *dev_status, void *stream);
+
+/* ABI version of this header (major * 100 + minor). */
+int dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,281 @@
+"""DSpark per-step speculative-decoding hot path on one GB300 (sm_103a).
+
+Python binding of ``libdspark.so`` (see ``include/dspark.h``).  The functions
+here only marshal arguments: they check tensor placement, dtypes and shapes,
+allocate outputs and workspaces with torch on the tensors' device, and call the
+C ABI on the current CUDA stream.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.  If the library has
+not been built, every call raises ``DsparkUnavailable``.
+
+Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+Semi-Autoregressive Generation" (S2.1 acceptance rule, S3.1 Markov head,
+S3.2.2 Algorithm 1).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "DsparkError", "DsparkUnavailable", "lib", "library_path", "draft_markov_sample", "schedule_survival",
+    "verify_ragged", "check", "status_string", "draft_workspace_bytes", "schedule_workspace_bytes",
+    "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "STATUS_NAMES", "Dims",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libdspark.so")
+
+F32, BF16 = 0, 1
+FLAG_FORCE_SIMT = 1
+
+STATUS_NAMES = {
+    0: "DSPARK_OK", 1: "DSPARK_ERR_NULL", 2: "DSPARK_ERR_DIMS", 3: "DSPARK_ERR_DTYPE",
+    4: "DSPARK_ERR_TEMPERATURE", 5: "DSPARK_ERR_SPS_TOO_SHORT", 6: "DSPARK_ERR_OFFSETS",
+    7: "DSPARK_ERR_TOKEN_RANGE", 8: "DSPARK_ERR_LENGTHS", 9: "DSPARK_ERR_CONFIDENCE",
+    10: "DSPARK_ERR_WORKSPACE", 11: "DSPARK_ERR_DEVICE_TIMEOUT", 12: "DSPARK_ERR_CUDA",
+    13: "DSPARK_ERR_UNSUPPORTED",
+}
+
+EXPORTED_SYMBOLS = [
+    "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_schedule_workspace_bytes",
+    "dspark_schedule_survival", "dspark_verify_workspace_bytes", "dspark_verify_ragged",
+    "dspark_status_string", "dspark_check", "dspark_version",
+]
+
+
+class DsparkUnavailable(RuntimeError):
+    pass
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS_NAMES.get(code, f"DSPARK_ERR_{code}")
+        super().__init__(f"{where}: {self.name}")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("K_max", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("rank", ctypes.c_int64), ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdspark.so (raises DsparkUnavailable when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise DsparkUnavailable(f"{_LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(_LIB_PATH)
+    P, i64, u64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+    st = ctypes.c_int
+    L.dspark_draft_workspace_bytes.argtypes = [i64, i64, i64]
+    L.dspark_draft_workspace_bytes.restype = sz
+    L.dspark_draft_markov_sample.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
+    L.dspark_draft_markov_sample.restype = st
+    L.dspark_schedule_workspace_bytes.argtypes = [i64, i64]
+    L.dspark_schedule_workspace_bytes.restype = sz
+    L.dspark_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, sz, P, P]
+    L.dspark_schedule_survival.restype = st
+    L.dspark_verify_workspace_bytes.argtypes = [i64, i64]
+    L.dspark_verify_workspace_bytes.restype = sz
+    L.dspark_verify_ragged.argtypes = [P, P, P, P, P, P, P, u64, Dims, P, P, P, sz, P, P]
+    L.dspark_verify_ragged.restype = st
+    L.dspark_status_string.argtypes = [st]
+    L.dspark_status_string.restype = ctypes.c_char_p
+    L.dspark_check.argtypes = [P, P]
+    L.dspark_check.restype = st
+    L.dspark_version.argtypes = []
+    L.dspark_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    if ws is not None and ws.numel() >= nbytes and ws.data_ptr() % 256 == 0:
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _raise(code: int, where: str):
+    if code != 0:
+        raise DsparkError(code, where)
+
+
+def status_string(code: int) -> str:
+    return lib().dspark_status_string(int(code)).decode()
+
+
+def check(dev_status: torch.Tensor, stream=None) -> str:
+    """Synchronise, read and reset the device status word; returns its name."""
+    code = lib().dspark_check(_ptr(dev_status), _stream(stream))
+    return STATUS_NAMES.get(code, f"DSPARK_ERR_{code}")
+
+
+def draft_workspace_bytes(B: int, K_max: int, V: int) -> int:
+    return int(lib().dspark_draft_workspace_bytes(B, K_max, V))
+
+
+def schedule_workspace_bytes(B: int, K_max: int) -> int:
+    return int(lib().dspark_schedule_workspace_bytes(B, K_max))
+
+
+def verify_workspace_bytes(B: int, V: int) -> int:
+    return int(lib().dspark_verify_workspace_bytes(B, V))
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
+                        want_lse: bool = True, force_simt: bool = False, out: Optional[dict] = None,
+                        workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                        stream=None) -> dict:
+    """Markov-head draft sampling (C ABI dspark_draft_markov_sample).
+
+    U [B,K_max,V], E [V,rank], W [rank,V] (float32 or bfloat16, one dtype);
+    anchor, K_r [B] int32; temperature [B] float32.  Returns a dict with
+    draft_tok [B,K_max] int32, draft_logits (U's dtype) or None, draft_lse
+    [B,K_max] float32 or None, and the status / workspace tensors used.
+    """
+    dt = _dtype_code(_dev(U, "U"))
+    B, K_max, V = U.shape
+    rank = E.shape[1]
+    _dev(E, "E", U.dtype, (V, rank))
+    _dev(W, "W", U.dtype, (rank, V))
+    _dev(anchor, "anchor", torch.int32, (B,))
+    _dev(K_r, "K_r", torch.int32, (B,))
+    _dev(temperature, "temperature", torch.float32, (B,))
+    dev = U.device
+    out = {} if out is None else out
+    tok = out.get("draft_tok")
+    if tok is None:
+        tok = torch.empty(B, K_max, dtype=torch.int32, device=dev)
+    logits = out.get("draft_logits") if want_logits else None
+    if want_logits and logits is None:
+        logits = torch.empty_like(U)
+    lse = out.get("draft_lse") if want_lse else None
+    if want_lse and lse is None:
+        lse = torch.empty(B, K_max, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    nbytes = draft_workspace_bytes(B, K_max, V)
+    ws = _workspace(nbytes, dev, workspace)
+    dims = Dims(B, K_max, V, rank, dt, FLAG_FORCE_SIMT if force_simt else 0)
+    code = lib().dspark_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r), _ptr(temperature),
+                                            ctypes.c_uint64(seed), dims, _ptr(tok), _ptr(logits), _ptr(lse),
+                                            _ptr(ws), ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
+    _raise(code, "dspark_draft_markov_sample")
+    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, status=status, workspace=ws)
+
+
+def schedule_survival(conf, K_r, sps, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                      status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Hardware-aware prefix scheduler (C ABI dspark_schedule_survival).
+
+    conf [B,K_max] float32, K_r [B] int32, sps float64 (CUDA).  Returns ell [B],
+    tgt_off [B+1] (int32), theta_best [1] float64, b_star [1] int64 and survival
+    [B,K_max] float32.
+    """
+    _dev(conf, "conf", torch.float32)
+    B, K_max = conf.shape
+    _dev(K_r, "K_r", torch.int32, (B,))
+    _dev(sps, "sps", torch.float64)
+    dev = conf.device
+    out = {} if out is None else out
+    ell = out.get("ell") if out.get("ell") is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    off = out.get("tgt_off") if out.get("tgt_off") is not None else torch.empty(B + 1, dtype=torch.int32, device=dev)
+    th = out.get("theta_best") if out.get("theta_best") is not None else torch.empty(1, dtype=torch.float64, device=dev)
+    bs = out.get("b_star") if out.get("b_star") is not None else torch.empty(1, dtype=torch.int64, device=dev)
+    surv = out.get("survival") if out.get("survival") is not None else torch.empty(B, K_max, dtype=torch.float32,
+                                                                                   device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _workspace(schedule_workspace_bytes(B, K_max), dev, workspace)
+    code = lib().dspark_schedule_survival(_ptr(conf), _ptr(K_r), _ptr(sps), sps.numel(), B, K_max, _ptr(ell),
+                                          _ptr(off), _ptr(th), _ptr(bs), _ptr(surv), _ptr(ws),
+                                          ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
+    _raise(code, "dspark_schedule_survival")
+    return dict(ell=ell, tgt_off=off, theta_best=th, b_star=bs, survival=surv, status=status, workspace=ws)
+
+
+def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature, seed: int, *,
+                  draft_lse=None, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Ragged rejection-sampling verification (C ABI dspark_verify_ragged).
+
+    draft_logits [B,K_max,V], tgt_logits [sum(ell+1),V] (one dtype), tgt_off
+    [B+1], ell [B], draft_tok [B,K_max] int32, temperature [B] float32,
+    draft_lse [B,K_max] float32 or None.  Returns n_acc [B] and out_tok
+    [B,K_max+1] (int32).
+    """
+    dt = _dtype_code(_dev(draft_logits, "draft_logits"))
+    B, K_max, V = draft_logits.shape
+    _dev(tgt_logits, "tgt_logits", draft_logits.dtype)
+    if tgt_logits.dim() != 2 or tgt_logits.shape[1] != V:
+        raise ValueError("tgt_logits must be [rows, V]")
+    _dev(tgt_off, "tgt_off", torch.int32, (B + 1,))
+    _dev(ell, "ell", torch.int32, (B,))
+    _dev(draft_tok, "draft_tok", torch.int32, (B, K_max))
+    _dev(temperature, "temperature", torch.float32, (B,))
+    if draft_lse is not None:
+        _dev(draft_lse, "draft_lse", torch.float32, (B, K_max))
+    dev = draft_logits.device
+    out = {} if out is None else out
+    n_acc = out.get("n_acc") if out.get("n_acc") is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    out_tok = out.get("out_tok") if out.get("out_tok") is not None else torch.empty(B, K_max + 1, dtype=torch.int32,
+                                                                                    device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _workspace(verify_workspace_bytes(B, V), dev, workspace)
+    dims = Dims(B, K_max, V, 0, dt, 0)
+    code = lib().dspark_verify_ragged(_ptr(draft_logits), _ptr(draft_lse), _ptr(tgt_logits), _ptr(tgt_off),
+                                      _ptr(ell), _ptr(draft_tok), _ptr(temperature), ctypes.c_uint64(seed), dims,
+                                      _ptr(n_acc), _ptr(out_tok), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                      _ptr(status), _stream(stream))
+    _raise(code, "dspark_verify_ragged")
+    return dict(n_acc=n_acc, out_tok=out_tok, status=status, workspace=ws)

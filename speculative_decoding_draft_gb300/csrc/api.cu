@@ -1,0 +1,237 @@
+// Host side of the C ABI declared in include/dspark.h: argument validation,
+// workspace carving, kernel-path selection and the status helpers.
+#include <cstdio>
+#include <cstring>
+
+#include "dspark_internal.cuh"
+
+using namespace dspark;
+
+namespace {
+
+constexpr int64_t kMaxB = 1 << 20;
+constexpr int64_t kMaxV = (int64_t)1 << 30;
+constexpr int64_t kMaxRank = 8192;
+constexpr int kDraftSimtChunk = 2048;        // must match draft_simt.cu
+constexpr int64_t kTcPartialSlots = 1024 * 128;
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned256(const void *p) { return ((uintptr_t)p & 255u) == 0; }
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+bool device_info(DeviceInfo *out) {
+  static DeviceInfo cache[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!have[dev]) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+int64_t draft_partial_slots(int64_t B, int64_t V) {
+  const int64_t simt = B * ((V + kDraftSimtChunk - 1) / kDraftSimtChunk);
+  return simt > kTcPartialSlots ? simt : kTcPartialSlots;
+}
+
+dspark_status check_dims(const dspark_dims &d, bool need_rank) {
+  if (d.B < 1 || d.B > kMaxB || d.K_max < 1 || d.K_max > kMaxK || d.V < 2 || d.V > kMaxV)
+    return DSPARK_ERR_DIMS;
+  if (need_rank && (d.rank < 1 || d.rank > kMaxRank)) return DSPARK_ERR_DIMS;
+  if (d.dtype != DSPARK_F32 && d.dtype != DSPARK_BF16) return DSPARK_ERR_DTYPE;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_version(void) { return 100; }
+
+const char *dspark_status_string(dspark_status s) {
+  switch (s) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_ERR_NULL: return "DSPARK_ERR_NULL";
+    case DSPARK_ERR_DIMS: return "DSPARK_ERR_DIMS";
+    case DSPARK_ERR_DTYPE: return "DSPARK_ERR_DTYPE";
+    case DSPARK_ERR_TEMPERATURE: return "DSPARK_ERR_TEMPERATURE";
+    case DSPARK_ERR_SPS_TOO_SHORT: return "DSPARK_ERR_SPS_TOO_SHORT";
+    case DSPARK_ERR_OFFSETS: return "DSPARK_ERR_OFFSETS";
+    case DSPARK_ERR_TOKEN_RANGE: return "DSPARK_ERR_TOKEN_RANGE";
+    case DSPARK_ERR_LENGTHS: return "DSPARK_ERR_LENGTHS";
+    case DSPARK_ERR_CONFIDENCE: return "DSPARK_ERR_CONFIDENCE";
+    case DSPARK_ERR_WORKSPACE: return "DSPARK_ERR_WORKSPACE";
+    case DSPARK_ERR_DEVICE_TIMEOUT: return "DSPARK_ERR_DEVICE_TIMEOUT";
+    case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
+    case DSPARK_ERR_UNSUPPORTED: return "DSPARK_ERR_UNSUPPORTED";
+  }
+  return "DSPARK_ERR_UNKNOWN";
+}
+
+dspark_status dspark_check(int32_t *dev_status, void *stream) {
+  if (!dev_status) return DSPARK_ERR_NULL;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+  return (dspark_status)host;
+}
+
+// ---------------------------------------------------------------------------
+// draft
+// ---------------------------------------------------------------------------
+size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V) {
+  if (B < 1 || K_max < 1 || V < 2) return 0;
+  return al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
+         al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) +
+         al256(sizeof(Partial) * (size_t)draft_partial_slots(B, V));
+}
+
+dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
+                                         const int32_t *K_r, const float *temperature, uint64_t seed,
+                                         dspark_dims dims, int32_t *draft_tok, void *draft_logits,
+                                         float *draft_lse, void *workspace, size_t workspace_bytes,
+                                         int32_t *dev_status, void *stream) {
+  if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok || !dev_status) return DSPARK_ERR_NULL;
+  dspark_status st = check_dims(dims, true);
+  if (st != DSPARK_OK) return st;
+  if (!workspace || !aligned256(workspace) ||
+      workspace_bytes < dspark_draft_workspace_bytes(dims.B, dims.K_max, dims.V))
+    return DSPARK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return DSPARK_ERR_CUDA;
+  DraftArgs a;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.anchor = anchor;
+  a.K_r = K_r;
+  a.temperature = temperature;
+  a.draft_tok = draft_tok;
+  a.draft_logits = draft_logits;
+  a.draft_lse = draft_lse;
+  a.dev_status = dev_status;
+  a.B = dims.B;
+  a.K_max = dims.K_max;
+  a.V = dims.V;
+  a.rank = dims.rank;
+  a.dtype = dims.dtype;
+  a.key = make_philox_key(seed);
+  char *p = (char *)workspace;
+  a.perm = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)dims.B);
+  a.nact = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 2));
+  a.counters = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)(dims.B > 4096 ? dims.B : 4096));
+  a.partials = (Partial *)p;
+  a.partial_slots = draft_partial_slots(dims.B, dims.V);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_draft_prologue(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  const bool use_tc = !(dims.flags & DSPARK_FLAG_FORCE_SIMT) && dev.major == 10 && dev.minor == 3 &&
+                      draft_tc_supported(a);
+  cudaError_t e = use_tc ? launch_draft_tc(a, s, dev.sms) : launch_draft_simt(a, s);
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// schedule
+// ---------------------------------------------------------------------------
+size_t dspark_schedule_workspace_bytes(int64_t B, int64_t K_max) {
+  if (B < 1 || K_max < 1) return 0;
+  return schedule_ws_bytes(B, K_max);
+}
+
+dspark_status dspark_schedule_survival(const float *conf, const int32_t *K_r, const double *sps, int64_t sps_len,
+                                       int64_t B, int64_t K_max, int32_t *ell, int32_t *tgt_off,
+                                       double *theta_best, int64_t *b_star, float *survival, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (!conf || !K_r || !sps || !ell || !tgt_off || !dev_status) return DSPARK_ERR_NULL;
+  if (B < 1 || B > kMaxB || K_max < 1 || K_max > kMaxK || sps_len < 1) return DSPARK_ERR_DIMS;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_schedule_workspace_bytes(B, K_max))
+    return DSPARK_ERR_WORKSPACE;
+  ScheduleArgs a;
+  a.conf = conf;
+  a.K_r = K_r;
+  a.sps = sps;
+  a.sps_len = sps_len;
+  a.B = B;
+  a.K_max = K_max;
+  a.ell = ell;
+  a.tgt_off = tgt_off;
+  a.theta_best = theta_best;
+  a.b_star = b_star;
+  a.survival = survival;
+  a.dev_status = dev_status;
+  a.ws = workspace;
+  return launch_schedule(a, (cudaStream_t)stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// verify
+// ---------------------------------------------------------------------------
+size_t dspark_verify_workspace_bytes(int64_t B, int64_t V) {
+  if (B < 1 || V < 2) return 0;
+  return verify_ws_bytes(B, V, nullptr);
+}
+
+dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_lse, const void *tgt_logits,
+                                   const int32_t *tgt_off, const int32_t *ell, const int32_t *draft_tok,
+                                   const float *temperature, uint64_t seed, dspark_dims dims, int32_t *n_acc,
+                                   int32_t *out_tok, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream) {
+  if (!draft_logits || !tgt_logits || !tgt_off || !ell || !draft_tok || !temperature || !n_acc || !out_tok ||
+      !dev_status)
+    return DSPARK_ERR_NULL;
+  dspark_status st = check_dims(dims, false);
+  if (st != DSPARK_OK) return st;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_verify_workspace_bytes(dims.B, dims.V))
+    return DSPARK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return DSPARK_ERR_CUDA;
+  VerifyArgs a;
+  a.D = draft_logits;
+  a.D_lse = draft_lse;
+  a.tgt = tgt_logits;
+  a.tgt_off = tgt_off;
+  a.ell = ell;
+  a.draft_tok = draft_tok;
+  a.temperature = temperature;
+  a.n_acc = n_acc;
+  a.out_tok = out_tok;
+  a.dev_status = dev_status;
+  a.B = dims.B;
+  a.K_max = dims.K_max;
+  a.V = dims.V;
+  a.dtype = dims.dtype;
+  a.key = make_philox_key(seed);
+  int chunks = 1;
+  verify_ws_bytes(dims.B, dims.V, &chunks);
+  a.chunks = chunks;
+  char *p = (char *)workspace;
+  a.jobs = (VerifyJob *)p;
+  p += al256(sizeof(VerifyJob) * (size_t)dims.B);
+  a.counters = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)dims.B);
+  a.partials = (Partial *)p;
+  return launch_verify(a, (cudaStream_t)stream, dev.sms) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+}  // extern "C"

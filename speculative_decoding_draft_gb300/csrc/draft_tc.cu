@@ -1,0 +1,522 @@
+// Markov-head draft sampling, tensor-core path (sm_103a: tcgen05 + TMA + TMEM).
+//
+// "DSpark" S3.1 (Markov head B(x_{k-1}, .) = W1[x_{k-1}] . W2, rank r) and
+// "Speculative decoding, from zero to DSpark" S6 (p_k = softmax(U_k + B_k)).
+//
+// One launch per draft position k.  The active requests (K_r >= k) form the
+// first n_k entries of `perm`; they are cut into M-tiles of 128 rows.  A
+// persistent grid of one CTA per SM gives every M-tile floor(G / M-tiles) CTAs,
+// each owning a contiguous range of 64-wide vocabulary tiles, so the gathered
+// 128 x r operand is staged once per CTA and reused across its whole range.
+//
+// Warp roles (320 threads):
+//   warp 0     producer: per vocabulary tile, one TMA tile load of W2[:, n:n+64]
+//              (128-byte swizzle, r x 64 bf16) and one 1-D bulk copy per active row
+//              of U[r, k-1, n:n+64] into a padded row-major slot; both complete on
+//              the stage's full barrier.
+//   warp 1     allocates TMEM (4 accumulators of 128 x 64 fp32) and one elected
+//              lane issues r/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate,
+//              A K-major from shared memory, B MN-major from shared memory) per tile,
+//              committing to the stage's empty barrier and the accumulator's full
+//              barrier.
+//   warps 2-9  epilogue, two warps per TMEM lane quadrant (one per 32-column half):
+//              gather W1[x_{k-1}] rows into the swizzled A operand at the start of a
+//              tile range, then per tile tcgen05.ld the 32 fp32 bias values of their
+//              row, add U, round to bf16, optionally store the logits, and run the
+//              Gumbel race / greedy argmax with the online softmax.  No 128 x V
+//              logits tile ever goes back to HBM unless the caller asks for it.
+// Block partials per row are merged by the last CTA of each M-tile, which
+// writes the token and the log-sum-exp.  Every wait is bounded; on a timeout
+// the kernel records DSPARK_ERR_DEVICE_TIMEOUT, drains what it issued, frees
+// TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dspark_internal.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileN = 64;
+constexpr int kStages = 3;
+constexpr int kAccBufs = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
+constexpr int kTmemCols = kAccBufs * kTileN;               // 256
+constexpr int kAChunk = kTileM * 128;                      // 16 KB: 128 rows x 64 bf16
+constexpr int kASize = 4 * kAChunk;                        // rank <= 256
+constexpr int kWSlot = 256 * 128;                          // r rows x 128 B
+constexpr int kUPitch = kTileN * 2 + 16;                   // 144 B: padded against bank conflicts
+constexpr int kUSlot = kTileM * kUPitch;
+constexpr int kOffA = 0;
+constexpr int kOffW = kOffA + kASize;
+constexpr int kOffU = kOffW + kStages * kWSlot;
+constexpr int kOffSh = kOffU + kStages * kUSlot;
+constexpr long long kTimeoutCycles = 4000000000LL;
+
+struct TcShared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t accf[kAccBufs];
+  uint64_t acce[kAccBufs];
+  uint64_t aready;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int last;
+  int skip;
+  int row_req[kTileM];
+  int row_prev[kTileM];
+  float row_invT[kTileM];
+  Partial half[kTileM];
+};
+
+constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// ---- PTX wrappers ---------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier phase.  Returns false (and raises the CTA abort
+// flag) when the wait gave up or another role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
+// offsets (>> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
+// B MN-major, N = 64, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kTileN >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void named_sync_epi() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    draft_tc_step(const __grid_constant__ DraftArgs a, const __grid_constant__ CUtensorMap tmap_w, int k) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t *gb = smem_raw + (sb - raw);
+  TcShared &sh = *reinterpret_cast<TcShared *>(gb + kOffSh);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) sh.skip = read_status(a.dev_status);
+  __syncthreads();
+  if (sh.skip) return;
+
+  const int n_k = a.nact[k];
+  const int K = (int)a.K_max, V = (int)a.V, rank = (int)a.rank;
+  const int m_tiles = (n_k + kTileM - 1) / kTileM;
+  if (m_tiles == 0) return;
+  const int G = gridDim.x;
+  const int n_tiles = (V + kTileN - 1) / kTileN;
+  const int gm = max(1, min(G / m_tiles, n_tiles));
+  const int units = m_tiles * gm;
+  if ((int)blockIdx.x >= units) return;
+  const int ksteps = rank / 16;
+  const uint32_t w_bytes = (uint32_t)(kTileN * rank * 2);
+
+  const uint32_t bar_full = smem_u32(&sh.full[0]);
+  const uint32_t bar_empty = smem_u32(&sh.empty[0]);
+  const uint32_t bar_accf = smem_u32(&sh.accf[0]);
+  const uint32_t bar_acce = smem_u32(&sh.acce[0]);
+  const uint32_t bar_aready = smem_u32(&sh.aready);
+  const uint32_t bar_drain = smem_u32(&sh.drain);
+  volatile int *abort = &sh.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1 + kEpiWarps);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(bar_accf + 8 * b, 1);
+      mbar_init(bar_acce + 8 * b, kEpiWarps);
+    }
+    mbar_init(bar_aready, kEpiWarps);
+    mbar_init(bar_drain, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  uint32_t it = 0;   // global tile counter of this CTA (same progression in every role)
+  int unit_no = 0;
+  uint32_t issued_use[kStages];   // producer: last issued use of each stage (for the abort drain)
+  bool issued[kStages];
+  for (int s = 0; s < kStages; ++s) {
+    issued_use[s] = 0;
+    issued[s] = false;
+  }
+  for (int u = blockIdx.x; u < units; u += G, ++unit_no) {
+    const int m = u / gm, j = u % gm;
+    const int nt0 = (int)((int64_t)j * n_tiles / gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / gm);
+    const int row0 = m * kTileM;
+    const int nrows = min(kTileM, n_k - row0);
+    __syncthreads();
+    if (threadIdx.x < kTileM) {
+      const int i = threadIdx.x;
+      if (i < nrows) {
+        const int r = a.perm[row0 + i];
+        sh.row_req[i] = r;
+        sh.row_prev[i] = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
+        const float T = a.temperature[r];
+        sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
+      } else {
+        sh.row_req[i] = -1;
+        sh.row_prev[i] = 0;
+        sh.row_invT[i] = 0.0f;
+      }
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+      // ---------------- producer ----------------
+      for (int t = nt0; t < nt1 && !*abort; ++t) {
+        const uint32_t idx = it + (uint32_t)(t - nt0);
+        const int s = (int)(idx % kStages);
+        const uint32_t use = idx / kStages;
+        if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
+        const int cols = min(kTileN, V - t * kTileN);
+        const uint32_t ubytes = (uint32_t)cols * 2u;
+        if (lane == 0) {
+          mbar_arrive_tx(bar_full + 8 * s, w_bytes + (uint32_t)nrows * ubytes);
+          tma_load_2d(sb + kOffW + s * kWSlot, &tmap_w, t * kTileN, 0, bar_full + 8 * s);
+        }
+        issued_use[s] = use;
+        issued[s] = true;
+        __syncwarp();
+        for (int rr = lane; rr < nrows; rr += 32) {
+          const int r = sh.row_req[rr];
+          const unsigned short *src =
+              (const unsigned short *)a.U + ((int64_t)r * K + (k - 1)) * (int64_t)V + (int64_t)t * kTileN;
+          bulk_g2s(sb + kOffU + s * kUSlot + rr * kUPitch, src, ubytes, bar_full + 8 * s);
+        }
+        __syncwarp();
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      if (lane == 0) {
+        bool ok = mbar_wait(bar_aready, (uint32_t)(unit_no & 1), abort);
+        for (int t = nt0; ok && t < nt1; ++t) {
+          const uint32_t idx = it + (uint32_t)(t - nt0);
+          const int s = (int)(idx % kStages);
+          const uint32_t use = idx / kStages;
+          const int b = (int)(idx % kAccBufs);
+          const uint32_t ause = idx / kAccBufs;
+          if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
+          if (!mbar_wait(bar_acce + 8 * b, (ause & 1u) ^ 1u, abort)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(b * kTileN);
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = smem_desc(sb + kOffA + (kk >> 2) * kAChunk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(sb + kOffW + s * kWSlot + kk * 2048, (uint32_t)(rank * 128), 1024);
+            mma_bf16(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar_empty + 8 * s);
+          mma_commit(bar_accf + 8 * b);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ---------------- epilogue ----------------
+      const int eq = warp - 2;            // 0..7
+      const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
+      const int half = eq >> 2;           // 32-column half of the 64-wide tile
+      const int et = eq * 32 + lane;      // 0..255
+      // gather the A operand: row i, 16-byte unit c8 of chunk c goes to chunk c, row i,
+      // unit (c8 ^ (i & 7)) -- the 128-byte swizzle of a K-major tile.
+      const int units_per_row = rank / 8;
+      for (int e = et; e < kTileM * units_per_row; e += kEpiWarps * 32) {
+        const int i = e / units_per_row, uu = e % units_per_row;
+        const int c = uu >> 3, c8 = uu & 7;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (i < nrows) val = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * rank) + uu);
+        const uint32_t dst = sb + kOffA + c * kAChunk + i * 128 + ((c8 ^ (i & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y), "r"(val.z),
+                     "r"(val.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_aready);
+
+      const int row = quad * 32 + lane;
+      const bool valid = row < nrows;
+      const int r = valid ? sh.row_req[row] : 0;
+      const float invT = sh.row_invT[row];
+      const bool greedy = (invT == 0.0f);
+      const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
+      Race st;
+      race_init(st);
+      for (int t = nt0; t < nt1; ++t) {
+        const uint32_t idx = it + (uint32_t)(t - nt0);
+        const int s = (int)(idx % kStages);
+        const uint32_t use = idx / kStages;
+        const int b = (int)(idx % kAccBufs);
+        const uint32_t ause = idx / kAccBufs;
+        if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
+        if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
+        tc_fence_after();
+        uint32_t acc[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
+        tmem_wait_ld();
+        uint4 uv[4];
+        const uint32_t usrc = sb + kOffU + s * kUSlot + row * kUPitch + half * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(uv[q].x), "=r"(uv[q].y), "=r"(uv[q].z), "=r"(uv[q].w)
+                       : "r"(usrc + 16 * q));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_acce + 8 * b);
+          mbar_arrive(bar_empty + 8 * s);
+        }
+        if (!valid) continue;
+        const int c0 = t * kTileN + half * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t pk[4] = {uv[g].x, uv[g].y, uv[g].z, uv[g].w};
+          float sv[8];
+          uint32_t packed[4];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t hbits = (e & 1) ? (pk[e >> 1] & 0xffff0000u) : (pk[e >> 1] << 16);
+            const float zf = __uint_as_float(hbits) + __uint_as_float(acc[g * 8 + e]);
+            const __nv_bfloat16 zb = __float2bfloat16_rn(zf);
+            const float z = __bfloat162float(zb);
+            const uint32_t zbits = (uint32_t)__bfloat16_as_ushort(zb);
+            if (e & 1) packed[e >> 1] |= zbits << 16;
+            else packed[e >> 1] = zbits;
+            const bool in = (c0 + g * 8 + e) < V;
+            sv[e] = in ? (greedy ? z : z * invT) : -INFINITY;
+          }
+          if (a.draft_logits && c0 + g * 8 + 8 <= V) {
+            uint4 *dst = (uint4 *)((unsigned short *)a.draft_logits + urow + c0 + g * 8);
+            *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          }
+          if (greedy) {
+            argmax_update<8>(st, sv, c0 + g * 8);
+          } else {
+            const uint32_t cb = (uint32_t)((c0 + g * 8) >> 2);
+            const uint4 w0 = philox(a.key, cb, (uint32_t)k, (uint32_t)r, kTagDraft);
+            const uint4 w1 = philox(a.key, cb + 1u, (uint32_t)k, (uint32_t)r, kTagDraft);
+            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            race_update<8>(st, sv, w, c0 + g * 8);
+          }
+        }
+      }
+      // merge the two column halves of each row, publish the CTA partial
+      if (half == 1) sh.half[row] = to_partial(st);
+      named_sync_epi();
+      if (half == 0) {
+        race_merge(st, from_partial(sh.half[row]));
+        a.partials[(int64_t)u * kTileM + row] = to_partial(st);
+      }
+      __threadfence();
+      named_sync_epi();
+      if (et == 0) sh.last = (atomicAdd(&a.counters[m], 1) == gm - 1);
+      named_sync_epi();
+      if (sh.last) {
+        __threadfence();
+        if (half == 0 && valid) {
+          Race tot;
+          race_init(tot);
+          for (int jj = 0; jj < gm; ++jj)
+            race_merge(tot, from_partial(load_partial(a.partials + ((int64_t)(m * gm + jj) * kTileM + row))));
+          a.draft_tok[(int64_t)r * K + k - 1] = tot.idx;
+          if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot.best : tot.m + logf(tot.S);
+        }
+        if (et == 0) a.counters[m] = 0;
+      }
+    }
+    it += (uint32_t)(nt1 - nt0);
+  }
+
+  // ---- teardown: drain issued MMAs, free TMEM -------------------------------
+  if (warp == 1) {
+    if (lane == 0) {
+      mma_commit(bar_drain);
+      const long long t0 = clock64();
+      while (!mbar_try(bar_drain, 0u) && clock64() - t0 < kTimeoutCycles) {
+      }
+    }
+    __syncwarp();
+  }
+  if (warp == 0 && lane == 0 && *abort) {
+    // wait (bounded) until the last copies issued into each stage have landed
+    for (int s = 0; s < kStages; ++s) {
+      if (!issued[s]) continue;
+      const long long t0 = clock64();
+      while (!mbar_try(bar_full + 8 * s, issued_use[s] & 1u) && clock64() - t0 < kTimeoutCycles / 4) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort && threadIdx.x == 0) set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool draft_tc_supported(const DraftArgs &a) {
+  if (a.dtype != DSPARK_BF16) return false;
+  if (a.rank % 64 != 0 || a.rank > 256) return false;
+  if (a.V % 8 != 0 || a.V > (int64_t)INT32_MAX - 64) return false;
+  if (((uintptr_t)a.U | (uintptr_t)a.E | (uintptr_t)a.W) & 15u) return false;
+  if (a.draft_logits && ((uintptr_t)a.draft_logits & 15u)) return false;
+  const int64_t m_tiles = (a.B + kTileM - 1) / kTileM;
+  const int64_t units = m_tiles > 1024 ? m_tiles : 1024;
+  if (units * kTileM > a.partial_slots) return false;
+  return get_encode() != nullptr;
+}
+
+cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)a.V, (cuuint64_t)a.rank};
+  const cuuint64_t gstride[1] = {(cuuint64_t)a.V * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)a.rank};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.W), gdim, gstride, box,
+                       estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(draft_tc_step, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = num_sms > 1024 ? 1024 : num_sms;
+  for (int k = 1; k <= (int)a.K_max; ++k) {
+    draft_tc_step<<<grid, kThreadsTc, kSmemBytes, s>>>(a, tmap, k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace dspark

@@ -1,0 +1,340 @@
+// Internal device helpers shared by the DSpark kernels (sm_103a).
+//
+// Random stream: Philox4x32-10 as specified in Salmon, Moraes, Dror, Shaw,
+// "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11), S4.  Round keys are
+// precomputed on the host and travel in the kernel parameter block, so the
+// rounds read them from the constant bank.
+//
+// Sampling: Gumbel-max, x = argmax_v (s_v + g_v), g_v = -log(-log u_v), which
+// draws x ~ softmax(s).  The hot loop evaluates it as an exponential race: with
+// E_v = -log u_v, x = argmin_v E_v / exp(s_v).  Because E_v >= 1 - u_v, an element
+// can only beat the running best when (1 - u_v) < exp(s_v - best); that test
+// costs one multiply against exp(s_v - m), which the online softmax computes
+// anyway, and the exact score (two accurate logarithms) is evaluated only for
+// the rare elements that pass it.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+constexpr uint32_t kTagDraft = 0;
+constexpr uint32_t kTagAccept = 1;
+constexpr uint32_t kTagResid = 2;
+constexpr int kMaxK = 16;
+constexpr float kMinPositiveT = 1e-3f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kFilterSlack = 1.0f + 1.0f / 1024.0f;   // keeps the race filter conservative
+constexpr float kFilterMax = 1.2676506002282294e30f;    // 2^100: "no best yet"
+
+struct PhiloxKey {
+  uint32_t k0[10];
+  uint32_t k1[10];
+};
+
+inline PhiloxKey make_philox_key(uint64_t seed) {
+  PhiloxKey k;
+  uint32_t a = (uint32_t)(seed & 0xffffffffu), b = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    k.k0[i] = a;
+    k.k1[i] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
+// Ten Philox rounds on counter (c0, c1, c2, c3).
+__device__ __forceinline__ uint4 philox(const PhiloxKey &key, uint32_t c0, uint32_t c1, uint32_t c2,
+                                        uint32_t c3) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint32_t lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ key.k0[i];
+    const uint32_t n2 = hi0 ^ c3 ^ key.k1[i];
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &w, int i) {
+  return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+}
+
+// ((w >> 9) + 0.5) * 2^-23: exact, in (0, 1).
+__device__ __forceinline__ float uniform_open(uint32_t w) {
+  return __uint_as_float((w >> 9) | 0x3F800000u) - 0.99999994039535522f;   // 1 - 2^-24
+}
+
+// (w >> 8) * 2^-24: exact, in [0, 1).
+__device__ __forceinline__ float uniform_accept(uint32_t w) {
+  return __uint2float_rn(w >> 8) * 5.9604644775390625e-08f;
+}
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(((uint32_t)h) << 16);
+}
+
+__device__ __forceinline__ float round_to_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ void set_status(int32_t *st, int code) {
+  atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ int read_status(const int32_t *st) {
+  return *(volatile const int32_t *)st;
+}
+
+__device__ __forceinline__ bool temperature_ok(float t) {
+  return (t == 0.0f) || (t >= kMinPositiveT && t <= 3.0e38f);
+}
+
+// -------------------------------------------------------------------------
+// Gumbel race state (one per thread; merged across threads and blocks).
+// -------------------------------------------------------------------------
+struct Race {
+  float best;  // best perturbed score s_v + g_v seen
+  int idx;     // its index
+  float m;     // running max of s_v
+  float S;     // sum exp(s_v - m)
+  float c;     // filter factor: exp(m - best) * slack (kFilterMax when no best)
+};
+
+__device__ __forceinline__ void race_init(Race &r) {
+  r.best = -INFINITY;
+  r.idx = -1;
+  r.m = -INFINITY;
+  r.S = 0.0f;
+  r.c = kFilterMax;
+}
+
+__device__ __forceinline__ float race_filter(float m, float best) {
+  if (best == -INFINITY) return kFilterMax;
+  const float x = (m - best) * kLog2e;
+  return x > 100.0f ? kFilterMax : fast_ex2(x) * kFilterSlack;
+}
+
+// Exact perturbed score of a candidate and the update of the running best.
+__device__ __forceinline__ void race_exact(Race &r, float s, uint32_t w, int v) {
+  const float u = uniform_open(w);
+  const float E = -logf(u);
+  const float t = s - logf(E);
+  if (t > r.best || (t == r.best && v < r.idx)) {
+    r.best = t;
+    r.idx = v;
+    r.c = race_filter(r.m, r.best);
+  }
+}
+
+// Process N scaled logits s[q] at indices v0 + q (invalid entries hold -INF)
+// with their stream words w[q].
+template <int N>
+__device__ __forceinline__ void race_update(Race &r, const float (&s)[N], const uint32_t (&w)[N], int v0) {
+  float cm = s[0];
+#pragma unroll
+  for (int q = 1; q < N; ++q) cm = fmaxf(cm, s[q]);
+  if (cm == -INFINITY) return;
+  if (cm > r.m) {
+    r.S = (r.m == -INFINITY) ? 0.0f : r.S * fast_ex2((r.m - cm) * kLog2e);
+    r.m = cm;
+    r.c = race_filter(r.m, r.best);
+  }
+  const float mL = r.m * kLog2e;
+  uint32_t cand = 0;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const float e = fast_ex2(fmaf(s[q], kLog2e, -mL));
+    r.S += e;
+    const float d1 = 1.0f - uniform_open(w[q]);
+    if (d1 < e * r.c) cand |= 1u << q;
+  }
+  while (cand) {
+    const int q = __ffs(cand) - 1;
+    cand &= cand - 1;
+    float sq = s[0];
+    uint32_t wq = w[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i)
+      if (i == q) { sq = s[i]; wq = w[i]; }
+    race_exact(r, sq, wq, v0 + q);
+  }
+}
+
+// Greedy: running max with smallest index.
+template <int N>
+__device__ __forceinline__ void argmax_update(Race &r, const float (&s)[N], int v0) {
+#pragma unroll
+  for (int q = 0; q < N; ++q)
+    if (s[q] > r.best) { r.best = s[q]; r.idx = v0 + q; }
+}
+
+// Merge b into a: best by (score desc, index asc); softmax (m, S).
+__device__ __forceinline__ void race_merge(Race &a, const Race &b) {
+  if (b.best > a.best || (b.best == a.best && b.idx >= 0 && (a.idx < 0 || b.idx < a.idx))) {
+    a.best = b.best;
+    a.idx = b.idx;
+  }
+  if (b.m > a.m) {
+    a.S = (a.m == -INFINITY ? 0.0f : a.S * fast_ex2((a.m - b.m) * kLog2e)) + b.S;
+    a.m = b.m;
+  } else if (b.m != -INFINITY) {
+    a.S += b.S * fast_ex2((b.m - a.m) * kLog2e);
+  }
+}
+
+__device__ __forceinline__ Race race_shfl_down(const Race &r, int d) {
+  Race o;
+  o.best = __shfl_down_sync(0xffffffffu, r.best, d);
+  o.idx = __shfl_down_sync(0xffffffffu, r.idx, d);
+  o.m = __shfl_down_sync(0xffffffffu, r.m, d);
+  o.S = __shfl_down_sync(0xffffffffu, r.S, d);
+  o.c = 0.0f;
+  return o;
+}
+
+// Block-wide merge; the result is valid in thread 0.  `scratch` holds one Race per warp.
+__device__ __forceinline__ Race race_block_reduce(Race r, Race *scratch) {
+  for (int d = 16; d > 0; d >>= 1) {
+    Race o = race_shfl_down(r, d);
+    race_merge(r, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = (blockDim.x + 31) >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = r;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < nw; ++i) race_merge(r, scratch[i]);
+  }
+  return r;
+}
+
+// Partial result of one block, as stored in the workspace (16 bytes).
+struct Partial {
+  float best;
+  int idx;
+  float m;
+  float S;
+};
+
+__device__ __forceinline__ Partial to_partial(const Race &r) {
+  Partial p;
+  p.best = r.best;
+  p.idx = r.idx;
+  p.m = r.m;
+  p.S = r.S;
+  return p;
+}
+
+// Load a partial written by another block (L2, bypassing L1).
+__device__ __forceinline__ Partial load_partial(const Partial *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  Partial o;
+  o.best = __int_as_float(v.x);
+  o.idx = v.y;
+  o.m = __int_as_float(v.z);
+  o.S = __int_as_float(v.w);
+  return o;
+}
+
+__device__ __forceinline__ Race from_partial(const Partial &p) {
+  Race r;
+  r.best = p.best;
+  r.idx = p.idx;
+  r.m = p.m;
+  r.S = p.S;
+  r.c = 0.0f;
+  return r;
+}
+
+// -------------------------------------------------------------------------
+// Host-side launchers (defined in the kernel translation units).
+// -------------------------------------------------------------------------
+struct DraftArgs {
+  const void *U, *E, *W;
+  const int32_t *anchor, *K_r;
+  const float *temperature;
+  int32_t *draft_tok;
+  void *draft_logits;
+  float *draft_lse;
+  int32_t *dev_status;
+  int64_t B, K_max, V, rank;
+  int dtype;
+  PhiloxKey key;
+  // workspace carve-out
+  int32_t *perm;      // [B] requests ordered by K_r descending
+  int32_t *nact;      // [K_max + 2] active requests per position
+  int32_t *counters;  // [B] per-row arrival counters (zero between steps)
+  Partial *partials;  // [partial_slots]
+  int64_t partial_slots;
+};
+
+cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s);
+cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s);
+cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms);
+bool draft_tc_supported(const DraftArgs &a);
+
+struct ScheduleArgs {
+  const float *conf;
+  const int32_t *K_r;
+  const double *sps;
+  int64_t sps_len, B, K_max;
+  int32_t *ell, *tgt_off;
+  double *theta_best;
+  int64_t *b_star;
+  float *survival;
+  int32_t *dev_status;
+  void *ws;
+};
+
+size_t schedule_ws_bytes(int64_t B, int64_t K_max);
+cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s);
+
+struct VerifyJob {
+  int mode;      // 0 none, 1 residual (T > 0), 2 bonus (T > 0), 3 bonus (greedy)
+  int pos;       // stream position (j, or ell + 1 for the bonus)
+  int64_t trow;  // target row
+  int64_t drow;  // draft row (residual only)
+  float lse_t, lse_q, invT;
+  int out_slot;  // index into out_tok
+};
+
+struct VerifyArgs {
+  const void *D;
+  const float *D_lse;
+  const void *tgt;
+  const int32_t *tgt_off, *ell, *draft_tok;
+  const float *temperature;
+  int32_t *n_acc, *out_tok, *dev_status;
+  int64_t B, K_max, V;
+  int dtype;
+  PhiloxKey key;
+  VerifyJob *jobs;     // [B]
+  int32_t *counters;   // [B]
+  Partial *partials;   // [B * chunks]
+  int chunks;          // vocabulary chunks of the sampling pass
+};
+
+size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks);
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms);
+
+}  // namespace dspark

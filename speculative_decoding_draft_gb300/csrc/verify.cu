@@ -1,0 +1,467 @@
+// Ragged rejection-sampling verification ("DSpark", S2.1; "Speculative
+// decoding, from zero to DSpark", S2 and Appendix A1).
+//
+// Two kernels:
+//  1. verify_chain: one thread-block cluster per request walks positions
+//     j = 1..ell_r left to right.  Each CTA of the cluster streams its slice of
+//     the target row (and of the draft row when no draft normaliser is given)
+//     with 16-byte loads, reduces the online-softmax statistics (max, sum of
+//     exponentials) of z/T, and publishes them in shared memory; after a
+//     cluster barrier every CTA combines the slices in rank order, so all of
+//     them take the same accept decision u < min(1, p(x)/q(x)).  Rows after
+//     the deciding position are never read.  The decision also produces the
+//     sampling job of the request: the residual at the rejecting position, the
+//     bonus row when every position is accepted, or nothing for greedy
+//     rejections (their correction is the argmax already found).
+//  2. verify_sample: the residual / bonus Gumbel-max over the vocabulary,
+//     spread over the whole GPU (request x vocabulary chunk), with the last
+//     block of each request merging the chunk partials.
+#include "dspark_internal.cuh"
+
+#include <cooperative_groups.h>
+
+namespace cg = cooperative_groups;
+
+namespace dspark {
+namespace {
+
+constexpr int kChainThreads = 512;
+constexpr int kSampleThreads = 256;
+constexpr int kSampleChunk = 8192;
+
+struct Stats {
+  float m, S;   // online softmax
+  float best;   // greedy max
+  int idx;      // greedy argmax
+};
+
+__device__ __forceinline__ void stats_init(Stats &s) {
+  s.m = -INFINITY;
+  s.S = 0.0f;
+  s.best = -INFINITY;
+  s.idx = -1;
+}
+
+__device__ __forceinline__ void stats_merge(Stats &a, const Stats &b) {
+  if (b.best > a.best || (b.best == a.best && b.idx >= 0 && (a.idx < 0 || b.idx < a.idx))) {
+    a.best = b.best;
+    a.idx = b.idx;
+  }
+  if (b.m > a.m) {
+    a.S = (a.m == -INFINITY ? 0.0f : a.S * fast_ex2((a.m - b.m) * kLog2e)) + b.S;
+    a.m = b.m;
+  } else if (b.m != -INFINITY) {
+    a.S += b.S * fast_ex2((b.m - a.m) * kLog2e);
+  }
+}
+
+// Online softmax of 8 scaled values.
+__device__ __forceinline__ void stats_add8(Stats &st, const float (&s)[8]) {
+  float cm = s[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) cm = fmaxf(cm, s[q]);
+  if (cm == -INFINITY) return;
+  if (cm > st.m) {
+    st.S = (st.m == -INFINITY) ? 0.0f : st.S * fast_ex2((st.m - cm) * kLog2e);
+    st.m = cm;
+  }
+  const float mL = st.m * kLog2e;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) st.S += fast_ex2(fmaf(s[q], kLog2e, -mL));
+}
+
+__device__ __forceinline__ void argmax_add8(Stats &st, const float (&s)[8], int v0) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (s[q] > st.best) { st.best = s[q]; st.idx = v0 + q; }
+}
+
+template <int DT>
+__device__ __forceinline__ float load1(const void *base, int64_t i) {
+  if (DT == DSPARK_F32) return __ldg((const float *)base + i);
+  return bf16_bits_to_float(__ldg((const unsigned short *)base + i));
+}
+
+// Load 8 consecutive elements starting at element i (i multiple of 8 and the
+// row 16-byte aligned when VEC; scalar with -INF padding otherwise).
+template <int DT, bool VEC>
+__device__ __forceinline__ void load8(const void *base, int64_t row_off, int v0, int V, float (&x)[8]) {
+  if (VEC && v0 + 8 <= V) {
+    if (DT == DSPARK_BF16) {
+      const uint4 q = __ldcs((const uint4 *)((const unsigned short *)base + row_off + v0));
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(u[i] << 16);
+        x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+      }
+    } else {
+      const float4 *p = (const float4 *)((const float *)base + row_off + v0);
+      const float4 a = __ldcs(p), b = __ldcs(p + 1);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = (v0 + q < V) ? load1<DT>(base, row_off + v0 + q) : -INFINITY;
+  }
+}
+
+__device__ __forceinline__ Stats stats_shfl_down(const Stats &s, int d) {
+  Stats o;
+  o.m = __shfl_down_sync(0xffffffffu, s.m, d);
+  o.S = __shfl_down_sync(0xffffffffu, s.S, d);
+  o.best = __shfl_down_sync(0xffffffffu, s.best, d);
+  o.idx = __shfl_down_sync(0xffffffffu, s.idx, d);
+  return o;
+}
+
+// Block reduction; result valid in thread 0.
+__device__ __forceinline__ Stats stats_block_reduce(Stats s, Stats *scratch) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) stats_merge(s, stats_shfl_down(s, d));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) scratch[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) stats_merge(s, scratch[i]);
+  __syncthreads();
+  return s;
+}
+
+struct ChainShared {
+  Stats slot_t[2];
+  Stats slot_d[2];
+  Stats red[kChainThreads / 32];
+  int skip;
+  int decision;    // 1 accept, 0 reject
+  int amax;
+  float lse_t, lse_q;
+};
+
+// Slice [lo, hi) of the vocabulary owned by cluster rank `rank` (8-aligned).
+__device__ __forceinline__ void slice(int V, int rank, int ncta, int &lo, int &hi) {
+  const int per = ((V + ncta - 1) / ncta + 7) & ~7;
+  lo = min(V, rank * per);
+  hi = min(V, lo + per);
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kChainThreads) verify_chain(const __grid_constant__ VerifyArgs a) {
+  __shared__ ChainShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int ncta = (int)cluster.num_blocks();
+  const int r = blockIdx.x / ncta;
+  const int tid = threadIdx.x;
+  const int V = (int)a.V, K = (int)a.K_max;
+
+  // rank 0 decides for the whole cluster whether an earlier error stops the work
+  if (rank == 0 && tid == 0) sh.skip = read_status(a.dev_status);
+  cluster.sync();
+  const int skip = *cluster.map_shared_rank(&sh.skip, 0);
+  if (skip) { cluster.sync(); return; }
+
+  // -- validation (identical in every CTA of the cluster) --------------------
+  const int l = a.ell[r];
+  const float T = a.temperature[r];
+  int err = 0;
+  if (l < 0 || l > K) err = DSPARK_ERR_LENGTHS;
+  else if (a.tgt_off[r + 1] - a.tgt_off[r] != l + 1 || (r == 0 && a.tgt_off[0] != 0)) err = DSPARK_ERR_OFFSETS;
+  else if (!temperature_ok(T)) err = DSPARK_ERR_TEMPERATURE;
+  else
+    for (int j = 0; j < l; ++j) {
+      const int x = a.draft_tok[(int64_t)r * K + j];
+      if (x < 0 || x >= V) { err = DSPARK_ERR_TOKEN_RANGE; break; }
+    }
+  if (err) {
+    if (rank == 0 && tid == 0) set_status(a.dev_status, err);
+    cluster.sync();
+    return;
+  }
+
+  const bool greedy = (T == 0.0f);
+  const float invT = greedy ? 1.0f : 1.0f / T;
+  const int64_t off = a.tgt_off[r];
+  const bool have_lse = (a.D_lse != nullptr);
+  int lo, hi;
+  slice(V, rank, ncta, lo, hi);
+
+  int n = 0;
+  bool rejected = false;
+  int rej_j = 0;
+  float lse_t = 0.0f, lse_q = 0.0f;
+  int greedy_tok = -1;
+  for (int j = 1; j <= l; ++j) {
+    const int x = a.draft_tok[(int64_t)r * K + j - 1];
+    const int64_t trow = (off + j - 1) * (int64_t)V;
+    const int64_t drow = ((int64_t)r * K + j - 1) * (int64_t)V;
+    const bool stream_d = !greedy && !have_lse;
+    Stats st, sd;
+    stats_init(st);
+    stats_init(sd);
+    for (int v0 = lo + tid * 8; v0 < hi; v0 += kChainThreads * 8) {
+      float x8[8];
+      load8<DT, VEC>(a.tgt, trow, v0, hi, x8);
+      if (greedy) {
+        argmax_add8(st, x8, v0);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x8[q] *= invT;
+        stats_add8(st, x8);
+        if (stream_d) {
+          float y8[8];
+          load8<DT, VEC>(a.D, drow, v0, hi, y8);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) y8[q] *= invT;
+          stats_add8(sd, y8);
+        }
+      }
+    }
+    st = stats_block_reduce(st, sh.red);
+    if (stream_d) sd = stats_block_reduce(sd, sh.red);
+    if (tid == 0) {
+      sh.slot_t[j & 1] = st;
+      sh.slot_d[j & 1] = sd;
+    }
+    cluster.sync();
+    if (tid == 0) {
+      Stats ct, cd;
+      stats_init(ct);
+      stats_init(cd);
+      for (int q = 0; q < ncta; ++q) {
+        stats_merge(ct, *cluster.map_shared_rank(&sh.slot_t[j & 1], q));
+        if (stream_d) stats_merge(cd, *cluster.map_shared_rank(&sh.slot_d[j & 1], q));
+      }
+      if (greedy) {
+        sh.decision = (x == ct.idx);
+        sh.amax = ct.idx;
+      } else {
+        const float lt = ct.m + logf(ct.S);
+        const float lq = have_lse ? a.D_lse[(int64_t)r * K + j - 1] : cd.m + logf(cd.S);
+        const float lp_x = load1<DT>(a.tgt, trow + x) * invT - lt;
+        const float lq_x = load1<DT>(a.D, drow + x) * invT - lq;
+        const uint4 w = philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept);
+        const float u = uniform_accept(w.x);
+        sh.decision = u < expf(lp_x - lq_x);
+        sh.lse_t = lt;
+        sh.lse_q = lq;
+      }
+    }
+    __syncthreads();
+    if (!sh.decision) {
+      rejected = true;
+      rej_j = j;
+      lse_t = sh.lse_t;
+      lse_q = sh.lse_q;
+      greedy_tok = sh.amax;
+      break;
+    }
+    if (rank == 0 && tid == 0) a.out_tok[(int64_t)r * (K + 1) + n] = x;
+    ++n;
+  }
+
+  if (rank == 0 && tid == 0) {
+    a.n_acc[r] = n;
+    for (int q = n + 1; q <= K; ++q) a.out_tok[(int64_t)r * (K + 1) + q] = -1;
+    VerifyJob job;
+    job.mode = 0;
+    job.pos = 0;
+    job.trow = 0;
+    job.drow = 0;
+    job.lse_t = lse_t;
+    job.lse_q = lse_q;
+    job.invT = invT;
+    job.out_slot = r * (K + 1) + n;
+    if (rejected) {
+      if (greedy) {
+        a.out_tok[(int64_t)r * (K + 1) + n] = greedy_tok;
+      } else {
+        job.mode = 1;
+        job.pos = rej_j;
+        job.trow = off + rej_j - 1;
+        job.drow = (int64_t)r * K + rej_j - 1;
+      }
+    } else {
+      job.mode = greedy ? 3 : 2;
+      job.pos = l + 1;
+      job.trow = off + l;
+    }
+    a.jobs[r] = job;
+    a.counters[r] = 0;
+  }
+  cluster.sync();   // peers may still read this CTA's slots
+}
+
+// --------------------------------------------------------------------------
+// residual / bonus sampling
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float resid_filter(float best) {
+  if (best == -INFINITY) return kFilterMax;
+  const float x = -best * kLog2e;
+  return x > 100.0f ? kFilterMax : fast_ex2(x) * kFilterSlack;
+}
+
+// Exact residual score log(p - q) + g for a candidate with log p = la > log q = lb.
+__device__ __forceinline__ void resid_exact(Race &rc, float la, float lb, uint32_t w, int v) {
+  const float logr = la + logf(-expm1f(lb - la));
+  const float u = uniform_open(w);
+  const float t = logr - logf(-logf(u));
+  if (t > rc.best || (t == rc.best && v < rc.idx)) {
+    rc.best = t;
+    rc.idx = v;
+    rc.c = resid_filter(t);
+  }
+}
+
+template <int DT, bool VEC>
+__device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, int lo, int hi, int tid,
+                             int nthreads, Race &rc, bool &any_cand, bool from_p) {
+  const int V = (int)a.V;
+  const int64_t trow = job.trow * (int64_t)V;
+  const int64_t drow = job.drow * (int64_t)V;
+  const int mode = from_p ? 2 : job.mode;
+  for (int v0 = lo + tid * 8; v0 < hi; v0 += nthreads * 8) {
+    float t8[8];
+    load8<DT, VEC>(a.tgt, trow, v0, hi, t8);
+    if (mode == 3) {
+      argmax_update<8>(rc, t8, v0);
+      continue;
+    }
+    const uint4 w0 = philox(a.key, (uint32_t)(v0 >> 2), (uint32_t)job.pos, (uint32_t)r, kTagResid);
+    const uint4 w1 = philox(a.key, (uint32_t)((v0 >> 2) + 1), (uint32_t)job.pos, (uint32_t)r, kTagResid);
+    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    if (mode == 2) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t8[q] *= job.invT;
+      race_update<8>(rc, t8, w, v0);
+      continue;
+    }
+    // residual
+    float d8[8];
+    load8<DT, VEC>(a.D, drow, v0, hi, d8);
+    uint32_t cand = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float la = t8[q] * job.invT - job.lse_t;
+      const float lb = d8[q] * job.invT - job.lse_q;
+      if (la > lb) {
+        any_cand = true;
+        const float p = fast_ex2(la * kLog2e);
+        const float d1 = 1.0f - uniform_open(w[q]);
+        if (d1 < p * rc.c) cand |= 1u << q;
+      }
+    }
+    while (cand) {
+      const int q = __ffs(cand) - 1;
+      cand &= cand - 1;
+      float tq = t8[0], dq = d8[0];
+      uint32_t wq = w[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+        if (i == q) { tq = t8[i]; dq = d8[i]; wq = w[i]; }
+      resid_exact(rc, tq * job.invT - job.lse_t, dq * job.invT - job.lse_q, wq, v0 + q);
+    }
+  }
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_constant__ VerifyArgs a) {
+  __shared__ Race red[kSampleThreads / 32];
+  __shared__ int s_any[kSampleThreads / 32];
+  __shared__ int s_last;
+  const int r = blockIdx.y, cx = blockIdx.x, tid = threadIdx.x;
+  if (read_status(a.dev_status)) return;
+  const VerifyJob job = a.jobs[r];
+  if (job.mode == 0) return;
+  const int V = (int)a.V;
+  const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
+  Race rc;
+  race_init(rc);
+  bool any_cand = false;
+  sample_range<DT, VEC>(a, job, r, lo, hi, tid, kSampleThreads, rc, any_cand, false);
+  const int any = __syncthreads_or(any_cand ? 1 : 0);
+  rc = race_block_reduce(rc, red);
+  if (tid == 0) {
+    Partial p = to_partial(rc);
+    p.m = any ? 1.0f : 0.0f;    // the sampling pass needs no softmax: reuse the field as a flag
+    a.partials[(int64_t)r * a.chunks + cx] = p;
+    __threadfence();
+    const int prev = atomicAdd(&a.counters[r], 1);
+    s_last = (prev == a.chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  Race tot;
+  race_init(tot);
+  int any_all = 0;
+  if (tid == 0) {
+    for (int q = 0; q < a.chunks; ++q) {
+      const Partial p = load_partial(a.partials + ((int64_t)r * a.chunks + q));
+      Race x = from_partial(p);
+      x.m = -INFINITY;
+      x.S = 0.0f;
+      race_merge(tot, x);
+      any_all |= (p.m != 0.0f);
+    }
+    s_any[0] = any_all;
+  }
+  __syncthreads();
+  if (job.mode == 1 && !s_any[0]) {
+    // no element with p > q survived rounding: sample the correction from p instead
+    Race rp;
+    race_init(rp);
+    bool dummy = false;
+    sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, rp, dummy, true);
+    rp = race_block_reduce(rp, red);
+    if (tid == 0) tot = rp;
+  }
+  if (tid == 0) {
+    a.out_tok[job.out_slot] = tot.idx;
+    a.counters[r] = 0;
+  }
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, int num_sms) {
+  int cl = 1;
+  const int64_t target = 2LL * num_sms;
+  while (cl < 8 && a.B * cl * 2 <= target) cl *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * cl), 1, 1);
+  cfg.blockDim = dim3(kChainThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_chain<DT, VEC>, a);
+  if (e != cudaSuccess) return e;
+  verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)a.B), kSampleThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
+  const int c = (int)((V + kSampleChunk - 1) / kSampleChunk);
+  if (chunks) *chunks = c;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return al(sizeof(VerifyJob) * (size_t)B) + al(sizeof(int32_t) * (size_t)B) +
+         al(sizeof(Partial) * (size_t)B * (size_t)c);
+}
+
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms) {
+  const int esz = a.dtype == DSPARK_F32 ? 4 : 2;
+  const bool vec = ((a.V * esz) % 16 == 0) && ((uintptr_t)a.tgt % 16 == 0) && ((uintptr_t)a.D % 16 == 0);
+  if (a.dtype == DSPARK_F32)
+    return vec ? launch_typed<DSPARK_F32, true>(a, s, num_sms) : launch_typed<DSPARK_F32, false>(a, s, num_sms);
+  return vec ? launch_typed<DSPARK_BF16, true>(a, s, num_sms) : launch_typed<DSPARK_BF16, false>(a, s, num_sms);
+}
+
+}  // namespace dspark

@@ -99,12 +99,9 @@ def _randn(shape, std, g, device):
 # ---------------------------------------------------------------------------
 # draft inputs
 # ---------------------------------------------------------------------------
-def draft_inputs(cfg: Config, device="cpu") -> dict:
-    """U [B,K_max,V], E [V,rank], W [rank,V] (storage dtype), anchor [B], K_r [B], temperature [B]."""
-    g = _gen(cfg, device, 1)
-    U = _randn((cfg.B, cfg.K_max, cfg.V), cfg.u_std, g, device).to(cfg.torch_dtype)
-    E = _randn((cfg.V, cfg.rank), cfg.ew_std, g, device).to(cfg.torch_dtype)
-    W = _randn((cfg.rank, cfg.V), cfg.ew_std, g, device).to(cfg.torch_dtype)
+def request_params(cfg: Config, device="cpu") -> dict:
+    """anchor [B] int32, K_r [B] int32, temperature [B] float32."""
+    g = _gen(cfg, device, 5)
     anchor = torch.randint(0, cfg.V, (cfg.B,), generator=g, device=device, dtype=torch.int32)
     if cfg.ragged_k:
         K_r = torch.randint(1, cfg.K_max + 1, (cfg.B,), generator=g, device=device, dtype=torch.int32)
@@ -114,7 +111,16 @@ def draft_inputs(cfg: Config, device="cpu") -> dict:
     if cfg.greedy_frac > 0:
         r = torch.arange(cfg.B, device=device)
         temperature[(r % 10) < int(round(10 * cfg.greedy_frac))] = 0.0
-    return dict(U=U, E=E, W=W, anchor=anchor, K_r=K_r, temperature=temperature)
+    return dict(anchor=anchor, K_r=K_r, temperature=temperature)
+
+
+def draft_inputs(cfg: Config, device="cpu") -> dict:
+    """U [B,K_max,V], E [V,rank], W [rank,V] (storage dtype), anchor [B], K_r [B], temperature [B]."""
+    g = _gen(cfg, device, 1)
+    U = _randn((cfg.B, cfg.K_max, cfg.V), cfg.u_std, g, device).to(cfg.torch_dtype)
+    E = _randn((cfg.V, cfg.rank), cfg.ew_std, g, device).to(cfg.torch_dtype)
+    W = _randn((cfg.rank, cfg.V), cfg.ew_std, g, device).to(cfg.torch_dtype)
+    return dict(U=U, E=E, W=W, **request_params(cfg, device))
 
 
 # ---------------------------------------------------------------------------

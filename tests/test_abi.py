@@ -1,0 +1,77 @@
+"""The C-ABI library loads and exports every entry point declared in include/dspark.h.
+
+Runs without a GPU: nothing here launches work.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_draft_gb300 import build
+    build.build()
+    import speculative_decoding_draft_gb300 as ds
+    return ds.lib()
+
+
+def test_header_declares_the_three_operations():
+    names = _declared()
+    for op in ("dspark_draft_markov_sample", "dspark_schedule_survival", "dspark_verify_ragged"):
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import speculative_decoding_draft_gb300 as ds
+    names = _declared()
+    assert set(names) == set(ds.EXPORTED_SYMBOLS)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    import speculative_decoding_draft_gb300 as ds
+    assert lib.dspark_version() == 100
+    for code, name in ds.STATUS_NAMES.items():
+        assert ds.status_string(code) == name
+
+
+def test_workspace_queries(lib):
+    import speculative_decoding_draft_gb300 as ds
+    assert ds.draft_workspace_bytes(2048, 7, 151936) > 2048 * 75 * 16
+    assert ds.schedule_workspace_bytes(2048, 7) >= 2048 * 7 * 24
+    assert ds.verify_workspace_bytes(64, 151936) > 0
+    assert lib.dspark_draft_workspace_bytes(0, 7, 10) == 0
+
+
+def test_host_validation_needs_no_device(lib):
+    # argument errors are reported before any CUDA call
+    import speculative_decoding_draft_gb300 as ds
+    dims = ds.Dims(4, 7, 1000, 16, ds.F32, 0)
+    null = None
+    assert lib.dspark_draft_markov_sample(null, null, null, null, null, null, 0, dims, null, null, null, null, 0,
+                                          null, null) == 1
+    one = ctypes.c_void_p(256)
+    bad = ds.Dims(4, 17, 1000, 16, ds.F32, 0)
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, one, 1 << 20, one,
+                                          null) == 2
+    bad = ds.Dims(4, 7, 1000, 16, 7, 0)
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, one, 1 << 20, one,
+                                          null) == 3
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, dims, one, null, null, one, 16, one,
+                                          null) == 10
+    assert lib.dspark_schedule_survival(one, one, one, 10, 4, 0, one, one, null, null, null, one, 1 << 20, one,
+                                        null) == 2
+    vd = ds.Dims(4, 7, 1000, 0, ds.BF16, 0)
+    assert lib.dspark_verify_ragged(one, null, one, one, one, one, one, 0, vd, one, one, ctypes.c_void_p(300),
+                                    1 << 30, one, null) == 10
