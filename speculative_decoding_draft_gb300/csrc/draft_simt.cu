@@ -23,20 +23,22 @@ constexpr int kSimtChunk = 2048;   // vocabulary columns per block
 
 __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a) {
   __shared__ int s_err, s_skip;
-  __shared__ int wsum[kPrologueThreads / 32];
-  __shared__ int s_base;
+  __shared__ int cnt[kMaxK + 2];          // requests per length value
+  __shared__ int base[kMaxK + 2];         // next free slot per length value
+  __shared__ int wc[kPrologueThreads / 32][kMaxK + 2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_skip = read_status(a.dev_status);
     s_err = 0;
-    s_base = 0;
   }
+  if (tid < kMaxK + 2) cnt[tid] = 0;
   __syncthreads();
   if (s_skip) return;
   const int B = (int)a.B, K = (int)a.K_max, V = (int)a.V;
   for (int r = tid; r < B; r += kPrologueThreads) {
     const int kr = a.K_r[r];
     if (kr < 1 || kr > K) atomicCAS(&s_err, 0, (int)DSPARK_ERR_LENGTHS);
+    else atomicAdd(&cnt[kr], 1);
     const int x0 = a.anchor[r];
     if (x0 < 0 || x0 >= V) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TOKEN_RANGE);
     if (!temperature_ok(a.temperature[r])) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TEMPERATURE);
@@ -49,43 +51,37 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     if (tid == 0) set_status(a.dev_status, s_err);
     return;
   }
-  // stable order by K_r descending: one block scan per length value
-  const int per = (B + kPrologueThreads - 1) / kPrologueThreads;
-  const int rb = tid * per, re = min(B, rb + per);
-  for (int val = K; val >= 1; --val) {
-    int cnt = 0;
-    for (int r = rb; r < re; ++r) cnt += (a.K_r[r] == val);
-    int x = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int y = wsum[lane];
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int z = __shfl_up_sync(0xffffffffu, y, d);
-        if (lane >= d) y += z;
-      }
-      wsum[lane] = y;
-    }
-    __syncthreads();
-    int pos = s_base + (warp ? wsum[warp - 1] : 0) + x - cnt;
-    for (int r = rb; r < re; ++r)
-      if (a.K_r[r] == val) a.perm[pos++] = r;
-    __syncthreads();
-    if (tid == 0) {
-      s_base += wsum[kPrologueThreads / 32 - 1];
-      a.nact[val] = s_base;   // requests with K_r >= val
-    }
-    __syncthreads();
-  }
   if (tid == 0) {
+    int run = 0;
+    for (int val = K; val >= 1; --val) {   // longest drafts first
+      base[val] = run;
+      run += cnt[val];
+      a.nact[val] = run;                   // requests with K_r >= val
+    }
     a.nact[0] = B;
     a.nact[K + 1] = 0;
+  }
+  __syncthreads();
+  // stable scatter, 1024 requests per round: rank among equal lengths by warp match + warp prefix
+  for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
+    const int r = c0 + tid;
+    const int v = r < B ? a.K_r[r] : 0;
+    const uint32_t peers = __match_any_sync(0xffffffffu, v);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
+    __syncthreads();
+    if (lane == __ffs(peers) - 1) wc[warp][v] = __popc(peers);
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][v];
+    if (r < B) a.perm[base[v] + before + rank] = r;
+    __syncthreads();
+    if (tid >= 1 && tid <= K) {
+      int tot = 0;
+      for (int w2 = 0; w2 < kPrologueThreads / 32; ++w2) tot += wc[w2][tid];
+      base[tid] += tot;
+    }
+    __syncthreads();
   }
 }
 
@@ -108,65 +104,70 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_step(const __grid_con
   __shared__ Race red[kSimtThreads / 32];
   __shared__ int s_last;
   if (read_status(a.dev_status)) return;
-  const int i = blockIdx.y;
-  if (i >= a.nact[k]) return;
   const int K = (int)a.K_max, V = (int)a.V, rank = (int)a.rank;
-  const int r = a.perm[i];
-  const int prev = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
-  for (int q = threadIdx.x; q < rank; q += kSimtThreads) e_s[q] = ld<DT>(a.E, (int64_t)prev * rank + q);
-  __syncthreads();
-  const float T = a.temperature[r];
-  const bool greedy = (T == 0.0f);
-  const float invT = greedy ? 1.0f : 1.0f / T;
-  const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
-  const int lo = blockIdx.x * kSimtChunk, hi = min(V, lo + kSimtChunk);
-  Race st;
-  race_init(st);
-  for (int v0 = lo + threadIdx.x * 4; v0 < hi; v0 += kSimtThreads * 4) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int q = 0; q < rank; ++q) {
-      const float e = e_s[q];
-      const int64_t wrow = (int64_t)q * V;
+  const int n_k = a.nact[k];
+  const PhiloxKey key = a.key;   // round keys in registers for the hot loop
+  for (int i = blockIdx.y; i < n_k; i += gridDim.y) {
+    const int r = a.perm[i];
+    const int prev = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
+    __syncthreads();
+    for (int q = threadIdx.x; q < rank; q += kSimtThreads) e_s[q] = ld<DT>(a.E, (int64_t)prev * rank + q);
+    __syncthreads();
+    const float T = a.temperature[r];
+    const bool greedy = (T == 0.0f);
+    const float invT = greedy ? 1.0f : 1.0f / T;
+    const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
+    const int lo = blockIdx.x * kSimtChunk, hi = min(V, lo + kSimtChunk);
+    Race st;
+    race_init(st);
+    for (int v0 = lo + threadIdx.x * 4; v0 < hi; v0 += kSimtThreads * 4) {
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int q = 0; q < rank; ++q) {
+        const float e = e_s[q];
+        const int64_t wrow = (int64_t)q * V;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (v0 + c < hi) acc[c] = fmaf(e, ld<DT>(a.W, wrow + v0 + c), acc[c]);
-    }
-    float s[4];
+        for (int c = 0; c < 4; ++c)
+          if (v0 + c < hi) acc[c] = fmaf(e, ld<DT>(a.W, wrow + v0 + c), acc[c]);
+      }
+      float s[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (v0 + c < hi) {
-        float z = ld<DT>(a.U, urow + v0 + c) + acc[c];
-        if (DT == DSPARK_BF16) z = round_to_bf16(z);
-        if (a.draft_logits) st_logit<DT>(a.draft_logits, urow + v0 + c, z);
-        s[c] = greedy ? z : z * invT;
+      for (int c = 0; c < 4; ++c) {
+        if (v0 + c < hi) {
+          float z = ld<DT>(a.U, urow + v0 + c) + acc[c];
+          if (DT == DSPARK_BF16) z = round_to_bf16(z);
+          if (a.draft_logits) st_logit<DT>(a.draft_logits, urow + v0 + c, z);
+          s[c] = greedy ? z : z * invT;
+        } else {
+          s[c] = -INFINITY;
+        }
+      }
+      if (greedy) {
+        argmax_update<4>(st, s, v0);
       } else {
-        s[c] = -INFINITY;
+        const uint4 w4 = philox(key, (uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)r, kTagDraft);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        race_update<4>(st, s, w, v0);
       }
     }
-    if (greedy) {
-      argmax_update<4>(st, s, v0);
-    } else {
-      const uint4 w4 = philox(a.key, (uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)r, kTagDraft);
-      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-      race_update<4>(st, s, w, v0);
+    st = race_block_reduce(st, red);
+    if (threadIdx.x == 0) {
+      a.partials[(int64_t)i * chunks + blockIdx.x] = to_partial(st);
+      __threadfence();
+      s_last = (atomicAdd(&a.counters[i], 1) == chunks - 1);
+    }
+    __syncthreads();
+    if (s_last && threadIdx.x < 32) {
+      __threadfence();
+      const Partial *ptr[1] = {a.partials + (int64_t)i * chunks};
+      Race tot[1];
+      warp_merge_rows<1>(ptr, chunks, tot);
+      if (threadIdx.x == 0) {
+        a.draft_tok[(int64_t)r * K + k - 1] = tot[0].idx;
+        if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot[0].best : tot[0].m + logf(tot[0].S);
+        a.counters[i] = 0;
+      }
     }
   }
-  st = race_block_reduce(st, red);
-  if (threadIdx.x == 0) {
-    a.partials[(int64_t)i * chunks + blockIdx.x] = to_partial(st);
-    __threadfence();
-    s_last = (atomicAdd(&a.counters[i], 1) == chunks - 1);
-  }
-  __syncthreads();
-  if (!s_last || threadIdx.x != 0) return;
-  __threadfence();
-  Race tot;
-  race_init(tot);
-  for (int q = 0; q < chunks; ++q)
-    race_merge(tot, from_partial(load_partial(a.partials + ((int64_t)i * chunks + q))));
-  a.draft_tok[(int64_t)r * K + k - 1] = tot.idx;
-  if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot.best : tot.m + logf(tot.S);
-  a.counters[i] = 0;
 }
 
 }  // namespace
@@ -188,7 +189,7 @@ cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   for (int k = 1; k <= (int)a.K_max; ++k) {
-    dim3 grid(chunks, (unsigned)a.B);
+    dim3 grid(chunks, (unsigned)(a.B < 65535 ? a.B : 65535));
     if (a.dtype == DSPARK_F32) draft_simt_step<DSPARK_F32><<<grid, kSimtThreads, smem, s>>>(a, k, chunks);
     else draft_simt_step<DSPARK_BF16><<<grid, kSimtThreads, smem, s>>>(a, k, chunks);
     cudaError_t e = cudaGetLastError();

@@ -39,7 +39,7 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kTileN = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kAccBufs = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
@@ -47,12 +47,9 @@ constexpr int kTmemCols = kAccBufs * kTileN;               // 256
 constexpr int kAChunk = kTileM * 128;                      // 16 KB: 128 rows x 64 bf16
 constexpr int kASize = 4 * kAChunk;                        // rank <= 256
 constexpr int kWSlot = 256 * 128;                          // r rows x 128 B
-constexpr int kUPitch = kTileN * 2 + 16;                   // 144 B: padded against bank conflicts
-constexpr int kUSlot = kTileM * kUPitch;
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
-constexpr int kOffU = kOffW + kStages * kWSlot;
-constexpr int kOffSh = kOffU + kStages * kUSlot;
+constexpr int kOffSh = kOffW + kStages * kWSlot;
 constexpr long long kTimeoutCycles = 4000000000LL;
 
 struct TcShared {
@@ -69,7 +66,7 @@ struct TcShared {
   int row_req[kTileM];
   int row_prev[kTileM];
   float row_invT[kTileM];
-  Partial half[kTileM];
+  Partial part[2 * kTileM];   // per-row thread partials: [replica group x column half][row]
 };
 
 constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
@@ -165,11 +162,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
 // offsets (>> 4), descriptor version 1, 128-byte swizzle.
@@ -188,6 +180,16 @@ __device__ __forceinline__ void named_sync_epi() {
 }
 
 // ---------------------------------------------------------------------------
+// U row segment of one epilogue thread for one tile: 32 bf16 at column c0 of
+// its row (16-byte loads; columns past V are not read).
+__device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int V, uint4 (&u)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (c0 + 8 * q < V) u[q] = __ldg(reinterpret_cast<const uint4 *>(row + c0 + 8 * q));
+    else u[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 __global__ void __launch_bounds__(kThreadsTc, 1)
     draft_tc_step(const __grid_constant__ DraftArgs a, const __grid_constant__ CUtensorMap tmap_w, int k) {
   extern __shared__ uint8_t smem_raw[];
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1 + kEpiWarps);
+      mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
@@ -246,10 +248,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   uint32_t it = 0;   // global tile counter of this CTA (same progression in every role)
   int unit_no = 0;
-  uint32_t issued_use[kStages];   // producer: last issued use of each stage (for the abort drain)
+  uint32_t last_use[kStages];   // producer: last issued use of each stage (for the abort drain)
   bool issued[kStages];
+#pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    issued_use[s] = 0;
+    last_use[s] = 0;
     issued[s] = false;
   }
   for (int u = blockIdx.x; u < units; u += G, ++unit_no) {
@@ -257,6 +260,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int nt0 = (int)((int64_t)j * n_tiles / gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / gm);
     const int row0 = m * kTileM;
     const int nrows = min(kTileM, n_k - row0);
+    // replication: with few rows, every TMEM lane quadrant (= SM sub-partition) gets a copy of
+    // the rows and takes every F-th vocabulary tile
+    const int F = nrows <= 32 ? 4 : (nrows <= 64 ? 2 : 1);
+    const int rpg = kTileM / F;   // rows per replica group
     __syncthreads();
     if (threadIdx.x < kTileM) {
       const int i = threadIdx.x;
@@ -275,29 +282,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
 
     if (warp == 0) {
-      // ---------------- producer ----------------
-      for (int t = nt0; t < nt1 && !*abort; ++t) {
-        const uint32_t idx = it + (uint32_t)(t - nt0);
-        const int s = (int)(idx % kStages);
-        const uint32_t use = idx / kStages;
-        if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
-        const int cols = min(kTileN, V - t * kTileN);
-        const uint32_t ubytes = (uint32_t)cols * 2u;
-        if (lane == 0) {
-          mbar_arrive_tx(bar_full + 8 * s, w_bytes + (uint32_t)nrows * ubytes);
+      // ---------------- producer: W2 tiles ----------------
+      if (lane == 0) {
+        for (int t = nt0; t < nt1 && !*abort; ++t) {
+          const uint32_t idx = it + (uint32_t)(t - nt0);
+          const int s = (int)(idx % kStages);
+          const uint32_t use = idx / kStages;
+          if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
+          mbar_arrive_tx(bar_full + 8 * s, w_bytes);
           tma_load_2d(sb + kOffW + s * kWSlot, &tmap_w, t * kTileN, 0, bar_full + 8 * s);
+#pragma unroll
+          for (int q = 0; q < kStages; ++q)
+            if (q == s) { last_use[q] = use; issued[q] = true; }
         }
-        issued_use[s] = use;
-        issued[s] = true;
-        __syncwarp();
-        for (int rr = lane; rr < nrows; rr += 32) {
-          const int r = sh.row_req[rr];
-          const unsigned short *src =
-              (const unsigned short *)a.U + ((int64_t)r * K + (k - 1)) * (int64_t)V + (int64_t)t * kTileN;
-          bulk_g2s(sb + kOffU + s * kUSlot + rr * kUPitch, src, ubytes, bar_full + 8 * s);
-        }
-        __syncwarp();
       }
+      __syncwarp();
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
       if (lane == 0) {
@@ -328,15 +327,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
       const int half = eq >> 2;           // 32-column half of the 64-wide tile
       const int et = eq * 32 + lane;      // 0..255
-      // gather the A operand: row i, 16-byte unit c8 of chunk c goes to chunk c, row i,
-      // unit (c8 ^ (i & 7)) -- the 128-byte swizzle of a K-major tile.
+      // gather the A operand: M-row a holds request row (a mod rpg); 16-byte unit c8 of K-chunk
+      // c of that row goes to chunk c, row a, unit (c8 ^ (a & 7)) -- the 128-byte swizzle
       const int units_per_row = rank / 8;
       for (int e = et; e < kTileM * units_per_row; e += kEpiWarps * 32) {
-        const int i = e / units_per_row, uu = e % units_per_row;
+        const int ar = e / units_per_row, uu = e % units_per_row;
+        const int i = ar % rpg;
         const int c = uu >> 3, c8 = uu & 7;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (i < nrows) val = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * rank) + uu);
-        const uint32_t dst = sb + kOffA + c * kAChunk + i * 128 + ((c8 ^ (i & 7)) << 4);
+        const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y), "r"(val.z),
                      "r"(val.w)
                      : "memory");
@@ -345,59 +345,60 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_aready);
 
-      const int row = quad * 32 + lane;
+      const int arow = quad * 32 + lane;          // TMEM lane = M-row
+      const int grp = arow / rpg;                 // replica group: takes tiles t with (t - nt0) % F == grp
+      const int row = arow % rpg;                 // request row of this thread
       const bool valid = row < nrows;
       const int r = valid ? sh.row_req[row] : 0;
       const float invT = sh.row_invT[row];
       const bool greedy = (invT == 0.0f);
       const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
+      const unsigned short *uptr = (const unsigned short *)a.U + urow;
+      const PhiloxKey key = a.key;                // round keys in registers for the hot loop
       Race st;
       race_init(st);
+      uint4 ucur[4], unext[4];
+      int tmine = nt0 + grp;                      // first tile of this thread
+      if (valid && tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, ucur);
       for (int t = nt0; t < nt1; ++t) {
         const uint32_t idx = it + (uint32_t)(t - nt0);
-        const int s = (int)(idx % kStages);
-        const uint32_t use = idx / kStages;
         const int b = (int)(idx % kAccBufs);
         const uint32_t ause = idx / kAccBufs;
-        if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
         if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
         tc_fence_after();
         uint32_t acc[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
         tmem_wait_ld();
-        uint4 uv[4];
-        const uint32_t usrc = sb + kOffU + s * kUSlot + row * kUPitch + half * 64;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(uv[q].x), "=r"(uv[q].y), "=r"(uv[q].z), "=r"(uv[q].w)
-                       : "r"(usrc + 16 * q));
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar_acce + 8 * b);
-          mbar_arrive(bar_empty + 8 * s);
-        }
+        if (lane == 0) mbar_arrive(bar_acce + 8 * b);
+        if (t != tmine) continue;                 // another replica group owns this tile
+        tmine += F;
         if (!valid) continue;
+        if (tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, unext);   // prefetch
         const int c0 = t * kTileN + half * 32;
+        const bool full = (c0 + 32 <= V);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const uint32_t pk[4] = {uv[g].x, uv[g].y, uv[g].z, uv[g].w};
+          const uint32_t pk[4] = {ucur[g].x, ucur[g].y, ucur[g].z, ucur[g].w};
           float sv[8];
           uint32_t packed[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t hbits = (e & 1) ? (pk[e >> 1] & 0xffff0000u) : (pk[e >> 1] << 16);
-            const float zf = __uint_as_float(hbits) + __uint_as_float(acc[g * 8 + e]);
-            const __nv_bfloat16 zb = __float2bfloat16_rn(zf);
-            const float z = __bfloat162float(zb);
-            const uint32_t zbits = (uint32_t)__bfloat16_as_ushort(zb);
-            if (e & 1) packed[e >> 1] |= zbits << 16;
-            else packed[e >> 1] = zbits;
-            const bool in = (c0 + g * 8 + e) < V;
-            sv[e] = in ? (greedy ? z : z * invT) : -INFINITY;
+          for (int e = 0; e < 8; e += 2) {
+            const float z0 = __uint_as_float(pk[e >> 1] << 16) + __uint_as_float(acc[g * 8 + e]);
+            const float z1 = __uint_as_float(pk[e >> 1] & 0xffff0000u) + __uint_as_float(acc[g * 8 + e + 1]);
+            const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
+            packed[e >> 1] = *reinterpret_cast<const uint32_t *>(&zb);
+            const float2 zf = __bfloat1622float2(zb);
+            sv[e] = greedy ? zf.x : zf.x * invT;
+            sv[e + 1] = greedy ? zf.y : zf.y * invT;
           }
-          if (a.draft_logits && c0 + g * 8 + 8 <= V) {
+          if (!full) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (c0 + g * 8 + e >= V) sv[e] = -INFINITY;
+          }
+          if (a.draft_logits && (full || c0 + g * 8 + 8 <= V)) {
             uint4 *dst = (uint4 *)((unsigned short *)a.draft_logits + urow + c0 + g * 8);
             *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
@@ -405,19 +406,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             argmax_update<8>(st, sv, c0 + g * 8);
           } else {
             const uint32_t cb = (uint32_t)((c0 + g * 8) >> 2);
-            const uint4 w0 = philox(a.key, cb, (uint32_t)k, (uint32_t)r, kTagDraft);
-            const uint4 w1 = philox(a.key, cb + 1u, (uint32_t)k, (uint32_t)r, kTagDraft);
+            const uint4 w0 = philox(key, cb, (uint32_t)k, (uint32_t)r, kTagDraft);
+            const uint4 w1 = philox(key, cb + 1u, (uint32_t)k, (uint32_t)r, kTagDraft);
             const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
             race_update<8>(st, sv, w, c0 + g * 8);
           }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
       }
-      // merge the two column halves of each row, publish the CTA partial
-      if (half == 1) sh.half[row] = to_partial(st);
+      // merge the 2F thread partials of each row (replica groups x column halves),
+      // publish the CTA partial; layout [M-tile][row][CTA slot j]
+      sh.part[(grp * 2 + half) * rpg + row] = to_partial(st);
       named_sync_epi();
-      if (half == 0) {
-        race_merge(st, from_partial(sh.half[row]));
-        a.partials[(int64_t)u * kTileM + row] = to_partial(st);
+      if (grp == 0 && half == 0) {
+        for (int q = 1; q < 2 * F; ++q) race_merge(st, from_partial(sh.part[q * rpg + row]));
+        if (valid) a.partials[((int64_t)m * kTileM + row) * gm + j] = to_partial(st);
       }
       __threadfence();
       named_sync_epi();
@@ -425,13 +429,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       named_sync_epi();
       if (sh.last) {
         __threadfence();
-        if (half == 0 && valid) {
-          Race tot;
-          race_init(tot);
-          for (int jj = 0; jj < gm; ++jj)
-            race_merge(tot, from_partial(load_partial(a.partials + ((int64_t)(m * gm + jj) * kTileM + row))));
-          a.draft_tok[(int64_t)r * K + k - 1] = tot.idx;
-          if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot.best : tot.m + logf(tot.S);
+        // warp eq merges rows eq, eq + 8, ... in groups of 8 rows
+        for (int r0 = eq; r0 < nrows; r0 += 8 * kEpiWarps) {
+          const Partial *ptr[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = r0 + i * kEpiWarps;
+            ptr[i] = rr < nrows ? a.partials + ((int64_t)m * kTileM + rr) * gm : nullptr;
+          }
+          Race tot[8];
+          warp_merge_rows<8>(ptr, gm, tot);
+          if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = r0 + i * kEpiWarps;
+              if (rr >= nrows) continue;
+              const int rq = sh.row_req[rr];
+              a.draft_tok[(int64_t)rq * K + k - 1] = tot[i].idx;
+              if (a.draft_lse)
+                a.draft_lse[(int64_t)rq * K + k - 1] =
+                    sh.row_invT[rr] == 0.0f ? tot[i].best : tot[i].m + logf(tot[i].S);
+            }
+          }
         }
         if (et == 0) a.counters[m] = 0;
       }
@@ -439,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     it += (uint32_t)(nt1 - nt0);
   }
 
-  // ---- teardown: drain issued MMAs, free TMEM -------------------------------
+  // ---- teardown: drain issued MMAs and copies, free TMEM ---------------------
   if (warp == 1) {
     if (lane == 0) {
       mma_commit(bar_drain);
@@ -450,11 +469,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncwarp();
   }
   if (warp == 0 && lane == 0 && *abort) {
-    // wait (bounded) until the last copies issued into each stage have landed
+    // wait (bounded) until the last copy issued into each stage has landed
+#pragma unroll
     for (int s = 0; s < kStages; ++s) {
       if (!issued[s]) continue;
       const long long t0 = clock64();
-      while (!mbar_try(bar_full + 8 * s, issued_use[s] & 1u) && clock64() - t0 < kTimeoutCycles / 4) {
+      while (!mbar_try(bar_full + 8 * s, last_use[s] & 1u) && clock64() - t0 < kTimeoutCycles / 4) {
       }
     }
   }
@@ -488,7 +508,7 @@ bool draft_tc_supported(const DraftArgs &a) {
   if (a.draft_logits && ((uintptr_t)a.draft_logits & 15u)) return false;
   const int64_t m_tiles = (a.B + kTileM - 1) / kTileM;
   const int64_t units = m_tiles > 1024 ? m_tiles : 1024;
-  if (units * kTileM > a.partial_slots) return false;
+  if (units * kTileM > a.partial_slots) return false;   // slots used: M-tiles x 128 x CTAs per M-tile
   return get_encode() != nullptr;
 }
 

@@ -266,6 +266,44 @@ __device__ __forceinline__ Race from_partial(const Partial &p) {
   return r;
 }
 
+// Warp-cooperative merge of R rows of partials: row i has n consecutive
+// partials at p[i] (p[i] == nullptr: skip).  Every lane issues its loads for all
+// rows before merging, so many L2 reads are in flight at once.  The merged
+// result is valid in lane 0 of the warp.
+__device__ __forceinline__ Partial empty_partial() {
+  Partial q;
+  q.best = -INFINITY;
+  q.idx = -1;
+  q.m = -INFINITY;
+  q.S = 0.0f;
+  return q;
+}
+
+template <int R>
+__device__ __forceinline__ void warp_merge_rows(const Partial *const (&p)[R], int n, Race (&tot)[R]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < R; ++i) race_init(tot[i]);
+  for (int j0 = 0; j0 < n; j0 += 64) {
+    Partial q[R][2];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + h * 32 + lane;
+        q[i][h] = (p[i] != nullptr && j < n) ? load_partial(p[i] + j) : empty_partial();
+      }
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) race_merge(tot[i], from_partial(q[i][h]));
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) race_merge(tot[i], race_shfl_down(tot[i], d));
+}
+
 // -------------------------------------------------------------------------
 // Host-side launchers (defined in the kernel translation units).
 // -------------------------------------------------------------------------

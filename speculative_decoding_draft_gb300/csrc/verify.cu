@@ -25,9 +25,11 @@ namespace cg = cooperative_groups;
 namespace dspark {
 namespace {
 
-constexpr int kChainThreads = 512;
+constexpr int kChainThreads = 256;
+constexpr int kBatch = 4;          // loads in flight per thread in the accept chain (fp32 / unaligned)
+constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per thread
 constexpr int kSampleThreads = 256;
-constexpr int kSampleChunk = 8192;
+constexpr int kSampleChunk = 32768;   // long per-thread streams amortise the race start-up
 
 struct Stats {
   float m, S;   // online softmax
@@ -130,24 +132,31 @@ __device__ __forceinline__ Stats stats_block_reduce(Stats s, Stats *scratch) {
 }
 
 struct ChainShared {
-  Stats slot_t[2];
-  Stats slot_d[2];
+  Stats slot_t[2];          // this CTA's target-row statistics (double-buffered by position parity)
+  Stats slot_d[2];          // draft-row statistics when no normaliser is given
+  float zx_t[2], zx_d[2];   // scaled logit at the draft token, valid in the CTA whose slice holds it
   Stats red[kChainThreads / 32];
+  int tok[kMaxK];
+  float own_t, own_d;       // written by the thread that streams the draft token's element
   int skip;
-  int decision;    // 1 accept, 0 reject
+  int decision;             // 1 accept, 0 reject
   int amax;
   float lse_t, lse_q;
 };
 
 // Slice [lo, hi) of the vocabulary owned by cluster rank `rank` (8-aligned).
-__device__ __forceinline__ void slice(int V, int rank, int ncta, int &lo, int &hi) {
-  const int per = ((V + ncta - 1) / ncta + 7) & ~7;
-  lo = min(V, rank * per);
-  hi = min(V, lo + per);
+__device__ __forceinline__ int slice_per(int V, int ncta) { return ((V + ncta - 1) / ncta + 7) & ~7; }
+
+__device__ __forceinline__ float pick8(const float (&x)[8], int q) {
+  float v = x[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+    if (i == q) v = x[i];
+  return v;
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kChainThreads) verify_chain(const __grid_constant__ VerifyArgs a) {
+__global__ void __launch_bounds__(kChainThreads, 2) verify_chain(const __grid_constant__ VerifyArgs a) {
   __shared__ ChainShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -179,13 +188,16 @@ __global__ void __launch_bounds__(kChainThreads) verify_chain(const __grid_const
     cluster.sync();
     return;
   }
+  if (tid < l) sh.tok[tid] = a.draft_tok[(int64_t)r * K + tid];
 
   const bool greedy = (T == 0.0f);
   const float invT = greedy ? 1.0f : 1.0f / T;
   const int64_t off = a.tgt_off[r];
   const bool have_lse = (a.D_lse != nullptr);
-  int lo, hi;
-  slice(V, rank, ncta, lo, hi);
+  const bool stream_d = !greedy && !have_lse;
+  const int per = slice_per(V, ncta);
+  const int lo = min(V, rank * per), hi = min(V, lo + per);
+  __syncthreads();
 
   int n = 0;
   bool rejected = false;
@@ -193,28 +205,103 @@ __global__ void __launch_bounds__(kChainThreads) verify_chain(const __grid_const
   float lse_t = 0.0f, lse_q = 0.0f;
   int greedy_tok = -1;
   for (int j = 1; j <= l; ++j) {
-    const int x = a.draft_tok[(int64_t)r * K + j - 1];
+    const int x = sh.tok[j - 1];
     const int64_t trow = (off + j - 1) * (int64_t)V;
     const int64_t drow = ((int64_t)r * K + j - 1) * (int64_t)V;
-    const bool stream_d = !greedy && !have_lse;
+    // values only thread 0 needs, requested before the row stream so their latency overlaps it
+    float u = 0.0f, dx = 0.0f, lq_given = 0.0f;
+    if (tid == 0 && !greedy) {
+      u = uniform_accept(philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept).x);
+      if (have_lse) {
+        dx = load1<DT>(a.D, drow + x);
+        lq_given = a.D_lse[(int64_t)r * K + j - 1];
+      }
+    }
+    const int xv = x & ~7;   // start of the 8-element group holding x
     Stats st, sd;
     stats_init(st);
     stats_init(sd);
-    for (int v0 = lo + tid * 8; v0 < hi; v0 += kChainThreads * 8) {
-      float x8[8];
-      load8<DT, VEC>(a.tgt, trow, v0, hi, x8);
-      if (greedy) {
-        argmax_add8(st, x8, v0);
-      } else {
+    if (DT == DSPARK_BF16 && VEC) {
+      // bf16 rows: keep kPkBatch packed 16-byte loads per thread in flight, unpack when consumed
+      const int nb = stream_d ? kPkBatch / 2 : kPkBatch;
+      for (int base = lo + tid * 8; base < hi; base += kChainThreads * 8 * nb) {
+        uint4 pt[kPkBatch];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x8[q] *= invT;
-        stats_add8(st, x8);
+        for (int uu = 0; uu < kPkBatch; ++uu) {
+          const int v0 = base + uu * kChainThreads * 8;
+          const bool in = (uu < nb) && (v0 + 8 <= hi);
+          pt[uu] = in ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + trow + v0)) : make_uint4(0, 0, 0, 0);
+        }
+        uint4 pd[kPkBatch / 2];
         if (stream_d) {
-          float y8[8];
-          load8<DT, VEC>(a.D, drow, v0, hi, y8);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) y8[q] *= invT;
-          stats_add8(sd, y8);
+          for (int uu = 0; uu < kPkBatch / 2; ++uu) {
+            const int v0 = base + uu * kChainThreads * 8;
+            pd[uu] = (v0 + 8 <= hi) ? __ldcs((const uint4 *)((const unsigned short *)a.D + drow + v0))
+                                    : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < kPkBatch; ++uu) {
+          const int v0 = base + uu * kChainThreads * 8;
+          if (uu >= nb || v0 + 8 > hi) continue;
+          float x8[8];
+          const uint32_t w4[4] = {pt[uu].x, pt[uu].y, pt[uu].z, pt[uu].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            x8[2 * i] = __uint_as_float(w4[i] << 16);
+            x8[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+          }
+          if (greedy) {
+            argmax_add8(st, x8, v0);
+            continue;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x8[q] *= invT;
+          if (v0 == xv) sh.own_t = pick8(x8, x & 7);
+          stats_add8(st, x8);
+          if (stream_d && uu < kPkBatch / 2) {
+            float y8[8];
+            const uint32_t d4[4] = {pd[uu].x, pd[uu].y, pd[uu].z, pd[uu].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              y8[2 * i] = __uint_as_float(d4[i] << 16) * invT;
+              y8[2 * i + 1] = __uint_as_float(d4[i] & 0xffff0000u) * invT;
+            }
+            if (v0 == xv) sh.own_d = pick8(y8, x & 7);
+            stats_add8(sd, y8);
+          }
+        }
+      }
+    } else {
+      // kBatch 16-byte loads per thread are issued before any of them is consumed
+      for (int base = lo + tid * 8; base < hi; base += kChainThreads * 8 * kBatch) {
+        float x8[kBatch][8];
+#pragma unroll
+        for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.tgt, trow, base + uu * kChainThreads * 8, hi, x8[uu]);
+        if (greedy) {
+#pragma unroll
+          for (int uu = 0; uu < kBatch; ++uu) argmax_add8(st, x8[uu], base + uu * kChainThreads * 8);
+          continue;
+        }
+        float y8[kBatch][8];
+        if (stream_d) {
+#pragma unroll
+          for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.D, drow, base + uu * kChainThreads * 8, hi, y8[uu]);
+        }
+#pragma unroll
+        for (int uu = 0; uu < kBatch; ++uu) {
+          const int v0 = base + uu * kChainThreads * 8;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x8[uu][q] *= invT;
+          if (v0 == xv) sh.own_t = pick8(x8[uu], x & 7);
+          stats_add8(st, x8[uu]);
+          if (stream_d) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) y8[uu][q] *= invT;
+            if (v0 == xv) sh.own_d = pick8(y8[uu], x & 7);
+            stats_add8(sd, y8[uu]);
+          }
         }
       }
     }
@@ -223,29 +310,47 @@ __global__ void __launch_bounds__(kChainThreads) verify_chain(const __grid_const
     if (tid == 0) {
       sh.slot_t[j & 1] = st;
       sh.slot_d[j & 1] = sd;
+      const bool mine = (x >= lo && x < hi);
+      sh.zx_t[j & 1] = mine ? sh.own_t : 0.0f;
+      sh.zx_d[j & 1] = mine ? sh.own_d : 0.0f;
     }
     cluster.sync();
     if (tid == 0) {
+      Stats parts_t[8], parts_d[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < ncta) {
+          parts_t[q] = *cluster.map_shared_rank(&sh.slot_t[j & 1], q);
+          if (stream_d) parts_d[q] = *cluster.map_shared_rank(&sh.slot_d[j & 1], q);
+        }
       Stats ct, cd;
       stats_init(ct);
       stats_init(cd);
-      for (int q = 0; q < ncta; ++q) {
-        stats_merge(ct, *cluster.map_shared_rank(&sh.slot_t[j & 1], q));
-        if (stream_d) stats_merge(cd, *cluster.map_shared_rank(&sh.slot_d[j & 1], q));
-      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < ncta) {
+          stats_merge(ct, parts_t[q]);
+          if (stream_d) stats_merge(cd, parts_d[q]);
+        }
       if (greedy) {
         sh.decision = (x == ct.idx);
         sh.amax = ct.idx;
       } else {
+        const int owner = x / per;
+        const float sx = *cluster.map_shared_rank(&sh.zx_t[j & 1], owner);
         const float lt = ct.m + logf(ct.S);
-        const float lq = have_lse ? a.D_lse[(int64_t)r * K + j - 1] : cd.m + logf(cd.S);
-        const float lp_x = load1<DT>(a.tgt, trow + x) * invT - lt;
-        const float lq_x = load1<DT>(a.D, drow + x) * invT - lq;
-        const uint4 w = philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept);
-        const float u = uniform_accept(w.x);
-        sh.decision = u < expf(lp_x - lq_x);
+        float lq_x;
+        if (have_lse) {
+          lq_x = dx * invT - lq_given;
+          sh.lse_q = lq_given;
+        } else {
+          const float sdx = *cluster.map_shared_rank(&sh.zx_d[j & 1], owner);
+          const float ld = cd.m + logf(cd.S);
+          lq_x = sdx - ld;
+          sh.lse_q = ld;
+        }
+        sh.decision = u < expf((sx - lt) - lq_x);
         sh.lse_t = lt;
-        sh.lse_q = lq;
       }
     }
     __syncthreads();
@@ -321,6 +426,7 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
   const int64_t trow = job.trow * (int64_t)V;
   const int64_t drow = job.drow * (int64_t)V;
   const int mode = from_p ? 2 : job.mode;
+  const PhiloxKey key = a.key;   // round keys in registers for the hot loop
   for (int v0 = lo + tid * 8; v0 < hi; v0 += nthreads * 8) {
     float t8[8];
     load8<DT, VEC>(a.tgt, trow, v0, hi, t8);
@@ -328,8 +434,8 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
       argmax_update<8>(rc, t8, v0);
       continue;
     }
-    const uint4 w0 = philox(a.key, (uint32_t)(v0 >> 2), (uint32_t)job.pos, (uint32_t)r, kTagResid);
-    const uint4 w1 = philox(a.key, (uint32_t)((v0 >> 2) + 1), (uint32_t)job.pos, (uint32_t)r, kTagResid);
+    const uint4 w0 = philox(key, (uint32_t)(v0 >> 2), (uint32_t)job.pos, (uint32_t)r, kTagResid);
+    const uint4 w1 = philox(key, (uint32_t)((v0 >> 2) + 1), (uint32_t)job.pos, (uint32_t)r, kTagResid);
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     if (mode == 2) {
 #pragma unroll
@@ -369,57 +475,65 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_constant__ VerifyArgs a) {
   __shared__ Race red[kSampleThreads / 32];
   __shared__ int s_any[kSampleThreads / 32];
-  __shared__ int s_last;
-  const int r = blockIdx.y, cx = blockIdx.x, tid = threadIdx.x;
+  __shared__ int s_last, s_tok;
+  const int cx = blockIdx.x, tid = threadIdx.x;
   if (read_status(a.dev_status)) return;
-  const VerifyJob job = a.jobs[r];
-  if (job.mode == 0) return;
-  const int V = (int)a.V;
-  const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
-  Race rc;
-  race_init(rc);
-  bool any_cand = false;
-  sample_range<DT, VEC>(a, job, r, lo, hi, tid, kSampleThreads, rc, any_cand, false);
-  const int any = __syncthreads_or(any_cand ? 1 : 0);
-  rc = race_block_reduce(rc, red);
-  if (tid == 0) {
-    Partial p = to_partial(rc);
-    p.m = any ? 1.0f : 0.0f;    // the sampling pass needs no softmax: reuse the field as a flag
-    a.partials[(int64_t)r * a.chunks + cx] = p;
-    __threadfence();
-    const int prev = atomicAdd(&a.counters[r], 1);
-    s_last = (prev == a.chunks - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  Race tot;
-  race_init(tot);
-  int any_all = 0;
-  if (tid == 0) {
-    for (int q = 0; q < a.chunks; ++q) {
-      const Partial p = load_partial(a.partials + ((int64_t)r * a.chunks + q));
-      Race x = from_partial(p);
-      x.m = -INFINITY;
-      x.S = 0.0f;
-      race_merge(tot, x);
-      any_all |= (p.m != 0.0f);
+  for (int r = blockIdx.y; r < (int)a.B; r += gridDim.y) {
+    const VerifyJob job = a.jobs[r];
+    if (job.mode == 0) continue;
+    const int V = (int)a.V;
+    const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
+    Race rc;
+    race_init(rc);
+    bool any_cand = false;
+    sample_range<DT, VEC>(a, job, r, lo, hi, tid, kSampleThreads, rc, any_cand, false);
+    const int any = __syncthreads_or(any_cand ? 1 : 0);
+    rc = race_block_reduce(rc, red);
+    if (tid == 0) {
+      Partial p = to_partial(rc);
+      p.m = any ? 1.0f : 0.0f;    // the sampling pass needs no softmax: the field carries a flag
+      a.partials[(int64_t)r * a.chunks + cx] = p;
+      __threadfence();
+      const int prev = atomicAdd(&a.counters[r], 1);
+      s_last = (prev == a.chunks - 1);
     }
-    s_any[0] = any_all;
-  }
-  __syncthreads();
-  if (job.mode == 1 && !s_any[0]) {
-    // no element with p > q survived rounding: sample the correction from p instead
-    Race rp;
-    race_init(rp);
-    bool dummy = false;
-    sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, rp, dummy, true);
-    rp = race_block_reduce(rp, red);
-    if (tid == 0) tot = rp;
-  }
-  if (tid == 0) {
-    a.out_tok[job.out_slot] = tot.idx;
-    a.counters[r] = 0;
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    if (tid < 32) {
+      Race tot;
+      race_init(tot);
+      int any_all = 0;
+      for (int q = tid; q < a.chunks; q += 32) {
+        const Partial p = load_partial(a.partials + ((int64_t)r * a.chunks + q));
+        Race x = from_partial(p);
+        x.m = -INFINITY;
+        x.S = 0.0f;
+        race_merge(tot, x);
+        any_all |= (p.m != 0.0f);
+      }
+      for (int d = 16; d > 0; d >>= 1) race_merge(tot, race_shfl_down(tot, d));
+      any_all = __any_sync(0xffffffffu, any_all);
+      if (tid == 0) {
+        s_any[0] = any_all;
+        s_tok = tot.idx;
+      }
+    }
+    __syncthreads();
+    if (job.mode == 1 && !s_any[0]) {
+      // no element with p > q survived rounding: sample the correction from p instead
+      Race rp;
+      race_init(rp);
+      bool dummy = false;
+      sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, rp, dummy, true);
+      rp = race_block_reduce(rp, red);
+      if (tid == 0) s_tok = rp.idx;
+    }
+    if (tid == 0) {
+      a.out_tok[job.out_slot] = s_tok;
+      a.counters[r] = 0;
+    }
+    __syncthreads();
   }
 }
 
@@ -442,7 +556,7 @@ cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, int num_sms) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, verify_chain<DT, VEC>, a);
   if (e != cudaSuccess) return e;
-  verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)a.B), kSampleThreads, 0, s>>>(a);
+  verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)(a.B < 65535 ? a.B : 65535)), kSampleThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
