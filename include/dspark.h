@@ -150,6 +150,33 @@ dspark_status dspark_schedule_survival(const float *conf, const int32_t *K_r, co
                                        int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Schedule without a caller workspace.
+ *
+ * The paper has no counterpart to this entry point: it exists for callers that
+ * cannot allocate device memory where they schedule -- a serving loop that must
+ * not call cudaMalloc between steps (it synchronises the device), or a plugin
+ * whose host process owns every device allocation and hands it no workspace.
+ * It computes exactly what dspark_schedule_survival computes, with the same
+ * arguments except the workspace, on scratch memory that is a static array of
+ * this library (DSPARK_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ * library, held until the process exits).  It allocates and frees nothing.
+ *   - B * K_max must not exceed DSPARK_NOALLOC_MAX_CANDIDATES; larger calls
+ *     return DSPARK_ERR_WORKSPACE and enqueue nothing.
+ *   - The first call on a device (with that device current) looks up the
+ *     scratch address once; make that first call before any stream capture.
+ *   - Every call shares the one scratch array: calls whose kernels may overlap
+ *     on the GPU (unordered streams) race on it.  Nothing in it needs clearing
+ *     between calls.
+ * ------------------------------------------------------------------------ */
+#define DSPARK_NOALLOC_MAX_CANDIDATES 32768
+#define DSPARK_NOALLOC_SCRATCH_BYTES (1088u * 1024u)
+
+dspark_status dspark_schedule_survival_noalloc(const float *conf, const int32_t *K_r, const double *sps,
+                                               int64_t sps_len, int64_t B, int64_t K_max, int32_t *ell,
+                                               int32_t *tgt_off, double *theta_best, int64_t *b_star,
+                                               float *survival, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Verify: ragged rejection-sampling verification ("DSpark" S2.1;
  * "Speculative decoding, from zero to DSpark" S2 and Appendix A1).
  *

@@ -41,7 +41,8 @@ STATUS_NAMES = {
 
 EXPORTED_SYMBOLS = [
     "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_schedule_workspace_bytes",
-    "dspark_schedule_survival", "dspark_verify_workspace_bytes", "dspark_verify_ragged",
+    "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_verify_workspace_bytes",
+    "dspark_verify_ragged",
     "dspark_status_string", "dspark_check", "dspark_version",
 ]
 
@@ -87,6 +88,8 @@ def lib() -> ctypes.CDLL:
     L.dspark_schedule_workspace_bytes.restype = sz
     L.dspark_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, sz, P, P]
     L.dspark_schedule_survival.restype = st
+    L.dspark_schedule_survival_noalloc.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P]
+    L.dspark_schedule_survival_noalloc.restype = st
     L.dspark_verify_workspace_bytes.argtypes = [i64, i64]
     L.dspark_verify_workspace_bytes.restype = sz
     L.dspark_verify_ragged.argtypes = [P, P, P, P, P, P, P, u64, Dims, P, P, P, sz, P, P]

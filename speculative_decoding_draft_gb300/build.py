@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdspark.so")
-SOURCES = ["api.cu", "schedule.cu", "verify.cu", "draft_simt.cu", "draft_tc.cu"]
+SOURCES = ["api.cu", "schedule.cu", "schedule_noalloc.cu", "verify.cu", "draft_simt.cu", "draft_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
