@@ -13,7 +13,6 @@ constexpr int64_t kMaxB = 1 << 20;
 constexpr int64_t kMaxV = (int64_t)1 << 30;
 constexpr int64_t kMaxRank = 8192;
 constexpr int kDraftSimtChunk = 2048;        // must match draft_simt.cu
-constexpr int64_t kTcPartialSlots = 1024 * 128;
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -41,9 +40,10 @@ bool device_info(DeviceInfo *out) {
   return true;
 }
 
-int64_t draft_partial_slots(int64_t B, int64_t V) {
+int64_t draft_partial_slots(int64_t B, int64_t K_max, int64_t V) {
   const int64_t simt = B * ((V + kDraftSimtChunk - 1) / kDraftSimtChunk);
-  return simt > kTcPartialSlots ? simt : kTcPartialSlots;
+  const int64_t tc = K_max * dspark::kTcPartialsPerStep;
+  return simt > tc ? simt : tc;
 }
 
 dspark_status check_dims(const dspark_dims &d, bool need_rank) {
@@ -99,9 +99,9 @@ dspark_status dspark_check(int32_t *dev_status, void *stream) {
 // ---------------------------------------------------------------------------
 size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V) {
   if (B < 1 || K_max < 1 || V < 2) return 0;
-  return al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
-         al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) +
-         al256(sizeof(Partial) * (size_t)draft_partial_slots(B, V));
+  return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
+         al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
+         al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V));
 }
 
 dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
@@ -137,12 +137,16 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   char *p = (char *)workspace;
   a.perm = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)dims.B);
+  a.iperm = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)dims.B);
   a.nact = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 2));
   a.counters = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)(dims.B > 4096 ? dims.B : 4096));
+  a.best_key = (unsigned long long *)p;
+  p += al256(8 * (size_t)(dims.B * dims.K_max));
   a.partials = (Partial *)p;
-  a.partial_slots = draft_partial_slots(dims.B, dims.V);
+  a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_draft_prologue(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
   const bool use_tc = !(dims.flags & DSPARK_FLAG_FORCE_SIMT) && dev.major == 10 && dev.minor == 3 &&

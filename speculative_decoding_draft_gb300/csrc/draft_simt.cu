@@ -43,8 +43,10 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     if (x0 < 0 || x0 >= V) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TOKEN_RANGE);
     if (!temperature_ok(a.temperature[r])) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TEMPERATURE);
     a.counters[r] = 0;
-    for (int k = 0; k < K; ++k)
+    for (int k = 0; k < K; ++k) {
+      a.best_key[(int64_t)r * K + k] = 0ull;
       if (k >= kr) a.draft_tok[(int64_t)r * K + k] = -1;
+    }
   }
   __syncthreads();
   if (s_err) {
@@ -74,7 +76,10 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     __syncthreads();
     int before = 0;
     for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][v];
-    if (r < B) a.perm[base[v] + before + rank] = r;
+    if (r < B) {
+      a.perm[base[v] + before + rank] = r;
+      a.iperm[r] = base[v] + before + rank;
+    }
     __syncthreads();
     if (tid >= 1 && tid <= K) {
       int tot = 0;

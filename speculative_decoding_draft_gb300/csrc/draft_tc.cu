@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (i < nrows) {
         const int r = a.perm[row0 + i];
         sh.row_req[i] = r;
-        sh.row_prev[i] = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
+        sh.row_prev[i] = (k == 1) ? a.anchor[r] : key_index(a.best_key[(int64_t)r * K + k - 2]);
         const float T = a.temperature[r];
         sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
       } else {
@@ -327,19 +327,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
       const int half = eq >> 2;           // 32-column half of the 64-wide tile
       const int et = eq * 32 + lane;      // 0..255
-      // gather the A operand: M-row a holds request row (a mod rpg); 16-byte unit c8 of K-chunk
-      // c of that row goes to chunk c, row a, unit (c8 ^ (a & 7)) -- the 128-byte swizzle
-      const int units_per_row = rank / 8;
-      for (int e = et; e < kTileM * units_per_row; e += kEpiWarps * 32) {
-        const int ar = e / units_per_row, uu = e % units_per_row;
-        const int i = ar % rpg;
-        const int c = uu >> 3, c8 = uu & 7;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (i < nrows) val = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * rank) + uu);
-        const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y), "r"(val.z),
-                     "r"(val.w)
-                     : "memory");
+      // gather the A operand: request row i's 16-byte unit c8 of K-chunk c goes to every replica
+      // M-row a = g * rpg + i, chunk c, unit (c8 ^ (a & 7)) -- the 128-byte swizzle.  All loads of
+      // a thread are issued before its stores, so the row fetches overlap.
+      {
+        const int units_per_row = rank / 8;
+        const int total = nrows * units_per_row;     // <= 128 * 32
+        uint4 val[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int e = et + q * kEpiWarps * 32;
+          val[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (e < total) {
+            const int i = e / units_per_row, uu = e % units_per_row;
+            val[q] = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * rank) + uu);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int e = et + q * kEpiWarps * 32;
+          if (e >= total) continue;
+          const int i = e / units_per_row, uu = e % units_per_row;
+          const int c = uu >> 3, c8 = uu & 7;
+          for (int g = 0; g < F; ++g) {
+            const int ar = g * rpg + i;
+            const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val[q].x), "r"(val[q].y),
+                         "r"(val[q].z), "r"(val[q].w)
+                         : "memory");
+          }
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -365,6 +382,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int b = (int)(idx % kAccBufs);
         const uint32_t ause = idx / kAccBufs;
         if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
+        if (t != tmine) {                         // another replica group owns this tile
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce + 8 * b);
+          continue;
+        }
         tc_fence_after();
         uint32_t acc[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
@@ -372,12 +394,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acce + 8 * b);
-        if (t != tmine) continue;                 // another replica group owns this tile
         tmine += F;
         if (!valid) continue;
         if (tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, unext);   // prefetch
         const int c0 = t * kTileN + half * 32;
         const bool full = (c0 + 32 <= V);
+        uint32_t w[32];
+        if (!greedy) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {             // eight independent Philox blocks: ILP
+            const uint4 wq = philox(key, (uint32_t)(c0 >> 2) + (uint32_t)q, (uint32_t)k, (uint32_t)r, kTagDraft);
+            w[4 * q] = wq.x;
+            w[4 * q + 1] = wq.y;
+            w[4 * q + 2] = wq.z;
+            w[4 * q + 3] = wq.w;
+          }
+        }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const uint32_t pk[4] = {ucur[g].x, ucur[g].y, ucur[g].z, ucur[g].w};
@@ -405,54 +437,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (greedy) {
             argmax_update<8>(st, sv, c0 + g * 8);
           } else {
-            const uint32_t cb = (uint32_t)((c0 + g * 8) >> 2);
-            const uint4 w0 = philox(key, cb, (uint32_t)k, (uint32_t)r, kTagDraft);
-            const uint4 w1 = philox(key, cb + 1u, (uint32_t)k, (uint32_t)r, kTagDraft);
-            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            race_update<8>(st, sv, w, c0 + g * 8);
+            const uint32_t wg[8] = {w[8 * g], w[8 * g + 1], w[8 * g + 2], w[8 * g + 3],
+                                    w[8 * g + 4], w[8 * g + 5], w[8 * g + 6], w[8 * g + 7]};
+            race_update<8>(st, sv, wg, c0 + g * 8);
           }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
       }
-      // merge the 2F thread partials of each row (replica groups x column halves),
-      // publish the CTA partial; layout [M-tile][row][CTA slot j]
+      // merge the 2F thread partials of each row (replica groups x column halves); the row's
+      // home thread folds its maximum into the packed (score, index) key of the position with one
+      // 64-bit atomicMax -- all the next position needs -- and keeps its softmax partial for the
+      // normaliser, which the finalize kernel merges once per call
       sh.part[(grp * 2 + half) * rpg + row] = to_partial(st);
       named_sync_epi();
-      if (grp == 0 && half == 0) {
+      if (grp == 0 && half == 0 && valid) {
         for (int q = 1; q < 2 * F; ++q) race_merge(st, from_partial(sh.part[q * rpg + row]));
-        if (valid) a.partials[((int64_t)m * kTileM + row) * gm + j] = to_partial(st);
-      }
-      __threadfence();
-      named_sync_epi();
-      if (et == 0) sh.last = (atomicAdd(&a.counters[m], 1) == gm - 1);
-      named_sync_epi();
-      if (sh.last) {
-        __threadfence();
-        // warp eq merges rows eq, eq + 8, ... in groups of 8 rows
-        for (int r0 = eq; r0 < nrows; r0 += 8 * kEpiWarps) {
-          const Partial *ptr[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = r0 + i * kEpiWarps;
-            ptr[i] = rr < nrows ? a.partials + ((int64_t)m * kTileM + rr) * gm : nullptr;
-          }
-          Race tot[8];
-          warp_merge_rows<8>(ptr, gm, tot);
-          if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rr = r0 + i * kEpiWarps;
-              if (rr >= nrows) continue;
-              const int rq = sh.row_req[rr];
-              a.draft_tok[(int64_t)rq * K + k - 1] = tot[i].idx;
-              if (a.draft_lse)
-                a.draft_lse[(int64_t)rq * K + k - 1] =
-                    sh.row_invT[rr] == 0.0f ? tot[i].best : tot[i].m + logf(tot[i].S);
-            }
-          }
-        }
-        if (et == 0) a.counters[m] = 0;
+        if (st.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(st.best, st.idx));
+        a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * gm + j] = to_partial(st);
       }
     }
     it += (uint32_t)(nt1 - nt0);
@@ -498,6 +500,33 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+// Once per call, after the last position: tokens from the packed maxima and the
+// normaliser from the CTA partials of each (request, position), one warp each.
+__global__ void __launch_bounds__(256) draft_tc_finalize(const __grid_constant__ DraftArgs a, int G) {
+  if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max, B = (int)a.B;
+  const int n_tiles = (int)((a.V + kTileN - 1) / kTileN);
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < (int64_t)B * K; item += nw) {
+    const int k = (int)(item / B) + 1, i = (int)(item % B);
+    const int n_k = a.nact[k];
+    if (i >= n_k) continue;
+    const int m_tiles = (n_k + kTileM - 1) / kTileM;
+    const int gm = max(1, min(G / m_tiles, n_tiles));
+    const int r = a.perm[i];
+    const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * gm};
+    Race tot[1];
+    warp_merge_rows<1>(ptr, gm, tot);
+    if (lane == 0) {
+      const unsigned long long key = a.best_key[(int64_t)r * K + k - 1];
+      a.draft_tok[(int64_t)r * K + k - 1] = key_index(key);
+      if (a.draft_lse)
+        a.draft_lse[(int64_t)r * K + k - 1] = a.temperature[r] == 0.0f ? tot[0].best : tot[0].m + logf(tot[0].S);
+    }
+  }
+}
+
 }  // namespace
 
 bool draft_tc_supported(const DraftArgs &a) {
@@ -506,9 +535,11 @@ bool draft_tc_supported(const DraftArgs &a) {
   if (a.V % 8 != 0 || a.V > (int64_t)INT32_MAX - 64) return false;
   if (((uintptr_t)a.U | (uintptr_t)a.E | (uintptr_t)a.W) & 15u) return false;
   if (a.draft_logits && ((uintptr_t)a.draft_logits & 15u)) return false;
+  // partial slots of one position: (M-tiles x 128 rows) x CTAs per M-tile <= 128 x max(grid, M-tiles)
   const int64_t m_tiles = (a.B + kTileM - 1) / kTileM;
   const int64_t units = m_tiles > 1024 ? m_tiles : 1024;
-  if (units * kTileM > a.partial_slots) return false;   // slots used: M-tiles x 128 x CTAs per M-tile
+  if (units * kTileM > kTcPartialsPerStep) return false;
+  if (a.K_max * kTcPartialsPerStep > a.partial_slots) return false;
   return get_encode() != nullptr;
 }
 
@@ -536,7 +567,10 @@ cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  const int64_t items = a.B * a.K_max;
+  const int fblocks = (int)((items + 7) / 8 < 4096 ? (items + 7) / 8 : 4096);
+  draft_tc_finalize<<<fblocks, 256, 0, s>>>(a, grid);
+  return cudaGetLastError();
 }
 
 }  // namespace dspark

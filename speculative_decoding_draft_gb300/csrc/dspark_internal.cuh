@@ -320,15 +320,29 @@ struct DraftArgs {
   PhiloxKey key;
   // workspace carve-out
   int32_t *perm;      // [B] requests ordered by K_r descending
+  int32_t *iperm;     // [B] position of each request in perm
   int32_t *nact;      // [K_max + 2] active requests per position
   int32_t *counters;  // [B] per-row arrival counters (zero between steps)
+  unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path
   Partial *partials;  // [partial_slots]
   int64_t partial_slots;
 };
 
+// Total order key of a perturbed score and its index: larger score first, then the
+// smaller index, so a 64-bit atomicMax merges (score desc, index asc).
+__device__ __forceinline__ unsigned long long score_key(float s, int idx) {
+  const uint32_t u = __float_as_uint(s);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+__device__ __forceinline__ int key_index(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+
 cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms);
+constexpr int64_t kTcPartialsPerStep = 128 * 1024;   // slots per draft position on the tensor-core path
 bool draft_tc_supported(const DraftArgs &a);
 
 struct ScheduleArgs {
