@@ -101,7 +101,7 @@ size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V) {
   if (B < 1 || K_max < 1 || V < 2) return 0;
   return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
          al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
-         al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V));
+         al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V));
 }
 
 dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
@@ -145,6 +145,8 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   p += al256(sizeof(int32_t) * (size_t)(dims.B > 4096 ? dims.B : 4096));
   a.best_key = (unsigned long long *)p;
   p += al256(8 * (size_t)(dims.B * dims.K_max));
+  a.gbar = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 1));
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   cudaStream_t s = (cudaStream_t)stream;

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
   if (tid < kMaxK + 2) cnt[tid] = 0;
   __syncthreads();
   if (s_skip) return;
+  if (tid <= a.K_max) a.gbar[tid] = 0;
   const int B = (int)a.B, K = (int)a.K_max, V = (int)a.V;
   for (int r = tid; r < B; r += kPrologueThreads) {
     const int kr = a.K_r[r];

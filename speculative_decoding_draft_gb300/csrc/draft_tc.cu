@@ -155,12 +155,43 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// L2 policies: the projection W2 is re-read at every draft position and should stay in
+// L2; the base logits U and the stored draft logits are touched once.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_u4_hint(const void *ptr, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ void st_u4_hint(void *ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
@@ -179,19 +210,43 @@ __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
 
-// ---------------------------------------------------------------------------
 // U row segment of one epilogue thread for one tile: 32 bf16 at column c0 of
 // its row (16-byte loads; columns past V are not read).
-__device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int V, uint4 (&u)[4]) {
+__device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int V, uint4 (&u)[4], uint64_t pol) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    if (c0 + 8 * q < V) u[q] = __ldg(reinterpret_cast<const uint4 *>(row + c0 + 8 * q));
+    if (c0 + 8 * q < V) u[q] = ld_u4_hint(row + c0 + 8 * q, pol);
     else u[q] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
+// Work split of one draft position: M-tiles of 128 active rows, each shared by gm CTAs
+// that own contiguous ranges of 64-wide vocabulary tiles.
+struct StepPlan {
+  int n_k, m_tiles, gm, units;
+};
+__device__ __forceinline__ StepPlan plan_step(const DraftArgs &a, int k, int G, int n_tiles) {
+  StepPlan p;
+  p.n_k = a.nact[k];
+  p.m_tiles = (p.n_k + kTileM - 1) / kTileM;
+  p.gm = p.m_tiles ? max(1, min(G / p.m_tiles, n_tiles)) : 1;
+  p.units = p.m_tiles * p.gm;
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// One persistent CTA per SM walks every draft position k = 1..K_max.  The producer
+// and MMA roles run ahead through positions on their own barriers (W2 does not
+// depend on the drafted tokens); the epilogue waits on a grid-wide barrier before
+// it reads the previous position's tokens, so the next position's W2 tiles and U
+// segments are already in flight while the barrier completes.
+template <int RCH>   // rank / 64
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    draft_tc_step(const __grid_constant__ DraftArgs a, const __grid_constant__ CUtensorMap tmap_w, int k) {
+    draft_tc_persistent(const __grid_constant__ DraftArgs a, const __grid_constant__ CUtensorMap tmap_w) {
+  constexpr int kRank = RCH * 64;
+  constexpr int kKsteps = kRank / 16;
+  constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
+  constexpr uint32_t kWBytes = (uint32_t)(kTileN * kRank * 2);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -201,19 +256,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (threadIdx.x == 0) sh.skip = read_status(a.dev_status);
   __syncthreads();
-  if (sh.skip) return;
+  if (sh.skip) return;   // an earlier error: every CTA sees the same word and leaves
 
-  const int n_k = a.nact[k];
-  const int K = (int)a.K_max, V = (int)a.V, rank = (int)a.rank;
-  const int m_tiles = (n_k + kTileM - 1) / kTileM;
-  if (m_tiles == 0) return;
+  const int K = (int)a.K_max, V = (int)a.V;
   const int G = gridDim.x;
   const int n_tiles = (V + kTileN - 1) / kTileN;
-  const int gm = max(1, min(G / m_tiles, n_tiles));
-  const int units = m_tiles * gm;
-  if ((int)blockIdx.x >= units) return;
-  const int ksteps = rank / 16;
-  const uint32_t w_bytes = (uint32_t)(kTileN * rank * 2);
 
   const uint32_t bar_full = smem_u32(&sh.full[0]);
   const uint32_t bar_empty = smem_u32(&sh.empty[0]);
@@ -246,8 +293,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  uint32_t it = 0;   // global tile counter of this CTA (same progression in every role)
-  int unit_no = 0;
   uint32_t last_use[kStages];   // producer: last issued use of each stage (for the abort drain)
   bool issued[kStages];
 #pragma unroll
@@ -255,212 +300,259 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     last_use[s] = 0;
     issued[s] = false;
   }
-  for (int u = blockIdx.x; u < units; u += G, ++unit_no) {
-    const int m = u / gm, j = u % gm;
-    const int nt0 = (int)((int64_t)j * n_tiles / gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / gm);
-    const int row0 = m * kTileM;
-    const int nrows = min(kTileM, n_k - row0);
-    // replication: with few rows, every TMEM lane quadrant (= SM sub-partition) gets a copy of
-    // the rows and takes every F-th vocabulary tile
-    const int F = nrows <= 32 ? 4 : (nrows <= 64 ? 2 : 1);
-    const int rpg = kTileM / F;   // rows per replica group
-    __syncthreads();
-    if (threadIdx.x < kTileM) {
-      const int i = threadIdx.x;
-      if (i < nrows) {
-        const int r = a.perm[row0 + i];
-        sh.row_req[i] = r;
-        sh.row_prev[i] = (k == 1) ? a.anchor[r] : key_index(a.best_key[(int64_t)r * K + k - 2]);
-        const float T = a.temperature[r];
-        sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
-      } else {
-        sh.row_req[i] = -1;
-        sh.row_prev[i] = 0;
-        sh.row_invT[i] = 0.0f;
+
+  if (warp == 0) {
+    // ---------------- producer: W2 tiles of every position ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_last();
+      uint32_t it = 0;
+      for (int k = 1; k <= K && !*abort; ++k) {
+        const StepPlan pl = plan_step(a, k, G, n_tiles);
+        if (pl.n_k == 0) break;
+        for (int u = blockIdx.x; u < pl.units && !*abort; u += G) {
+          const int j = u % pl.gm;
+          const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
+          for (int t = nt0; t < nt1; ++t, ++it) {
+            const int s = (int)(it % kStages);
+            const uint32_t use = it / kStages;
+            if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
+            mbar_arrive_tx(bar_full + 8 * s, kWBytes);
+            tma_load_2d(sb + kOffW + s * kWSlot, &tmap_w, t * kTileN, 0, bar_full + 8 * s, pol_w);
+#pragma unroll
+            for (int q = 0; q < kStages; ++q)
+              if (q == s) { last_use[q] = use; issued[q] = true; }
+          }
+        }
       }
     }
-    __syncthreads();
-
-    if (warp == 0) {
-      // ---------------- producer: W2 tiles ----------------
-      if (lane == 0) {
-        for (int t = nt0; t < nt1 && !*abort; ++t) {
-          const uint32_t idx = it + (uint32_t)(t - nt0);
-          const int s = (int)(idx % kStages);
-          const uint32_t use = idx / kStages;
-          if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
-          mbar_arrive_tx(bar_full + 8 * s, w_bytes);
-          tma_load_2d(sb + kOffW + s * kWSlot, &tmap_w, t * kTileN, 0, bar_full + 8 * s);
-#pragma unroll
-          for (int q = 0; q < kStages; ++q)
-            if (q == s) { last_use[q] = use; issued[q] = true; }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      int unit_no = 0;
+      bool ok = true;
+      for (int k = 1; k <= K && ok; ++k) {
+        const StepPlan pl = plan_step(a, k, G, n_tiles);
+        if (pl.n_k == 0) break;
+        for (int u = blockIdx.x; u < pl.units && ok; u += G, ++unit_no) {
+          const int j = u % pl.gm;
+          const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
+          ok = mbar_wait(bar_aready, (uint32_t)(unit_no & 1), abort);
+          for (int t = nt0; ok && t < nt1; ++t, ++it) {
+            const int s = (int)(it % kStages);
+            const uint32_t use = it / kStages;
+            const int b = (int)(it % kAccBufs);
+            const uint32_t ause = it / kAccBufs;
+            if (!(ok = mbar_wait(bar_full + 8 * s, use & 1u, abort))) break;
+            if (!(ok = mbar_wait(bar_acce + 8 * b, (ause & 1u) ^ 1u, abort))) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(b * kTileN);
+#pragma unroll 1
+            for (int kk = 0; kk < kKsteps; ++kk) {
+              const uint64_t ad = smem_desc(sb + kOffA + (kk >> 2) * kAChunk + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc(sb + kOffW + s * kWSlot + kk * 2048, (uint32_t)(kRank * 128), 1024);
+              mma_bf16(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_empty + 8 * s);
+            mma_commit(bar_accf + 8 * b);
+          }
         }
       }
-      __syncwarp();
-    } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
-        bool ok = mbar_wait(bar_aready, (uint32_t)(unit_no & 1), abort);
-        for (int t = nt0; ok && t < nt1; ++t) {
-          const uint32_t idx = it + (uint32_t)(t - nt0);
-          const int s = (int)(idx % kStages);
-          const uint32_t use = idx / kStages;
-          const int b = (int)(idx % kAccBufs);
-          const uint32_t ause = idx / kAccBufs;
-          if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
-          if (!mbar_wait(bar_acce + 8 * b, (ause & 1u) ^ 1u, abort)) break;
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue ----------------
+    const int eq = warp - 2;            // 0..7
+    const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
+    const int half = eq >> 2;           // 32-column half of the 64-wide tile
+    const int et = eq * 32 + lane;      // 0..255
+    const uint64_t pol_stream = policy_evict_first();
+    uint32_t it = 0;
+    int unit_no = 0;
+    for (int k = 1; k <= K && !*abort; ++k) {
+      const StepPlan pl = plan_step(a, k, G, n_tiles);
+      if (pl.n_k == 0) break;
+      bool waited = (k == 1);
+      for (int u = blockIdx.x; u < pl.units && !*abort; u += G, ++unit_no) {
+        const int m = u / pl.gm, j = u % pl.gm;
+        const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
+        const int row0 = m * kTileM;
+        const int nrows = min(kTileM, pl.n_k - row0);
+        // replication: with few rows, every TMEM lane quadrant (= SM sub-partition) gets a copy
+        // of the rows and takes every F-th vocabulary tile
+        const int F = nrows <= 32 ? 4 : (nrows <= 64 ? 2 : 1);
+        const int rpg = kTileM / F;
+        named_sync_epi();             // readers of the previous unit's row table are done
+        if (et < kTileM) {
+          const int i = et;
+          if (i < nrows) {
+            const int r = a.perm[row0 + i];
+            sh.row_req[i] = r;
+            const float T = a.temperature[r];
+            sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
+          } else {
+            sh.row_req[i] = -1;
+            sh.row_invT[i] = 0.0f;
+          }
+        }
+        named_sync_epi();
+        const int arow = quad * 32 + lane;        // TMEM lane = M-row
+        const int grp = arow / rpg;               // replica group: takes tiles t with (t - nt0) % F == grp
+        const int row = arow % rpg;               // request row of this thread
+        const bool valid = row < nrows;
+        const int r = valid ? sh.row_req[row] : 0;
+        const float invT = sh.row_invT[row];
+        const bool greedy = (invT == 0.0f);
+        const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
+        const unsigned short *uptr = (const unsigned short *)a.U + urow;
+        uint4 ucur[4], unext[4];
+        int tmine = nt0 + grp;                    // first tile of this thread
+        if (valid && tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, ucur, pol_stream);   // before the barrier
+        if (!waited) {
+          // every CTA has folded its position k-1 maxima into the packed keys
+          if (et == 0) {
+            const long long t0 = clock64();
+            while (ld_acquire(a.gbar + (k - 1)) < G) {
+              if (*abort) break;
+              if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }
+            }
+          }
+          named_sync_epi();
+          waited = true;
+          if (*abort) break;
+        }
+        if (et < kTileM && et < nrows) {
+          const int rq = sh.row_req[et];
+          sh.row_prev[et] = (k == 1) ? a.anchor[rq] : key_index(__ldcg(a.best_key + (int64_t)rq * K + k - 2));
+        }
+        named_sync_epi();
+        // gather the A operand: request row i's 16-byte unit c8 of K-chunk c goes to every replica
+        // M-row a = g * rpg + i, chunk c, unit (c8 ^ (a & 7)) -- the 128-byte swizzle.  All loads of a
+        // thread are issued before its stores, so the row fetches overlap.
+        {
+          const int total = nrows * kUpr;
+#pragma unroll 1
+          for (int q0 = 0; q0 < 16; q0 += 8) {     // two batches of eight 16-byte loads per thread
+            uint4 val[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int e = et + (q0 + q) * kEpiWarps * 32;
+              val[q] = make_uint4(0u, 0u, 0u, 0u);
+              if (e < total) {
+                const int i = e / kUpr, uu = e % kUpr;
+                val[q] = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * kRank) + uu);
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int e = et + (q0 + q) * kEpiWarps * 32;
+              if (e >= total) continue;
+              const int i = e / kUpr, uu = e % kUpr;
+              const int c = uu >> 3, c8 = uu & 7;
+              for (int g = 0; g < F; ++g) {
+                const int ar = g * rpg + i;
+                const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val[q].x), "r"(val[q].y),
+                             "r"(val[q].z), "r"(val[q].w)
+                             : "memory");
+              }
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_aready);
+
+        Race st;
+        race_init(st);
+        for (int t = nt0; t < nt1; ++t, ++it) {
+          const int b = (int)(it % kAccBufs);
+          const uint32_t ause = it / kAccBufs;
+          if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
+          if (t != tmine) {                       // another replica group owns this tile
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce + 8 * b);
+            continue;
+          }
           tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(b * kTileN);
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t ad = smem_desc(sb + kOffA + (kk >> 2) * kAChunk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(sb + kOffW + s * kWSlot + kk * 2048, (uint32_t)(rank * 128), 1024);
-            mma_bf16(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar_empty + 8 * s);
-          mma_commit(bar_accf + 8 * b);
-        }
-      }
-      __syncwarp();
-    } else {
-      // ---------------- epilogue ----------------
-      const int eq = warp - 2;            // 0..7
-      const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
-      const int half = eq >> 2;           // 32-column half of the 64-wide tile
-      const int et = eq * 32 + lane;      // 0..255
-      // gather the A operand: request row i's 16-byte unit c8 of K-chunk c goes to every replica
-      // M-row a = g * rpg + i, chunk c, unit (c8 ^ (a & 7)) -- the 128-byte swizzle.  All loads of
-      // a thread are issued before its stores, so the row fetches overlap.
-      {
-        const int units_per_row = rank / 8;
-        const int total = nrows * units_per_row;     // <= 128 * 32
-        uint4 val[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int e = et + q * kEpiWarps * 32;
-          val[q] = make_uint4(0u, 0u, 0u, 0u);
-          if (e < total) {
-            const int i = e / units_per_row, uu = e % units_per_row;
-            val[q] = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * rank) + uu);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int e = et + q * kEpiWarps * 32;
-          if (e >= total) continue;
-          const int i = e / units_per_row, uu = e % units_per_row;
-          const int c = uu >> 3, c8 = uu & 7;
-          for (int g = 0; g < F; ++g) {
-            const int ar = g * rpg + i;
-            const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val[q].x), "r"(val[q].y),
-                         "r"(val[q].z), "r"(val[q].w)
-                         : "memory");
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_aready);
-
-      const int arow = quad * 32 + lane;          // TMEM lane = M-row
-      const int grp = arow / rpg;                 // replica group: takes tiles t with (t - nt0) % F == grp
-      const int row = arow % rpg;                 // request row of this thread
-      const bool valid = row < nrows;
-      const int r = valid ? sh.row_req[row] : 0;
-      const float invT = sh.row_invT[row];
-      const bool greedy = (invT == 0.0f);
-      const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
-      const unsigned short *uptr = (const unsigned short *)a.U + urow;
-      const PhiloxKey key = a.key;                // round keys in registers for the hot loop
-      Race st;
-      race_init(st);
-      uint4 ucur[4], unext[4];
-      int tmine = nt0 + grp;                      // first tile of this thread
-      if (valid && tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, ucur);
-      for (int t = nt0; t < nt1; ++t) {
-        const uint32_t idx = it + (uint32_t)(t - nt0);
-        const int b = (int)(idx % kAccBufs);
-        const uint32_t ause = idx / kAccBufs;
-        if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
-        if (t != tmine) {                         // another replica group owns this tile
+          uint32_t acc[32];
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
+          tmem_wait_ld();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acce + 8 * b);
-          continue;
+          tmine += F;
+          if (!valid) continue;
+          if (tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, unext, pol_stream);   // prefetch
+          const int c0 = t * kTileN + half * 32;
+          const bool full = (c0 + 32 <= V);
+          uint32_t w[32];
+          if (!greedy) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {           // eight independent Philox blocks: ILP
+              const uint4 wq = philox(a.key, (uint32_t)(c0 >> 2) + (uint32_t)q, (uint32_t)k, (uint32_t)r, kTagDraft);
+              w[4 * q] = wq.x;
+              w[4 * q + 1] = wq.y;
+              w[4 * q + 2] = wq.z;
+              w[4 * q + 3] = wq.w;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t pk[4] = {ucur[g].x, ucur[g].y, ucur[g].z, ucur[g].w};
+            float sv[8];
+            uint32_t packed[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float z0 = __uint_as_float(pk[e >> 1] << 16) + __uint_as_float(acc[g * 8 + e]);
+              const float z1 = __uint_as_float(pk[e >> 1] & 0xffff0000u) + __uint_as_float(acc[g * 8 + e + 1]);
+              const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
+              packed[e >> 1] = *reinterpret_cast<const uint32_t *>(&zb);
+              const float2 zf = __bfloat1622float2(zb);
+              sv[e] = greedy ? zf.x : zf.x * invT;
+              sv[e + 1] = greedy ? zf.y : zf.y * invT;
+            }
+            if (!full) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (c0 + g * 8 + e >= V) sv[e] = -INFINITY;
+            }
+            if (a.draft_logits && (full || c0 + g * 8 + 8 <= V))
+              st_u4_hint((unsigned short *)a.draft_logits + urow + c0 + g * 8,
+                         make_uint4(packed[0], packed[1], packed[2], packed[3]), pol_stream);
+            if (greedy) {
+              argmax_update<8>(st, sv, c0 + g * 8);
+            } else {
+              const uint32_t wg[8] = {w[8 * g], w[8 * g + 1], w[8 * g + 2], w[8 * g + 3],
+                                      w[8 * g + 4], w[8 * g + 5], w[8 * g + 6], w[8 * g + 7]};
+              race_update<8>(st, sv, wg, c0 + g * 8);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
         }
-        tc_fence_after();
-        uint32_t acc[32];
-        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acce + 8 * b);
-        tmine += F;
-        if (!valid) continue;
-        if (tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, unext);   // prefetch
-        const int c0 = t * kTileN + half * 32;
-        const bool full = (c0 + 32 <= V);
-        uint32_t w[32];
-        if (!greedy) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {             // eight independent Philox blocks: ILP
-            const uint4 wq = philox(key, (uint32_t)(c0 >> 2) + (uint32_t)q, (uint32_t)k, (uint32_t)r, kTagDraft);
-            w[4 * q] = wq.x;
-            w[4 * q + 1] = wq.y;
-            w[4 * q + 2] = wq.z;
-            w[4 * q + 3] = wq.w;
-          }
+        // merge the 2F thread partials of each row (replica groups x column halves); the row's
+        // home thread folds its maximum into the packed (score, index) key of the position with one
+        // 64-bit atomicMax -- all the next position needs -- and keeps its softmax partial for the
+        // normaliser, which the finalize kernel merges once per call
+        sh.part[(grp * 2 + half) * rpg + row] = to_partial(st);
+        named_sync_epi();
+        if (grp == 0 && half == 0 && valid) {
+          for (int q = 1; q < 2 * F; ++q) race_merge(st, from_partial(sh.part[q * rpg + row]));
+          if (st.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(st.best, st.idx));
+          a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j] =
+              to_partial(st);
         }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t pk[4] = {ucur[g].x, ucur[g].y, ucur[g].z, ucur[g].w};
-          float sv[8];
-          uint32_t packed[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float z0 = __uint_as_float(pk[e >> 1] << 16) + __uint_as_float(acc[g * 8 + e]);
-            const float z1 = __uint_as_float(pk[e >> 1] & 0xffff0000u) + __uint_as_float(acc[g * 8 + e + 1]);
-            const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
-            packed[e >> 1] = *reinterpret_cast<const uint32_t *>(&zb);
-            const float2 zf = __bfloat1622float2(zb);
-            sv[e] = greedy ? zf.x : zf.x * invT;
-            sv[e + 1] = greedy ? zf.y : zf.y * invT;
-          }
-          if (!full) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (c0 + g * 8 + e >= V) sv[e] = -INFINITY;
-          }
-          if (a.draft_logits && (full || c0 + g * 8 + 8 <= V)) {
-            uint4 *dst = (uint4 *)((unsigned short *)a.draft_logits + urow + c0 + g * 8);
-            *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          }
-          if (greedy) {
-            argmax_update<8>(st, sv, c0 + g * 8);
-          } else {
-            const uint32_t wg[8] = {w[8 * g], w[8 * g + 1], w[8 * g + 2], w[8 * g + 3],
-                                    w[8 * g + 4], w[8 * g + 5], w[8 * g + 6], w[8 * g + 7]};
-            race_update<8>(st, sv, wg, c0 + g * 8);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
       }
-      // merge the 2F thread partials of each row (replica groups x column halves); the row's
-      // home thread folds its maximum into the packed (score, index) key of the position with one
-      // 64-bit atomicMax -- all the next position needs -- and keeps its softmax partial for the
-      // normaliser, which the finalize kernel merges once per call
-      sh.part[(grp * 2 + half) * rpg + row] = to_partial(st);
+      // this CTA is done with position k (every CTA arrives, with or without work)
+      __threadfence();
       named_sync_epi();
-      if (grp == 0 && half == 0 && valid) {
-        for (int q = 1; q < 2 * F; ++q) race_merge(st, from_partial(sh.part[q * rpg + row]));
-        if (st.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(st.best, st.idx));
-        a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * gm + j] = to_partial(st);
-      }
+      if (et == 0) atomicAdd(a.gbar + k, 1);
     }
-    it += (uint32_t)(nt1 - nt0);
   }
 
-  // ---- teardown: drain issued MMAs and copies, free TMEM ---------------------
+  // ---- teardown: drain issued MMAs and copies, free TMEM -----------------------
   if (warp == 1) {
     if (lane == 0) {
       mma_commit(bar_drain);
@@ -555,18 +647,36 @@ cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_tc_step, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static bool attr_set[5] = {false, false, false, false, false};
+  const int rch = (int)(a.rank / 64);
+  void *fn = nullptr;
+  switch (rch) {
+    case 1: fn = (void *)draft_tc_persistent<1>; break;
+    case 2: fn = (void *)draft_tc_persistent<2>; break;
+    case 3: fn = (void *)draft_tc_persistent<3>; break;
+    default: fn = (void *)draft_tc_persistent<4>; break;
+  }
+  if (!attr_set[rch]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[rch] = true;
   }
   const int grid = num_sms > 1024 ? 1024 : num_sms;
-  for (int k = 1; k <= (int)a.K_max; ++k) {
-    draft_tc_step<<<grid, kThreadsTc, kSmemBytes, s>>>(a, tmap, k);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  // cooperative launch: all CTAs are co-resident, so the bounded grid barrier between
+  // positions can always complete
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[2] = {(void *)&a, (void *)&tmap};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return e;
   const int64_t items = a.B * a.K_max;
   const int fblocks = (int)((items + 7) / 8 < 4096 ? (items + 7) / 8 : 4096);
   draft_tc_finalize<<<fblocks, 256, 0, s>>>(a, grid);

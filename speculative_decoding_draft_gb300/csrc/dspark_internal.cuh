@@ -324,6 +324,7 @@ struct DraftArgs {
   int32_t *nact;      // [K_max + 2] active requests per position
   int32_t *counters;  // [B] per-row arrival counters (zero between steps)
   unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path
+  int32_t *gbar;      // [K_max + 1] grid-barrier arrival counters of the tensor-core path
   Partial *partials;  // [partial_slots]
   int64_t partial_slots;
 };
