@@ -44,7 +44,7 @@ STATUS = {
 }
 
 F32, BF16 = 0, 1
-TAG_DRAFT, TAG_ACCEPT, TAG_RESID = 0, 1, 2
+TAG_DRAFT, TAG_ACCEPT, TAG_RESID, TAG_DRAFT_PICK, TAG_RESID_PICK = 0, 1, 2, 3, 4
 
 
 class OracleError(RuntimeError):
@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
         L.dso_verify_ragged.restype = i32
         L.dso_row_lse.argtypes = [P, i32, i64, i64, P, P]
         L.dso_row_lse.restype = i32
+        L.dso_block_race.argtypes = [P, P, i64, u64, u32, u32, u32, u32, P, P, P, P]
+        L.dso_block_race.restype = i64
         _lib = L
     return _lib
 
@@ -161,6 +163,24 @@ def gumbel(w):
 
 def round_bf16(x):
     return float(lib().dso_round_bf16(float(x)))
+
+
+def block_race(log_w, seed, position, request, tag_block, tag_pick, log_err=None):
+    """Two-level categorical draw over weights exp(log_w) (-inf = zero weight).
+
+    Returns dict(pick, block, score, margin, near_block, near_pick, near_err).
+    """
+    lw = _c(log_w, np.float64)
+    le = None if log_err is None else _c(log_err, np.float64)
+    blk = ctypes.c_int64(0)
+    score = ctypes.c_double(0)
+    margin = ctypes.c_double(0)
+    near = np.zeros(3, np.int32)
+    pick = lib().dso_block_race(_ptr(lw), _ptr(le), lw.size, int(seed), int(position), int(request),
+                                int(tag_block), int(tag_pick), ctypes.byref(blk), ctypes.byref(score),
+                                ctypes.byref(margin), _ptr(near))
+    return dict(pick=int(pick), block=int(blk.value), score=score.value, margin=margin.value,
+                near_block=bool(near[0]), near_pick=bool(near[1]), near_err=bool(near[2]))
 
 
 # ---------------------------------------------------------------------------

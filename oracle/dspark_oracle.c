@@ -34,11 +34,24 @@
  *   tag     DRAFT = 0 (draft sampling, position k = 1..K_r),
  *           ACCEPT = 1 (accept uniform, position j = 1..ell_r, c0 = 0, word 0),
  *           RESID = 2 (residual at the rejecting position j, or bonus at
- *                      position ell_r + 1)
- *   element v uses word (v & 3) of the block with c0 = v >> 2
+ *                      position ell_r + 1),
+ *           DRAFT_PICK = 3, RESID_PICK = 4 (the in-block draw of the
+ *                      two-level sampler below, same positions)
+ *   index i of a stream uses word (i & 3) of the block with c0 = i >> 2
  *   gumbel uniform  u = ((w >> 9) + 0.5) * 2^-23  in (0, 1), exact in fp32
  *   accept uniform  u = (w >> 8) * 2^-24          in [0, 1), exact in fp32
  *   gumbel noise    g = -log(-log(u))
+ *
+ * Categorical sampling (the pages only say "sample"; this is the reading both
+ * implementations follow).  Weights w_v >= 0 over v = 0..n-1 are cut into
+ * 32-wide blocks g = v >> 5.  Block g with mass L_g = sum of its weights gets
+ * the score log L_g + gumbel(word g of the tag's stream); the block with the
+ * largest score wins (ties: smaller g), and inside it the element is the
+ * first v whose running weight sum exceeds u' * L_g, u' the accept-style
+ * uniform of word g of the PICK stream.  This draws v with probability
+ * w_v / sum(w) exactly: the Gumbel-max over blocks picks block g with
+ * probability L_g / sum(L) and the inverse-CDF step picks v within it with
+ * probability w_v / L_g.  It needs one random word per 32 elements.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -63,12 +76,14 @@ enum {
 };
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
-enum { TAG_DRAFT = 0, TAG_ACCEPT = 1, TAG_RESID = 2 };
+enum { TAG_DRAFT = 0, TAG_ACCEPT = 1, TAG_RESID = 2, TAG_DRAFT_PICK = 3, TAG_RESID_PICK = 4 };
 
 #define ORC_MAX_K 16
 #define ORC_MIN_POS_T 1e-3
 #define ORC_SAMPLE_TIE 1e-4 /* sampling near-tie margin (score units) */
 #define ORC_ACCEPT_TIE 1e-5 /* |u - min(1, p/q)| near-tie margin        */
+#define ORC_PICK_TIE 1e-5   /* |u' - cumulative fraction| near-tie margin */
+#define ORC_BLOCK 32        /* block width of the two-level sampler       */
 
 /* ---------------------------------------------------------------------- */
 /* Philox4x32-10 [PRX S4].                                                 */
@@ -187,6 +202,104 @@ static void set_threads(int nthreads) {
 }
 
 /* ---------------------------------------------------------------------- */
+/* Two-level categorical sampler (see the stream specification above).      */
+/* lw[v]: log-weights (-INFINITY for zero weight).  le[v] (optional): log of */
+/* an absolute uncertainty on w_v (how far an fp32 evaluation may be off);    */
+/* -INFINITY or NULL for none.  Reports whether a rounding-sized change could */
+/* move the decision: near_block (runner-up block score within               */
+/* ORC_SAMPLE_TIE * max(1, |score|)), near_pick (u' within ORC_PICK_TIE of a   */
+/* cumulative boundary of the winning block), near_err (the decision moves   */
+/* within the uncertainty le).                                              */
+/* Pins: Monte-Carlo law against w / sum(w) on ragged block counts, single-  */
+/* block and single-element limits, scale invariance.                      */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t pick, block;
+  double score, margin;
+  int near_block, near_pick, near_err;
+} race_t;
+
+static race_t block_race(const double *lw, const double *le, int64_t n, uint64_t seed, uint32_t pos,
+                         uint32_t rid, uint32_t tag_block, uint32_t tag_pick) {
+  race_t o = {-1, -1, -INFINITY, INFINITY, 0, 0, 0};
+  const int64_t nb = (n + ORC_BLOCK - 1) / ORC_BLOCK;
+  double *t = (double *)malloc(sizeof(double) * (size_t)nb);    /* block score                    */
+  double *hi = (double *)malloc(sizeof(double) * (size_t)nb);   /* score with the mass raised by le */
+  double *lo = (double *)malloc(sizeof(double) * (size_t)nb);   /* score with the mass lowered     */
+  for (int64_t g = 0; g < nb; ++g) {
+    const int64_t v0 = g * ORC_BLOCK, v1 = (v0 + ORC_BLOCK < n) ? v0 + ORC_BLOCK : n;
+    double ref = -INFINITY;
+    for (int64_t v = v0; v < v1; ++v) {
+      if (lw[v] > ref) ref = lw[v];
+      if (le && le[v] > ref) ref = le[v];
+    }
+    t[g] = hi[g] = lo[g] = -INFINITY;
+    if (ref == -INFINITY) continue;
+    double lam = 0.0, er = 0.0;
+    for (int64_t v = v0; v < v1; ++v) {
+      lam += exp(lw[v] - ref);
+      if (le) er += exp(le[v] - ref);
+    }
+    const double noise = dso_gumbel(dso_stream_word(seed, (uint64_t)g, pos, rid, tag_block));
+    if (lam > 0.0) t[g] = ref + log(lam) + noise;
+    hi[g] = ref + log(lam + er) + noise;
+    if (lam > er) lo[g] = ref + log(lam - er) + noise;
+    if (t[g] > o.score) { o.score = t[g]; o.block = g; }
+  }
+  if (o.block >= 0) {
+    const int64_t gs = o.block;
+    const double tol = ORC_SAMPLE_TIE * fmax(1.0, fabs(o.score));
+    double second = -INFINITY;
+    for (int64_t g = 0; g < nb; ++g) {
+      if (g == gs) continue;
+      if (t[g] > second) second = t[g];
+      if (hi[g] >= lo[gs] - tol) o.near_err = 1;
+    }
+    o.margin = o.score - second;
+    o.near_block = o.margin <= tol;
+    /* in-block inverse CDF */
+    const int64_t v0 = gs * ORC_BLOCK, v1 = (v0 + ORC_BLOCK < n) ? v0 + ORC_BLOCK : n;
+    double ref = -INFINITY;
+    for (int64_t v = v0; v < v1; ++v) if (lw[v] > ref) ref = lw[v];
+    double lam = 0.0, er = 0.0;
+    for (int64_t v = v0; v < v1; ++v) {
+      lam += exp(lw[v] - ref);
+      if (le) er += exp(le[v] - ref);
+    }
+    const double u = dso_uniform_accept(dso_stream_word(seed, (uint64_t)gs, pos, rid, tag_pick));
+    double P = 0.0, dmin = INFINITY;
+    int64_t last = -1;
+    for (int64_t v = v0; v < v1; ++v) {
+      const double w = exp(lw[v] - ref) / lam;
+      if (w > 0.0) last = v;
+      P += w;
+      if (o.pick < 0 && P > u) o.pick = v;
+      if (fabs(P - u) < dmin) dmin = fabs(P - u);
+    }
+    if (o.pick < 0) o.pick = last;   /* only when u sits within rounding of 1 */
+    o.near_pick = dmin < ORC_PICK_TIE;
+    if (dmin < ORC_PICK_TIE + 2.0 * er / lam) o.near_err = 1;
+  }
+  o.near_err = o.near_err || o.near_block || o.near_pick;
+  free(t);
+  free(hi);
+  free(lo);
+  return o;
+}
+
+/* Exposed for the sampler's own pins: returns the pick and the diagnostics. */
+int64_t dso_block_race(const double *lw, const double *le, int64_t n, uint64_t seed, uint32_t pos,
+                       uint32_t rid, uint32_t tag_block, uint32_t tag_pick, int64_t *block, double *score,
+                       double *margin, int32_t *near) {
+  race_t o = block_race(lw, le, n, seed, pos, rid, tag_block, tag_pick);
+  if (block) *block = o.block;
+  if (score) *score = o.score;
+  if (margin) *margin = o.margin;
+  if (near) { near[0] = o.near_block; near[1] = o.near_pick; near[2] = o.near_err; }
+  return o.pick;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Draft: Markov-head semi-autoregressive sampling.                        */
 /* [DSP S3.1], [ZTD S6]:                                                   */
 /*   p_k(v | x_0, x_<k) = softmax(U_k(v) + B(x_{k-1}, v)),                  */
@@ -198,17 +311,29 @@ static void set_threads(int nthreads) {
 /*     nearest-even from the exact value) and the draft samples from those  */
 /*     stored logits, so verification sees exactly the sampled distribution;*/
 /*   - temperature T divides the biased logit; T = 0 means argmax;          */
-/*   - sampling is Gumbel-max on the stream (seed, k, request, DRAFT);      */
-/*   - ties go to the smallest vocabulary index.                            */
+/*   - sampling is the two-level sampler of the stream specification on the */
+/*     weights exp(z / T), streams (seed, k, request, DRAFT / DRAFT_PICK);   */
+/*   - T = 0: the largest logit, ties to the smallest vocabulary index.     */
 /* Outputs per (request, position): token, log-sum-exp of z/T (the draft    */
-/* distribution's normaliser; for T = 0 the largest logit), top-2 margin,   */
-/* near-tie flags: bit0 sampling margin < 1e-4 (fp32 storage or T > 0),      */
-/* bit1 a bf16 rounding ambiguity could change the token, bit2 a bf16        */
-/* rounding ambiguity moves the log-sum-exp by more than 1e-6 relative.      */
+/* distribution's normaliser; for T = 0 the largest logit), margin (block   */
+/* scores for T > 0, top-2 logits for T = 0), near-tie flags: bit0 block or */
+/* greedy margin within tolerance (greedy: fp32 storage only), bit1 a bf16   */
+/* rounding ambiguity could change the token, bit2 a bf16 rounding           */
+/* ambiguity moves the log-sum-exp by more than 1e-6 relative, bit3 the      */
+/* in-block draw sits within 1e-5 of a cumulative boundary.                 */
 /* Pins: exact joint law by enumeration vs Monte Carlo; zero bias equals    */
 /* independent sampling; one-hot rank-1 transition; hand-computed logits;   */
 /* normalisation of the log-sum-exp.                                        */
 /* ---------------------------------------------------------------------- */
+/* log sum_v exp(z_v / T), fp64 */
+static double row_lse_scaled(const double *z, int64_t V, double T) {
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) if (z[v] / T > m) m = z[v] / T;
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v) S += exp(z[v] / T - m);
+  return m + log(S);
+}
+
 int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dtype,
                             const int32_t *anchor, const int32_t *K_r, const float *temperature,
                             const int64_t *req_id, uint64_t seed,
@@ -229,6 +354,8 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
   for (b = 0; b < B; ++b) {
     double *bias = (double *)malloc(sizeof(double) * (size_t)V);
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    double *lw = (double *)malloc(sizeof(double) * (size_t)V);
+    double *le = (double *)malloc(sizeof(double) * (size_t)V);
     uint32_t rid = (uint32_t)(req_id ? req_id[b] : b);
     int32_t x_prev = anchor[b];
     double T = (double)temperature[b];
@@ -247,42 +374,59 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
         z[v] = (dtype == ORC_F32) ? (double)(float)exact : round_bf16(exact);
       }
       if (draft_logits) for (int64_t v = 0; v < V; ++v) store_elem(draft_logits, dtype, ubase + v, z[v]);
-      /* scores */
-      int64_t best = -1, second = -1;
-      double sb = -INFINITY, ss = -INFINITY;
-      double m = -INFINITY;
-      for (int64_t v = 0; v < V; ++v) {
-        double s = (T > 0.0) ? z[v] / T + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)k, rid, TAG_DRAFT))
-                             : z[v];
-        if (best < 0 || s > sb) { ss = sb; second = best; sb = s; best = v; }
-        else if (second < 0 || s > ss) { ss = s; second = v; }
-        double zt = (T > 0.0) ? z[v] / T : z[v];
-        if (zt > m) m = zt;
-      }
-      double l;
-      if (T > 0.0) {
-        double S = 0.0;
-        for (int64_t v = 0; v < V; ++v) S += exp(z[v] / T - m);
-        l = m + log(S);
-      } else {
-        l = z[best];
-      }
+      int64_t best;
+      double l, mg;
       uint8_t f = 0;
-      double mg = sb - ss;
-      if ((T > 0.0 || dtype == ORC_F32) && mg < ORC_SAMPLE_TIE) f |= 1;
-      if (dtype == ORC_BF16) {
-        double lse_shift = 0.0;
+      if (T > 0.0) {
+        /* two-level sampler on the weights exp(z / T); a bf16 rounding ambiguity */
+        /* enters as the uncertainty |exp(alt / T) - exp(z / T)| of its weight.  */
+        int amb = 0;
         for (int64_t v = 0; v < V; ++v) {
-          double exact = load_elem(U, dtype, ubase + v) + bias[v];
-          double alt;
-          if (!bf16_ambiguous(exact, &alt)) continue;
-          double noise = (T > 0.0) ? dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)k, rid, TAG_DRAFT)) : 0.0;
-          double s_alt = (T > 0.0) ? alt / T + noise : alt;
-          if (v == best) { if (s_alt <= ss + ORC_SAMPLE_TIE) f |= 2; }
-          else if (s_alt >= sb - ORC_SAMPLE_TIE) f |= 2;
-          if (T > 0.0) lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
+          lw[v] = z[v] / T;
+          le[v] = -INFINITY;
+          if (dtype == ORC_BF16) {
+            double alt;
+            if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) {
+              le[v] = lw[v] + log(fabs(expm1((alt - z[v]) / T)));
+              amb = 1;
+            }
+          }
         }
-        if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
+        race_t rc = block_race(lw, amb ? le : NULL, V, seed, (uint32_t)k, rid, TAG_DRAFT, TAG_DRAFT_PICK);
+        best = rc.pick;
+        mg = rc.margin;
+        if (rc.near_block) f |= 1;
+        if (rc.near_pick) f |= 8;
+        if (rc.near_err && !(f & 9)) f |= 2;
+        l = row_lse_scaled(z, V, T);
+        if (dtype == ORC_BF16) {
+          double lse_shift = 0.0;
+          for (int64_t v = 0; v < V; ++v) {
+            double alt;
+            if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt))
+              lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
+          }
+          if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
+        }
+      } else {
+        /* greedy: largest logit, smallest index on ties */
+        int64_t second = -1;
+        best = 0;
+        for (int64_t v = 1; v < V; ++v) {
+          if (z[v] > z[best]) { second = best; best = v; }
+          else if (second < 0 || z[v] > z[second]) second = v;
+        }
+        mg = z[best] - z[second];
+        l = z[best];
+        if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE) f |= 1;
+        if (dtype == ORC_BF16) {
+          for (int64_t v = 0; v < V; ++v) {
+            double alt;
+            if (!bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) continue;
+            if (v == best) { if (alt <= z[second] + ORC_SAMPLE_TIE) f |= 2; }
+            else if (alt >= z[best] - ORC_SAMPLE_TIE) f |= 2;
+          }
+        }
       }
       draft_tok[slot] = (int32_t)best;
       if (lse) lse[slot] = l;
@@ -292,6 +436,8 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
     }
     free(bias);
     free(z);
+    free(lw);
+    free(le);
   }
   return ORC_OK;
 }
@@ -389,12 +535,14 @@ int dso_schedule_survival(const float *conf, const int32_t *K_r, const double *s
 /* the bonus; tgt_off[r+1] - tgt_off[r] = ell_r + 1.                         */
 /* Readings: q and p both use the request's temperature; T = 0 means greedy */
 /* (accept iff x_j is the argmax of p_j, correction/bonus = argmax of p);    */
-/* the residual is sampled by Gumbel-max of log(p_v - q_v) over p_v > q_v    */
-/* on stream (seed, j, request, RESID); if no element has p_v > q_v in       */
-/* floating point the correction is sampled from p instead (rounding guard);  */
-/* the bonus is Gumbel-max of z/T on stream (seed, ell+1, request, RESID).    */
+/* the residual is drawn by the two-level sampler on the weights            */
+/* max(0, p_v - q_v), streams (seed, j, request, RESID / RESID_PICK); if no    */
+/* element has p_v > q_v in floating point the correction is drawn from p    */
+/* instead (rounding guard); the bonus is the two-level sampler on exp(z/T)  */
+/* of the next target row, streams (seed, ell+1, request, RESID / RESID_PICK).*/
 /* Flags per request: bit0 an accept decision with |u - min(1, p/q)| < 1e-5,  */
-/* bit1 the correction/bonus sample has top-2 margin < 1e-4, bit2 the        */
+/* bit1 the correction/bonus draw is within rounding of another outcome     */
+/* (block scores, in-block boundary, or the fp32 error of p - q), bit2 the   */
 /* residual mass was below 1e-5 (rounding guard region).  flag_pos is the   */
 /* first position whose decision is flagged (ell + 1 for the final sample),  */
 /* 0 when unflagged.                                                         */
@@ -452,7 +600,8 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
   for (r = 0; r < B; ++r) {
     double *st = (double *)malloc(sizeof(double) * (size_t)V);
     double *sd = (double *)malloc(sizeof(double) * (size_t)V);
-    double *sc = (double *)malloc(sizeof(double) * (size_t)V);
+    double *lw = (double *)malloc(sizeof(double) * (size_t)V);
+    double *le = (double *)malloc(sizeof(double) * (size_t)V);
     uint32_t rid = (uint32_t)(req_id ? req_id[r] : r);
     const double T = (double)temperature[r];
     const int64_t l = ell[r];
@@ -484,25 +633,30 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
       if (!accept) {
         rejected = 1;
         if (T > 0.0) {
+          /* residual weights max(0, p - q); each carries the uncertainty of an fp32 */
+          /* evaluation of p - q (relative 4e-6 of p + q plus the exponent rounding)  */
           double lt = row_lse(st, V), ld = row_lse(sd, V);
           double mass = 0.0;
           int any = 0;
           for (int64_t v = 0; v < V; ++v) {
-            double res = exp(st[v] - lt) - exp(sd[v] - ld);
-            if (res > 0.0) {
-              mass += res;
-              any = 1;
-              sc[v] = log(res) + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)j, rid, TAG_RESID));
-            } else {
-              sc[v] = -INFINITY;
-            }
+            double p = exp(st[v] - lt), q = exp(sd[v] - ld);
+            double res = p - q;
+            double err = 4e-6 * (p + q) + 6e-8 * (fabs(st[v] - lt) * p + fabs(sd[v] - ld) * q);
+            lw[v] = res > 0.0 ? log(res) : -INFINITY;
+            le[v] = err > 0.0 ? log(err) : -INFINITY;
+            if (res > 0.0) { mass += res; any = 1; }
           }
           if (mass < 1e-5 && !fpos) { f |= 4; fpos = (int32_t)j; }
-          if (!any)
-            for (int64_t v = 0; v < V; ++v)
-              sc[v] = st[v] + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)j, rid, TAG_RESID));
-          token = (int32_t)row_argmax(sc, V, &mg);
-          if (mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)j; }
+          race_t rc;
+          if (any) {
+            rc = block_race(lw, le, V, seed, (uint32_t)j, rid, TAG_RESID, TAG_RESID_PICK);
+            if (rc.near_err && !fpos) { f |= 2; fpos = (int32_t)j; }
+          } else {
+            rc = block_race(st, NULL, V, seed, (uint32_t)j, rid, TAG_RESID, TAG_RESID_PICK);
+            if (rc.near_err && !fpos) { f |= 2; fpos = (int32_t)j; }
+          }
+          token = (int32_t)rc.pick;
+          mg = rc.margin;
         } else {
           token = (int32_t)row_argmax(st, V, &mg);
           if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)j; }
@@ -515,10 +669,10 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
     if (!rejected) {
       row_scaled(tgt_logits, dtype, (int64_t)tgt_off[r] + l, V, T, st);
       if (T > 0.0) {
-        for (int64_t v = 0; v < V; ++v)
-          sc[v] = st[v] + dso_gumbel(dso_stream_word(seed, (uint64_t)v, (uint32_t)(l + 1), rid, TAG_RESID));
-        token = (int32_t)row_argmax(sc, V, &mg);
-        if (mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)(l + 1); }
+        race_t rc = block_race(st, NULL, V, seed, (uint32_t)(l + 1), rid, TAG_RESID, TAG_RESID_PICK);
+        token = (int32_t)rc.pick;
+        mg = rc.margin;
+        if (rc.near_err && !fpos) { f |= 2; fpos = (int32_t)(l + 1); }
       } else {
         token = (int32_t)row_argmax(st, V, &mg);
         if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE && !fpos) { f |= 2; fpos = (int32_t)(l + 1); }
@@ -532,7 +686,8 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
     if (sample_margin) sample_margin[r] = mg;
     free(st);
     free(sd);
-    free(sc);
+    free(lw);
+    free(le);
   }
   return ORC_OK;
 }
