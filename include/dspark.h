@@ -30,13 +30,21 @@
  *   - All randomness comes from one counter-based stream, Philox4x32-10
  *     (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11):
  *       key = (seed low 32 bits, seed high 32 bits),
- *       counter = (v >> 2 | 0, position, request, tag), word (v & 3) for element v,
- *       tag 0 = draft sampling (position k), 1 = accept uniform (position j,
- *       counter word 0 = 0, word 0), 2 = residual / bonus sample (the rejecting
- *       position j, or ell_r + 1 for the bonus);
+ *       counter = (i >> 2, position, request, tag), word (i & 3) for stream index i,
+ *       tag 0 = draft block noise (position k), 1 = accept uniform (position j,
+ *       i = 0), 2 = residual / bonus block noise (the rejecting position j, or
+ *       ell_r + 1 for the bonus), 3 and 4 = the in-block draws of tags 0 and 2;
  *       Gumbel uniform u = ((w >> 9) + 0.5) * 2^-23, g = -log(-log u);
  *       accept uniform u = (w >> 8) * 2^-24.
  *     Requests are identified by their index r in the call.
+ *   - Categorical draws ("sample v with probability w_v / sum w"; the pages fix
+ *     no mechanism) use a two-level draw over blocks of 32 indices: block
+ *     g = v >> 5 with mass L_g enters a Gumbel race with score
+ *     log L_g - log(-log u_g), u_g the Gumbel uniform of stream index g; the
+ *     block with the largest score wins (ties to the smaller g), and inside it
+ *     the first v whose running weight sum exceeds u'_g L_g is drawn, u'_g the
+ *     accept uniform of stream index g of the in-block tag.  The draw has law
+ *     w / sum(w) exactly and needs one random word per 32 indices.
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -69,6 +77,7 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 
 /* dims.flags bits */
 #define DSPARK_FLAG_FORCE_SIMT 1u /* draft: use the CUDA-core bias path even when the tensor-core path applies */
+#define DSPARK_FLAG_W_PACKED 2u   /* draft: W is the packed projection of dspark_draft_pack_projection */
 
 typedef struct {
   int64_t B;      /* requests in the call                                  */
@@ -86,13 +95,15 @@ typedef struct {
  * For each request r and position k = 1..K_r[r], left to right:
  *   z_k(v) = U[r, k-1, v] + sum_i E[x_{k-1}, i] * W[i, v]     (x_0 = anchor[r])
  *   stored in the call dtype (bf16 values are rounded to nearest even), then
- *   x_k = argmax_v ( z_k(v) / T_r + g(seed, k, r, v) )         (T_r > 0)
- *   x_k = argmax_v z_k(v)                                      (T_r = 0)
- * ties to the smallest v.  This samples x_k ~ softmax(z_k / T_r).
+ *   x_k ~ softmax(z_k / T_r) by the two-level draw (streams tag 0 and 3,
+ *   position k)                                                (T_r > 0)
+ *   x_k = argmax_v z_k(v), ties to the smallest v              (T_r = 0)
  *
  *   U            [B, K_max, V]  base logits of the parallel backbone.
  *   E            [V, rank]      W1, the Markov embedding table (row per previous token).
- *   W            [rank, V]      W2, the logit projection.
+ *   W            [rank, V]      W2, the logit projection; or, with
+ *                DSPARK_FLAG_W_PACKED, the packed projection written by
+ *                dspark_draft_pack_projection (tensor-core path only).
  *   anchor       [B] int32      x_0, the previous round's bonus/correction token.
  *   K_r          [B] int32      draft length per request, 1..K_max.
  *   temperature  [B] float      T_r: 0 (greedy) or >= 1e-3.
@@ -102,13 +113,40 @@ typedef struct {
  *   draft_lse    [B, K_max] float out, optional: log sum_v exp(z_k(v) / T_r), the
  *                draft distribution's normaliser (for T_r = 0: max_v z_k(v));
  *                entries k > K_r are not written.
- *   workspace    >= dspark_draft_workspace_bytes(B, K_max, V) bytes, 256-byte aligned.
+ *   workspace    >= dspark_draft_workspace_bytes(dims) bytes (the same dims and
+ *                flags as the call), 256-byte aligned.
  * The tensor-core path is used when dtype = DSPARK_BF16, rank is a multiple of
- * 64 and <= 256, V is a multiple of 8 and the device is sm_103; otherwise (or
- * with DSPARK_FLAG_FORCE_SIMT) the CUDA-core path runs.  Both give the same
- * tokens except where two perturbed scores are within fp32 rounding.
+ * 64 and <= 256, V is a multiple of 8, U, E, W and draft_logits are 16-byte
+ * aligned and the device is sm_103; otherwise (or with DSPARK_FLAG_FORCE_SIMT)
+ * the CUDA-core path runs.  Without DSPARK_FLAG_W_PACKED the tensor-core path
+ * first packs W into the workspace (one read and one write of W per call);
+ * weights that stay fixed across calls should be packed once instead.  A packed
+ * W with a call that cannot take the tensor-core path returns
+ * DSPARK_ERR_UNSUPPORTED.  Both paths give the same tokens except where a
+ * decision is within fp32 rounding.
  * ------------------------------------------------------------------------ */
-size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V);
+size_t dspark_draft_workspace_bytes(dspark_dims dims);
+
+/* ------------------------------------------------------------------------
+ * Packed projection for the tensor-core draft path (no counterpart on the
+ * pages: a storage layout of W2 = W).
+ *
+ * W_packed holds rank/64 x ceil(V/64) blocks of 8 KB; block (c, t), at byte
+ * offset (c * ceil(V/64) + t) * 8192, holds W[64c + i, 64t + n] for i, n < 64 as
+ * 64 rows of 128 bytes (row i = rank index 64c + i), and within row i the 16-byte
+ * unit at position u holds columns 64t + 8 (u ^ (i & 7)) .. + 7 (the 128-byte
+ * swizzle of the tensor-core operand).  Columns past V are zero.
+ *   dspark_draft_packed_projection_bytes: the size, or 0 when rank is not a
+ *     multiple of 64 in 64..256 or V is not a multiple of 8.
+ *   dspark_draft_pack_projection: W [rank, V] bf16 (dims.rank, dims.V, dims.dtype;
+ *     16-byte aligned) -> W_packed (256-byte aligned, >= the size).  Errors:
+ *     DSPARK_ERR_UNSUPPORTED for shapes or dtypes without a packed layout,
+ *     DSPARK_ERR_WORKSPACE for a short or misaligned W_packed.
+ * ------------------------------------------------------------------------ */
+size_t dspark_draft_packed_projection_bytes(int64_t rank, int64_t V);
+
+dspark_status dspark_draft_pack_projection(const void *W, dspark_dims dims, void *W_packed, size_t packed_bytes,
+                                           void *stream);
 
 dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W,
                                          const int32_t *anchor, const int32_t *K_r,
@@ -183,11 +221,11 @@ dspark_status dspark_schedule_survival_noalloc(const float *conf, const int32_t 
  * For request r with temperature T and length ell_r, with
  *   q_j = softmax(draft_logits[r, j-1] / T),  p_j = softmax(tgt_logits[tgt_off[r]+j-1] / T):
  *   for j = 1..ell_r: accept x_j = draft_tok[r, j-1] iff u_j < min(1, p_j(x_j) / q_j(x_j)),
- *   u_j the accept uniform of (seed, j, r); stop at the first rejection and sample the
- *   correction by Gumbel-max of log(p_j - q_j) over {v : p_j(v) > q_j(v)} on stream
- *   (seed, j, r, tag 2) (from p_j if that set is empty in floating point); if every
- *   position is accepted, sample the bonus from row tgt_off[r] + ell_r by Gumbel-max
- *   of z / T on stream (seed, ell_r + 1, r, tag 2).
+ *   u_j the accept uniform of (seed, j, r); stop at the first rejection and draw the
+ *   correction from norm(max(0, p_j - q_j)) by the two-level draw on streams
+ *   (seed, j, r, tags 2 and 4) (from p_j if no p_j(v) > q_j(v) in floating point); if
+ *   every position is accepted, draw the bonus from softmax(z / T) of row
+ *   tgt_off[r] + ell_r on streams (seed, ell_r + 1, r, tags 2 and 4).
  *   T = 0: accept iff x_j is the argmax of p_j; correction and bonus are argmaxes.
  *
  *   draft_logits [B, K_max, V]   the logits the drafts were sampled from.

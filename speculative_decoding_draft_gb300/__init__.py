@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "DsparkError", "DsparkUnavailable", "lib", "library_path", "draft_markov_sample", "schedule_survival",
     "verify_ragged", "check", "status_string", "draft_workspace_bytes", "schedule_workspace_bytes",
-    "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "STATUS_NAMES", "Dims",
+    "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_W_PACKED", "STATUS_NAMES", "Dims",
+    "PackedProjection", "pack_projection", "packed_projection_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "libdspark.so")
 
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
+FLAG_W_PACKED = 2
 
 STATUS_NAMES = {
     0: "DSPARK_OK", 1: "DSPARK_ERR_NULL", 2: "DSPARK_ERR_DIMS", 3: "DSPARK_ERR_DTYPE",
@@ -40,7 +42,8 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = [
-    "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_schedule_workspace_bytes",
+    "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_draft_packed_projection_bytes",
+    "dspark_draft_pack_projection", "dspark_schedule_workspace_bytes",
     "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_verify_workspace_bytes",
     "dspark_verify_ragged",
     "dspark_status_string", "dspark_check", "dspark_version",
@@ -80,8 +83,12 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(_LIB_PATH)
     P, i64, u64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
     st = ctypes.c_int
-    L.dspark_draft_workspace_bytes.argtypes = [i64, i64, i64]
+    L.dspark_draft_workspace_bytes.argtypes = [Dims]
     L.dspark_draft_workspace_bytes.restype = sz
+    L.dspark_draft_packed_projection_bytes.argtypes = [i64, i64]
+    L.dspark_draft_packed_projection_bytes.restype = sz
+    L.dspark_draft_pack_projection.argtypes = [P, Dims, P, sz, P]
+    L.dspark_draft_pack_projection.restype = st
     L.dspark_draft_markov_sample.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
     L.dspark_draft_markov_sample.restype = st
     L.dspark_schedule_workspace_bytes.argtypes = [i64, i64]
@@ -158,8 +165,36 @@ def check(dev_status: torch.Tensor, stream=None) -> str:
     return STATUS_NAMES.get(code, f"DSPARK_ERR_{code}")
 
 
-def draft_workspace_bytes(B: int, K_max: int, V: int) -> int:
-    return int(lib().dspark_draft_workspace_bytes(B, K_max, V))
+def draft_workspace_bytes(B: int, K_max: int, V: int, rank: int, dtype: int = BF16, flags: int = 0) -> int:
+    return int(lib().dspark_draft_workspace_bytes(Dims(B, K_max, V, rank, dtype, flags)))
+
+
+def packed_projection_bytes(rank: int, V: int) -> int:
+    return int(lib().dspark_draft_packed_projection_bytes(rank, V))
+
+
+class PackedProjection:
+    """W2 in the packed tensor-core layout (dspark_draft_pack_projection): a uint8 device
+    tensor plus the shape it was packed from."""
+
+    def __init__(self, data: torch.Tensor, rank: int, V: int):
+        self.data, self.rank, self.V = data, rank, V
+        self.dtype = torch.bfloat16
+        self.device = data.device
+
+
+def pack_projection(W, *, stream=None) -> PackedProjection:
+    """Pack W2 [rank, V] bfloat16 once for the tensor-core draft path."""
+    _dev(W, "W", torch.bfloat16)
+    rank, V = W.shape
+    nbytes = packed_projection_bytes(rank, V)
+    if nbytes == 0:
+        raise DsparkError(13, "dspark_draft_pack_projection")
+    data = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    code = lib().dspark_draft_pack_projection(_ptr(W), Dims(1, 1, V, rank, BF16, 0), _ptr(data),
+                                             ctypes.c_size_t(nbytes), _stream(stream))
+    _raise(code, "dspark_draft_pack_projection")
+    return PackedProjection(data, rank, V)
 
 
 def schedule_workspace_bytes(B: int, K_max: int) -> int:
@@ -183,7 +218,8 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
                         stream=None) -> dict:
     """Markov-head draft sampling (C ABI dspark_draft_markov_sample).
 
-    U [B,K_max,V], E [V,rank], W [rank,V] (float32 or bfloat16, one dtype);
+    U [B,K_max,V], E [V,rank], W [rank,V] (float32 or bfloat16, one dtype) or a
+    PackedProjection of W (bfloat16, tensor-core path);
     anchor, K_r [B] int32; temperature [B] float32.  Returns a dict with
     draft_tok [B,K_max] int32, draft_logits (U's dtype) or None, draft_lse
     [B,K_max] float32 or None, and the status / workspace tensors used.
@@ -192,7 +228,14 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     B, K_max, V = U.shape
     rank = E.shape[1]
     _dev(E, "E", U.dtype, (V, rank))
-    _dev(W, "W", U.dtype, (rank, V))
+    flags = FLAG_FORCE_SIMT if force_simt else 0
+    if isinstance(W, PackedProjection):
+        if (W.rank, W.V) != (rank, V) or W.device != U.device or U.dtype != W.dtype:
+            raise ValueError(f"packed projection of shape ({W.rank}, {W.V}) does not fit U/E")
+        flags |= FLAG_W_PACKED
+        W = W.data
+    else:
+        _dev(W, "W", U.dtype, (rank, V))
     _dev(anchor, "anchor", torch.int32, (B,))
     _dev(K_r, "K_r", torch.int32, (B,))
     _dev(temperature, "temperature", torch.float32, (B,))
@@ -208,9 +251,9 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     if want_lse and lse is None:
         lse = torch.empty(B, K_max, dtype=torch.float32, device=dev)
     status = new_status(dev) if status is None else status
-    nbytes = draft_workspace_bytes(B, K_max, V)
+    nbytes = draft_workspace_bytes(B, K_max, V, rank, dt, flags)
     ws = _workspace(nbytes, dev, workspace)
-    dims = Dims(B, K_max, V, rank, dt, FLAG_FORCE_SIMT if force_simt else 0)
+    dims = Dims(B, K_max, V, rank, dt, flags)
     code = lib().dspark_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r), _ptr(temperature),
                                             ctypes.c_uint64(seed), dims, _ptr(tok), _ptr(logits), _ptr(lse),
                                             _ptr(ws), ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))

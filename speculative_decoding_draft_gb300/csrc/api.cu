@@ -12,7 +12,6 @@ namespace {
 constexpr int64_t kMaxB = 1 << 20;
 constexpr int64_t kMaxV = (int64_t)1 << 30;
 constexpr int64_t kMaxRank = 8192;
-constexpr int kDraftSimtChunk = 2048;        // must match draft_simt.cu
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -97,11 +96,42 @@ dspark_status dspark_check(int32_t *dev_status, void *stream) {
 // ---------------------------------------------------------------------------
 // draft
 // ---------------------------------------------------------------------------
-size_t dspark_draft_workspace_bytes(int64_t B, int64_t K_max, int64_t V) {
-  if (B < 1 || K_max < 1 || V < 2) return 0;
+// Does a call with these dims pack W2 into its workspace (tensor-core shape, W not
+// pre-packed, CUDA-core path not forced)?
+static bool draft_packs_into_workspace(const dspark_dims &d) {
+  return d.dtype == DSPARK_BF16 && d.rank >= 64 && d.rank <= 256 && d.rank % 64 == 0 && d.V % 8 == 0 &&
+         !(d.flags & (DSPARK_FLAG_FORCE_SIMT | DSPARK_FLAG_W_PACKED));
+}
+
+static size_t draft_ws_base(int64_t B, int64_t K_max, int64_t V) {
   return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
          al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
          al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V));
+}
+
+size_t dspark_draft_workspace_bytes(dspark_dims dims) {
+  if (check_dims(dims, true) != DSPARK_OK) return 0;
+  size_t n = draft_ws_base(dims.B, dims.K_max, dims.V);
+  if (draft_packs_into_workspace(dims)) n += al256(draft_packed_bytes(dims.rank, dims.V));
+  return n;
+}
+
+size_t dspark_draft_packed_projection_bytes(int64_t rank, int64_t V) {
+  if (rank < 64 || rank > 256 || rank % 64 != 0 || V < 2 || V > kMaxV || V % 8 != 0) return 0;
+  return draft_packed_bytes(rank, V);
+}
+
+dspark_status dspark_draft_pack_projection(const void *W, dspark_dims dims, void *W_packed, size_t packed_bytes,
+                                           void *stream) {
+  if (!W || !W_packed) return DSPARK_ERR_NULL;
+  if (dims.rank < 1 || dims.rank > kMaxRank || dims.V < 2 || dims.V > kMaxV) return DSPARK_ERR_DIMS;
+  if (dims.dtype != DSPARK_F32 && dims.dtype != DSPARK_BF16) return DSPARK_ERR_DTYPE;
+  const size_t need = dspark_draft_packed_projection_bytes(dims.rank, dims.V);
+  if (dims.dtype != DSPARK_BF16 || need == 0 || ((uintptr_t)W & 15u)) return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned256(W_packed) || packed_bytes < need) return DSPARK_ERR_WORKSPACE;
+  return launch_pack_projection(W, dims.rank, dims.V, W_packed, (cudaStream_t)stream) == cudaSuccess
+             ? DSPARK_OK
+             : DSPARK_ERR_CUDA;
 }
 
 dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
@@ -112,15 +142,16 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok || !dev_status) return DSPARK_ERR_NULL;
   dspark_status st = check_dims(dims, true);
   if (st != DSPARK_OK) return st;
-  if (!workspace || !aligned256(workspace) ||
-      workspace_bytes < dspark_draft_workspace_bytes(dims.B, dims.K_max, dims.V))
+  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_draft_workspace_bytes(dims))
     return DSPARK_ERR_WORKSPACE;
   DeviceInfo dev;
   if (!device_info(&dev)) return DSPARK_ERR_CUDA;
+  const bool packed_in = (dims.flags & DSPARK_FLAG_W_PACKED) != 0;
   DraftArgs a;
   a.U = U;
   a.E = E;
   a.W = W;
+  a.Wp = nullptr;
   a.anchor = anchor;
   a.K_r = K_r;
   a.temperature = temperature;
@@ -149,10 +180,21 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 1));
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
+  p += al256(sizeof(Partial) * (size_t)a.partial_slots);
+  const bool use_tc = !(dims.flags & DSPARK_FLAG_FORCE_SIMT) && dev.major == 10 && dev.minor == 3 &&
+                      draft_tc_shape_ok(a);
+  if (packed_in) {
+    // a packed projection only feeds the tensor-core path
+    if (!use_tc || ((uintptr_t)W & 15u)) return DSPARK_ERR_UNSUPPORTED;
+    a.Wp = W;
+  } else if (use_tc) {
+    if (((uintptr_t)W & 15u) || !draft_packs_into_workspace(dims)) return DSPARK_ERR_UNSUPPORTED;
+    a.Wp = p;   // packed into the workspace by this call
+  }
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_draft_prologue(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-  const bool use_tc = !(dims.flags & DSPARK_FLAG_FORCE_SIMT) && dev.major == 10 && dev.minor == 3 &&
-                      draft_tc_supported(a);
+  if (use_tc && !packed_in && launch_pack_projection(W, dims.rank, dims.V, (void *)a.Wp, s) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   cudaError_t e = use_tc ? launch_draft_tc(a, s, dev.sms) : launch_draft_simt(a, s);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }

@@ -8,8 +8,8 @@
 // CUDA-core step: grid (vocabulary chunk, active row).  Each block loads the
 // previous token's embedding row W1[x_{k-1}] into shared memory, forms
 // z = U + W1[x_{k-1}] . W2 for its chunk with fp32 FMAs, rounds z to the
-// storage dtype, optionally writes it, and runs the Gumbel race (or the greedy
-// argmax) with the online softmax.  Block partials go to the workspace; the
+// storage dtype, optionally writes it, and runs the two-level draw (one 32-wide
+// block per thread and iteration; or the greedy argmax) with the online softmax.  Block partials go to the workspace; the
 // last block of a row merges them and writes the token and the log-sum-exp.
 // This path serves fp32 inputs and shapes the tensor-core kernel does not take.
 #include "dspark_internal.cuh"
@@ -19,7 +19,6 @@ namespace {
 
 constexpr int kPrologueThreads = 1024;
 constexpr int kSimtThreads = 256;
-constexpr int kSimtChunk = 2048;   // vocabulary columns per block
 
 __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a) {
   __shared__ int s_err, s_skip;
@@ -121,40 +120,46 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_step(const __grid_con
     __syncthreads();
     const float T = a.temperature[r];
     const bool greedy = (T == 0.0f);
-    const float invT = greedy ? 1.0f : 1.0f / T;
+    const float a2 = (greedy ? 1.0f : 1.0f / T) * kLog2e;
     const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
-    const int lo = blockIdx.x * kSimtChunk, hi = min(V, lo + kSimtChunk);
-    Race st;
-    race_init(st);
-    for (int v0 = lo + threadIdx.x * 4; v0 < hi; v0 += kSimtThreads * 4) {
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int lo = blockIdx.x * kDraftSimtChunk, hi = min(V, lo + kDraftSimtChunk);
+    BRace br;
+    brace_init(br);
+    // one 32-wide block of the two-level draw per thread and iteration
+    for (int v0 = lo + threadIdx.x * kBlockW; v0 < hi; v0 += kSimtThreads * kBlockW) {
+      float z[kBlockW];
+#pragma unroll
+      for (int c = 0; c < kBlockW; ++c) z[c] = 0.0f;
       for (int q = 0; q < rank; ++q) {
         const float e = e_s[q];
         const int64_t wrow = (int64_t)q * V;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (v0 + c < hi) acc[c] = fmaf(e, ld<DT>(a.W, wrow + v0 + c), acc[c]);
+        for (int c = 0; c < kBlockW; ++c)
+          if (v0 + c < hi) z[c] = fmaf(e, ld<DT>(a.W, wrow + v0 + c), z[c]);
       }
-      float s[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kBlockW; ++c) {
         if (v0 + c < hi) {
-          float z = ld<DT>(a.U, urow + v0 + c) + acc[c];
-          if (DT == DSPARK_BF16) z = round_to_bf16(z);
-          if (a.draft_logits) st_logit<DT>(a.draft_logits, urow + v0 + c, z);
-          s[c] = greedy ? z : z * invT;
+          float zz = ld<DT>(a.U, urow + v0 + c) + z[c];
+          if (DT == DSPARK_BF16) zz = round_to_bf16(zz);
+          if (a.draft_logits) st_logit<DT>(a.draft_logits, urow + v0 + c, zz);
+          z[c] = zz;
         } else {
-          s[c] = -INFINITY;
+          z[c] = -INFINITY;
         }
       }
+      const float mz = block_max(z);
       if (greedy) {
-        argmax_update<4>(st, s, v0);
+        brace_argmax_block(br, z, mz, v0);
       } else {
-        const uint4 w4 = philox(key, (uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)r, kTagDraft);
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-        race_update<4>(st, s, w, v0);
+        const uint32_t g = (uint32_t)(v0 / kBlockW);
+        const uint32_t wb = word_of(philox(key, g >> 2, (uint32_t)k, (uint32_t)r, kTagDraft), (int)(g & 3u));
+        brace_softmax_block(br, z, mz, a2, wb, v0, [&] {
+          return word_of(philox(key, g >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(g & 3u));
+        });
       }
     }
+    Race st = from_partial(to_partial(br));
     st = race_block_reduce(st, red);
     if (threadIdx.x == 0) {
       a.partials[(int64_t)i * chunks + blockIdx.x] = to_partial(st);
@@ -184,7 +189,7 @@ cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s) {
-  const int chunks = (int)((a.V + kSimtChunk - 1) / kSimtChunk);
+  const int chunks = (int)((a.V + kDraftSimtChunk - 1) / kDraftSimtChunk);
   const size_t smem = sizeof(float) * (size_t)a.rank;
   if (smem > 48 * 1024) {
     cudaError_t e = a.dtype == DSPARK_F32

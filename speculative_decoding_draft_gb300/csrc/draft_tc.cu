@@ -1,55 +1,57 @@
-// Markov-head draft sampling, tensor-core path (sm_103a: tcgen05 + TMA + TMEM).
+// Markov-head draft sampling, tensor-core path (sm_103a: tcgen05 + bulk copies + TMEM).
 //
 // "DSpark" S3.1 (Markov head B(x_{k-1}, .) = W1[x_{k-1}] . W2, rank r) and
 // "Speculative decoding, from zero to DSpark" S6 (p_k = softmax(U_k + B_k)).
 //
-// One launch per draft position k.  The active requests (K_r >= k) form the
-// first n_k entries of `perm`; they are cut into M-tiles of 128 rows.  A
-// persistent grid of one CTA per SM gives every M-tile floor(G / M-tiles) CTAs,
-// each owning a contiguous range of 64-wide vocabulary tiles, so the gathered
-// 128 x r operand is staged once per CTA and reused across its whole range.
+// One persistent cooperative launch walks every draft position k = 1..K_max.  The
+// active requests at position k (K_r >= k) are the first n_k entries of `perm`;
+// they are cut into M-tiles of 128 rows, and every M-tile is shared by gm CTAs that
+// own contiguous ranges of 64-wide vocabulary blocks.  A CTA stages the gathered
+// operand W1[x_{k-1}] (128 x r) once per range and streams W2 through it.
+//
+// W2 arrives packed (dspark_draft_pack_projection): block (c, t) holds rank rows
+// 64c..64c+63 of vocabulary columns 64t..64t+63 as the 128-byte-swizzled image of
+// the MN-major tensor-core operand, and the blocks of one rank chunk are
+// consecutive, so the up-to-four blocks of one MMA tile and one rank chunk are a
+// single contiguous bulk copy.
 //
 // Warp roles (320 threads):
-//   warp 0     producer: per vocabulary tile, one TMA tile load of W2[:, n:n+64]
-//              (128-byte swizzle, r x 64 bf16) and one 1-D bulk copy per active row
-//              of U[r, k-1, n:n+64] into a padded row-major slot; both complete on
-//              the stage's full barrier.
-//   warp 1     allocates TMEM (4 accumulators of 128 x 64 fp32) and one elected
-//              lane issues r/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate,
-//              A K-major from shared memory, B MN-major from shared memory) per tile,
-//              committing to the stage's empty barrier and the accumulator's full
-//              barrier.
-//   warps 2-9  epilogue, two warps per TMEM lane quadrant (one per 32-column half):
-//              gather W1[x_{k-1}] rows into the swizzled A operand at the start of a
-//              tile range, then per tile tcgen05.ld the 32 fp32 bias values of their
-//              row, add U, round to bf16, optionally store the logits, and run the
-//              Gumbel race / greedy argmax with the online softmax.  No 128 x V
-//              logits tile ever goes back to HBM unless the caller asks for it.
-// Block partials per row are merged by the last CTA of each M-tile, which
-// writes the token and the log-sum-exp.  Every wait is bounded; on a timeout
-// the kernel records DSPARK_ERR_DEVICE_TIMEOUT, drains what it issued, frees
-// TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+//   warp 0     producer: per tile (N = 64 m columns, m <= 4) and rank chunk, one
+//              bulk copy of m x 8 KB into a 32 KB stage.
+//   warp 1     allocates TMEM (two accumulators of 128 x 256 fp32) and one elected
+//              lane issues the tcgen05.mma (kind::f16, bf16 in, fp32 accumulate, A
+//              K-major, B MN-major, both from shared memory, M = 128, N = 64 m).
+//   warps 2-9  epilogue, two warps per TMEM lane quadrant: gather W1[x_{k-1}] into
+//              the swizzled A operand, then per 32-column block tcgen05.ld the bias,
+//              add U, round to bf16, optionally store the logits, and run the
+//              two-level draw (or the greedy argmax) with the online softmax.
+// With fewer than 128 rows the rows are replicated F times in the M-tile and the F
+// replica groups split each tile's columns.  Per row, the CTA's maximum goes into
+// a packed 64-bit (score, index) key by atomicMax; a bounded grid barrier separates
+// positions, and a finalize kernel turns keys and partial normalisers into tokens
+// and log-sum-exps.  Every wait is bounded; on a timeout the kernel records
+// DSPARK_ERR_DEVICE_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include "dspark_internal.cuh"
 
 namespace dspark {
 namespace {
 
 constexpr int kTileM = 128;
-constexpr int kTileN = 64;
+constexpr int kBlkN = 64;                        // vocabulary columns per packed block
+constexpr int kMaxBlk = 4;                       // blocks per MMA tile (N <= 256)
 constexpr int kStages = 4;
-constexpr int kAccBufs = 4;
+constexpr int kAccBufs = 2;
+constexpr int kAccCols = kBlkN * kMaxBlk;        // 256
+constexpr int kTmemCols = kAccBufs * kAccCols;   // 512
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
-constexpr int kTmemCols = kAccBufs * kTileN;               // 256
-constexpr int kAChunk = kTileM * 128;                      // 16 KB: 128 rows x 64 bf16
-constexpr int kASize = 4 * kAChunk;                        // rank <= 256
-constexpr int kWSlot = 256 * 128;                          // r rows x 128 B
+constexpr int kAChunk = kTileM * 128;            // 16 KB: 128 rows x 64 rank values
+constexpr int kASize = 4 * kAChunk;              // rank <= 256
+constexpr int kPiece = kBlkN * 128;              // 8 KB: one packed block, 64 rank rows
+constexpr int kStageBytes = kMaxBlk * kPiece;    // 32 KB
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
-constexpr int kOffSh = kOffW + kStages * kWSlot;
+constexpr int kOffSh = kOffW + kStages * kStageBytes;
 constexpr long long kTimeoutCycles = 4000000000LL;
 
 struct TcShared {
@@ -61,12 +63,12 @@ struct TcShared {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int last;
   int skip;
+  int nact[kMaxK + 2];        // active requests per position (copied once per launch)
   int row_req[kTileM];
   int row_prev[kTileM];
   float row_invT[kTileM];
-  Partial part[2 * kTileM];   // per-row thread partials: [replica group x column half][row]
+  Partial part[2 * kTileM];   // per-row partials: [column worker][row of the replica group]
 };
 
 constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
@@ -155,12 +157,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
-                                            uint64_t policy) {
+// Contiguous global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -202,16 +205,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
-// B MN-major, N = 64, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kTileN >> 3) << 17) |
-                            ((uint32_t)(kTileM >> 4) << 24);
+// B MN-major, M = 128; N (a multiple of 64 here) goes into bits 17..22 as N >> 3.
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kTileM >> 4) << 24);
+__device__ __forceinline__ uint32_t idesc_n(int n) { return kIdescBase | ((uint32_t)(n >> 3) << 17); }
 
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
 
-// U row segment of one epilogue thread for one tile: 32 bf16 at column c0 of
-// its row (16-byte loads; columns past V are not read).
+// U row segment of one epilogue thread for one 32-wide block: 32 bf16 at column c0
+// of its row (16-byte loads; columns past V are not read).
 __device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int V, uint4 (&u)[4], uint64_t pol) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -221,32 +224,35 @@ __device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int 
 }
 
 // Work split of one draft position: M-tiles of 128 active rows, each shared by gm CTAs
-// that own contiguous ranges of 64-wide vocabulary tiles.
+// that own contiguous ranges of 64-wide vocabulary blocks.
 struct StepPlan {
   int n_k, m_tiles, gm, units;
 };
-__device__ __forceinline__ StepPlan plan_step(const DraftArgs &a, int k, int G, int n_tiles) {
+__device__ __forceinline__ StepPlan plan_step(const int *nact, int k, int G, int nb) {
   StepPlan p;
-  p.n_k = a.nact[k];
+  p.n_k = nact[k];
   p.m_tiles = (p.n_k + kTileM - 1) / kTileM;
-  p.gm = p.m_tiles ? max(1, min(G / p.m_tiles, n_tiles)) : 1;
+  p.gm = p.m_tiles ? max(1, min(G / p.m_tiles, nb)) : 1;
   p.units = p.m_tiles * p.gm;
   return p;
 }
+__device__ __forceinline__ int range_lo(int j, int nb, int gm) { return (int)((int64_t)j * nb / gm); }
+
+// Advance a column worker to its next 32-wide block: blocks wk, wk + nwk, ... of every
+// tile of up to kMaxBlk 64-wide blocks, tiles starting at b0, b0 + kMaxBlk, ... below b1.
+__device__ __forceinline__ void next_sub(int &bt, int &sbi, int wk, int nwk, int b1) {
+  sbi += nwk;
+  while (bt < b1 && sbi >= 2 * min(kMaxBlk, b1 - bt)) {
+    bt += kMaxBlk;
+    sbi = wk;
+  }
+}
 
 // ---------------------------------------------------------------------------
-// One persistent CTA per SM walks every draft position k = 1..K_max.  The producer
-// and MMA roles run ahead through positions on their own barriers (W2 does not
-// depend on the drafted tokens); the epilogue waits on a grid-wide barrier before
-// it reads the previous position's tokens, so the next position's W2 tiles and U
-// segments are already in flight while the barrier completes.
 template <int RCH>   // rank / 64
-__global__ void __launch_bounds__(kThreadsTc, 1)
-    draft_tc_persistent(const __grid_constant__ DraftArgs a, const __grid_constant__ CUtensorMap tmap_w) {
+__global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __grid_constant__ DraftArgs a) {
   constexpr int kRank = RCH * 64;
-  constexpr int kKsteps = kRank / 16;
   constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
-  constexpr uint32_t kWBytes = (uint32_t)(kTileN * kRank * 2);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -260,7 +266,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int K = (int)a.K_max, V = (int)a.V;
   const int G = gridDim.x;
-  const int n_tiles = (V + kTileN - 1) / kTileN;
+  const int nb = (V + kBlkN - 1) / kBlkN;          // 64-wide vocabulary blocks
+  const uint8_t *Wp = (const uint8_t *)a.Wp;
 
   const uint32_t bar_full = smem_u32(&sh.full[0]);
   const uint32_t bar_empty = smem_u32(&sh.empty[0]);
@@ -284,6 +291,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     sh.abort = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x < kMaxK + 2) sh.nact[threadIdx.x] = threadIdx.x <= K + 1 ? a.nact[threadIdx.x] : 0;
   if (warp == 1) {
     tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -302,60 +310,72 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 
   if (warp == 0) {
-    // ---------------- producer: W2 tiles of every position ----------------
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_last();
-      uint32_t it = 0;
-      for (int k = 1; k <= K && !*abort; ++k) {
-        const StepPlan pl = plan_step(a, k, G, n_tiles);
-        if (pl.n_k == 0) break;
-        for (int u = blockIdx.x; u < pl.units && !*abort; u += G) {
-          const int j = u % pl.gm;
-          const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
-          for (int t = nt0; t < nt1; ++t, ++it) {
+    // ---------------- producer: W2 stages of every position ----------------
+    // The warp walks the positions in lockstep (abort decided by lane 0 for all lanes);
+    // lane 0 issues the copies.
+    const uint64_t pol_w = policy_evict_last();
+    uint32_t it = 0;
+    for (int k = 1; k <= K; ++k) {
+      if (__shfl_sync(0xffffffffu, *abort ? 1 : 0, 0)) break;
+      const StepPlan pl = plan_step(sh.nact, k, G, nb);
+      if (pl.n_k == 0) break;
+      if (lane == 0)
+      for (int u = blockIdx.x; u < pl.units && !*abort; u += G) {
+        const int j = u % pl.gm;
+        const int b0 = range_lo(j, nb, pl.gm), b1 = range_lo(j + 1, nb, pl.gm);
+        for (int bt = b0; bt < b1 && !*abort; bt += kMaxBlk) {
+          const int m = min(kMaxBlk, b1 - bt);
+          for (int c = 0; c < RCH; ++c, ++it) {
             const int s = (int)(it % kStages);
             const uint32_t use = it / kStages;
             if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
-            mbar_arrive_tx(bar_full + 8 * s, kWBytes);
-            tma_load_2d(sb + kOffW + s * kWSlot, &tmap_w, t * kTileN, 0, bar_full + 8 * s, pol_w);
+            mbar_arrive_tx(bar_full + 8 * s, (uint32_t)(m * kPiece));
+            bulk_g2s(sb + kOffW + s * kStageBytes, Wp + ((int64_t)c * nb + bt) * kPiece, (uint32_t)(m * kPiece),
+                     bar_full + 8 * s, pol_w);
 #pragma unroll
             for (int q = 0; q < kStages; ++q)
               if (q == s) { last_use[q] = use; issued[q] = true; }
           }
         }
       }
+      __syncwarp();
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, tt = 0;
       int unit_no = 0;
       bool ok = true;
       for (int k = 1; k <= K && ok; ++k) {
-        const StepPlan pl = plan_step(a, k, G, n_tiles);
+        const StepPlan pl = plan_step(sh.nact, k, G, nb);
         if (pl.n_k == 0) break;
         for (int u = blockIdx.x; u < pl.units && ok; u += G, ++unit_no) {
           const int j = u % pl.gm;
-          const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
+          const int b0 = range_lo(j, nb, pl.gm), b1 = range_lo(j + 1, nb, pl.gm);
           ok = mbar_wait(bar_aready, (uint32_t)(unit_no & 1), abort);
-          for (int t = nt0; ok && t < nt1; ++t, ++it) {
-            const int s = (int)(it % kStages);
-            const uint32_t use = it / kStages;
-            const int b = (int)(it % kAccBufs);
-            const uint32_t ause = it / kAccBufs;
-            if (!(ok = mbar_wait(bar_full + 8 * s, use & 1u, abort))) break;
+          for (int bt = b0; ok && bt < b1; bt += kMaxBlk, ++tt) {
+            const int m = min(kMaxBlk, b1 - bt);
+            const int b = (int)(tt % kAccBufs);
+            const uint32_t ause = tt / kAccBufs;
             if (!(ok = mbar_wait(bar_acce + 8 * b, (ause & 1u) ^ 1u, abort))) break;
             tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(b * kTileN);
-#pragma unroll 1
-            for (int kk = 0; kk < kKsteps; ++kk) {
-              const uint64_t ad = smem_desc(sb + kOffA + (kk >> 2) * kAChunk + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc(sb + kOffW + s * kWSlot + kk * 2048, (uint32_t)(kRank * 128), 1024);
-              mma_bf16(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            const uint32_t d = tmem + (uint32_t)(b * kAccCols);
+            const uint32_t idesc = idesc_n(m * kBlkN);
+            for (int c = 0; ok && c < RCH; ++c, ++it) {
+              const int s = (int)(it % kStages);
+              const uint32_t use = it / kStages;
+              if (!(ok = mbar_wait(bar_full + 8 * s, use & 1u, abort))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc(sb + kOffA + c * kAChunk + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc(sb + kOffW + s * kStageBytes + kk * 2048, kPiece, 1024);
+                mma_bf16(d, ad, bd, idesc, (c | kk) ? 1u : 0u);
+              }
+              mma_commit(bar_empty + 8 * s);
             }
-            mma_commit(bar_empty + 8 * s);
-            mma_commit(bar_accf + 8 * b);
+            if (ok) mma_commit(bar_accf + 8 * b);
           }
         }
       }
@@ -365,50 +385,60 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ---------------- epilogue ----------------
     const int eq = warp - 2;            // 0..7
     const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
-    const int half = eq >> 2;           // 32-column half of the 64-wide tile
+    const int half = eq >> 2;
     const int et = eq * 32 + lane;      // 0..255
     const uint64_t pol_stream = policy_evict_first();
-    uint32_t it = 0;
+    uint32_t tt = 0;
     int unit_no = 0;
+    int tab_m = -1;                     // M-tile whose rows sh.row_req / sh.row_invT hold
     for (int k = 1; k <= K && !*abort; ++k) {
-      const StepPlan pl = plan_step(a, k, G, n_tiles);
+      const StepPlan pl = plan_step(sh.nact, k, G, nb);
       if (pl.n_k == 0) break;
       bool waited = (k == 1);
       for (int u = blockIdx.x; u < pl.units && !*abort; u += G, ++unit_no) {
         const int m = u / pl.gm, j = u % pl.gm;
-        const int nt0 = (int)((int64_t)j * n_tiles / pl.gm), nt1 = (int)((int64_t)(j + 1) * n_tiles / pl.gm);
+        const int b0 = range_lo(j, nb, pl.gm), b1 = range_lo(j + 1, nb, pl.gm);
         const int row0 = m * kTileM;
         const int nrows = min(kTileM, pl.n_k - row0);
         // replication: with few rows, every TMEM lane quadrant (= SM sub-partition) gets a copy
-        // of the rows and takes every F-th vocabulary tile
+        // of the rows, and the F replica groups split each tile's columns
         const int F = nrows <= 32 ? 4 : (nrows <= 64 ? 2 : 1);
         const int rpg = kTileM / F;
-        named_sync_epi();             // readers of the previous unit's row table are done
-        if (et < kTileM) {
-          const int i = et;
-          if (i < nrows) {
-            const int r = a.perm[row0 + i];
-            sh.row_req[i] = r;
-            const float T = a.temperature[r];
-            sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
-          } else {
-            sh.row_req[i] = -1;
-            sh.row_invT[i] = 0.0f;
+        if (m != tab_m) {                // the same decision in every epilogue thread
+          // rows of M-tile m (perm order) and their 1/T: fixed for the whole call, so
+          // loaded only when this CTA moves to another M-tile
+          named_sync_epi();           // readers of the previous table are done
+          if (et < kTileM) {
+            const int i = et;
+            if (row0 + i < (int)a.B) {
+              const int r = a.perm[row0 + i];
+              sh.row_req[i] = r;
+              const float T = a.temperature[r];
+              sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
+            } else {
+              sh.row_req[i] = -1;
+              sh.row_invT[i] = 0.0f;
+            }
           }
+          named_sync_epi();
+          tab_m = m;
         }
-        named_sync_epi();
         const int arow = quad * 32 + lane;        // TMEM lane = M-row
-        const int grp = arow / rpg;               // replica group: takes tiles t with (t - nt0) % F == grp
+        const int grp = arow / rpg;               // replica group (warp-uniform: rpg >= 32)
         const int row = arow % rpg;               // request row of this thread
+        const int wk = grp * 2 + half;            // column worker of this warp
+        const int nwk = 2 * F;
         const bool valid = row < nrows;
         const int r = valid ? sh.row_req[row] : 0;
         const float invT = sh.row_invT[row];
         const bool greedy = (invT == 0.0f);
+        const float a2 = invT * kLog2e;           // scaled logits in log2 units
         const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
         const unsigned short *uptr = (const unsigned short *)a.U + urow;
         uint4 ucur[4], unext[4];
-        int tmine = nt0 + grp;                    // first tile of this thread
-        if (valid && tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, ucur, pol_stream);   // before the barrier
+        int pbt = b0, psb = wk - nwk;             // first 32-wide block of this worker
+        next_sub(pbt, psb, wk, nwk, b1);
+        if (valid && pbt < b1) load_u32(uptr, pbt * kBlkN + psb * 32, V, ucur, pol_stream);   // before the barrier
         if (!waited) {
           // every CTA has folded its position k-1 maxima into the packed keys
           if (et == 0) {
@@ -424,131 +454,120 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (et < kTileM && et < nrows) {
           const int rq = sh.row_req[et];
-          sh.row_prev[et] = (k == 1) ? a.anchor[rq] : key_index(__ldcg(a.best_key + (int64_t)rq * K + k - 2));
+          sh.row_prev[et] = (k == 1) ? a.anchor[rq] : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2));
         }
         named_sync_epi();
-        // gather the A operand: request row i's 16-byte unit c8 of K-chunk c goes to every replica
-        // M-row a = g * rpg + i, chunk c, unit (c8 ^ (a & 7)) -- the 128-byte swizzle.  All loads of a
-        // thread are issued before its stores, so the row fetches overlap.
+        // gather the A operand with asynchronous 16-byte copies, all in flight at once: request
+        // row i's unit c8 of K-chunk c goes to every replica M-row ar = g * rpg + i, chunk c,
+        // unit (c8 ^ (ar & 7)) -- the 128-byte swizzle
         {
           const int total = nrows * kUpr;
-#pragma unroll 1
-          for (int q0 = 0; q0 < 16; q0 += 8) {     // two batches of eight 16-byte loads per thread
-            uint4 val[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int e = et + (q0 + q) * kEpiWarps * 32;
-              val[q] = make_uint4(0u, 0u, 0u, 0u);
-              if (e < total) {
-                const int i = e / kUpr, uu = e % kUpr;
-                val[q] = __ldg((const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * kRank) + uu);
-              }
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int e = et + (q0 + q) * kEpiWarps * 32;
-              if (e >= total) continue;
-              const int i = e / kUpr, uu = e % kUpr;
-              const int c = uu >> 3, c8 = uu & 7;
-              for (int g = 0; g < F; ++g) {
-                const int ar = g * rpg + i;
-                const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val[q].x), "r"(val[q].y),
-                             "r"(val[q].z), "r"(val[q].w)
-                             : "memory");
-              }
+          for (int e = et; e < total; e += kEpiWarps * 32) {
+            const int i = e / kUpr, uu = e % kUpr;
+            const int c = uu >> 3, c8 = uu & 7;
+            const uint4 *src = (const uint4 *)((const unsigned short *)a.E + (int64_t)sh.row_prev[i] * kRank) + uu;
+            for (int g = 0; g < F; ++g) {
+              const int ar = g * rpg + i;
+              const uint32_t dst = sb + kOffA + c * kAChunk + ar * 128 + ((c8 ^ (ar & 7)) << 4);
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
             }
           }
+          asm volatile("cp.async.wait_all;" ::: "memory");
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_aready);
 
-        Race st;
-        race_init(st);
-        for (int t = nt0; t < nt1; ++t, ++it) {
-          const int b = (int)(it % kAccBufs);
-          const uint32_t ause = it / kAccBufs;
+        BRace st;
+        brace_init(st);
+        for (int bt = b0; bt < b1; bt += kMaxBlk, ++tt) {
+          const int mt = min(kMaxBlk, b1 - bt);
+          const int b = (int)(tt % kAccBufs);
+          const uint32_t ause = tt / kAccBufs;
           if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
-          if (t != tmine) {                       // another replica group owns this tile
+          tc_fence_after();
+          const int nsub = 2 * mt;                // 32-wide blocks in this tile
+          if (wk >= nsub) {                       // nothing for this worker in a short last tile
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             continue;
           }
-          tc_fence_after();
-          uint32_t acc[32];
-          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kTileN + half * 32), acc);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_acce + 8 * b);
-          tmine += F;
-          if (!valid) continue;
-          if (tmine < nt1) load_u32(uptr, tmine * kTileN + half * 32, V, unext, pol_stream);   // prefetch
-          const int c0 = t * kTileN + half * 32;
-          const bool full = (c0 + 32 <= V);
-          uint32_t w[32];
-          if (!greedy) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {           // eight independent Philox blocks: ILP
-              const uint4 wq = philox(a.key, (uint32_t)(c0 >> 2) + (uint32_t)q, (uint32_t)k, (uint32_t)r, kTagDraft);
-              w[4 * q] = wq.x;
-              w[4 * q + 1] = wq.y;
-              w[4 * q + 2] = wq.z;
-              w[4 * q + 3] = wq.w;
+          for (int sbi = wk; sbi < nsub; sbi += nwk) {
+            uint32_t acc[32];
+            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kAccCols + sbi * 32), acc);
+            tmem_wait_ld();
+            if (sbi + nwk >= nsub) {              // this warp's last read of the accumulator
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             }
-          }
+            int nbt = bt, nsbi = sbi;
+            next_sub(nbt, nsbi, wk, nwk, b1);
+            if (!valid) continue;
+            if (nbt < b1) load_u32(uptr, nbt * kBlkN + nsbi * 32, V, unext, pol_stream);   // prefetch
+            const int c0 = bt * kBlkN + sbi * 32;     // this thread's 32-wide block of the two-level draw
+            const bool full = (c0 + 32 <= V);
+            float z[32];
+            uint32_t packed[16];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t pk[4] = {ucur[g].x, ucur[g].y, ucur[g].z, ucur[g].w};
-            float sv[8];
-            uint32_t packed[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float z0 = __uint_as_float(pk[e >> 1] << 16) + __uint_as_float(acc[g * 8 + e]);
-              const float z1 = __uint_as_float(pk[e >> 1] & 0xffff0000u) + __uint_as_float(acc[g * 8 + e + 1]);
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t pk = word_of(ucur[e >> 2], e & 3);
+              const float z0 = __uint_as_float(pk << 16) + __uint_as_float(acc[2 * e]);
+              const float z1 = __uint_as_float(pk & 0xffff0000u) + __uint_as_float(acc[2 * e + 1]);
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
-              packed[e >> 1] = *reinterpret_cast<const uint32_t *>(&zb);
-              const float2 zf = __bfloat1622float2(zb);
-              sv[e] = greedy ? zf.x : zf.x * invT;
-              sv[e + 1] = greedy ? zf.y : zf.y * invT;
+              packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
+              z[2 * e] = __uint_as_float(packed[e] << 16);
+              z[2 * e + 1] = __uint_as_float(packed[e] & 0xffff0000u);
             }
             if (!full) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (c0 + g * 8 + e >= V) sv[e] = -INFINITY;
+              for (int q = 0; q < 32; ++q)
+                if (c0 + q >= V) z[q] = -INFINITY;
             }
-            if (a.draft_logits && (full || c0 + g * 8 + 8 <= V))
-              st_u4_hint((unsigned short *)a.draft_logits + urow + c0 + g * 8,
-                         make_uint4(packed[0], packed[1], packed[2], packed[3]), pol_stream);
-            if (greedy) {
-              argmax_update<8>(st, sv, c0 + g * 8);
-            } else {
-              const uint32_t wg[8] = {w[8 * g], w[8 * g + 1], w[8 * g + 2], w[8 * g + 3],
-                                      w[8 * g + 4], w[8 * g + 5], w[8 * g + 6], w[8 * g + 7]};
-              race_update<8>(st, sv, wg, c0 + g * 8);
-            }
-          }
+            if (a.draft_logits) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
+              for (int g = 0; g < 4; ++g)
+                if (full || c0 + g * 8 + 8 <= V)
+                  st_u4_hint((unsigned short *)a.draft_logits + urow + c0 + g * 8,
+                             make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]),
+                             pol_stream);
+            }
+            const float mz = block_max(z);
+            if (greedy) {
+              brace_argmax_block(st, z, mz, c0);
+            } else {
+              const uint32_t gblk = (uint32_t)c0 >> 5;
+              const uint32_t wb =
+                  word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraft), (int)(gblk & 3u));
+              brace_softmax_block(st, z, mz, a2, wb, c0, [&] {
+                return word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(gblk & 3u));
+              });
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
+          }
         }
-        // merge the 2F thread partials of each row (replica groups x column halves); the row's
-        // home thread folds its maximum into the packed (score, index) key of the position with one
-        // 64-bit atomicMax -- all the next position needs -- and keeps its softmax partial for the
-        // normaliser, which the finalize kernel merges once per call
-        sh.part[(grp * 2 + half) * rpg + row] = to_partial(st);
+        // merge the 2F worker partials of each row; the row's home thread folds its maximum
+        // into the packed (score, index) key of the position with one 64-bit atomicMax -- all
+        // the next position needs -- and keeps its softmax partial for the finalize kernel
+        sh.part[wk * rpg + row] = to_partial(st);
         named_sync_epi();
-        if (grp == 0 && half == 0 && valid) {
-          for (int q = 1; q < 2 * F; ++q) race_merge(st, from_partial(sh.part[q * rpg + row]));
-          if (st.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(st.best, st.idx));
+        if (wk == 0 && valid) {
+          Race tot = from_partial(sh.part[row]);
+          for (int q = 1; q < nwk; ++q) race_merge(tot, from_partial(sh.part[q * rpg + row]));
+          if (tot.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(tot.best, tot.idx));
           a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j] =
-              to_partial(st);
+              to_partial(tot);
         }
       }
-      // this CTA is done with position k (every CTA arrives, with or without work)
-      __threadfence();
+      // this CTA is done with position k (every CTA arrives, with or without work): the
+      // barrier gathers the epilogue's atomics, the arriving thread's fence releases them
       named_sync_epi();
-      if (et == 0) atomicAdd(a.gbar + k, 1);
+      if (et == 0) {
+        __threadfence();
+        atomicAdd(a.gbar + k, 1);
+      }
     }
   }
 
@@ -579,25 +598,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-  }
-  return fn;
-}
-
 // Once per call, after the last position: tokens from the packed maxima and the
 // normaliser from the CTA partials of each (request, position), one warp each.
 __global__ void __launch_bounds__(256) draft_tc_finalize(const __grid_constant__ DraftArgs a, int G) {
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B;
-  const int n_tiles = (int)((a.V + kTileN - 1) / kTileN);
+  const int nb = (int)((a.V + kBlkN - 1) / kBlkN);
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < (int64_t)B * K; item += nw) {
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(256) draft_tc_finalize(const __grid_constant__
     const int n_k = a.nact[k];
     if (i >= n_k) continue;
     const int m_tiles = (n_k + kTileM - 1) / kTileM;
-    const int gm = max(1, min(G / m_tiles, n_tiles));
+    const int gm = max(1, min(G / m_tiles, nb));
     const int r = a.perm[i];
     const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * gm};
     Race tot[1];
@@ -619,34 +625,55 @@ __global__ void __launch_bounds__(256) draft_tc_finalize(const __grid_constant__
   }
 }
 
+// W2 [rank, V] -> packed blocks: 16-byte unit e = ((c * nb + t) * 64 + kr) * 8 + u of
+// the output holds W2[64c + kr, 64t + 8u' .. 64t + 8u' + 7] with u' = u ^ (kr & 7);
+// columns past V are zero.  V is a multiple of 8.
+__global__ void __launch_bounds__(256) pack_projection(const uint4 *__restrict__ W, int64_t rank, int64_t V,
+                                                       int nb, uint4 *__restrict__ Wp) {
+  const int64_t total = (rank / 64) * (int64_t)nb * 64 * 8;
+  const int64_t row_units = V / 8;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+    const int u = (int)(e & 7), kr = (int)((e >> 3) & 63);
+    const int64_t ct = e >> 9;
+    const int64_t t = ct % nb, c = ct / nb;
+    const int64_t cu = t * 8 + (u ^ (kr & 7));     // source 16-byte unit along the W2 row
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (cu < row_units) v = __ldg(W + (c * 64 + kr) * row_units + cu);
+    Wp[e] = v;
+  }
+}
+
 }  // namespace
 
-bool draft_tc_supported(const DraftArgs &a) {
+size_t draft_packed_bytes(int64_t rank, int64_t V) {
+  if (rank < 64 || rank % 64 != 0 || V < 1) return 0;
+  return (size_t)(rank / 64) * (size_t)((V + kBlkN - 1) / kBlkN) * (size_t)kPiece;
+}
+
+bool draft_tc_shape_ok(const DraftArgs &a) {
   if (a.dtype != DSPARK_BF16) return false;
   if (a.rank % 64 != 0 || a.rank > 256) return false;
   if (a.V % 8 != 0 || a.V > (int64_t)INT32_MAX - 64) return false;
-  if (((uintptr_t)a.U | (uintptr_t)a.E | (uintptr_t)a.W) & 15u) return false;
+  if (((uintptr_t)a.U | (uintptr_t)a.E) & 15u) return false;
   if (a.draft_logits && ((uintptr_t)a.draft_logits & 15u)) return false;
   // partial slots of one position: (M-tiles x 128 rows) x CTAs per M-tile <= 128 x max(grid, M-tiles)
   const int64_t m_tiles = (a.B + kTileM - 1) / kTileM;
   const int64_t units = m_tiles > 1024 ? m_tiles : 1024;
   if (units * kTileM > kTcPartialsPerStep) return false;
   if (a.K_max * kTcPartialsPerStep > a.partial_slots) return false;
-  return get_encode() != nullptr;
+  return true;
+}
+
+cudaError_t launch_pack_projection(const void *W, int64_t rank, int64_t V, void *Wp, cudaStream_t s) {
+  const int nb = (int)((V + kBlkN - 1) / kBlkN);
+  const int64_t units = (rank / 64) * (int64_t)nb * 64 * 8;
+  const int blocks = (int)((units + 255) / 256 < 65535 ? (units + 255) / 256 : 65535);
+  pack_projection<<<blocks, 256, 0, s>>>((const uint4 *)W, rank, V, nb, (uint4 *)Wp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
-  CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {(cuuint64_t)a.V, (cuuint64_t)a.rank};
-  const cuuint64_t gstride[1] = {(cuuint64_t)a.V * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)a.rank};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.W), gdim, gstride, box,
-                       estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (!a.Wp || ((uintptr_t)a.Wp & 15u)) return cudaErrorInvalidValue;
   static bool attr_set[5] = {false, false, false, false, false};
   const int rch = (int)(a.rank / 64);
   void *fn = nullptr;
@@ -674,7 +701,7 @@ cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void *args[2] = {(void *)&a, (void *)&tmap};
+  void *args[1] = {(void *)&a};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return e;
   const int64_t items = a.B * a.K_max;

@@ -5,13 +5,18 @@
 // precomputed on the host and travel in the kernel parameter block, so the
 // rounds read them from the constant bank.
 //
-// Sampling: Gumbel-max, x = argmax_v (s_v + g_v), g_v = -log(-log u_v), which
-// draws x ~ softmax(s).  The hot loop evaluates it as an exponential race: with
-// E_v = -log u_v, x = argmin_v E_v / exp(s_v).  Because E_v >= 1 - u_v, an element
-// can only beat the running best when (1 - u_v) < exp(s_v - best); that test
-// costs one multiply against exp(s_v - m), which the online softmax computes
-// anyway, and the exact score (two accurate logarithms) is evaluated only for
-// the rare elements that pass it.
+// Sampling: a two-level draw over blocks of 32 consecutive indices.  Block g
+// (indices 32g .. 32g+31) with mass L_g = sum of its weights enters a Gumbel race
+// with score log L_g + g_g, g_g = -log(-log u_g), u_g from word (g & 3) of the
+// stream block c0 = g >> 2; the block with the largest score wins, which picks
+// block g with probability L_g / sum L.  Inside the winner the index is drawn by
+// inverse CDF: the first v whose running weight sum exceeds u' L_g, u' the
+// accept-style uniform of word (g & 3) of the PICK stream.  Together this draws
+// v with probability w_v / sum w, with one stream word per 32 elements.  The
+// race over block scores runs as an exponential race: with E = -log u, a block
+// can only beat the running best when (1 - u) < exp(log L_g - best), so the two
+// accurate logarithms of the exact score are evaluated only for blocks that
+// pass that test, and the inverse-CDF pass only for blocks that take the lead.
 #pragma once
 
 #include <cstdint>
@@ -25,6 +30,10 @@ namespace dspark {
 constexpr uint32_t kTagDraft = 0;
 constexpr uint32_t kTagAccept = 1;
 constexpr uint32_t kTagResid = 2;
+constexpr uint32_t kTagDraftPick = 3;
+constexpr uint32_t kTagResidPick = 4;
+constexpr int kBlockW = 32;   // indices per block of the two-level draw
+constexpr int kDraftSimtChunk = 8192;   // vocabulary columns per CTA of the CUDA-core draft step
 constexpr int kMaxK = 16;
 constexpr float kMinPositiveT = 1e-3f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -82,9 +91,20 @@ __device__ __forceinline__ float uniform_accept(uint32_t w) {
   return __uint2float_rn(w >> 8) * 5.9604644775390625e-08f;
 }
 
+// 1 - u for the Gumbel uniform of word w: ((~w >> 9) + 0.5) * 2^-23, exact.
+__device__ __forceinline__ float one_minus_uniform_open(uint32_t w) {
+  return __uint_as_float((w >> 9) ^ 0x3FFFFFFFu) - 0.99999994039535522f;
+}
+
 __device__ __forceinline__ float fast_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -245,9 +265,14 @@ __device__ __forceinline__ Partial to_partial(const Race &r) {
   return p;
 }
 
-// Load a partial written by another block (L2, bypassing L1).
+// Load a partial written by another block: a gpu-scope relaxed load, which (after the
+// acquire that observed the writer's release) sees the writer's value.
 __device__ __forceinline__ Partial load_partial(const Partial *p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  int4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
   Partial o;
   o.best = __int_as_float(v.x);
   o.idx = v.y;
@@ -264,6 +289,98 @@ __device__ __forceinline__ Race from_partial(const Partial &p) {
   r.S = p.S;
   r.c = 0.0f;
   return r;
+}
+
+// -------------------------------------------------------------------------
+// Two-level draw: per-thread state and block steps.
+// -------------------------------------------------------------------------
+struct BRace {
+  float best;  // best block score seen (natural log units of the scaled weights)
+  int idx;     // index drawn inside that block
+  float M2;    // running max of the scaled logits, log2 units
+  float S;     // sum of 2^(y - M2) over the scaled logits y seen
+};
+
+__device__ __forceinline__ void brace_init(BRace &r) {
+  r.best = -INFINITY;
+  r.idx = -1;
+  r.M2 = -INFINITY;
+  r.S = 0.0f;
+}
+
+__device__ __forceinline__ Partial to_partial(const BRace &r) {
+  Partial p;
+  p.best = r.best;
+  p.idx = r.idx;
+  p.m = r.M2 == -INFINITY ? -INFINITY : r.M2 * kLn2;
+  p.S = r.S;
+  return p;
+}
+
+// Race entry of a block with log-mass ell and noise word wb; true when the block
+// takes the lead (r.best updated), after which the caller draws inside it.
+__device__ __forceinline__ bool brace_enter(BRace &r, float ell, uint32_t wb) {
+  if (!(one_minus_uniform_open(wb) < fast_ex2((ell - r.best) * kLog2e) * kFilterSlack)) return false;
+  const float t = ell - logf(-logf(uniform_open(wb)));
+  if (!(t > r.best)) return false;   // equal scores keep the earlier (smaller) block
+  r.best = t;
+  return true;
+}
+
+// Block of softmax weights 2^(z_q a - Mb) (a = log2(e) / T, Mb = max(z) a): folds
+// the block into the running softmax, enters the race and, when the block leads,
+// draws the index.  Entries past the vocabulary hold -inf.  pick_word() returns
+// the PICK stream word of the block (evaluated only when needed).
+// Returns true when the block took the lead.
+template <int N, class PickWord>
+__device__ __forceinline__ bool brace_softmax_block(BRace &r, const float (&z)[N], float mz, float a, uint32_t wb,
+                                                    int v0, PickWord pick_word) {
+  if (mz == -INFINITY) return false;
+  const float Mb = mz * a;
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < N; ++q) s[q & 3] += fast_ex2(fmaf(z[q], a, -Mb));
+  const float Sb = (s[0] + s[1]) + (s[2] + s[3]);
+  if (Mb > r.M2) {
+    r.S = r.S * fast_ex2(r.M2 - Mb) + Sb;
+    r.M2 = Mb;
+  } else {
+    r.S = fmaf(Sb, fast_ex2(Mb - r.M2), r.S);
+  }
+  const float ell = (Mb + fast_lg2(Sb)) * kLn2;
+  if (!brace_enter(r, ell, wb)) return false;
+  const float target = uniform_accept(pick_word()) * Sb;
+  float P = 0.0f;
+  int pick = -1, last = 0;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const float e = fast_ex2(fmaf(z[q], a, -Mb));
+    P += e;
+    if (e > 0.0f) last = q;
+    if (pick < 0 && P > target) pick = q;
+  }
+  r.idx = v0 + (pick < 0 ? last : pick);   // no crossing only when u' is within rounding of 1
+  return true;
+}
+
+// Greedy block: running maximum, smallest index on ties.
+template <int N>
+__device__ __forceinline__ void brace_argmax_block(BRace &r, const float (&z)[N], float mz, int v0) {
+  if (!(mz > r.best)) return;
+  r.best = mz;
+  int q0 = N - 1;
+#pragma unroll
+  for (int q = N - 1; q >= 0; --q)
+    if (z[q] == mz) q0 = q;
+  r.idx = v0 + q0;
+}
+
+template <int N>
+__device__ __forceinline__ float block_max(const float (&z)[N]) {
+  float m[4] = {z[0], z[1], z[2], z[3]};
+#pragma unroll
+  for (int q = 4; q < N; ++q) m[q & 3] = fmaxf(m[q & 3], z[q]);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
 // Warp-cooperative merge of R rows of partials: row i has n consecutive
@@ -309,6 +426,7 @@ __device__ __forceinline__ void warp_merge_rows(const Partial *const (&p)[R], in
 // -------------------------------------------------------------------------
 struct DraftArgs {
   const void *U, *E, *W;
+  const void *Wp;     // W2 in the packed tensor-core layout (tensor-core path only)
   const int32_t *anchor, *K_r;
   const float *temperature;
   int32_t *draft_tok;
@@ -336,6 +454,14 @@ __device__ __forceinline__ unsigned long long score_key(float s, int idx) {
   const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
+// Packed key written by other CTAs: a gpu-scope relaxed load (after an acquire that
+// observed the writers' release it sees their values).
+__device__ __forceinline__ unsigned long long load_key(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int key_index(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
@@ -344,7 +470,9 @@ cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms);
 constexpr int64_t kTcPartialsPerStep = 128 * 1024;   // slots per draft position on the tensor-core path
-bool draft_tc_supported(const DraftArgs &a);
+bool draft_tc_shape_ok(const DraftArgs &a);
+size_t draft_packed_bytes(int64_t rank, int64_t V);  // 0 when rank is not a positive multiple of 64
+cudaError_t launch_pack_projection(const void *W, int64_t rank, int64_t V, void *Wp, cudaStream_t s);
 
 struct ScheduleArgs {
   const float *conf;

@@ -13,9 +13,10 @@
 //     sampling job of the request: the residual at the rejecting position, the
 //     bonus row when every position is accepted, or nothing for greedy
 //     rejections (their correction is the argmax already found).
-//  2. verify_sample: the residual / bonus Gumbel-max over the vocabulary,
-//     spread over the whole GPU (request x vocabulary chunk), with the last
-//     block of each request merging the chunk partials.
+//  2. verify_sample: the residual / bonus two-level draw over the vocabulary,
+//     spread over the whole GPU (request x vocabulary chunk, one 32-wide block
+//     per thread), with the last block of each request merging the chunk
+//     partials.
 #include "dspark_internal.cuh"
 
 #include <cooperative_groups.h>
@@ -29,7 +30,7 @@ constexpr int kChainThreads = 256;
 constexpr int kBatch = 4;          // loads in flight per thread in the accept chain (fp32 / unaligned)
 constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per thread
 constexpr int kSampleThreads = 256;
-constexpr int kSampleChunk = 32768;   // long per-thread streams amortise the race start-up
+constexpr int kSampleChunk = kSampleThreads * kBlockW;   // one 32-wide block per thread
 
 struct Stats {
   float m, S;   // online softmax
@@ -401,73 +402,79 @@ __global__ void __launch_bounds__(kChainThreads, 2) verify_chain(const __grid_co
 // --------------------------------------------------------------------------
 // residual / bonus sampling
 // --------------------------------------------------------------------------
-__device__ __forceinline__ float resid_filter(float best) {
-  if (best == -INFINITY) return kFilterMax;
-  const float x = -best * kLog2e;
-  return x > 100.0f ? kFilterMax : fast_ex2(x) * kFilterSlack;
-}
-
-// Exact residual score log(p - q) + g for a candidate with log p = la > log q = lb.
-__device__ __forceinline__ void resid_exact(Race &rc, float la, float lb, uint32_t w, int v) {
-  const float logr = la + logf(-expm1f(lb - la));
-  const float u = uniform_open(w);
-  const float t = logr - logf(-logf(u));
-  if (t > rc.best || (t == rc.best && v < rc.idx)) {
-    rc.best = t;
-    rc.idx = v;
-    rc.c = resid_filter(t);
+template <int DT, bool VEC>
+__device__ __forceinline__ void load32(const void *base, int64_t row_off, int v0, int V, float (&x)[kBlockW]) {
+#pragma unroll
+  for (int h = 0; h < kBlockW / 8; ++h) {
+    float t[8];
+    load8<DT, VEC>(base, row_off, v0 + 8 * h, V, t);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[8 * h + q] = t[q];
   }
 }
 
+// Residual weight max(0, p - q) with p = 2^(t a - lt2), q = 2^(d a - ld2).
+__device__ __forceinline__ float resid_weight(float t, float d, float a, float lt2, float ld2) {
+  return fmaxf(fast_ex2(fmaf(t, a, -lt2)) - fast_ex2(fmaf(d, a, -ld2)), 0.0f);
+}
+
+// One block of residual weights in the two-level draw.
+template <class PickWord>
+__device__ __forceinline__ void brace_resid_block(BRace &r, const float (&t)[kBlockW], const float (&d)[kBlockW],
+                                                  float a, float lt2, float ld2, uint32_t wb, int v0, bool &any_pos,
+                                                  PickWord pick_word) {
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < kBlockW; ++q) s[q & 3] += resid_weight(t[q], d[q], a, lt2, ld2);
+  const float L = (s[0] + s[1]) + (s[2] + s[3]);
+  if (!(L > 0.0f)) return;
+  any_pos = true;
+  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) {
+    const float target = uniform_accept(pick_word()) * L;
+    float P = 0.0f;
+    int pick = -1, last = 0;
+#pragma unroll
+    for (int q = 0; q < kBlockW; ++q) {
+      const float w = resid_weight(t[q], d[q], a, lt2, ld2);
+      P += w;
+      if (w > 0.0f) last = q;
+      if (pick < 0 && P > target) pick = q;
+    }
+    r.idx = v0 + (pick < 0 ? last : pick);
+  }
+}
+
+// The draw of one request over [lo, hi): residual (mode 1), bonus from the
+// target row (mode 2, also the rounding guard of mode 1), greedy bonus (mode 3).
 template <int DT, bool VEC>
 __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, int lo, int hi, int tid,
-                             int nthreads, Race &rc, bool &any_cand, bool from_p) {
+                             int nthreads, BRace &rc, bool &any_pos, bool from_p) {
   const int V = (int)a.V;
   const int64_t trow = job.trow * (int64_t)V;
   const int64_t drow = job.drow * (int64_t)V;
   const int mode = from_p ? 2 : job.mode;
   const PhiloxKey key = a.key;   // round keys in registers for the hot loop
-  for (int v0 = lo + tid * 8; v0 < hi; v0 += nthreads * 8) {
-    float t8[8];
-    load8<DT, VEC>(a.tgt, trow, v0, hi, t8);
+  const float a2 = job.invT * kLog2e;
+  const float lt2 = job.lse_t * kLog2e, ld2 = job.lse_q * kLog2e;
+  for (int v0 = lo + tid * kBlockW; v0 < hi; v0 += nthreads * kBlockW) {
+    float t[kBlockW];
+    load32<DT, VEC>(a.tgt, trow, v0, hi, t);
     if (mode == 3) {
-      argmax_update<8>(rc, t8, v0);
+      brace_argmax_block(rc, t, block_max(t), v0);
       continue;
     }
-    const uint4 w0 = philox(key, (uint32_t)(v0 >> 2), (uint32_t)job.pos, (uint32_t)r, kTagResid);
-    const uint4 w1 = philox(key, (uint32_t)((v0 >> 2) + 1), (uint32_t)job.pos, (uint32_t)r, kTagResid);
-    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t g = (uint32_t)v0 >> 5;
+    const uint32_t wb = word_of(philox(key, g >> 2, (uint32_t)job.pos, (uint32_t)r, kTagResid), (int)(g & 3u));
+    auto pick_word = [&] {
+      return word_of(philox(key, g >> 2, (uint32_t)job.pos, (uint32_t)r, kTagResidPick), (int)(g & 3u));
+    };
     if (mode == 2) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) t8[q] *= job.invT;
-      race_update<8>(rc, t8, w, v0);
+      brace_softmax_block(rc, t, block_max(t), a2, wb, v0, pick_word);
       continue;
     }
-    // residual
-    float d8[8];
-    load8<DT, VEC>(a.D, drow, v0, hi, d8);
-    uint32_t cand = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float la = t8[q] * job.invT - job.lse_t;
-      const float lb = d8[q] * job.invT - job.lse_q;
-      if (la > lb) {
-        any_cand = true;
-        const float p = fast_ex2(la * kLog2e);
-        const float d1 = 1.0f - uniform_open(w[q]);
-        if (d1 < p * rc.c) cand |= 1u << q;
-      }
-    }
-    while (cand) {
-      const int q = __ffs(cand) - 1;
-      cand &= cand - 1;
-      float tq = t8[0], dq = d8[0];
-      uint32_t wq = w[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (i == q) { tq = t8[i]; dq = d8[i]; wq = w[i]; }
-      resid_exact(rc, tq * job.invT - job.lse_t, dq * job.invT - job.lse_q, wq, v0 + q);
-    }
+    float d[kBlockW];
+    load32<DT, VEC>(a.D, drow, v0, hi, d);
+    brace_resid_block(rc, t, d, a2, lt2, ld2, wb, v0, any_pos, pick_word);
   }
 }
 
@@ -483,12 +490,12 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
     if (job.mode == 0) continue;
     const int V = (int)a.V;
     const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
-    Race rc;
-    race_init(rc);
-    bool any_cand = false;
-    sample_range<DT, VEC>(a, job, r, lo, hi, tid, kSampleThreads, rc, any_cand, false);
-    const int any = __syncthreads_or(any_cand ? 1 : 0);
-    rc = race_block_reduce(rc, red);
+    BRace br;
+    brace_init(br);
+    bool any_pos = false;
+    sample_range<DT, VEC>(a, job, r, lo, hi, tid, kSampleThreads, br, any_pos, false);
+    const int any = __syncthreads_or(any_pos ? 1 : 0);
+    Race rc = race_block_reduce(from_partial(to_partial(br)), red);
     if (tid == 0) {
       Partial p = to_partial(rc);
       p.m = any ? 1.0f : 0.0f;    // the sampling pass needs no softmax: the field carries a flag
@@ -522,11 +529,11 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
     __syncthreads();
     if (job.mode == 1 && !s_any[0]) {
       // no element with p > q survived rounding: sample the correction from p instead
-      Race rp;
-      race_init(rp);
+      BRace bp;
+      brace_init(bp);
       bool dummy = false;
-      sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, rp, dummy, true);
-      rp = race_block_reduce(rp, red);
+      sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, bp, dummy, true);
+      const Race rp = race_block_reduce(from_partial(to_partial(bp)), red);
       if (tid == 0) s_tok = rp.idx;
     }
     if (tid == 0) {

@@ -48,10 +48,19 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_queries(lib):
     import speculative_decoding_draft_gb300 as ds
-    assert ds.draft_workspace_bytes(2048, 7, 151936) > 2048 * 75 * 16
+    base = ds.draft_workspace_bytes(2048, 7, 151936, 256, ds.BF16, ds.FLAG_W_PACKED)
+    assert base > 2048 * 75 * 16
+    # without a pre-packed projection the tensor-core shape packs W2 into the workspace
+    packed = ds.packed_projection_bytes(256, 151936)
+    assert packed == 4 * ((151936 + 63) // 64) * 8192
+    assert ds.draft_workspace_bytes(2048, 7, 151936, 256, ds.BF16, 0) >= base + packed
+    assert ds.draft_workspace_bytes(2048, 7, 151936, 256, ds.BF16, ds.FLAG_FORCE_SIMT) == base
+    assert ds.draft_workspace_bytes(2048, 7, 151936, 256, ds.F32, 0) == base
+    assert ds.packed_projection_bytes(100, 151936) == 0 and ds.packed_projection_bytes(256, 1003) == 0
+    assert ds.packed_projection_bytes(320, 1024) == 0
     assert ds.schedule_workspace_bytes(2048, 7) >= 2048 * 7 * 24
     assert ds.verify_workspace_bytes(64, 151936) > 0
-    assert lib.dspark_draft_workspace_bytes(0, 7, 10) == 0
+    assert lib.dspark_draft_workspace_bytes(ds.Dims(0, 7, 10, 16, ds.F32, 0)) == 0
 
 
 def test_host_validation_needs_no_device(lib):
@@ -68,6 +77,12 @@ def test_host_validation_needs_no_device(lib):
     bad = ds.Dims(4, 7, 1000, 16, 7, 0)
     assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, one, 1 << 20, one,
                                           null) == 3
+    # packing: null pointers, unsupported shapes and dtypes, short output
+    pdims = ds.Dims(1, 1, 1024, 256, ds.BF16, 0)
+    assert lib.dspark_draft_pack_projection(null, pdims, one, 1 << 30, null) == 1
+    assert lib.dspark_draft_pack_projection(one, ds.Dims(1, 1, 1024, 96, ds.BF16, 0), one, 1 << 30, null) == 13
+    assert lib.dspark_draft_pack_projection(one, ds.Dims(1, 1, 1024, 256, ds.F32, 0), one, 1 << 30, null) == 13
+    assert lib.dspark_draft_pack_projection(one, pdims, one, 1024, null) == 10
     assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, dims, one, null, null, one, 16, one,
                                           null) == 10
     assert lib.dspark_schedule_survival(one, one, one, 10, 4, 0, one, one, null, null, null, one, 1 << 20, one,
