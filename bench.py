@@ -269,19 +269,28 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+KERNEL_SOURCES = {"draft": ("draft_tc.cu", "dspark_internal.cuh"), "verify": ("verify.cu", "dspark_internal.cuh")}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over the sources a kernel is built from (in order)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_draft_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch recorded by ncu in profiles/, if the kernel source is unchanged."""
-    src = {"draft": "draft_tc.cu", "verify": "verify.cu"}.get(kernel)
+    """DRAM bytes per call recorded by ncu in profiles/, if the kernel sources are unchanged."""
     summ = os.path.join(ROOT, "profiles", f"traffic_{kernel}.md")
-    if not src or not os.path.exists(summ):
+    if kernel not in KERNEL_SOURCES or not os.path.exists(summ):
         return None
     text = open(summ).read()
     m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"dram_bytes_per_launch_scaled:\s*([0-9.eE+]+)", text)
     if not m or not t:
         return None
-    h = hashlib.sha256(open(os.path.join(ROOT, "speculative_decoding_draft_gb300", "csrc", src), "rb").read())
-    return float(t.group(1)) if h.hexdigest() == m.group(1) else None
+    return float(t.group(1)) if kernel_source_hash(kernel) == m.group(1) else None
 
 
 def cpu_baseline(cfg, w, sample_requests):
