@@ -44,6 +44,7 @@ constexpr int kAccBufs = 2;
 constexpr int kAccCols = kBlkN * kMaxBlk;        // 256
 constexpr int kTmemCols = kAccBufs * kAccCols;   // 512
 constexpr int kEpiWarps = 8;
+constexpr int kWpq = kEpiWarps / 4;             // epilogue warps per TMEM lane quadrant
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
 constexpr int kAChunk = kTileM * 128;            // 16 KB: 128 rows x 64 rank values
 constexpr int kASize = 4 * kAChunk;              // rank <= 256
@@ -68,7 +69,7 @@ struct TcShared {
   int row_req[kTileM];
   int row_prev[kTileM];
   float row_invT[kTileM];
-  Partial part[2 * kTileM];   // per-row partials: [column worker][row of the replica group]
+  Partial part[kWpq * kTileM];   // per-row partials: [column worker][row of the replica group]
 };
 
 constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
@@ -191,6 +192,12 @@ __device__ __forceinline__ void st_u4_hint(void *ptr, uint4 v, uint64_t policy) 
                "r"(v.z), "r"(v.w), "l"(policy)
                : "memory");
 }
+// 32-byte (one whole sector) global store, 32-byte aligned address.
+__device__ __forceinline__ void st_u8_hint(void *ptr, uint4 lo, uint4 hi, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr), "r"(lo.x),
+               "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ int ld_acquire(const int32_t *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -208,6 +215,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // B MN-major, M = 128; N (a multiple of 64 here) goes into bits 17..22 as N >> 3.
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kTileM >> 4) << 24);
 __device__ __forceinline__ uint32_t idesc_n(int n) { return kIdescBase | ((uint32_t)(n >> 3) << 17); }
+
+__device__ __forceinline__ __nv_bfloat162 bf162_of(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); }
 
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
@@ -237,16 +246,6 @@ __device__ __forceinline__ StepPlan plan_step(const int *nact, int k, int G, int
   return p;
 }
 __device__ __forceinline__ int range_lo(int j, int nb, int gm) { return (int)((int64_t)j * nb / gm); }
-
-// Advance a column worker to its next 32-wide block: blocks wk, wk + nwk, ... of every
-// tile of up to kMaxBlk 64-wide blocks, tiles starting at b0, b0 + kMaxBlk, ... below b1.
-__device__ __forceinline__ void next_sub(int &bt, int &sbi, int wk, int nwk, int b1) {
-  sbi += nwk;
-  while (bt < b1 && sbi >= 2 * min(kMaxBlk, b1 - bt)) {
-    bt += kMaxBlk;
-    sbi = wk;
-  }
-}
 
 // ---------------------------------------------------------------------------
 template <int RCH>   // rank / 64
@@ -385,9 +384,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
     // ---------------- epilogue ----------------
     const int eq = warp - 2;            // 0..7
     const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
-    const int half = eq >> 2;
+    const int wq = eq >> 2;             // this warp's rank among the warps of its quadrant
     const int et = eq * 32 + lane;      // 0..255
     const uint64_t pol_stream = policy_evict_first();
+    // every lane stores to another row, so the logits go out in whole 32-byte sectors where
+    // the rows start on 32-byte boundaries (V % 16 == 0 from a 32-byte aligned base)
+    const bool wide_s = (V % 16 == 0) && ((uintptr_t)a.draft_logits % 32 == 0);
     uint32_t tt = 0;
     int unit_no = 0;
     int tab_m = -1;                     // M-tile whose rows sh.row_req / sh.row_invT hold
@@ -426,8 +428,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const int arow = quad * 32 + lane;        // TMEM lane = M-row
         const int grp = arow / rpg;               // replica group (warp-uniform: rpg >= 32)
         const int row = arow % rpg;               // request row of this thread
-        const int wk = grp * 2 + half;            // column worker of this warp
-        const int nwk = 2 * F;
+        const int wk = grp * kWpq + wq;           // column worker of this warp
+        const int nwk = kWpq * F;
         const bool valid = row < nrows;
         const int r = valid ? sh.row_req[row] : 0;
         const float invT = sh.row_invT[row];
@@ -436,14 +438,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
         const unsigned short *uptr = (const unsigned short *)a.U + urow;
         uint4 ucur[4], unext[4];
-        int pbt = b0, psb = wk - nwk;             // first 32-wide block of this worker
-        next_sub(pbt, psb, wk, nwk, b1);
-        if (valid && pbt < b1) load_u32(uptr, pbt * kBlkN + psb * 32, V, ucur, pol_stream);   // before the barrier
+        // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles; worker wk
+        // takes blocks wk, wk + nwk, ...
+        const int nsub_u = 2 * (b1 - b0);
+        if (valid && wk < nsub_u) load_u32(uptr, b0 * kBlkN + wk * 32, V, ucur, pol_stream);   // before the barrier
         if (!waited) {
           // every CTA has folded its position k-1 maxima into the packed keys
           if (et == 0) {
             const long long t0 = clock64();
             while (ld_acquire(a.gbar + (k - 1)) < G) {
+              __nanosleep(100);        // back off: many pollers slow the CTAs still working
               if (*abort) break;
               if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }
             }
@@ -486,29 +490,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           const uint32_t ause = tt / kAccBufs;
           if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
           tc_fence_after();
-          const int nsub = 2 * mt;                // 32-wide blocks in this tile
-          if (wk >= nsub) {                       // nothing for this worker in a short last tile
+          const int s0 = 2 * (bt - b0), s1 = s0 + 2 * mt;   // the tile's blocks in unit numbering
+          int gs = s0 + (wk - s0 % nwk + nwk) % nwk;         // this worker's first block in the tile
+          if (gs >= s1) {                         // nothing for this worker in this tile
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             continue;
           }
-          for (int sbi = wk; sbi < nsub; sbi += nwk) {
+          for (; gs < s1; gs += nwk) {
             uint32_t acc[32];
-            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kAccCols + sbi * 32), acc);
+            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kAccCols + (gs - s0) * 32), acc);
             tmem_wait_ld();
-            if (sbi + nwk >= nsub) {              // this warp's last read of the accumulator
+            if (gs + nwk >= s1) {                 // this warp's last read of the accumulator
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             }
-            int nbt = bt, nsbi = sbi;
-            next_sub(nbt, nsbi, wk, nwk, b1);
             if (!valid) continue;
-            if (nbt < b1) load_u32(uptr, nbt * kBlkN + nsbi * 32, V, unext, pol_stream);   // prefetch
-            const int c0 = bt * kBlkN + sbi * 32;     // this thread's 32-wide block of the two-level draw
-            const bool full = (c0 + 32 <= V);
-            float z[32];
+            if (gs + nwk < nsub_u) load_u32(uptr, b0 * kBlkN + (gs + nwk) * 32, V, unext, pol_stream);   // prefetch
+            const int c0 = b0 * kBlkN + gs * 32;      // this thread's 32-wide block of the two-level draw
             uint32_t packed[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -517,23 +518,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               const float z1 = __uint_as_float(pk & 0xffff0000u) + __uint_as_float(acc[2 * e + 1]);
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
+            }
+            if (a.draft_logits) {
+              unsigned short *drow = (unsigned short *)a.draft_logits + urow;
+              if (wide_s) {                           // whole sectors: 32-byte stores
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (c0 + 16 * h + 16 <= V)
+                    st_u8_hint(drow + c0 + 16 * h,
+                               make_uint4(packed[8 * h], packed[8 * h + 1], packed[8 * h + 2], packed[8 * h + 3]),
+                               make_uint4(packed[8 * h + 4], packed[8 * h + 5], packed[8 * h + 6], packed[8 * h + 7]),
+                               pol_stream);
+              } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  if (c0 + g * 8 + 8 <= V)
+                    st_u4_hint(drow + c0 + g * 8,
+                               make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]),
+                               pol_stream);
+              }
+            }
+            if (c0 + 32 > V) {                        // ragged tail: whole pairs past V (V is even)
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (c0 + 2 * e >= V) packed[e] = 0xFF80FF80u;   // two bf16 -inf
+            }
+            // block maximum on bf16 pairs (exact), then across the pair
+            __nv_bfloat162 m2[4] = {bf162_of(packed[0]), bf162_of(packed[1]), bf162_of(packed[2]), bf162_of(packed[3])};
+#pragma unroll
+            for (int e = 4; e < 16; ++e) m2[e & 3] = __hmax2(m2[e & 3], bf162_of(packed[e]));
+            m2[0] = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
+            const float mz = fmaxf(__low2float(m2[0]), __high2float(m2[0]));
+            float z[32];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
               z[2 * e] = __uint_as_float(packed[e] << 16);
               z[2 * e + 1] = __uint_as_float(packed[e] & 0xffff0000u);
             }
-            if (!full) {
-#pragma unroll
-              for (int q = 0; q < 32; ++q)
-                if (c0 + q >= V) z[q] = -INFINITY;
-            }
-            if (a.draft_logits) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (full || c0 + g * 8 + 8 <= V)
-                  st_u4_hint((unsigned short *)a.draft_logits + urow + c0 + g * 8,
-                             make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]),
-                             pol_stream);
-            }
-            const float mz = block_max(z);
             if (greedy) {
               brace_argmax_block(st, z, mz, c0);
             } else {

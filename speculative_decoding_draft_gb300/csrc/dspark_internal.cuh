@@ -327,19 +327,44 @@ __device__ __forceinline__ bool brace_enter(BRace &r, float ell, uint32_t wb) {
   return true;
 }
 
+// Inverse CDF inside a block of non-negative weights: the first q whose running sum
+// (left to right, fp32) exceeds target.  The running sums are monotone, so that index
+// is the number of running sums <= target.  No crossing happens only when u' is within
+// rounding of 1; the draw then takes the last positive weight.
+template <int N>
+__device__ __forceinline__ int pick_in_block(const float (&w)[N], float target) {
+  float P = 0.0f;
+  int cnt = 0;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    P += w[q];
+    cnt += (P <= target) ? 1 : 0;
+  }
+  if (cnt < N) return cnt;
+  int last = 0;
+#pragma unroll
+  for (int q = 0; q < N; ++q)
+    if (w[q] > 0.0f) last = q;
+  return last;
+}
+
 // Block of softmax weights 2^(z_q a - Mb) (a = log2(e) / T, Mb = max(z) a): folds
 // the block into the running softmax, enters the race and, when the block leads,
-// draws the index.  Entries past the vocabulary hold -inf.  pick_word() returns
-// the PICK stream word of the block (evaluated only when needed).
+// draws the index.  Entries past the vocabulary hold -inf.  z is overwritten with
+// the weights, which the in-block draw reuses.  pick_word() returns the PICK
+// stream word of the block (evaluated only when needed).
 // Returns true when the block took the lead.
 template <int N, class PickWord>
-__device__ __forceinline__ bool brace_softmax_block(BRace &r, const float (&z)[N], float mz, float a, uint32_t wb,
+__device__ __forceinline__ bool brace_softmax_block(BRace &r, float (&z)[N], float mz, float a, uint32_t wb,
                                                     int v0, PickWord pick_word) {
   if (mz == -INFINITY) return false;
   const float Mb = mz * a;
   float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int q = 0; q < N; ++q) s[q & 3] += fast_ex2(fmaf(z[q], a, -Mb));
+  for (int q = 0; q < N; ++q) {
+    z[q] = fast_ex2(fmaf(z[q], a, -Mb));
+    s[q & 3] += z[q];
+  }
   const float Sb = (s[0] + s[1]) + (s[2] + s[3]);
   if (Mb > r.M2) {
     r.S = r.S * fast_ex2(r.M2 - Mb) + Sb;
@@ -349,17 +374,7 @@ __device__ __forceinline__ bool brace_softmax_block(BRace &r, const float (&z)[N
   }
   const float ell = (Mb + fast_lg2(Sb)) * kLn2;
   if (!brace_enter(r, ell, wb)) return false;
-  const float target = uniform_accept(pick_word()) * Sb;
-  float P = 0.0f;
-  int pick = -1, last = 0;
-#pragma unroll
-  for (int q = 0; q < N; ++q) {
-    const float e = fast_ex2(fmaf(z[q], a, -Mb));
-    P += e;
-    if (e > 0.0f) last = q;
-    if (pick < 0 && P > target) pick = q;
-  }
-  r.idx = v0 + (pick < 0 ? last : pick);   // no crossing only when u' is within rounding of 1
+  r.idx = v0 + pick_in_block(z, uniform_accept(pick_word()) * Sb);
   return true;
 }
 

@@ -420,28 +420,19 @@ __device__ __forceinline__ float resid_weight(float t, float d, float a, float l
 
 // One block of residual weights in the two-level draw.
 template <class PickWord>
-__device__ __forceinline__ void brace_resid_block(BRace &r, const float (&t)[kBlockW], const float (&d)[kBlockW],
+__device__ __forceinline__ void brace_resid_block(BRace &r, float (&t)[kBlockW], const float (&d)[kBlockW],
                                                   float a, float lt2, float ld2, uint32_t wb, int v0, bool &any_pos,
                                                   PickWord pick_word) {
   float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int q = 0; q < kBlockW; ++q) s[q & 3] += resid_weight(t[q], d[q], a, lt2, ld2);
+  for (int q = 0; q < kBlockW; ++q) {
+    t[q] = resid_weight(t[q], d[q], a, lt2, ld2);   // t now holds the weights
+    s[q & 3] += t[q];
+  }
   const float L = (s[0] + s[1]) + (s[2] + s[3]);
   if (!(L > 0.0f)) return;
   any_pos = true;
-  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) {
-    const float target = uniform_accept(pick_word()) * L;
-    float P = 0.0f;
-    int pick = -1, last = 0;
-#pragma unroll
-    for (int q = 0; q < kBlockW; ++q) {
-      const float w = resid_weight(t[q], d[q], a, lt2, ld2);
-      P += w;
-      if (w > 0.0f) last = q;
-      if (pick < 0 && P > target) pick = q;
-    }
-    r.idx = v0 + (pick < 0 ? last : pick);
-  }
+  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(t, uniform_accept(pick_word()) * L);
 }
 
 // The draw of one request over [lo, hi): residual (mode 1), bonus from the
