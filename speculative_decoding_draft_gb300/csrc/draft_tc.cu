@@ -87,14 +87,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
+// One bounded probe of a barrier phase: the thread sleeps until the phase completes or
+// about 20 us pass, so waiting roles do not spin on the issue slots of the epilogue.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(20000)
       : "memory");
   return ok != 0;
 }
@@ -192,6 +194,14 @@ __device__ __forceinline__ void st_u4_hint(void *ptr, uint4 v, uint64_t policy) 
                "r"(v.z), "r"(v.w), "l"(policy)
                : "memory");
 }
+// z = bf16 value + fp32 value, rounded once to fp32, for the two halves of a bf16 pair
+// word (low half first).
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t w, float a0, float a1, float &z0, float &z1) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(z0), "=f"(z1)
+      : "r"(w), "f"(a0), "f"(a1));
+}
+
 // 32-byte (one whole sector) global store, 32-byte aligned address.
 __device__ __forceinline__ void st_u8_hint(void *ptr, uint4 lo, uint4 hi, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr), "r"(lo.x),
@@ -513,9 +523,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             uint32_t packed[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const uint32_t pk = word_of(ucur[e >> 2], e & 3);
-              const float z0 = __uint_as_float(pk << 16) + __uint_as_float(acc[2 * e]);
-              const float z1 = __uint_as_float(pk & 0xffff0000u) + __uint_as_float(acc[2 * e + 1]);
+              float z0, z1;
+              add_bf16x2_f32(word_of(ucur[e >> 2], e & 3), __uint_as_float(acc[2 * e]),
+                             __uint_as_float(acc[2 * e + 1]), z0, z1);
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
             }
@@ -549,19 +559,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             for (int e = 4; e < 16; ++e) m2[e & 3] = __hmax2(m2[e & 3], bf162_of(packed[e]));
             m2[0] = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
             const float mz = fmaxf(__low2float(m2[0]), __high2float(m2[0]));
-            float z[32];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              z[2 * e] = __uint_as_float(packed[e] << 16);
-              z[2 * e + 1] = __uint_as_float(packed[e] & 0xffff0000u);
-            }
             if (greedy) {
+              float z[32];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                z[2 * e] = __uint_as_float(packed[e] << 16);
+                z[2 * e + 1] = __uint_as_float(packed[e] & 0xffff0000u);
+              }
               brace_argmax_block(st, z, mz, c0);
             } else {
               const uint32_t gblk = (uint32_t)c0 >> 5;
               const uint32_t wb =
                   word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraft), (int)(gblk & 3u));
-              brace_softmax_block(st, z, mz, a2, wb, c0, [&] {
+              brace_softmax_bf16x32(st, packed, mz, a2, wb, c0, [&] {
                 return word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(gblk & 3u));
               });
             }

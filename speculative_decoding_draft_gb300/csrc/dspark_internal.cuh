@@ -354,6 +354,23 @@ __device__ __forceinline__ int pick_in_block(const float (&w)[N], float target) 
 // the weights, which the in-block draw reuses.  pick_word() returns the PICK
 // stream word of the block (evaluated only when needed).
 // Returns true when the block took the lead.
+// Folds a block with scaled maximum Mb (log2 units) and weights w (sum Sb) into the
+// running softmax, enters the race and, when the block leads, draws the index.
+template <int N, class PickWord>
+__device__ __forceinline__ bool brace_fold_block(BRace &r, const float (&w)[N], float Mb, float Sb, uint32_t wb,
+                                                 int v0, PickWord pick_word) {
+  if (Mb > r.M2) {
+    r.S = r.S * fast_ex2(r.M2 - Mb) + Sb;
+    r.M2 = Mb;
+  } else {
+    r.S = fmaf(Sb, fast_ex2(Mb - r.M2), r.S);
+  }
+  const float ell = (Mb + fast_lg2(Sb)) * kLn2;
+  if (!brace_enter(r, ell, wb)) return false;
+  r.idx = v0 + pick_in_block(w, uniform_accept(pick_word()) * Sb);
+  return true;
+}
+
 template <int N, class PickWord>
 __device__ __forceinline__ bool brace_softmax_block(BRace &r, float (&z)[N], float mz, float a, uint32_t wb,
                                                     int v0, PickWord pick_word) {
@@ -365,17 +382,56 @@ __device__ __forceinline__ bool brace_softmax_block(BRace &r, float (&z)[N], flo
     z[q] = fast_ex2(fmaf(z[q], a, -Mb));
     s[q & 3] += z[q];
   }
-  const float Sb = (s[0] + s[1]) + (s[2] + s[3]);
-  if (Mb > r.M2) {
-    r.S = r.S * fast_ex2(r.M2 - Mb) + Sb;
-    r.M2 = Mb;
-  } else {
-    r.S = fmaf(Sb, fast_ex2(Mb - r.M2), r.S);
+  return brace_fold_block(r, z, Mb, (s[0] + s[1]) + (s[2] + s[3]), wb, v0, pick_word);
+}
+
+// ---- paired fp32 arithmetic: one sm_100 instruction for two independent lanes, each
+// rounded exactly like the scalar operation ----
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Softmax block of 32 bf16 logits held as 16 pairs (low half first); the same fp32
+// operations in the same order as brace_softmax_block on the unpacked values.
+template <class PickWord>
+__device__ __forceinline__ bool brace_softmax_bf16x32(BRace &r, const uint32_t (&pk)[16], float mz, float a,
+                                                      uint32_t wb, int v0, PickWord pick_word) {
+  if (mz == -INFINITY) return false;
+  const float Mb = mz * a;
+  const unsigned long long aa = f2_pack(a, a), mb = f2_pack(-Mb, -Mb);
+  unsigned long long s01 = f2_pack(0.0f, 0.0f), s23 = s01;   // (s0, s1), (s2, s3): s[q & 3]
+  float w[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const unsigned long long zz = f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u));
+    float y0, y1;
+    f2_unpack(f2_fma(zz, aa, mb), y0, y1);
+    w[2 * j] = fast_ex2(y0);
+    w[2 * j + 1] = fast_ex2(y1);
+    const unsigned long long ee = f2_pack(w[2 * j], w[2 * j + 1]);
+    if (j & 1) s23 = f2_add(s23, ee);
+    else s01 = f2_add(s01, ee);
   }
-  const float ell = (Mb + fast_lg2(Sb)) * kLn2;
-  if (!brace_enter(r, ell, wb)) return false;
-  r.idx = v0 + pick_in_block(z, uniform_accept(pick_word()) * Sb);
-  return true;
+  float s0, s1, s2, s3;
+  f2_unpack(s01, s0, s1);
+  f2_unpack(s23, s2, s3);
+  return brace_fold_block(r, w, Mb, (s0 + s1) + (s2 + s3), wb, v0, pick_word);
 }
 
 // Greedy block: running maximum, smallest index on ties.
