@@ -233,6 +233,8 @@ dspark_status dspark_schedule_survival_noalloc(const float *conf, const int32_t 
  *                (as written by dspark_draft_markov_sample).  When given, draft rows
  *                are read only at the rejecting position; when NULL they are
  *                streamed at every verified position.
+ * The target rows j <= ell_r of every request are streamed at once (one pass over
+ * all of them, in parallel), so rows past a request's first rejection are read too.
  *   tgt_logits   [tgt_off[B], V]  flattened target logits, ell_r + 1 rows per request.
  *   tgt_off      [B+1] int32      row offsets; tgt_off[r+1] - tgt_off[r] = ell_r + 1.
  *   ell          [B] int32        verification lengths, 0..K_max.

@@ -270,15 +270,7 @@ dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_
   a.V = dims.V;
   a.dtype = dims.dtype;
   a.key = make_philox_key(seed);
-  int chunks = 1;
-  verify_ws_bytes(dims.B, dims.V, &chunks);
-  a.chunks = chunks;
-  char *p = (char *)workspace;
-  a.jobs = (VerifyJob *)p;
-  p += al256(sizeof(VerifyJob) * (size_t)dims.B);
-  a.counters = (int32_t *)p;
-  p += al256(sizeof(int32_t) * (size_t)dims.B);
-  a.partials = (Partial *)p;
+  verify_carve(a, workspace);
   return launch_verify(a, (cudaStream_t)stream, dev.sms) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

@@ -401,6 +401,11 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
   unsigned long long r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -570,6 +575,14 @@ struct VerifyJob {
   int out_slot;  // index into out_tok
 };
 
+// Merged statistics of one drafted row: lse_t = log sum exp(target / T) (the maximum for
+// T = 0), amax its argmax, zx_t the scaled target logit at the draft token, and the
+// same two for the draft row when no draft normaliser is given.
+struct RowRes {
+  float lse_t, zx_t, lse_q, zx_d;
+  int amax;
+};
+
 struct VerifyArgs {
   const void *D;
   const float *D_lse;
@@ -580,13 +593,17 @@ struct VerifyArgs {
   int64_t B, K_max, V;
   int dtype;
   PhiloxKey key;
-  VerifyJob *jobs;     // [B]
-  int32_t *counters;   // [B]
+  int32_t *counters;   // [B] chunk arrivals of the sampling pass, zeroed per call
   Partial *partials;   // [B * chunks]
   int chunks;          // vocabulary chunks of the sampling pass
+  Partial *row_t, *row_d;   // [B * kMaxK * row_slices] target / draft row statistics per slice
+  float *zx_t, *zx_d;       // [B * kMaxK] scaled logits at the draft tokens
+  int row_slices;           // vocabulary slices per row of the statistics pass
 };
 
+int verify_row_slices(int64_t V);
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks);
+void verify_carve(VerifyArgs &a, void *workspace);   // jobs, counters, partials, row statistics
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms);
 
 }  // namespace dspark

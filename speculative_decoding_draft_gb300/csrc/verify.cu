@@ -1,34 +1,35 @@
 // Ragged rejection-sampling verification ("DSpark", S2.1; "Speculative
 // decoding, from zero to DSpark", S2 and Appendix A1).
 //
-// Two kernels:
-//  1. verify_chain: one thread-block cluster per request walks positions
-//     j = 1..ell_r left to right.  Each CTA of the cluster streams its slice of
-//     the target row (and of the draft row when no draft normaliser is given)
-//     with 16-byte loads, reduces the online-softmax statistics (max, sum of
-//     exponentials) of z/T, and publishes them in shared memory; after a
-//     cluster barrier every CTA combines the slices in rank order, so all of
-//     them take the same accept decision u < min(1, p(x)/q(x)).  Rows after
-//     the deciding position are never read.  The decision also produces the
-//     sampling job of the request: the residual at the rejecting position, the
-//     bonus row when every position is accepted, or nothing for greedy
-//     rejections (their correction is the argmax already found).
+// Two kernels (after a reset of the per-request arrival counters):
+//  1. verify_rows: one CTA per (drafted row, vocabulary slice) for every position
+//     j = 1..ell_r of every request at once.  Each CTA streams its slice of target
+//     row j (and of the draft row when no draft normaliser is given) with 16-byte
+//     loads, reduces the online-softmax statistics (max, sum of exponentials) of
+//     z/T -- the argmax for T = 0 -- and stores them with the scaled logit at the
+//     draft token.  The last CTA of a request merges the slices of each row in a
+//     fixed order and walks the positions, one lane per position: the first j with
+//     u_j >= min(1, p(x_j)/q(x_j)) (or x_j != argmax for T = 0) ends the walk.  The
+//     walk also produces the sampling job of the request: the residual at the
+//     rejecting position, the bonus row when every position is accepted, or
+//     nothing for greedy rejections (their correction is the argmax already found).
+//     Rows past the first rejection are read too: all rows stream in parallel
+//     instead of one position after another.
 //  2. verify_sample: the residual / bonus two-level draw over the vocabulary,
 //     spread over the whole GPU (request x vocabulary chunk, one 32-wide block
 //     per thread), with the last block of each request merging the chunk
 //     partials.
 #include "dspark_internal.cuh"
 
-#include <cooperative_groups.h>
-
-namespace cg = cooperative_groups;
-
 namespace dspark {
 namespace {
 
-constexpr int kChainThreads = 256;
+constexpr int kRowThreads = 128;
+constexpr int kRowCtasPerSm = 4;
 constexpr int kBatch = 4;          // loads in flight per thread in the accept chain (fp32 / unaligned)
 constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per thread
+constexpr int kRowPk = 8;          // packed bf16 16-byte loads per thread and row item
+constexpr int kRowSlice = kRowThreads * 8 * kRowPk;     // vocabulary slice of one row item
 constexpr int kSampleThreads = 256;
 constexpr int kSampleChunk = kSampleThreads * kBlockW;   // one 32-wide block per thread
 
@@ -132,22 +133,6 @@ __device__ __forceinline__ Stats stats_block_reduce(Stats s, Stats *scratch) {
   return s;
 }
 
-struct ChainShared {
-  Stats slot_t[2];          // this CTA's target-row statistics (double-buffered by position parity)
-  Stats slot_d[2];          // draft-row statistics when no normaliser is given
-  float zx_t[2], zx_d[2];   // scaled logit at the draft token, valid in the CTA whose slice holds it
-  Stats red[kChainThreads / 32];
-  int tok[kMaxK];
-  float own_t, own_d;       // written by the thread that streams the draft token's element
-  int skip;
-  int decision;             // 1 accept, 0 reject
-  int amax;
-  float lse_t, lse_q;
-};
-
-// Slice [lo, hi) of the vocabulary owned by cluster rank `rank` (8-aligned).
-__device__ __forceinline__ int slice_per(int V, int ncta) { return ((V + ncta - 1) / ncta + 7) & ~7; }
-
 __device__ __forceinline__ float pick8(const float (&x)[8], int q) {
   float v = x[0];
 #pragma unroll
@@ -156,247 +141,333 @@ __device__ __forceinline__ float pick8(const float (&x)[8], int q) {
   return v;
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kChainThreads, 2) verify_chain(const __grid_constant__ VerifyArgs a) {
-  __shared__ ChainShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int ncta = (int)cluster.num_blocks();
-  const int r = blockIdx.x / ncta;
-  const int tid = threadIdx.x;
-  const int V = (int)a.V, K = (int)a.K_max;
+__device__ __forceinline__ __nv_bfloat162 bf162_word(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); }
 
-  // rank 0 decides for the whole cluster whether an earlier error stops the work
-  if (rank == 0 && tid == 0) sh.skip = read_status(a.dev_status);
-  cluster.sync();
-  const int skip = *cluster.map_shared_rank(&sh.skip, 0);
-  if (skip) { cluster.sync(); return; }
+__device__ __forceinline__ Partial stats_to_partial(const Stats &s) {
+  Partial p;
+  p.best = s.best;
+  p.idx = s.idx;
+  p.m = s.m;
+  p.S = s.S;
+  return p;
+}
+__device__ __forceinline__ Stats partial_to_stats(const Partial &p) {
+  Stats s;
+  s.best = p.best;
+  s.idx = p.idx;
+  s.m = p.m;
+  s.S = p.S;
+  return s;
+}
 
-  // -- validation (identical in every CTA of the cluster) --------------------
+// Request checks shared by every CTA of the request (identical results everywhere).
+// o0, o1: tgt_off[r], tgt_off[r + 1]; of: tgt_off[0].
+__device__ __forceinline__ int request_error(int K, int r, int l, float T, int64_t o0, int64_t o1, int64_t of) {
+  if (l < 0 || l > K) return DSPARK_ERR_LENGTHS;
+  if (o1 - o0 != l + 1 || (r == 0 && of != 0)) return DSPARK_ERR_OFFSETS;
+  if (!temperature_ok(T)) return DSPARK_ERR_TEMPERATURE;
+  return 0;
+}
+
+// One row item of the statistics pass: vocabulary slice sl of drafted row rowi = r K + j - 1.
+struct RowItem {
+  int rowi, x, lo, hi;   // the slice is [lo, hi)
+  int kind;              // 0 nothing to stream, 1 softmax statistics (T > 0), 2 argmax (T = 0)
+  float invT;
+  int64_t trow;          // first element of the target row
+};
+
+// Metadata of item `item` (row-major over rows, then slices), the same in every thread.
+// An invalid request raises the status word once (slice 0 of row 1, or of the row with
+// the bad token) and streams nothing.
+__device__ __forceinline__ RowItem row_item(const VerifyArgs &a, int item, int tid) {
+  const int K = (int)a.K_max, V = (int)a.V, S = a.row_slices;
+  RowItem it;
+  it.rowi = item / S;
+  const int sl = item % S;
+  const int r = it.rowi / K, j = it.rowi % K + 1;
+  it.kind = 0;
+  // every value is requested before any is used: one round trip
   const int l = a.ell[r];
   const float T = a.temperature[r];
-  int err = 0;
-  if (l < 0 || l > K) err = DSPARK_ERR_LENGTHS;
-  else if (a.tgt_off[r + 1] - a.tgt_off[r] != l + 1 || (r == 0 && a.tgt_off[0] != 0)) err = DSPARK_ERR_OFFSETS;
-  else if (!temperature_ok(T)) err = DSPARK_ERR_TEMPERATURE;
-  else
-    for (int j = 0; j < l; ++j) {
-      const int x = a.draft_tok[(int64_t)r * K + j];
-      if (x < 0 || x >= V) { err = DSPARK_ERR_TOKEN_RANGE; break; }
-    }
+  const int x = a.draft_tok[it.rowi];
+  const int64_t o0 = a.tgt_off[r], o1 = a.tgt_off[r + 1], of = a.tgt_off[0];
+  const int err = request_error(K, r, l, T, o0, o1, of);
   if (err) {
-    if (rank == 0 && tid == 0) set_status(a.dev_status, err);
-    cluster.sync();
+    if (sl == 0 && j == 1 && tid == 0) set_status(a.dev_status, err);
+    return it;
+  }
+  if (j > l) return it;
+  if (x < 0 || x >= V) {
+    if (sl == 0 && tid == 0) set_status(a.dev_status, DSPARK_ERR_TOKEN_RANGE);
+    return it;
+  }
+  it.x = x;
+  it.kind = (T == 0.0f) ? 2 : 1;
+  it.invT = (T == 0.0f) ? 1.0f : 1.0f / T;
+  it.trow = (o0 + j - 1) * (int64_t)V;
+  it.lo = min(V, sl * kRowSlice);
+  it.hi = min(V, it.lo + kRowSlice);
+  return it;
+}
+
+// bf16 rows, 16-byte aligned: the item's kRowPk packed loads per thread.
+__device__ __forceinline__ void row_issue(const VerifyArgs &a, const RowItem &it, int tid, uint4 (&pk)[kRowPk]) {
+#pragma unroll
+  for (int uu = 0; uu < kRowPk; ++uu) {
+    const int v0 = it.lo + (uu * kRowThreads + tid) * 8;
+    pk[uu] = (it.kind && v0 + 8 <= it.hi) ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + it.trow + v0))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The item's statistics from its packed loads: the thread's maximum over its 8 kRowPk
+// values first (bf16 pairs, exact), then one pass of exponentials against it, two lanes per
+// fp32 instruction; slots past the slice hold -inf.
+__device__ __forceinline__ void row_consume(const RowItem &it, uint4 (&pk)[kRowPk], int tid, Stats &st,
+                                            float *own_t) {
+#pragma unroll
+  for (int uu = 0; uu < kRowPk; ++uu)
+    if (it.lo + (uu * kRowThreads + tid) * 8 + 8 > it.hi) pk[uu] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  // the 32 pair words of the thread, in element order
+#define W_(e) word_of(pk[(e) >> 2], (e) & 3)
+  __nv_bfloat162 m2[4] = {bf162_word(W_(0)), bf162_word(W_(1)), bf162_word(W_(2)), bf162_word(W_(3))};
+#pragma unroll
+  for (int e = 4; e < 4 * kRowPk; ++e) m2[e & 3] = __hmax2(m2[e & 3], bf162_word(W_(e)));
+  m2[0] = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
+  const float zmax = fmaxf(__low2float(m2[0]), __high2float(m2[0]));
+  if (zmax == -INFINITY) return;
+  if (it.kind == 2) {                     // argmax: the first element equal to the maximum
+    int idx = -1;
+#pragma unroll
+    for (int e = 4 * kRowPk - 1; e >= 0; --e) {
+      const int v = it.lo + ((e >> 2) * kRowThreads + tid) * 8 + 2 * (e & 3);
+      if (__uint_as_float(W_(e) & 0xffff0000u) == zmax) idx = v + 1;
+      if (__uint_as_float(W_(e) << 16) == zmax) idx = v;
+    }
+    st.best = zmax;
+    st.idx = idx;
     return;
   }
-  if (tid < l) sh.tok[tid] = a.draft_tok[(int64_t)r * K + tid];
+  const float m = zmax * it.invT;         // max(z) / T = max(z / T): scaling by 1/T > 0 is monotone
+  const float mL = m * kLog2e;
+  const unsigned long long ti = f2_pack(it.invT, it.invT), l2 = f2_pack(kLog2e, kLog2e), nm = f2_pack(-mL, -mL);
+  unsigned long long s0 = f2_pack(0.0f, 0.0f), s1 = s0;
+#pragma unroll
+  for (int e = 0; e < 4 * kRowPk; ++e) {
+    const uint32_t we = W_(e);
+    const unsigned long long sc = f2_mul(f2_pack(__uint_as_float(we << 16), __uint_as_float(we & 0xffff0000u)), ti);
+    float y0, y1;
+    f2_unpack(f2_fma(sc, l2, nm), y0, y1);
+    const unsigned long long ee = f2_pack(fast_ex2(y0), fast_ex2(y1));
+    if (e & 1) s1 = f2_add(s1, ee);
+    else s0 = f2_add(s0, ee);
+    if (it.lo + ((e >> 2) * kRowThreads + tid) * 8 + 2 * (e & 3) == (it.x & ~1)) {   // the pair holding x
+      *own_t = __uint_as_float((it.x & 1) ? (we & 0xffff0000u) : (we << 16)) * it.invT;
+    }
+  }
+  float a0, a1, b0, b1;
+  f2_unpack(s0, a0, a1);
+  f2_unpack(s1, b0, b1);
+  st.m = m;
+  st.S = (a0 + a1) + (b0 + b1);
+#undef W_
+}
 
+// Any dtype / alignment, and the draft row when no draft normaliser is given.
+template <int DT, bool VEC>
+__device__ __forceinline__ void row_generic(const VerifyArgs &a, const RowItem &it, bool stream_d, int tid, Stats &st,
+                                            Stats &sd, float *own_t, float *own_d) {
+  const int xv = it.x & ~7;
+  const int64_t it_V = a.V;
+  for (int base = it.lo + tid * 8; base < it.hi; base += kRowThreads * 8 * kBatch) {
+    float x8[kBatch][8];
+#pragma unroll
+    for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.tgt, it.trow, base + uu * kRowThreads * 8, it.hi, x8[uu]);
+    if (it.kind == 2) {
+#pragma unroll
+      for (int uu = 0; uu < kBatch; ++uu) argmax_add8(st, x8[uu], base + uu * kRowThreads * 8);
+      continue;
+    }
+    float y8[kBatch][8];
+    if (stream_d) {
+#pragma unroll
+      for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.D, (int64_t)it.rowi * it_V, base + uu * kRowThreads * 8, it.hi, y8[uu]);
+    }
+#pragma unroll
+    for (int uu = 0; uu < kBatch; ++uu) {
+      const int v0 = base + uu * kRowThreads * 8;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) x8[uu][q] *= it.invT;
+      if (v0 == xv) *own_t = pick8(x8[uu], it.x & 7);
+      stats_add8(st, x8[uu]);
+      if (stream_d) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y8[uu][q] *= it.invT;
+        if (v0 == xv) *own_d = pick8(y8[uu], it.x & 7);
+        stats_add8(sd, y8[uu]);
+      }
+    }
+  }
+}
+
+// Merge of the slice statistics of drafted row rowi (one warp, lanes over slices, then a
+// fixed shuffle tree: the result does not depend on which CTA streamed which slice).
+// Valid in lane 0.
+__device__ __forceinline__ RowRes row_merge(const VerifyArgs &a, int64_t rowi, bool greedy, bool stream_d, int lane) {
+  const int S = a.row_slices;
+  const bool sd_on = !greedy && stream_d;
+  Stats ct, cd;
+  stats_init(ct);
+  stats_init(cd);
+  const float zt = greedy ? 0.0f : __ldcg(a.zx_t + rowi);
+  const float zd = sd_on ? __ldcg(a.zx_d + rowi) : 0.0f;
+  for (int q = lane; q < S; q += 32) {
+    stats_merge(ct, partial_to_stats(load_partial(a.row_t + rowi * S + q)));
+    if (sd_on) stats_merge(cd, partial_to_stats(load_partial(a.row_d + rowi * S + q)));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    stats_merge(ct, stats_shfl_down(ct, d));
+    if (sd_on) stats_merge(cd, stats_shfl_down(cd, d));
+  }
+  RowRes rr;
+  rr.amax = ct.idx;
+  rr.lse_t = greedy ? ct.best : ct.m + logf(ct.S);
+  rr.zx_t = zt;
+  rr.lse_q = sd_on ? cd.m + logf(cd.S) : 0.0f;
+  rr.zx_d = zd;
+  return rr;
+}
+
+// Statistics pass: persistent CTAs walk the row items (every drafted row of every request,
+// cut into vocabulary slices) with the next item's loads in flight while the current one is
+// reduced.  Per item: the online-softmax statistics (max, sum of exponentials) of the
+// slice of target row j / T -- its argmax for T = 0 -- and of the draft row when no draft
+// normaliser is given, and the scaled logits at the draft token in the slice that holds it.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows(const __grid_constant__ VerifyArgs a) {
+  constexpr bool kPacked = (DT == DSPARK_BF16) && VEC;
+  __shared__ Stats red[kRowThreads / 32];
+  __shared__ float s_own_t, s_own_d;
+  const int tid = threadIdx.x;
+  if (read_status(a.dev_status)) return;
+  const int S = a.row_slices;
+  const int total = (int)(a.B * a.K_max) * S;
+  const bool stream_d = (a.D_lse == nullptr);
+  int item = blockIdx.x;
+  if (item >= total) return;
+  RowItem cur = row_item(a, item, tid);
+  uint4 pc[kRowPk];
+  if (kPacked) row_issue(a, cur, tid, pc);
+  for (; item < total; item += gridDim.x) {
+    const int nitem = item + gridDim.x;
+    RowItem nxt;
+    nxt.kind = 0;
+    if (nitem < total) nxt = row_item(a, nitem, tid);
+    uint4 pn[kRowPk];
+    if (kPacked) row_issue(a, nxt, tid, pn);   // in flight while this item is reduced
+    if (cur.kind) {
+      const bool sd_on = stream_d && cur.kind == 1;
+      Stats st, sd;
+      stats_init(st);
+      stats_init(sd);
+      if (kPacked && !sd_on) row_consume(cur, pc, tid, st, &s_own_t);
+      else row_generic<DT, VEC>(a, cur, sd_on, tid, st, sd, &s_own_t, &s_own_d);
+      st = stats_block_reduce(st, red);
+      if (sd_on) sd = stats_block_reduce(sd, red);
+      if (tid == 0) {
+        const int sl = cur.lo / kRowSlice;
+        a.row_t[(int64_t)cur.rowi * S + sl] = stats_to_partial(st);
+        if (sd_on) a.row_d[(int64_t)cur.rowi * S + sl] = stats_to_partial(sd);
+        if (cur.kind == 1 && cur.x >= cur.lo && cur.x < cur.hi) {
+          a.zx_t[cur.rowi] = s_own_t;
+          if (sd_on) a.zx_d[cur.rowi] = s_own_d;
+        }
+      }
+      __syncthreads();   // s_own_* and the reduction scratch are reused by the next item
+    }
+    cur = nxt;
+#pragma unroll
+    for (int q = 0; q < kRowPk; ++q) pc[q] = pn[q];
+  }
+}
+
+// The accept walk of request r from its merged rows (one warp; lane j - 1 tests position
+// j, the first rejection ends the walk): the sampling job, and with write_out the
+// accepted tokens, the padding and n_acc.  A greedy rejection's correction (the argmax)
+// is written here too.
+template <int DT>
+__device__ void decide_request(const VerifyArgs &a, int r, int lane, bool write_out, const RowRes *rows,
+                               VerifyJob *out_job) {
+  const int K = (int)a.K_max;
+  const int l = a.ell[r];
+  const float T = a.temperature[r];
   const bool greedy = (T == 0.0f);
   const float invT = greedy ? 1.0f : 1.0f / T;
   const int64_t off = a.tgt_off[r];
-  const bool have_lse = (a.D_lse != nullptr);
-  const bool stream_d = !greedy && !have_lse;
-  const int per = slice_per(V, ncta);
-  const int lo = min(V, rank * per), hi = min(V, lo + per);
-  __syncthreads();
-
-  int n = 0;
-  bool rejected = false;
-  int rej_j = 0;
-  float lse_t = 0.0f, lse_q = 0.0f;
-  int greedy_tok = -1;
-  for (int j = 1; j <= l; ++j) {
-    const int x = sh.tok[j - 1];
-    const int64_t trow = (off + j - 1) * (int64_t)V;
-    const int64_t drow = ((int64_t)r * K + j - 1) * (int64_t)V;
-    // values only thread 0 needs, requested before the row stream so their latency overlaps it
-    float u = 0.0f, dx = 0.0f, lq_given = 0.0f;
-    if (tid == 0 && !greedy) {
-      u = uniform_accept(philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept).x);
-      if (have_lse) {
-        dx = load1<DT>(a.D, drow + x);
-        lq_given = a.D_lse[(int64_t)r * K + j - 1];
-      }
-    }
-    const int xv = x & ~7;   // start of the 8-element group holding x
-    Stats st, sd;
-    stats_init(st);
-    stats_init(sd);
-    if (DT == DSPARK_BF16 && VEC) {
-      // bf16 rows: keep kPkBatch packed 16-byte loads per thread in flight, unpack when consumed
-      const int nb = stream_d ? kPkBatch / 2 : kPkBatch;
-      for (int base = lo + tid * 8; base < hi; base += kChainThreads * 8 * nb) {
-        uint4 pt[kPkBatch];
-#pragma unroll
-        for (int uu = 0; uu < kPkBatch; ++uu) {
-          const int v0 = base + uu * kChainThreads * 8;
-          const bool in = (uu < nb) && (v0 + 8 <= hi);
-          pt[uu] = in ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + trow + v0)) : make_uint4(0, 0, 0, 0);
-        }
-        uint4 pd[kPkBatch / 2];
-        if (stream_d) {
-#pragma unroll
-          for (int uu = 0; uu < kPkBatch / 2; ++uu) {
-            const int v0 = base + uu * kChainThreads * 8;
-            pd[uu] = (v0 + 8 <= hi) ? __ldcs((const uint4 *)((const unsigned short *)a.D + drow + v0))
-                                    : make_uint4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int uu = 0; uu < kPkBatch; ++uu) {
-          const int v0 = base + uu * kChainThreads * 8;
-          if (uu >= nb || v0 + 8 > hi) continue;
-          float x8[8];
-          const uint32_t w4[4] = {pt[uu].x, pt[uu].y, pt[uu].z, pt[uu].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            x8[2 * i] = __uint_as_float(w4[i] << 16);
-            x8[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
-          }
-          if (greedy) {
-            argmax_add8(st, x8, v0);
-            continue;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x8[q] *= invT;
-          if (v0 == xv) sh.own_t = pick8(x8, x & 7);
-          stats_add8(st, x8);
-          if (stream_d && uu < kPkBatch / 2) {
-            float y8[8];
-            const uint32_t d4[4] = {pd[uu].x, pd[uu].y, pd[uu].z, pd[uu].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              y8[2 * i] = __uint_as_float(d4[i] << 16) * invT;
-              y8[2 * i + 1] = __uint_as_float(d4[i] & 0xffff0000u) * invT;
-            }
-            if (v0 == xv) sh.own_d = pick8(y8, x & 7);
-            stats_add8(sd, y8);
-          }
-        }
-      }
+  const int j = lane + 1;
+  bool reject = false;
+  int amax = -1, x = -1;
+  float lt = 0.0f, lq = 0.0f;
+  if (j <= l) {
+    const int64_t rowi = (int64_t)r * K + j - 1;
+    x = a.draft_tok[rowi];
+    const RowRes rr = rows[j - 1];
+    amax = rr.amax;
+    if (greedy) {
+      reject = (x != rr.amax);
     } else {
-      // kBatch 16-byte loads per thread are issued before any of them is consumed
-      for (int base = lo + tid * 8; base < hi; base += kChainThreads * 8 * kBatch) {
-        float x8[kBatch][8];
-#pragma unroll
-        for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.tgt, trow, base + uu * kChainThreads * 8, hi, x8[uu]);
-        if (greedy) {
-#pragma unroll
-          for (int uu = 0; uu < kBatch; ++uu) argmax_add8(st, x8[uu], base + uu * kChainThreads * 8);
-          continue;
-        }
-        float y8[kBatch][8];
-        if (stream_d) {
-#pragma unroll
-          for (int uu = 0; uu < kBatch; ++uu) load8<DT, VEC>(a.D, drow, base + uu * kChainThreads * 8, hi, y8[uu]);
-        }
-#pragma unroll
-        for (int uu = 0; uu < kBatch; ++uu) {
-          const int v0 = base + uu * kChainThreads * 8;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x8[uu][q] *= invT;
-          if (v0 == xv) sh.own_t = pick8(x8[uu], x & 7);
-          stats_add8(st, x8[uu]);
-          if (stream_d) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) y8[uu][q] *= invT;
-            if (v0 == xv) sh.own_d = pick8(y8[uu], x & 7);
-            stats_add8(sd, y8[uu]);
-          }
-        }
-      }
-    }
-    st = stats_block_reduce(st, sh.red);
-    if (stream_d) sd = stats_block_reduce(sd, sh.red);
-    if (tid == 0) {
-      sh.slot_t[j & 1] = st;
-      sh.slot_d[j & 1] = sd;
-      const bool mine = (x >= lo && x < hi);
-      sh.zx_t[j & 1] = mine ? sh.own_t : 0.0f;
-      sh.zx_d[j & 1] = mine ? sh.own_d : 0.0f;
-    }
-    cluster.sync();
-    if (tid == 0) {
-      Stats parts_t[8], parts_d[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < ncta) {
-          parts_t[q] = *cluster.map_shared_rank(&sh.slot_t[j & 1], q);
-          if (stream_d) parts_d[q] = *cluster.map_shared_rank(&sh.slot_d[j & 1], q);
-        }
-      Stats ct, cd;
-      stats_init(ct);
-      stats_init(cd);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < ncta) {
-          stats_merge(ct, parts_t[q]);
-          if (stream_d) stats_merge(cd, parts_d[q]);
-        }
-      if (greedy) {
-        sh.decision = (x == ct.idx);
-        sh.amax = ct.idx;
+      const float u = uniform_accept(philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept).x);
+      lt = rr.lse_t;
+      float lq_x;
+      if (a.D_lse != nullptr) {
+        lq = a.D_lse[rowi];
+        lq_x = load1<DT>(a.D, rowi * a.V + x) * invT - lq;
       } else {
-        const int owner = x / per;
-        const float sx = *cluster.map_shared_rank(&sh.zx_t[j & 1], owner);
-        const float lt = ct.m + logf(ct.S);
-        float lq_x;
-        if (have_lse) {
-          lq_x = dx * invT - lq_given;
-          sh.lse_q = lq_given;
-        } else {
-          const float sdx = *cluster.map_shared_rank(&sh.zx_d[j & 1], owner);
-          const float ld = cd.m + logf(cd.S);
-          lq_x = sdx - ld;
-          sh.lse_q = ld;
-        }
-        sh.decision = u < expf((sx - lt) - lq_x);
-        sh.lse_t = lt;
+        lq = rr.lse_q;
+        lq_x = rr.zx_d - lq;
       }
+      reject = !(u < expf((rr.zx_t - lt) - lq_x));
     }
-    __syncthreads();
-    if (!sh.decision) {
-      rejected = true;
-      rej_j = j;
-      lse_t = sh.lse_t;
-      lse_q = sh.lse_q;
-      greedy_tok = sh.amax;
-      break;
-    }
-    if (rank == 0 && tid == 0) a.out_tok[(int64_t)r * (K + 1) + n] = x;
-    ++n;
   }
-
-  if (rank == 0 && tid == 0) {
-    a.n_acc[r] = n;
-    for (int q = n + 1; q <= K; ++q) a.out_tok[(int64_t)r * (K + 1) + q] = -1;
+  const unsigned rej = __ballot_sync(0xffffffffu, reject);
+  const int n = rej ? __ffs(rej) - 1 : l;                 // accepted drafts
+  const float lt_n = __shfl_sync(0xffffffffu, lt, n & 31);
+  const float lq_n = __shfl_sync(0xffffffffu, lq, n & 31);
+  const int amax_n = __shfl_sync(0xffffffffu, amax, n & 31);
+  if (write_out && lane <= K) {
+    int32_t *out = a.out_tok + (int64_t)r * (K + 1);
+    if (lane < n) out[lane] = x;
+    else if (lane > n) out[lane] = -1;
+  }
+  if (lane == 0) {
     VerifyJob job;
     job.mode = 0;
     job.pos = 0;
     job.trow = 0;
     job.drow = 0;
-    job.lse_t = lse_t;
-    job.lse_q = lse_q;
+    job.lse_t = lt_n;
+    job.lse_q = lq_n;
     job.invT = invT;
     job.out_slot = r * (K + 1) + n;
-    if (rejected) {
+    if (rej) {
       if (greedy) {
-        a.out_tok[(int64_t)r * (K + 1) + n] = greedy_tok;
+        if (write_out) a.out_tok[(int64_t)r * (K + 1) + n] = amax_n;
       } else {
         job.mode = 1;
-        job.pos = rej_j;
-        job.trow = off + rej_j - 1;
-        job.drow = (int64_t)r * K + rej_j - 1;
+        job.pos = n + 1;
+        job.trow = off + n;
+        job.drow = (int64_t)r * K + n;
       }
     } else {
       job.mode = greedy ? 3 : 2;
       job.pos = l + 1;
       job.trow = off + l;
     }
-    a.jobs[r] = job;
-    a.counters[r] = 0;
+    if (write_out) a.n_acc[r] = n;
+    *out_job = job;
   }
-  cluster.sync();   // peers may still read this CTA's slots
 }
 
 // --------------------------------------------------------------------------
@@ -474,10 +545,28 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
   __shared__ Race red[kSampleThreads / 32];
   __shared__ int s_any[kSampleThreads / 32];
   __shared__ int s_last, s_tok;
+  __shared__ VerifyJob s_job;
+  __shared__ RowRes s_rows[kMaxK];
   const int cx = blockIdx.x, tid = threadIdx.x;
   if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max;
   for (int r = blockIdx.y; r < (int)a.B; r += gridDim.y) {
-    const VerifyJob job = a.jobs[r];
+    // every chunk merges the request's row statistics (a warp per row) and walks its
+    // positions -- the same decision everywhere; chunk 0 writes the accepted tokens
+    {
+      const bool greedy = a.temperature[r] == 0.0f;
+      const bool stream_d = (a.D_lse == nullptr);
+      const int l = a.ell[r];
+      for (int jw = tid >> 5; jw < l; jw += kSampleThreads / 32) {
+        const RowRes rr = row_merge(a, (int64_t)r * K + jw, greedy, stream_d, tid & 31);
+        if ((tid & 31) == 0) s_rows[jw] = rr;
+      }
+    }
+    __syncthreads();
+    if (tid < 32) decide_request<DT>(a, r, tid, cx == 0, s_rows, &s_job);
+    __syncthreads();
+    const VerifyJob job = s_job;
+    __syncthreads();
     if (job.mode == 0) continue;
     const int V = (int)a.V;
     const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
@@ -537,38 +626,59 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
 
 template <int DT, bool VEC>
 cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, int num_sms) {
-  int cl = 1;
-  const int64_t target = 2LL * num_sms;
-  while (cl < 8 && a.B * cl * 2 <= target) cl *= 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.B * cl), 1, 1);
-  cfg.blockDim = dim3(kChainThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_chain<DT, VEC>, a);
-  if (e != cudaSuccess) return e;
+  const int64_t items = a.B * a.K_max * (int64_t)a.row_slices;
+  const int64_t grid = items < (int64_t)kRowCtasPerSm * num_sms ? items : (int64_t)kRowCtasPerSm * num_sms;
+  if (grid > 0) {
+    verify_rows<DT, VEC><<<(unsigned)grid, kRowThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)(a.B < 65535 ? a.B : 65535)), kSampleThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice); }
+
+// Workspace layout (every part 256-byte aligned): chunk counters [B] (zeroed at the start
+// of every call), sampling partials [B * chunks], slice statistics of the target and draft
+// rows [B * kMaxK * slices] each, scaled logits at the draft tokens [B * kMaxK] each.  Rows
+// are sized for kMaxK positions so the size depends on B and V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   const int c = (int)((V + kSampleChunk - 1) / kSampleChunk);
   if (chunks) *chunks = c;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al(sizeof(VerifyJob) * (size_t)B) + al(sizeof(int32_t) * (size_t)B) +
-         al(sizeof(Partial) * (size_t)B * (size_t)c);
+  const size_t rows = (size_t)B * (size_t)kMaxK;
+  return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) +
+         2 * al(sizeof(Partial) * rows * verify_row_slices(V)) + 2 * al(sizeof(float) * rows);
+}
+
+void verify_carve(VerifyArgs &a, void *workspace) {
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t rows = (size_t)a.B * (size_t)kMaxK;
+  int chunks = 1;
+  verify_ws_bytes(a.B, a.V, &chunks);
+  a.chunks = chunks;
+  a.row_slices = verify_row_slices(a.V);
+  char *p = (char *)workspace;
+  a.counters = (int32_t *)p;
+  p += al(sizeof(int32_t) * (size_t)a.B);
+  a.partials = (Partial *)p;
+  p += al(sizeof(Partial) * (size_t)a.B * (size_t)chunks);
+  a.row_t = (Partial *)p;
+  p += al(sizeof(Partial) * rows * a.row_slices);
+  a.row_d = (Partial *)p;
+  p += al(sizeof(Partial) * rows * a.row_slices);
+  a.zx_t = (float *)p;
+  p += al(sizeof(float) * rows);
+  a.zx_d = (float *)p;
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms) {
+  // arrival counters start from zero on every call (the workspace may be fresh)
+  cudaError_t e0 = cudaMemsetAsync(a.counters, 0, sizeof(int32_t) * (size_t)a.B, s);
+  if (e0 != cudaSuccess) return e0;
   const int esz = a.dtype == DSPARK_F32 ? 4 : 2;
   const bool vec = ((a.V * esz) % 16 == 0) && ((uintptr_t)a.tgt % 16 == 0) && ((uintptr_t)a.D % 16 == 0);
   if (a.dtype == DSPARK_F32)
