@@ -16,9 +16,9 @@
 //     Rows past the first rejection are read too: all rows stream in parallel
 //     instead of one position after another.
 //  2. verify_sample: the residual / bonus two-level draw over the vocabulary,
-//     spread over the whole GPU (request x vocabulary chunk, one 32-wide block
-//     per thread), with the last block of each request merging the chunk
-//     partials.
+//     spread over the whole GPU (request x vocabulary chunk, about two CTAs per
+//     SM in one wave, each thread a run of 32-wide blocks), with the last block of
+//     each request merging the chunk partials.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -31,7 +31,7 @@ constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per th
 constexpr int kRowPk = 8;          // packed bf16 16-byte loads per thread and row item
 constexpr int kRowSlice = kRowThreads * 8 * kRowPk;     // vocabulary slice of one row item
 constexpr int kSampleThreads = 256;
-constexpr int kSampleChunk = kSampleThreads * kBlockW;   // one 32-wide block per thread
+constexpr int kSampleUnit = kSampleThreads * kBlockW;   // one 32-wide block per thread
 
 struct Stats {
   float m, S;   // online softmax
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
     __syncthreads();
     if (job.mode == 0) continue;
     const int V = (int)a.V;
-    const int lo = min(V, cx * kSampleChunk), hi = min(V, lo + kSampleChunk);
+    const int lo = min(V, cx * a.chunk_len), hi = min(V, lo + a.chunk_len);
     BRace br;
     brace_init(br);
     bool any_pos = false;
@@ -625,7 +625,16 @@ __global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_con
 }
 
 template <int DT, bool VEC>
-cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, int num_sms) {
+cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms) {
+  // sampling chunks: about two CTAs per SM over all requests in one wave, each chunk a
+  // multiple of 32 columns (the blocks of the two-level draw) and at most a.chunks of them
+  {
+    const int64_t want = (2LL * num_sms) / a.B;
+    const int c = (int)(want < 1 ? 1 : (want > a.chunks ? a.chunks : want));
+    const int64_t per = (a.V + c - 1) / c;
+    a.chunk_len = (int)((per + kBlockW - 1) / kBlockW * kBlockW);
+    a.chunks = (int)((a.V + a.chunk_len - 1) / a.chunk_len);
+  }
   const int64_t items = a.B * a.K_max * (int64_t)a.row_slices;
   const int64_t grid = items < (int64_t)kRowCtasPerSm * num_sms ? items : (int64_t)kRowCtasPerSm * num_sms;
   if (grid > 0) {
@@ -646,7 +655,7 @@ int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice)
 // rows [B * kMaxK * slices] each, scaled logits at the draft tokens [B * kMaxK] each.  Rows
 // are sized for kMaxK positions so the size depends on B and V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
-  const int c = (int)((V + kSampleChunk - 1) / kSampleChunk);
+  const int c = (int)((V + kSampleUnit - 1) / kSampleUnit);   // the most chunks a call uses
   if (chunks) *chunks = c;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)B * (size_t)kMaxK;
