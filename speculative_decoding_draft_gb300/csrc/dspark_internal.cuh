@@ -597,7 +597,7 @@ struct VerifyArgs {
   Partial *partials;   // [B * chunks]
   int chunks;          // vocabulary chunks of the sampling pass (at most the workspace's)
   int chunk_len;       // columns per chunk, a multiple of 32
-  Partial *row_t, *row_d;   // [B * kMaxK * row_slices] target / draft row statistics per slice
+  Partial *row_t, *row_d;   // [B * kMaxK * row_slices * 4] target / draft statistics per slice and warp
   float *zx_t, *zx_d;       // [B * kMaxK] scaled logits at the draft tokens
   int row_slices;           // vocabulary slices per row of the statistics pass
 };

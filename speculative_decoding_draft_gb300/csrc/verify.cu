@@ -25,11 +25,12 @@ namespace dspark {
 namespace {
 
 constexpr int kRowThreads = 128;
-constexpr int kRowCtasPerSm = 4;
+constexpr int kRowCtasPerSm = 3;
 constexpr int kBatch = 4;          // loads in flight per thread in the accept chain (fp32 / unaligned)
 constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per thread
-constexpr int kRowPk = 8;          // packed bf16 16-byte loads per thread and row item
+constexpr int kRowPk = 12;          // packed bf16 16-byte loads per thread and row item
 constexpr int kRowSlice = kRowThreads * 8 * kRowPk;     // vocabulary slice of one row item
+constexpr int kRowParts = kRowThreads / 32;              // partial statistics per item: one per warp
 constexpr int kSampleThreads = 256;
 constexpr int kSampleUnit = kSampleThreads * kBlockW;   // one 32-wide block per thread
 
@@ -322,9 +323,9 @@ __device__ __forceinline__ RowRes row_merge(const VerifyArgs &a, int64_t rowi, b
   stats_init(cd);
   const float zt = greedy ? 0.0f : __ldcg(a.zx_t + rowi);
   const float zd = sd_on ? __ldcg(a.zx_d + rowi) : 0.0f;
-  for (int q = lane; q < S; q += 32) {
-    stats_merge(ct, partial_to_stats(load_partial(a.row_t + rowi * S + q)));
-    if (sd_on) stats_merge(cd, partial_to_stats(load_partial(a.row_d + rowi * S + q)));
+  for (int q = lane; q < S * kRowParts; q += 32) {
+    stats_merge(ct, partial_to_stats(load_partial(a.row_t + rowi * S * kRowParts + q)));
+    if (sd_on) stats_merge(cd, partial_to_stats(load_partial(a.row_d + rowi * S * kRowParts + q)));
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -340,6 +341,33 @@ __device__ __forceinline__ RowRes row_merge(const VerifyArgs &a, int64_t rowi, b
   return rr;
 }
 
+// Warp reduction of one item's statistics, valid in lane 0: the softmax pair (m, S) for
+// T > 0 (a branch-free merge), the (maximum, smallest index) pair for T = 0.
+__device__ __forceinline__ Stats warp_reduce_row(Stats s, int kind) {
+  if (kind == 1) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float m2 = __shfl_down_sync(0xffffffffu, s.m, d), S2 = __shfl_down_sync(0xffffffffu, s.S, d);
+      const float M = fmaxf(s.m, m2);
+      if (M != -INFINITY) {
+        s.S = s.S * fast_ex2((s.m - M) * kLog2e) + S2 * fast_ex2((m2 - M) * kLog2e);
+        s.m = M;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float b2 = __shfl_down_sync(0xffffffffu, s.best, d);
+      const int i2 = __shfl_down_sync(0xffffffffu, s.idx, d);
+      if (i2 >= 0 && (b2 > s.best || (b2 == s.best && (s.idx < 0 || i2 < s.idx)))) {
+        s.best = b2;
+        s.idx = i2;
+      }
+    }
+  }
+  return s;
+}
+
 // Statistics pass: persistent CTAs walk the row items (every drafted row of every request,
 // cut into vocabulary slices) with the next item's loads in flight while the current one is
 // reduced.  Per item: the online-softmax statistics (max, sum of exponentials) of the
@@ -348,9 +376,7 @@ __device__ __forceinline__ RowRes row_merge(const VerifyArgs &a, int64_t rowi, b
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows(const __grid_constant__ VerifyArgs a) {
   constexpr bool kPacked = (DT == DSPARK_BF16) && VEC;
-  __shared__ Stats red[kRowThreads / 32];
-  __shared__ float s_own_t, s_own_d;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (read_status(a.dev_status)) return;
   const int S = a.row_slices;
   const int total = (int)(a.B * a.K_max) * S;
@@ -372,20 +398,16 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows(const 
       Stats st, sd;
       stats_init(st);
       stats_init(sd);
-      if (kPacked && !sd_on) row_consume(cur, pc, tid, st, &s_own_t);
-      else row_generic<DT, VEC>(a, cur, sd_on, tid, st, sd, &s_own_t, &s_own_d);
-      st = stats_block_reduce(st, red);
-      if (sd_on) sd = stats_block_reduce(sd, red);
-      if (tid == 0) {
-        const int sl = cur.lo / kRowSlice;
-        a.row_t[(int64_t)cur.rowi * S + sl] = stats_to_partial(st);
-        if (sd_on) a.row_d[(int64_t)cur.rowi * S + sl] = stats_to_partial(sd);
-        if (cur.kind == 1 && cur.x >= cur.lo && cur.x < cur.hi) {
-          a.zx_t[cur.rowi] = s_own_t;
-          if (sd_on) a.zx_d[cur.rowi] = s_own_d;
-        }
+      // the thread that holds the draft token writes its scaled logits directly
+      if (kPacked && !sd_on) row_consume(cur, pc, tid, st, a.zx_t + cur.rowi);
+      else row_generic<DT, VEC>(a, cur, sd_on, tid, st, sd, a.zx_t + cur.rowi, a.zx_d + cur.rowi);
+      st = warp_reduce_row(st, cur.kind);
+      if (sd_on) sd = warp_reduce_row(sd, 1);
+      if (lane == 0) {
+        const int64_t at = ((int64_t)cur.rowi * S + cur.lo / kRowSlice) * kRowParts + warp;
+        a.row_t[at] = stats_to_partial(st);
+        if (sd_on) a.row_d[at] = stats_to_partial(sd);
       }
-      __syncthreads();   // s_own_* and the reduction scratch are reused by the next item
     }
     cur = nxt;
 #pragma unroll
@@ -652,7 +674,7 @@ int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice)
 
 // Workspace layout (every part 256-byte aligned): chunk counters [B] (zeroed at the start
 // of every call), sampling partials [B * chunks], slice statistics of the target and draft
-// rows [B * kMaxK * slices] each, scaled logits at the draft tokens [B * kMaxK] each.  Rows
+// rows [B * kMaxK * slices * warps] each, scaled logits at the draft tokens [B * kMaxK] each.  Rows
 // are sized for kMaxK positions so the size depends on B and V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   const int c = (int)((V + kSampleUnit - 1) / kSampleUnit);   // the most chunks a call uses
@@ -660,7 +682,7 @@ size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)B * (size_t)kMaxK;
   return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) +
-         2 * al(sizeof(Partial) * rows * verify_row_slices(V)) + 2 * al(sizeof(float) * rows);
+         2 * al(sizeof(Partial) * rows * verify_row_slices(V) * kRowParts) + 2 * al(sizeof(float) * rows);
 }
 
 void verify_carve(VerifyArgs &a, void *workspace) {
@@ -676,9 +698,9 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   a.partials = (Partial *)p;
   p += al(sizeof(Partial) * (size_t)a.B * (size_t)chunks);
   a.row_t = (Partial *)p;
-  p += al(sizeof(Partial) * rows * a.row_slices);
+  p += al(sizeof(Partial) * rows * a.row_slices * kRowParts);
   a.row_d = (Partial *)p;
-  p += al(sizeof(Partial) * rows * a.row_slices);
+  p += al(sizeof(Partial) * rows * a.row_slices * kRowParts);
   a.zx_t = (float *)p;
   p += al(sizeof(float) * rows);
   a.zx_d = (float *)p;
