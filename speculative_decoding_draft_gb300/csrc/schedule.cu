@@ -10,6 +10,7 @@
 // Theta_i = tau_i * SPS(R + i) in fp64 with explicitly rounded operations, and
 // the first decline.  Every step is deterministic, so the lengths agree bit
 // for bit with a sequential evaluation of Algorithm 1 in the same arithmetic.
+// Pools whose working arrays fit in about 160 KB are kept in shared memory.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -17,6 +18,10 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+// Candidate pools up to this many bytes of working arrays live in shared memory (one
+// block, so every phase then exchanges data through shared memory instead of L2 round
+// trips); larger pools use the global workspace.
+constexpr size_t kSmemPoolMax = 160 * 1024;
 
 struct SchedWs {
   uint32_t *keyA, *keyB, *idxA, *idxB;
@@ -67,7 +72,8 @@ __device__ T block_exclusive_scan(T v, T *warp_sums, T *total) {
   return prefix + x - v;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_constant__ ScheduleArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_constant__ ScheduleArgs a, int in_smem) {
+  extern __shared__ __align__(256) uint8_t pool[];
   __shared__ uint32_t hist[kWarps][257];
   __shared__ uint32_t wsum32[kWarps];
   __shared__ unsigned long long wsum64[kWarps];
@@ -81,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
   __syncthreads();
   if (s_skip) return;
   const int64_t B = a.B, K = a.K_max, NC = B * K;
-  SchedWs w = carve(a.ws, NC);
+  SchedWs w = carve(in_smem ? (void *)pool : a.ws, NC);
   float *surv_slot = (float *)w.keyB;   // survival in position-major slot order, reused later
 
   // -- validation, survival products, zeroed lengths ------------------------
@@ -247,7 +253,18 @@ size_t schedule_ws_bytes(int64_t B, int64_t K_max) {
 }
 
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
-  schedule_kernel<<<1, kThreads, 0, s>>>(a);
+  const size_t pool_bytes = schedule_ws_bytes(a.B, a.K_max);
+  const bool in_smem = pool_bytes <= kSmemPoolMax;
+  if (in_smem) {
+    static size_t attr_bytes = 0;
+    if (pool_bytes > attr_bytes) {
+      cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemPoolMax);
+      if (e != cudaSuccess) return e;
+      attr_bytes = kSmemPoolMax;
+    }
+  }
+  schedule_kernel<<<1, kThreads, in_smem ? pool_bytes : 0, s>>>(a, in_smem ? 1 : 0);
   return cudaGetLastError();
 }
 
