@@ -78,6 +78,8 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 /* dims.flags bits */
 #define DSPARK_FLAG_FORCE_SIMT 1u /* draft: use the CUDA-core bias path even when the tensor-core path applies */
 #define DSPARK_FLAG_W_PACKED 2u   /* draft: W is the packed projection of dspark_draft_pack_projection */
+#define DSPARK_FLAG_SPARE_SM 4u   /* draft: the tensor-core path leaves one SM free, so that a kernel on
+                                     another stream (the scheduler) runs beside it */
 
 typedef struct {
   int64_t B;      /* requests in the call                                  */

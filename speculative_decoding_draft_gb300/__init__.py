@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "DsparkError", "DsparkUnavailable", "lib", "library_path", "draft_markov_sample", "schedule_survival",
     "verify_ragged", "check", "status_string", "draft_workspace_bytes", "schedule_workspace_bytes",
-    "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_W_PACKED", "STATUS_NAMES", "Dims",
+    "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_W_PACKED", "FLAG_SPARE_SM", "STATUS_NAMES", "Dims",
     "PackedProjection", "pack_projection", "packed_projection_bytes",
 ]
 
@@ -32,6 +32,7 @@ _LIB_PATH = os.path.join(_HERE, "libdspark.so")
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_W_PACKED = 2
+FLAG_SPARE_SM = 4
 
 STATUS_NAMES = {
     0: "DSPARK_OK", 1: "DSPARK_ERR_NULL", 2: "DSPARK_ERR_DIMS", 3: "DSPARK_ERR_DTYPE",
@@ -213,7 +214,8 @@ def new_status(device) -> torch.Tensor:
 # entry points
 # ---------------------------------------------------------------------------
 def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
-                        want_lse: bool = True, force_simt: bool = False, out: Optional[dict] = None,
+                        want_lse: bool = True, force_simt: bool = False, spare_sm: bool = False,
+                        out: Optional[dict] = None,
                         workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                         stream=None) -> dict:
     """Markov-head draft sampling (C ABI dspark_draft_markov_sample).
@@ -223,12 +225,14 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     anchor, K_r [B] int32; temperature [B] float32.  Returns a dict with
     draft_tok [B,K_max] int32, draft_logits (U's dtype) or None, draft_lse
     [B,K_max] float32 or None, and the status / workspace tensors used.
+    spare_sm leaves one SM free of the tensor-core path's persistent kernel, for a
+    kernel on another stream (the scheduler) to run beside it.
     """
     dt = _dtype_code(_dev(U, "U"))
     B, K_max, V = U.shape
     rank = E.shape[1]
     _dev(E, "E", U.dtype, (V, rank))
-    flags = FLAG_FORCE_SIMT if force_simt else 0
+    flags = (FLAG_FORCE_SIMT if force_simt else 0) | (FLAG_SPARE_SM if spare_sm else 0)
     if isinstance(W, PackedProjection):
         if (W.rank, W.V) != (rank, V) or W.device != U.device or U.dtype != W.dtype:
             raise ValueError(f"packed projection of shape ({W.rank}, {W.V}) does not fit U/E")

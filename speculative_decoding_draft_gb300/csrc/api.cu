@@ -195,7 +195,9 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   if (launch_draft_prologue(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (use_tc && !packed_in && launch_pack_projection(W, dims.rank, dims.V, (void *)a.Wp, s) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  cudaError_t e = use_tc ? launch_draft_tc(a, s, dev.sms) : launch_draft_simt(a, s);
+  // with DSPARK_FLAG_SPARE_SM the persistent kernel (one CTA per SM) leaves one SM free
+  const int tc_sms = (dims.flags & DSPARK_FLAG_SPARE_SM) && dev.sms > 1 ? dev.sms - 1 : dev.sms;
+  cudaError_t e = use_tc ? launch_draft_tc(a, s, tc_sms) : launch_draft_simt(a, s);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

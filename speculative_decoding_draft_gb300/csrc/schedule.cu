@@ -98,11 +98,17 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
       atomicCAS(&s_err, 0, (int)DSPARK_ERR_LENGTHS);
       continue;
     }
+    // the row's confidences are requested together, then multiplied in order
+    float cr[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) cr[j] = (j < kr) ? a.conf[r * K + j] : 0.0f;
     float s = 1.0f;
-    for (int64_t j = 0; j < K; ++j) {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= K) break;
       float v = 0.0f;
       if (j < kr) {
-        const float c = a.conf[r * K + j];
+        const float c = cr[j];
         if (!(c >= 0.0f && c <= 1.0f)) atomicCAS(&s_err, 0, (int)DSPARK_ERR_CONFIDENCE);
         s = __fmul_rn(s, c);
         v = s;
@@ -138,10 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
   }
   __syncthreads();
 
+  uint32_t *sk = w.keyA, *si = w.idxA, *dk = w.keyB, *di = w.idxB;
   // -- stable LSD radix sort, 4 passes of 8 bits -----------------------------
   const uint32_t per_w = (N + kWarps - 1) / kWarps;
   const uint32_t wb = warp * per_w, we = min(N, wb + per_w);
-  uint32_t *sk = w.keyA, *si = w.idxA, *dk = w.keyB, *di = w.idxB;
   for (int sh = 0; sh < 32; sh += 8) {
     for (int e = tid; e < kWarps * 257; e += kThreads) (&hist[0][0])[e] = 0;
     __syncthreads();

@@ -165,6 +165,23 @@ def test_draft_packed_equals_unpacked():
     assert e.value.name == "DSPARK_ERR_UNSUPPORTED"
 
 
+def test_draft_spare_sm_matches():
+    # leaving one SM free changes only the split of the vocabulary over CTAs: the same
+    # tokens and logits, normalisers equal up to the order of the partial sums
+    cfg = wl.small_config("qwen", B=64, K_max=3, V=64040)
+    g = _to(wl.draft_inputs(cfg, "cpu"))
+    pk = ds.pack_projection(g["W"])
+    a = ds.draft_markov_sample(g["U"], g["E"], pk, g["anchor"], g["K_r"], g["temperature"], 9)
+    b = ds.draft_markov_sample(g["U"], g["E"], pk, g["anchor"], g["K_r"], g["temperature"], 9, spare_sm=True)
+    assert ds.check(a["status"]) == "DSPARK_OK" and ds.check(b["status"]) == "DSPARK_OK"
+    assert torch.equal(a["draft_tok"], b["draft_tok"])
+    K_r = g["K_r"].cpu()
+    for r in range(cfg.B):
+        k = int(K_r[r])
+        assert torch.equal(a["draft_logits"][r, :k], b["draft_logits"][r, :k])
+        assert torch.allclose(a["draft_lse"][r, :k], b["draft_lse"][r, :k], rtol=1e-6, atol=0)
+
+
 def test_draft_paths_agree():
     # the tensor-core and CUDA-core kernels sample the same tokens (fp32 rounding aside)
     cfg = wl.small_config("ragged", B=130, K_max=3, V=2048)
