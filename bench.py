@@ -216,9 +216,9 @@ class Step:
                                 device=dev)
         self.ws_s = torch.empty(ds.schedule_workspace_bytes(B, K), dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(ds.verify_workspace_bytes(B, V), dtype=torch.uint8, device=dev)
-        # draft: prologue + persistent kernel + finalize (tensor cores) or prologue + one
+        # draft: prologue + persistent kernel (tensor cores) or prologue + one
         # launch per position (CUDA cores); schedule: 1; verify: row statistics + sample
-        self.draft_launches = 3 if self.tensor_core else 1 + K
+        self.draft_launches = 2 if self.tensor_core else 1 + K
         self.launches_per_step = self.draft_launches + 1 + 2
 
     def draft(self, inp=None):

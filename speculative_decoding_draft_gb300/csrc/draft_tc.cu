@@ -28,8 +28,8 @@
 // With fewer than 128 rows the rows are replicated F times in the M-tile and the F
 // replica groups split each tile's columns.  Per row, the CTA's maximum goes into
 // a packed 64-bit (score, index) key by atomicMax; a bounded grid barrier separates
-// positions, and a finalize kernel turns keys and partial normalisers into tokens
-// and log-sum-exps.  Every wait is bounded; on a timeout the kernel records
+// positions; after the last one the epilogue warps turn keys and partial normalisers
+// into tokens and log-sum-exps.  Every wait is bounded; on a timeout the kernel records
 // DSPARK_ERR_DEVICE_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include "dspark_internal.cuh"
 
@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
     uint32_t tt = 0;
     int unit_no = 0;
     int tab_m = -1;                     // M-tile whose rows sh.row_req / sh.row_invT hold
+    int k_last = 0;                     // last position this CTA arrived at
     for (int k = 1; k <= K && !*abort; ++k) {
       const StepPlan pl = plan_step(sh.nact, k, G, nb);
       if (pl.n_k == 0) break;
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         }
         // merge the 2F worker partials of each row; the row's home thread folds its maximum
         // into the packed (score, index) key of the position with one 64-bit atomicMax -- all
-        // the next position needs -- and keeps its softmax partial for the finalize kernel
+        // the next position needs -- and keeps its softmax partial for the merge after the last position
         sh.part[wk * rpg + row] = to_partial(st);
         named_sync_epi();
         if (wk == 0 && valid) {
@@ -598,6 +599,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
       if (et == 0) {
         __threadfence();
         atomicAdd(a.gbar + k, 1);
+      }
+      k_last = k;
+    }
+    // Once every CTA has arrived at the last position: the tokens from the packed maxima
+    // and the normalisers from the CTA partials, one warp per (position, request).
+    if (k_last > 0 && !*abort) {
+      if (et == 0) {
+        const long long t0 = clock64();
+        while (ld_acquire(a.gbar + k_last) < G) {
+          __nanosleep(100);
+          if (*abort) break;
+          if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }
+        }
+      }
+      named_sync_epi();
+      if (!*abort) {
+        const int B = (int)a.B;
+        const int64_t nw = (int64_t)G * kEpiWarps;
+        for (int64_t item = (int64_t)blockIdx.x * kEpiWarps + eq; item < (int64_t)B * K; item += nw) {
+          const int k = (int)(item / B) + 1, i = (int)(item % B);
+          if (k > k_last) break;
+          const StepPlan pl = plan_step(sh.nact, k, G, nb);
+          if (i >= pl.n_k) continue;
+          const int r = a.perm[i];
+          const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm};
+          Race tot[1];
+          warp_merge_rows<1>(ptr, pl.gm, tot);
+          if (lane == 0) {
+            const int64_t at = (int64_t)r * K + k - 1;
+            a.draft_tok[at] = key_index(load_key(a.best_key + at));
+            if (a.draft_lse) a.draft_lse[at] = a.temperature[r] == 0.0f ? tot[0].best : tot[0].m + logf(tot[0].S);
+          }
+        }
       }
     }
   }
@@ -627,33 +661,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
   tc_fence_after();
   if (*abort && threadIdx.x == 0) set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
-// Once per call, after the last position: tokens from the packed maxima and the
-// normaliser from the CTA partials of each (request, position), one warp each.
-__global__ void __launch_bounds__(256) draft_tc_finalize(const __grid_constant__ DraftArgs a, int G) {
-  if (read_status(a.dev_status)) return;
-  const int K = (int)a.K_max, B = (int)a.B;
-  const int nb = (int)((a.V + kBlkN - 1) / kBlkN);
-  const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < (int64_t)B * K; item += nw) {
-    const int k = (int)(item / B) + 1, i = (int)(item % B);
-    const int n_k = a.nact[k];
-    if (i >= n_k) continue;
-    const int m_tiles = (n_k + kTileM - 1) / kTileM;
-    const int gm = max(1, min(G / m_tiles, nb));
-    const int r = a.perm[i];
-    const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * gm};
-    Race tot[1];
-    warp_merge_rows<1>(ptr, gm, tot);
-    if (lane == 0) {
-      const unsigned long long key = a.best_key[(int64_t)r * K + k - 1];
-      a.draft_tok[(int64_t)r * K + k - 1] = key_index(key);
-      if (a.draft_lse)
-        a.draft_lse[(int64_t)r * K + k - 1] = a.temperature[r] == 0.0f ? tot[0].best : tot[0].m + logf(tot[0].S);
-    }
-  }
 }
 
 // W2 [rank, V] -> packed blocks: 16-byte unit e = ((c * nb + t) * 64 + kr) * 8 + u of
@@ -733,12 +740,7 @@ cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[1] = {(void *)&a};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e != cudaSuccess) return e;
-  const int64_t items = a.B * a.K_max;
-  const int fblocks = (int)((items + 7) / 8 < 4096 ? (items + 7) / 8 : 4096);
-  draft_tc_finalize<<<fblocks, 256, 0, s>>>(a, grid);
-  return cudaGetLastError();
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace dspark
