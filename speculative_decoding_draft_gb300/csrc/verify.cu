@@ -251,21 +251,27 @@ __device__ __forceinline__ void row_consume(const RowItem &it, uint4 (&pk)[kRowP
     return;
   }
   const float m = zmax * it.invT;         // max(z) / T = max(z / T): scaling by 1/T > 0 is monotone
-  const float mL = m * kLog2e;
-  const unsigned long long ti = f2_pack(it.invT, it.invT), l2 = f2_pack(kLog2e, kLog2e), nm = f2_pack(-mL, -mL);
+  const float a2 = it.invT * kLog2e, mL = m * kLog2e;
+  const unsigned long long aa = f2_pack(a2, a2), nm = f2_pack(-mL, -mL);
   unsigned long long s0 = f2_pack(0.0f, 0.0f), s1 = s0;
 #pragma unroll
   for (int e = 0; e < 4 * kRowPk; ++e) {
     const uint32_t we = W_(e);
-    const unsigned long long sc = f2_mul(f2_pack(__uint_as_float(we << 16), __uint_as_float(we & 0xffff0000u)), ti);
-    float y0, y1;
-    f2_unpack(f2_fma(sc, l2, nm), y0, y1);
+    float y0, y1;    // z a2 - m log2(e): one rounding per exponent argument
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(we << 16), __uint_as_float(we & 0xffff0000u)), aa, nm), y0, y1);
     const unsigned long long ee = f2_pack(fast_ex2(y0), fast_ex2(y1));
     if (e & 1) s1 = f2_add(s1, ee);
     else s0 = f2_add(s0, ee);
-    if (it.lo + ((e >> 2) * kRowThreads + tid) * 8 + 2 * (e & 3) == (it.x & ~1)) {   // the pair holding x
-      *own_t = __uint_as_float((it.x & 1) ? (we & 0xffff0000u) : (we << 16)) * it.invT;
-    }
+  }
+  // the scaled logit at the draft token, taken by the one thread whose loads hold it
+  const int xo = it.x - it.lo;
+  if (xo >= 0 && it.x < it.hi && ((xo >> 3) & (kRowThreads - 1)) == tid) {
+    const int ex = ((xo >> 3) / kRowThreads) * 4 + ((xo & 7) >> 1);
+    uint32_t wx = 0;
+#pragma unroll
+    for (int e = 0; e < 4 * kRowPk; ++e)
+      if (e == ex) wx = W_(e);
+    *own_t = __uint_as_float((it.x & 1) ? (wx & 0xffff0000u) : (wx << 16)) * it.invT;
   }
   float a0, a1, b0, b1;
   f2_unpack(s0, a0, a1);
