@@ -96,6 +96,12 @@ def lib() -> ctypes.CDLL:
         L.dso_draft_markov_sample.restype = i32
         L.dso_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P, P, P, P]
         L.dso_schedule_survival.restype = i32
+        L.dso_schedule_capacity.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P]
+        L.dso_schedule_capacity.restype = i32
+        L.dso_schedule_topk.argtypes = [P, P, i64, i64, i64, P, P, P, P, P, P]
+        L.dso_schedule_topk.restype = i32
+        L.dso_schedule_threshold.argtypes = [P, P, i64, i64, ctypes.c_float, i32, P, P, P]
+        L.dso_schedule_threshold.restype = i32
         L.dso_verify_ragged.argtypes = [P, P, i32, P, P, P, P, P, u64, i64, i64, i64,
                                         P, P, P, P, P, i32]
         L.dso_verify_ragged.restype = i32
@@ -245,6 +251,64 @@ def schedule_survival(conf, K_r, sps):
     return dict(ell=ell, tgt_off=off, theta_best=float(th[0]), B_star=int(bstar[0]),
                 tau_star=float(tau[0]), survival=surv, order=order[:n], n_cand=n,
                 n_admitted=int(nadm[0]), n_theta_ties=int(ties[0]))
+
+
+def schedule_capacity(conf, K_r, sps):
+    """Capacity of the asynchronous scheduler: the global maximum of Theta along the greedy path.
+
+    Returns dict(capacity, theta_best, ell, tgt_off, survival); ell is the admission at the maximum.
+    """
+    conf = _c(conf, np.float32)
+    B, K_max = conf.shape
+    K_r = _c(K_r, np.int32)
+    sps = _c(sps, np.float64)
+    cap = np.zeros(1, np.int64)
+    th = np.zeros(1, np.float64)
+    ell = np.zeros(B, np.int32)
+    off = np.zeros(B + 1, np.int32)
+    surv = np.zeros((B, K_max), np.float32)
+    st = lib().dso_schedule_capacity(_ptr(conf), _ptr(K_r), _ptr(sps), len(sps), B, K_max, _ptr(cap), _ptr(th),
+                                     _ptr(ell), _ptr(off), _ptr(surv))
+    if st:
+        raise OracleError(st)
+    return dict(capacity=int(cap[0]), theta_best=float(th[0]), ell=ell, tgt_off=off, survival=surv)
+
+
+def schedule_topk(conf, K_r, capacity):
+    """Dynamic top-K admission: the first min(capacity, N) candidates of the current ranking."""
+    conf = _c(conf, np.float32)
+    B, K_max = conf.shape
+    K_r = _c(K_r, np.int32)
+    ell = np.zeros(B, np.int32)
+    off = np.zeros(B + 1, np.int32)
+    nadm = np.zeros(1, np.int64)
+    surv = np.zeros((B, K_max), np.float32)
+    order = np.zeros(B * K_max, np.int32)
+    ncand = np.zeros(1, np.int64)
+    st = lib().dso_schedule_topk(_ptr(conf), _ptr(K_r), B, K_max, int(capacity), _ptr(ell), _ptr(off), _ptr(nadm),
+                                 _ptr(surv), _ptr(order), _ptr(ncand))
+    if st:
+        raise OracleError(st)
+    n = int(ncand[0])
+    return dict(ell=ell, tgt_off=off, n_admitted=int(nadm[0]), survival=surv, order=order[:n], n_cand=n)
+
+
+THRESHOLD_CONFIDENCE, THRESHOLD_SURVIVAL = 0, 1
+
+
+def schedule_threshold(conf, K_r, theta, mode=THRESHOLD_CONFIDENCE):
+    """Static-threshold lengths: the longest prefix whose confidences (mode 0) or survivals (mode 1) are >= theta."""
+    conf = _c(conf, np.float32)
+    B, K_max = conf.shape
+    K_r = _c(K_r, np.int32)
+    ell = np.zeros(B, np.int32)
+    off = np.zeros(B + 1, np.int32)
+    surv = np.zeros((B, K_max), np.float32)
+    st = lib().dso_schedule_threshold(_ptr(conf), _ptr(K_r), B, K_max, float(theta), int(mode), _ptr(ell),
+                                      _ptr(off), _ptr(surv))
+    if st:
+        raise OracleError(st)
+    return dict(ell=ell, tgt_off=off, survival=surv)
 
 
 def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature, seed, req_id=None,

@@ -524,6 +524,153 @@ int dso_schedule_survival(const float *conf, const int32_t *K_r, const double *s
 }
 
 /* ---------------------------------------------------------------------- */
+/* Schedule variants of the deployed scheduler and of the static baseline.  */
+/*                                                                          */
+/* Shared first steps (as in Algorithm 1): validation, survival products    */
+/* a_{r,j} (sequential fp32), the candidate pool {(r,j) : a_{r,j} > 0} and   */
+/* its ranking by a descending, ties to the smaller j, then the smaller r.  */
+/* ---------------------------------------------------------------------- */
+static int64_t ranked_candidates(const float *conf, const int32_t *K_r, int64_t B, int64_t K_max,
+                                 float *survival, cand_t *cand) {
+  int64_t N = 0;
+  for (int64_t r = 0; r < B; ++r) {
+    float a = 1.0f;
+    for (int64_t j = 1; j <= K_max; ++j) {
+      if (j > K_r[r]) { if (survival) survival[r * K_max + j - 1] = 0.0f; continue; }
+      a = a * conf[r * K_max + j - 1];
+      if (survival) survival[r * K_max + j - 1] = a;
+      if (a > 0.0f) { cand[N].a = a; cand[N].j = (int32_t)j; cand[N].r = (int32_t)r; ++N; }
+    }
+  }
+  qsort(cand, (size_t)N, sizeof(cand_t), cand_cmp);
+  return N;
+}
+
+static int check_schedule_inputs(const float *conf, const int32_t *K_r, int64_t B, int64_t K_max) {
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K) return ORC_ERR_DIMS;
+  for (int64_t r = 0; r < B; ++r)
+    if (K_r[r] < 1 || K_r[r] > K_max) return ORC_ERR_LENGTHS;
+  for (int64_t r = 0; r < B; ++r)
+    for (int64_t j = 0; j < K_r[r]; ++j) {
+      float c = conf[r * K_max + j];
+      if (!(c >= 0.0f && c <= 1.0f)) return ORC_ERR_CONFIDENCE;
+    }
+  return ORC_OK;
+}
+
+static void lengths_from_prefix(const cand_t *cand, int64_t admitted, int64_t B, int32_t *ell, int32_t *tgt_off) {
+  for (int64_t r = 0; r < B; ++r) ell[r] = 0;
+  for (int64_t i = 0; i < admitted; ++i) ell[cand[i].r] += 1;
+  if (tgt_off) {
+    tgt_off[0] = 0;
+    for (int64_t r = 0; r < B; ++r) tgt_off[r + 1] = tgt_off[r] + ell[r] + 1;
+  }
+}
+
+/* Capacity of the asynchronous scheduler [DSP S5.2], [ZTD S9]: the early-   */
+/* stopping break is removed and the search runs over the whole greedy       */
+/* admission path, Theta_i = tau_i * SPS(R + i) for i = 0..N (tau and Theta   */
+/* in the same arithmetic as Algorithm 1); the capacity is the i with the    */
+/* largest Theta_i.  Fed confidences from two steps earlier it fixes how many */
+/* draft tokens the next pass verifies.  Readings: the capacity counts draft- */
+/* token slots (the verify batch is R + capacity); ties in Theta go to the    */
+/* smaller i (the first maximum, fewer verified tokens for the same value).  */
+/* ell gets the lengths of that admission (the retrospective schedule of     */
+/* Appendix A when applied to the current confidences).                     */
+/* Pins: exhaustive search (Theta at the capacity = the maximum over every   */
+/* admissible length tuple); the Appendix A retrospective lengths; crossing */
+/* an SPS cliff that stops Algorithm 1.                                      */
+int dso_schedule_capacity(const float *conf, const int32_t *K_r, const double *sps, int64_t sps_len,
+                          int64_t B, int64_t K_max, int64_t *capacity, double *theta_best,
+                          int32_t *ell, int32_t *tgt_off, float *survival) {
+  if (!conf || !K_r || !sps || !capacity) return ORC_ERR_NULL;
+  int st = check_schedule_inputs(conf, K_r, B, K_max);
+  if (st) return st;
+  cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(B * K_max));
+  const int64_t N = ranked_candidates(conf, K_r, B, K_max, survival, cand);
+  const int64_t R = B;
+  if (sps_len < R + N + 1) { free(cand); return ORC_ERR_SPS_TOO_SHORT; }
+  uint64_t T = 0;
+  double th_best = (double)R * sps[R];
+  int64_t best = 0;
+  for (int64_t i = 1; i <= N; ++i) {
+    T += (uint64_t)nearbyint((double)cand[i - 1].a * 0x1p40);
+    double th = ((double)R + (double)T * 0x1p-40) * sps[R + i];
+    if (th > th_best) { th_best = th; best = i; }
+  }
+  *capacity = best;
+  if (theta_best) *theta_best = th_best;
+  if (ell) lengths_from_prefix(cand, best, B, ell, tgt_off);
+  free(cand);
+  return ORC_OK;
+}
+
+/* Dynamic top-K admission of the asynchronous scheduler [DSP S5.2],         */
+/* [ZTD S9]: the current step's candidates, ranked by their current survival */
+/* (ties to the smaller position, then the smaller request, so that token k  */
+/* cannot move its own rank), are admitted in order up to the capacity fixed */
+/* two steps earlier: the first min(capacity, N).  ell_r counts the admitted */
+/* candidates of r.  Pins: for every capacity the admitted set maximises tau */
+/* over all admissible tuples of that size (exhaustive search, the fixed-B   */
+/* argument of S3.2.2); exact enumeration of the output law with a Markov    */
+/* confidence (non-anticipation: the law equals the target's, where the      */
+/* retrospective search reproduces Appendix A's 0.85).                      */
+int dso_schedule_topk(const float *conf, const int32_t *K_r, int64_t B, int64_t K_max, int64_t capacity,
+                      int32_t *ell, int32_t *tgt_off, int64_t *n_admitted, float *survival, int32_t *order,
+                      int64_t *n_cand) {
+  if (!conf || !K_r || !ell) return ORC_ERR_NULL;
+  int st = check_schedule_inputs(conf, K_r, B, K_max);
+  if (st) return st;
+  if (capacity < 0) return ORC_ERR_LENGTHS;
+  cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(B * K_max));
+  const int64_t N = ranked_candidates(conf, K_r, B, K_max, survival, cand);
+  const int64_t admitted = capacity < N ? capacity : N;
+  lengths_from_prefix(cand, admitted, B, ell, tgt_off);
+  if (n_admitted) *n_admitted = admitted;
+  if (order) for (int64_t i = 0; i < N; ++i) order[i] = (int32_t)((cand[i].j - 1) * B + cand[i].r);
+  if (n_cand) *n_cand = N;
+  free(cand);
+  return ORC_OK;
+}
+
+/* Static-threshold verification length [DSP S3.2.2 (the prior methods it    */
+/* contrasts with), S4.3.3 (the threshold sweep of Fig. 5)]: a request       */
+/* verifies the longest prefix whose every position passes the threshold.   */
+/* mode 0: c_{r,i} >= theta for all i <= j; mode 1: a_{r,i} >= theta (the    */
+/* survival products, a prefix by monotonicity).  Readings: the pages do not */
+/* say whether the cut is on the raw confidence or on its product, so both   */
+/* are offered; a position passes on equality; as in Algorithm 1's candidate */
+/* pool a position with a = 0 is never verified.  Pins: theta <= 0 admits    */
+/* exactly Algorithm 1's empty-system schedule; theta > 1 admits nothing;    */
+/* hand-worked lengths; lengths fall monotonically as theta rises.           */
+int dso_schedule_threshold(const float *conf, const int32_t *K_r, int64_t B, int64_t K_max, float theta, int mode,
+                           int32_t *ell, int32_t *tgt_off, float *survival) {
+  if (!conf || !K_r || !ell) return ORC_ERR_NULL;
+  int st = check_schedule_inputs(conf, K_r, B, K_max);
+  if (st) return st;
+  if (theta != theta || (mode != 0 && mode != 1)) return ORC_ERR_CONFIDENCE;
+  for (int64_t r = 0; r < B; ++r) {
+    float a = 1.0f;
+    int32_t len = 0, open = 1;
+    for (int64_t j = 1; j <= K_max; ++j) {
+      if (j > K_r[r]) { if (survival) survival[r * K_max + j - 1] = 0.0f; continue; }
+      const float c = conf[r * K_max + j - 1];
+      a = a * c;
+      if (survival) survival[r * K_max + j - 1] = a;
+      const float tested = mode == 0 ? c : a;
+      if (open && a > 0.0f && tested >= theta) len = (int32_t)j;
+      else open = 0;
+    }
+    ell[r] = len;
+  }
+  if (tgt_off) {
+    tgt_off[0] = 0;
+    for (int64_t r = 0; r < B; ++r) tgt_off[r + 1] = tgt_off[r] + ell[r] + 1;
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Verify: ragged rejection-sampling verification.                          */
 /* [DSP S2.1], [ZTD S2, A1]:                                                */
 /*   for j = 1..ell_r, left to right: accept x_j iff u < min(1, p_j(x_j) /   */
