@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.dso_draft_markov_sample.restype = i32
         L.dso_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P, P, P, P]
         L.dso_schedule_survival.restype = i32
+        L.dso_draft_confidence.argtypes = [P, i32, i64, i64, P, P, P, P, P, i64, i64, P]
+        L.dso_draft_confidence.restype = i32
         L.dso_schedule_capacity.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P]
         L.dso_schedule_capacity.restype = i32
         L.dso_schedule_topk.argtypes = [P, P, i64, i64, i64, P, P, P, P, P, P]
@@ -224,6 +226,28 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed, req_id=None, wa
     if st:
         raise OracleError(st)
     return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags)
+
+
+def draft_confidence(E, anchor, draft_tok, K_r, conf_h, conf_w):
+    """Confidence head with the Markov term: c_k = sigmoid(conf_h[r, k] + conf_w . E[x_{k-1}]).
+
+    E [V, rank] float32 or bf16 bits (uint16); draft_tok [B, K_max] int32 (x_1..); conf_h
+    [B, K_max] float32 (w_h . h_k + b); conf_w [rank] float32.  Returns conf [B, K_max] float32.
+    """
+    Ea, dt = _logits(E)
+    V, rank = Ea.shape
+    draft_tok = _c(draft_tok, np.int32)
+    B, K_max = draft_tok.shape
+    anchor = _c(anchor, np.int32)
+    K_r = _c(K_r, np.int32)
+    conf_h = _c(conf_h, np.float32)
+    conf_w = _c(conf_w, np.float32)
+    out = np.zeros((B, K_max), np.float32)
+    st = lib().dso_draft_confidence(_ptr(Ea), dt, V, rank, _ptr(anchor), _ptr(draft_tok), _ptr(K_r), _ptr(conf_h),
+                                    _ptr(conf_w), B, K_max, _ptr(out))
+    if st:
+        raise OracleError(st)
+    return out
 
 
 def schedule_survival(conf, K_r, sps):

@@ -443,6 +443,42 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
 }
 
 /* ---------------------------------------------------------------------- */
+/* Confidence head, Markov term [DSP S3.2.1], [ZTD S8]: the head is one     */
+/* linear projection of [h_k ; W1[x_{k-1}]] followed by a sigmoid, so        */
+/*   c_k = sigmoid(w_h . h_k + b + w_e . W1[x_{k-1}]),   x_0 = anchor.      */
+/* The backbone term w_h . h_k + b has no sequential dependence and is an    */
+/* input (conf_h [B, K_max]); the Markov term needs the token sampled at     */
+/* position k-1.  Readings: the display equation is missing from the paper  */
+/* page; the tutorial (S8) and the paper's text give its inputs (backbone    */
+/* hidden state plus the Markov embedding of the previous token, one linear */
+/* projection, sigmoid), and the embedding is the draft's own table W1 (the */
+/* "Markov Embedding").  fp64 dot product and sigmoid, rounded once to fp32. */
+/* Entries k > K_r are set to 0.                                             */
+/* Pins: one-hot embedding rows select one weight; w_e = 0 gives            */
+/* sigmoid(conf_h) at every token; sigmoid(0) = 1/2 and the reflection      */
+/* c(-s) = 1 - c(s); c_k changes only with x_{k-1}.                          */
+/* ---------------------------------------------------------------------- */
+int dso_draft_confidence(const void *E, int dtype, int64_t V, int64_t rank, const int32_t *anchor,
+                         const int32_t *draft_tok, const int32_t *K_r, const float *conf_h, const float *conf_w,
+                         int64_t B, int64_t K_max, float *conf) {
+  if (!E || !anchor || !draft_tok || !K_r || !conf_h || !conf_w || !conf) return ORC_ERR_NULL;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2 || rank < 1) return ORC_ERR_DIMS;
+  for (int64_t r = 0; r < B; ++r) {
+    if (K_r[r] < 1 || K_r[r] > K_max) return ORC_ERR_LENGTHS;
+    for (int64_t k = 1; k <= K_max; ++k) {
+      if (k > K_r[r]) { conf[r * K_max + k - 1] = 0.0f; continue; }
+      const int32_t prev = k == 1 ? anchor[r] : draft_tok[r * K_max + k - 2];
+      if (prev < 0 || prev >= V) return ORC_ERR_TOKEN_RANGE;
+      double s = (double)conf_h[r * K_max + k - 1];
+      for (int64_t i = 0; i < rank; ++i) s += load_elem(E, dtype, prev * rank + i) * (double)conf_w[i];
+      conf[r * K_max + k - 1] = (float)(1.0 / (1.0 + exp(-s)));
+    }
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Schedule: confidence-scheduled verification lengths.                     */
 /* [DSP S3.2.2 Algorithm 1], [ZTD S8]:                                      */
 /*   a_{r,j} = prod_{i<=j} c_{r,i};  candidates {(r,j) : a_{r,j} > 0} sorted */
