@@ -190,6 +190,79 @@ dspark_status dspark_schedule_survival(const float *conf, const int32_t *K_r, co
                                        int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Deployed (asynchronous) scheduler, step 1: capacity ("DSpark" S5.2;
+ * "Speculative decoding, from zero to DSpark" S9).
+ *
+ * Algorithm 1's ranking and objective with the early-stopping break removed:
+ * Theta_i is evaluated for every i = 0..N along the greedy path (same survival
+ * products, ranking, fixed-point tau and fp64 Theta as dspark_schedule_survival)
+ * and the capacity is the i with the largest Theta_i, the smallest such i on
+ * ties.  Called on the confidences of two steps earlier, it fixes how many draft
+ * tokens the next verification pass admits, before that step's tokens exist, so
+ * a global search across the SPS cliffs no longer leaks them.  The capacity
+ * counts draft-token slots (the verify batch is B + capacity).
+ *
+ *   conf, K_r, sps, sps_len, B, K_max   as for dspark_schedule_survival.
+ *   capacity    [1] int32 out          the admitted candidates at the maximum.
+ *   theta_best  [1] double out, optional: Theta at the maximum.
+ *   ell, tgt_off  out, optional (both or neither): the lengths of that admission
+ *               (the retrospective schedule of Appendix A, for diagnostics).
+ *   workspace   >= dspark_schedule_workspace_bytes(B, K_max) bytes, 256-byte aligned.
+ * Errors as for dspark_schedule_survival.
+ * ------------------------------------------------------------------------ */
+dspark_status dspark_schedule_capacity(const float *conf, const int32_t *K_r, const double *sps,
+                                       int64_t sps_len, int64_t B, int64_t K_max, int32_t *capacity,
+                                       double *theta_best, int32_t *ell, int32_t *tgt_off, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Deployed (asynchronous) scheduler, step 2: dynamic top-K admission ("DSpark"
+ * S5.2; "Speculative decoding, from zero to DSpark" S9).
+ *
+ * The current step's candidates are ranked exactly as in Algorithm 1 (survival
+ * descending, ties to the smaller position, then the smaller request, so that a
+ * token never moves its own rank) and the first min(*capacity, N) are admitted;
+ * no SPS table is read.  ell[r] = admitted candidates of request r.
+ *
+ *   conf, K_r, B, K_max   as for dspark_schedule_survival.
+ *   capacity    [1] int32, DEVICE: admitted draft tokens, >= 0 (for instance the
+ *               output of dspark_schedule_capacity two steps earlier); a negative
+ *               value is DSPARK_ERR_LENGTHS on the device.
+ *   ell, tgt_off, b_star, survival   out as for dspark_schedule_survival
+ *               (b_star, survival optional).
+ *   workspace   >= dspark_schedule_workspace_bytes(B, K_max) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+dspark_status dspark_schedule_topk(const float *conf, const int32_t *K_r, const int32_t *capacity, int64_t B,
+                                   int64_t K_max, int32_t *ell, int32_t *tgt_off, int64_t *b_star,
+                                   float *survival, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Static-threshold verification lengths: the baseline that "DSpark" S3.2.2
+ * contrasts with its scheduler, and the threshold sweep of S4.3.3 (Fig. 5).
+ *
+ * ell[r] = the largest j <= K_r[r] such that every position i <= j passes:
+ *   DSPARK_THRESHOLD_CONFIDENCE  conf[r, i] >= threshold,
+ *   DSPARK_THRESHOLD_SURVIVAL    a[r, i] >= threshold (the survival products),
+ * and a[r, i] > 0 (as in Algorithm 1's candidate pool).
+ *
+ *   conf, K_r, B, K_max   as for dspark_schedule_survival.
+ *   threshold   any number but NaN (NaN: DSPARK_ERR_CONFIDENCE); <= 0 verifies
+ *               every candidate, > 1 verifies nothing.
+ *   mode        DSPARK_THRESHOLD_CONFIDENCE or DSPARK_THRESHOLD_SURVIVAL
+ *               (otherwise DSPARK_ERR_DIMS).
+ *   ell, tgt_off, b_star, survival   out as for dspark_schedule_survival
+ *               (b_star, survival optional).
+ * No workspace.
+ * ------------------------------------------------------------------------ */
+#define DSPARK_THRESHOLD_CONFIDENCE 0
+#define DSPARK_THRESHOLD_SURVIVAL 1
+
+dspark_status dspark_schedule_threshold(const float *conf, const int32_t *K_r, float threshold, int32_t mode,
+                                        int64_t B, int64_t K_max, int32_t *ell, int32_t *tgt_off,
+                                        int64_t *b_star, float *survival, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Schedule without a caller workspace.
  *
  * The paper has no counterpart to this entry point: it exists for callers that

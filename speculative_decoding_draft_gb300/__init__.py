@@ -45,7 +45,8 @@ STATUS_NAMES = {
 EXPORTED_SYMBOLS = [
     "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_draft_packed_projection_bytes",
     "dspark_draft_pack_projection", "dspark_schedule_workspace_bytes",
-    "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_verify_workspace_bytes",
+    "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_schedule_capacity",
+    "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_workspace_bytes",
     "dspark_verify_ragged",
     "dspark_status_string", "dspark_check", "dspark_version",
 ]
@@ -98,6 +99,12 @@ def lib() -> ctypes.CDLL:
     L.dspark_schedule_survival.restype = st
     L.dspark_schedule_survival_noalloc.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P]
     L.dspark_schedule_survival_noalloc.restype = st
+    L.dspark_schedule_capacity.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, sz, P, P]
+    L.dspark_schedule_capacity.restype = st
+    L.dspark_schedule_topk.argtypes = [P, P, P, i64, i64, P, P, P, P, P, sz, P, P]
+    L.dspark_schedule_topk.restype = st
+    L.dspark_schedule_threshold.argtypes = [P, P, ctypes.c_float, ctypes.c_int32, i64, i64, P, P, P, P, P, P]
+    L.dspark_schedule_threshold.restype = st
     L.dspark_verify_workspace_bytes.argtypes = [i64, i64]
     L.dspark_verify_workspace_bytes.restype = sz
     L.dspark_verify_ragged.argtypes = [P, P, P, P, P, P, P, u64, Dims, P, P, P, sz, P, P]
@@ -292,6 +299,83 @@ def schedule_survival(conf, K_r, sps, *, out: Optional[dict] = None, workspace: 
                                           ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
     _raise(code, "dspark_schedule_survival")
     return dict(ell=ell, tgt_off=off, theta_best=th, b_star=bs, survival=surv, status=status, workspace=ws)
+
+
+def _out(out, key, shape, dtype, dev):
+    t = out.get(key)
+    return t if t is not None else torch.empty(shape, dtype=dtype, device=dev)
+
+
+def schedule_capacity(conf, K_r, sps, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                      status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Capacity of the asynchronous scheduler (C ABI dspark_schedule_capacity).
+
+    conf [B,K_max] float32, K_r [B] int32, sps float64 (CUDA).  Returns capacity [1]
+    int32 (admitted draft tokens at the global maximum of Theta), theta_best [1] float64
+    and the retrospective lengths ell [B] / tgt_off [B+1] of that admission.
+    """
+    _dev(conf, "conf", torch.float32)
+    B, K_max = conf.shape
+    _dev(K_r, "K_r", torch.int32, (B,))
+    _dev(sps, "sps", torch.float64)
+    dev = conf.device
+    out = {} if out is None else out
+    cap = _out(out, "capacity", (1,), torch.int32, dev)
+    th = _out(out, "theta_best", (1,), torch.float64, dev)
+    ell = _out(out, "ell", (B,), torch.int32, dev)
+    off = _out(out, "tgt_off", (B + 1,), torch.int32, dev)
+    status = new_status(dev) if status is None else status
+    ws = _workspace(schedule_workspace_bytes(B, K_max), dev, workspace)
+    code = lib().dspark_schedule_capacity(_ptr(conf), _ptr(K_r), _ptr(sps), sps.numel(), B, K_max, _ptr(cap),
+                                          _ptr(th), _ptr(ell), _ptr(off), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                          _ptr(status), _stream(stream))
+    _raise(code, "dspark_schedule_capacity")
+    return dict(capacity=cap, theta_best=th, ell=ell, tgt_off=off, status=status, workspace=ws)
+
+
+def schedule_topk(conf, K_r, capacity, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Dynamic top-K admission (C ABI dspark_schedule_topk); capacity is a CUDA int32 [1] tensor."""
+    _dev(conf, "conf", torch.float32)
+    B, K_max = conf.shape
+    _dev(K_r, "K_r", torch.int32, (B,))
+    _dev(capacity, "capacity", torch.int32, (1,))
+    dev = conf.device
+    out = {} if out is None else out
+    ell = _out(out, "ell", (B,), torch.int32, dev)
+    off = _out(out, "tgt_off", (B + 1,), torch.int32, dev)
+    bs = _out(out, "b_star", (1,), torch.int64, dev)
+    surv = _out(out, "survival", (B, K_max), torch.float32, dev)
+    status = new_status(dev) if status is None else status
+    ws = _workspace(schedule_workspace_bytes(B, K_max), dev, workspace)
+    code = lib().dspark_schedule_topk(_ptr(conf), _ptr(K_r), _ptr(capacity), B, K_max, _ptr(ell), _ptr(off),
+                                      _ptr(bs), _ptr(surv), _ptr(ws), ctypes.c_size_t(ws.numel()), _ptr(status),
+                                      _stream(stream))
+    _raise(code, "dspark_schedule_topk")
+    return dict(ell=ell, tgt_off=off, b_star=bs, survival=surv, status=status, workspace=ws)
+
+
+THRESHOLD_CONFIDENCE, THRESHOLD_SURVIVAL = 0, 1
+
+
+def schedule_threshold(conf, K_r, threshold: float, mode: int = THRESHOLD_CONFIDENCE, *,
+                       out: Optional[dict] = None, status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Static-threshold lengths (C ABI dspark_schedule_threshold)."""
+    _dev(conf, "conf", torch.float32)
+    B, K_max = conf.shape
+    _dev(K_r, "K_r", torch.int32, (B,))
+    dev = conf.device
+    out = {} if out is None else out
+    ell = _out(out, "ell", (B,), torch.int32, dev)
+    off = _out(out, "tgt_off", (B + 1,), torch.int32, dev)
+    bs = _out(out, "b_star", (1,), torch.int64, dev)
+    surv = _out(out, "survival", (B, K_max), torch.float32, dev)
+    status = new_status(dev) if status is None else status
+    code = lib().dspark_schedule_threshold(_ptr(conf), _ptr(K_r), float(threshold), int(mode), B, K_max,
+                                           _ptr(ell), _ptr(off), _ptr(bs), _ptr(surv), _ptr(status),
+                                           _stream(stream))
+    _raise(code, "dspark_schedule_threshold")
+    return dict(ell=ell, tgt_off=off, b_star=bs, survival=surv, status=status)
 
 
 def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature, seed: int, *,

@@ -3,7 +3,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "dspark_internal.cuh"
+#include "schedule.cuh"
 
 using namespace dspark;
 
@@ -57,7 +57,7 @@ dspark_status check_dims(const dspark_dims &d, bool need_rank) {
 
 extern "C" {
 
-int dspark_version(void) { return 100; }
+int dspark_version(void) { return 101; }
 
 const char *dspark_status_string(dspark_status s) {
   switch (s) {
@@ -231,6 +231,86 @@ dspark_status dspark_schedule_survival(const float *conf, const int32_t *K_r, co
   a.survival = survival;
   a.dev_status = dev_status;
   a.ws = workspace;
+  return launch_schedule(a, (cudaStream_t)stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+dspark_status dspark_schedule_capacity(const float *conf, const int32_t *K_r, const double *sps, int64_t sps_len,
+                                       int64_t B, int64_t K_max, int32_t *capacity, double *theta_best,
+                                       int32_t *ell, int32_t *tgt_off, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream) {
+  if (!conf || !K_r || !sps || !capacity || !dev_status) return DSPARK_ERR_NULL;
+  if ((ell == nullptr) != (tgt_off == nullptr)) return DSPARK_ERR_NULL;
+  if (B < 1 || B > kMaxB || K_max < 1 || K_max > kMaxK || sps_len < 1) return DSPARK_ERR_DIMS;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_schedule_workspace_bytes(B, K_max))
+    return DSPARK_ERR_WORKSPACE;
+  ScheduleArgs a;
+  a.conf = conf;
+  a.K_r = K_r;
+  a.sps = sps;
+  a.sps_len = sps_len;
+  a.B = B;
+  a.K_max = K_max;
+  a.ell = ell;
+  a.tgt_off = tgt_off;
+  a.theta_best = theta_best;
+  a.b_star = nullptr;
+  a.survival = nullptr;
+  a.dev_status = dev_status;
+  a.ws = workspace;
+  a.mode = kSchedCapacity;
+  a.capacity_out = capacity;
+  return launch_schedule(a, (cudaStream_t)stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+dspark_status dspark_schedule_topk(const float *conf, const int32_t *K_r, const int32_t *capacity, int64_t B,
+                                   int64_t K_max, int32_t *ell, int32_t *tgt_off, int64_t *b_star, float *survival,
+                                   void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (!conf || !K_r || !capacity || !ell || !tgt_off || !dev_status) return DSPARK_ERR_NULL;
+  if (B < 1 || B > kMaxB || K_max < 1 || K_max > kMaxK) return DSPARK_ERR_DIMS;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_schedule_workspace_bytes(B, K_max))
+    return DSPARK_ERR_WORKSPACE;
+  ScheduleArgs a;
+  a.conf = conf;
+  a.K_r = K_r;
+  a.sps = nullptr;
+  a.sps_len = 0;
+  a.B = B;
+  a.K_max = K_max;
+  a.ell = ell;
+  a.tgt_off = tgt_off;
+  a.theta_best = nullptr;
+  a.b_star = b_star;
+  a.survival = survival;
+  a.dev_status = dev_status;
+  a.ws = workspace;
+  a.mode = kSchedTopK;
+  a.capacity_in = capacity;
+  return launch_schedule(a, (cudaStream_t)stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+dspark_status dspark_schedule_threshold(const float *conf, const int32_t *K_r, float threshold, int32_t mode,
+                                        int64_t B, int64_t K_max, int32_t *ell, int32_t *tgt_off, int64_t *b_star,
+                                        float *survival, int32_t *dev_status, void *stream) {
+  if (!conf || !K_r || !ell || !tgt_off || !dev_status) return DSPARK_ERR_NULL;
+  if (B < 1 || B > kMaxB || K_max < 1 || K_max > kMaxK) return DSPARK_ERR_DIMS;
+  if (mode != DSPARK_THRESHOLD_CONFIDENCE && mode != DSPARK_THRESHOLD_SURVIVAL) return DSPARK_ERR_DIMS;
+  if (threshold != threshold) return DSPARK_ERR_CONFIDENCE;
+  ScheduleArgs a;
+  a.conf = conf;
+  a.K_r = K_r;
+  a.sps = nullptr;
+  a.sps_len = 0;
+  a.B = B;
+  a.K_max = K_max;
+  a.ell = ell;
+  a.tgt_off = tgt_off;
+  a.theta_best = nullptr;
+  a.b_star = b_star;
+  a.survival = survival;
+  a.dev_status = dev_status;
+  a.ws = nullptr;
+  a.mode = mode == DSPARK_THRESHOLD_CONFIDENCE ? kSchedThresholdConf : kSchedThresholdSurv;
+  a.threshold = threshold;
   return launch_schedule(a, (cudaStream_t)stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

@@ -550,21 +550,6 @@ bool draft_tc_shape_ok(const DraftArgs &a);
 size_t draft_packed_bytes(int64_t rank, int64_t V);  // 0 when rank is not a positive multiple of 64
 cudaError_t launch_pack_projection(const void *W, int64_t rank, int64_t V, void *Wp, cudaStream_t s);
 
-struct ScheduleArgs {
-  const float *conf;
-  const int32_t *K_r;
-  const double *sps;
-  int64_t sps_len, B, K_max;
-  int32_t *ell, *tgt_off;
-  double *theta_best;
-  int64_t *b_star;
-  float *survival;
-  int32_t *dev_status;
-  void *ws;
-};
-
-size_t schedule_ws_bytes(int64_t B, int64_t K_max);
-cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s);
 
 struct VerifyJob {
   int mode;      // 0 none, 1 residual (T > 0), 2 bonus (T > 0), 3 bonus (greedy)

@@ -11,7 +11,15 @@
 // the first decline.  Every step is deterministic, so the lengths agree bit
 // for bit with a sequential evaluation of Algorithm 1 in the same arithmetic.
 // Pools whose working arrays fit in about 160 KB are kept in shared memory.
-#include "dspark_internal.cuh"
+//
+// The same kernel serves the deployed scheduler of "DSpark" S5.2 (tutorial S9):
+// the capacity mode takes the global maximum of Theta along the greedy path
+// (no early stop; the first maximum on ties), and the top-K mode admits the first
+// min(capacity, N) candidates of the current ranking without any SPS lookup.
+// The static-threshold modes (the prior methods of S3.2.2, the sweep of S4.3.3)
+// need no ranking: each request's length is the longest prefix whose
+// confidences, or survival products, reach the threshold.
+#include "schedule.cuh"
 
 namespace dspark {
 namespace {
@@ -72,13 +80,34 @@ __device__ T block_exclusive_scan(T v, T *warp_sums, T *total) {
   return prefix + x - v;
 }
 
+// ell -> tgt_off (exclusive scan of ell + 1); returns the number of verified draft tokens.
+__device__ int64_t write_offsets(const ScheduleArgs &a, uint32_t *wsum32) {
+  const int tid = threadIdx.x;
+  const int64_t B = a.B;
+  const int64_t per_r = (B + kThreads - 1) / kThreads;
+  const int64_t rb = tid * per_r, re = min(B, rb + per_r);
+  uint32_t lsum = 0;
+  for (int64_t r = rb; r < re; ++r) lsum += (uint32_t)a.ell[r] + 1u;
+  uint32_t tot;
+  uint32_t o = block_exclusive_scan<uint32_t>(lsum, wsum32, &tot);
+  for (int64_t r = rb; r < re; ++r) {
+    a.tgt_off[r] = (int32_t)o;
+    o += (uint32_t)a.ell[r] + 1u;
+  }
+  if (tid == 0) a.tgt_off[B] = (int32_t)tot;
+  return (int64_t)tot - B;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_constant__ ScheduleArgs a, int in_smem) {
   extern __shared__ __align__(256) uint8_t pool[];
   __shared__ uint32_t hist[kWarps][257];
   __shared__ uint32_t wsum32[kWarps];
   __shared__ unsigned long long wsum64[kWarps];
   __shared__ int s_err, s_stop, s_skip;
+  __shared__ double s_wmax[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int mode = a.mode;
+  const bool by_threshold = mode == kSchedThresholdConf || mode == kSchedThresholdSurv;
   if (tid == 0) {
     s_skip = read_status(a.dev_status);
     s_err = 0;
@@ -93,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
   // -- validation, survival products, zeroed lengths ------------------------
   for (int64_t r = tid; r < B; r += kThreads) {
     const int kr = a.K_r[r];
-    a.ell[r] = 0;
+    if (a.ell) a.ell[r] = 0;
     if (kr < 1 || kr > K) {
       atomicCAS(&s_err, 0, (int)DSPARK_ERR_LENGTHS);
       continue;
@@ -103,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) cr[j] = (j < kr) ? a.conf[r * K + j] : 0.0f;
     float s = 1.0f;
+    int len = 0;
+    bool open = true;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j >= K) break;
@@ -112,14 +143,24 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
         if (!(c >= 0.0f && c <= 1.0f)) atomicCAS(&s_err, 0, (int)DSPARK_ERR_CONFIDENCE);
         s = __fmul_rn(s, c);
         v = s;
+        // threshold modes: the prefix ends at the first position that fails (or has a = 0)
+        const float tested = mode == kSchedThresholdConf ? c : s;
+        if (open && s > 0.0f && tested >= a.threshold) len = j + 1;
+        else open = false;
       }
-      surv_slot[j * B + r] = v;
+      if (!by_threshold) surv_slot[j * B + r] = v;
       if (a.survival) a.survival[r * K + j] = v;
     }
+    if (by_threshold) a.ell[r] = len;
   }
   __syncthreads();
   if (s_err) {
     if (tid == 0) set_status(a.dev_status, s_err);
+    return;
+  }
+  if (by_threshold) {
+    const int64_t admitted = write_offsets(a, wsum32);
+    if (tid == 0 && a.b_star) *a.b_star = B + admitted;
     return;
   }
 
@@ -138,9 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
       ++pos;
     }
   }
-  if (a.sps_len < B + (int64_t)N + 1) {
+  if (mode != kSchedTopK && a.sps_len < B + (int64_t)N + 1) {
     if (tid == 0) set_status(a.dev_status, DSPARK_ERR_SPS_TOO_SHORT);
     return;
+  }
+  int64_t cap_in = 0;
+  if (mode == kSchedTopK) {
+    cap_in = *a.capacity_in;
+    if (cap_in < 0) {
+      if (tid == 0) set_status(a.dev_status, DSPARK_ERR_LENGTHS);
+      return;
+    }
   }
   __syncthreads();
 
@@ -202,52 +251,71 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const __grid_cons
   }
   // after 4 passes the sorted data is back in keyA / idxA
 
-  // -- exact fixed-point prefix of survivals and the objective ---------------
-  const uint32_t per_t = (N + kThreads - 1) / kThreads;
-  const uint32_t tb = tid * per_t, te = min(N, tb + per_t);
-  unsigned long long loc = 0;
-  for (uint32_t i = tb; i < te; ++i) {
-    const float av = __uint_as_float(~sk[i]);
-    const unsigned long long t = __double2ull_rn((double)av * 0x1p40);
-    w.tfix[i] = t;
-    loc += t;
+  int64_t admitted = 0;
+  if (mode == kSchedTopK) {
+    admitted = min(cap_in, (int64_t)N);
+  } else {
+    // -- exact fixed-point prefix of survivals and the objective ---------------
+    const uint32_t per_t = (N + kThreads - 1) / kThreads;
+    const uint32_t tb = tid * per_t, te = min(N, tb + per_t);
+    unsigned long long loc = 0;
+    for (uint32_t i = tb; i < te; ++i) {
+      const float av = __uint_as_float(~sk[i]);
+      const unsigned long long t = __double2ull_rn((double)av * 0x1p40);
+      w.tfix[i] = t;
+      loc += t;
+    }
+    unsigned long long totT;
+    unsigned long long run = block_exclusive_scan<unsigned long long>(loc, wsum64, &totT);
+    const double R = (double)B;
+    for (uint32_t i = tb; i < te; ++i) {
+      run += w.tfix[i];
+      const double tau = __dadd_rn(R, __dmul_rn(__ull2double_rn(run), 0x1p-40));
+      w.theta[i + 1] = __dmul_rn(tau, a.sps[B + i + 1]);
+    }
+    if (tid == 0) w.theta[0] = __dmul_rn(R, a.sps[B]);
+    __syncthreads();
+    if (mode == kSchedAlgorithm1) {
+      // first i in 1..N with Theta_i <= Theta_{i-1}
+      int my_stop = INT32_MAX;
+      for (uint32_t i = tb; i < te; ++i) {
+        if (!(w.theta[i + 1] > w.theta[i])) { my_stop = (int)(i + 1); break; }
+      }
+      if (my_stop != INT32_MAX) atomicMin(&s_stop, my_stop);
+      __syncthreads();
+      admitted = (s_stop == INT32_MAX) ? (int64_t)N : (int64_t)s_stop - 1;
+    } else {
+      // capacity: the first i in 0..N with the largest Theta_i (values compared exactly)
+      double best = -INFINITY;
+      int best_i = INT32_MAX;
+      if (tid == 0) { best = w.theta[0]; best_i = 0; }
+      for (uint32_t i = tb; i < te; ++i) {
+        const double th = w.theta[i + 1];
+        if (th > best) { best = th; best_i = (int)(i + 1); }
+      }
+      double m = best;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, d));
+      if (lane == 0) s_wmax[warp] = m;
+      __syncthreads();
+      m = s_wmax[0];
+      for (int q = 1; q < kWarps; ++q) m = fmax(m, s_wmax[q]);
+      if (best == m && best_i != INT32_MAX) atomicMin(&s_stop, best_i);
+      __syncthreads();
+      admitted = s_stop;
+    }
   }
-  unsigned long long totT;
-  unsigned long long run = block_exclusive_scan<unsigned long long>(loc, wsum64, &totT);
-  const double R = (double)B;
-  for (uint32_t i = tb; i < te; ++i) {
-    run += w.tfix[i];
-    const double tau = __dadd_rn(R, __dmul_rn(__ull2double_rn(run), 0x1p-40));
-    w.theta[i + 1] = __dmul_rn(tau, a.sps[B + i + 1]);
-  }
-  if (tid == 0) w.theta[0] = __dmul_rn(R, a.sps[B]);
-  __syncthreads();
-  // first i in 1..N with Theta_i <= Theta_{i-1}
-  int my_stop = INT32_MAX;
-  for (uint32_t i = tb; i < te; ++i) {
-    if (!(w.theta[i + 1] > w.theta[i])) { my_stop = (int)(i + 1); break; }
-  }
-  if (my_stop != INT32_MAX) atomicMin(&s_stop, my_stop);
-  __syncthreads();
-  const int64_t admitted = (s_stop == INT32_MAX) ? (int64_t)N : (int64_t)s_stop - 1;
 
   // -- lengths and offsets ----------------------------------------------------
-  for (int64_t i = tid; i < admitted; i += kThreads) atomicAdd(&a.ell[si[i] % (uint32_t)B], 1);
-  __syncthreads();
-  const int64_t per_r = (B + kThreads - 1) / kThreads;
-  const int64_t rb = tid * per_r, re = min(B, rb + per_r);
-  uint32_t lsum = 0;
-  for (int64_t r = rb; r < re; ++r) lsum += (uint32_t)a.ell[r] + 1u;
-  uint32_t tot;
-  uint32_t o = block_exclusive_scan<uint32_t>(lsum, wsum32, &tot);
-  for (int64_t r = rb; r < re; ++r) {
-    a.tgt_off[r] = (int32_t)o;
-    o += (uint32_t)a.ell[r] + 1u;
+  if (a.ell) {
+    for (int64_t i = tid; i < admitted; i += kThreads) atomicAdd(&a.ell[si[i] % (uint32_t)B], 1);
+    __syncthreads();
+    if (a.tgt_off) write_offsets(a, wsum32);
   }
   if (tid == 0) {
-    a.tgt_off[B] = (int32_t)tot;
-    if (a.theta_best) *a.theta_best = w.theta[admitted];
+    if (a.theta_best && mode != kSchedTopK) *a.theta_best = w.theta[admitted];
     if (a.b_star) *a.b_star = B + admitted;
+    if (a.capacity_out) *a.capacity_out = (int32_t)admitted;
   }
 }
 
@@ -259,6 +327,10 @@ size_t schedule_ws_bytes(int64_t B, int64_t K_max) {
 }
 
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
+  if (a.mode == kSchedThresholdConf || a.mode == kSchedThresholdSurv) {
+    schedule_kernel<<<1, kThreads, 0, s>>>(a, 0);   // no ranking, no working arrays
+    return cudaGetLastError();
+  }
   const size_t pool_bytes = schedule_ws_bytes(a.B, a.K_max);
   const bool in_smem = pool_bytes <= kSmemPoolMax;
   if (in_smem) {

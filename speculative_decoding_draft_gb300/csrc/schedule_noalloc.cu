@@ -18,7 +18,7 @@
 // array needs to start at zero and no clearing is done.
 #include <mutex>
 
-#include "dspark_internal.cuh"
+#include "schedule.cuh"
 
 namespace {
 

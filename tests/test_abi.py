@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     import speculative_decoding_draft_gb300 as ds
-    assert lib.dspark_version() == 100
+    assert lib.dspark_version() == 101
     for code, name in ds.STATUS_NAMES.items():
         assert ds.status_string(code) == name
 
@@ -87,6 +87,16 @@ def test_host_validation_needs_no_device(lib):
                                           null) == 10
     assert lib.dspark_schedule_survival(one, one, one, 10, 4, 0, one, one, null, null, null, one, 1 << 20, one,
                                         null) == 2
+    # scheduler variants
+    assert lib.dspark_schedule_capacity(one, one, one, 10, 4, 7, null, null, null, null, one, 1 << 20, one,
+                                        null) == 1
+    assert lib.dspark_schedule_capacity(one, one, one, 10, 4, 7, one, null, one, null, one, 1 << 20, one,
+                                        null) == 1                      # ell without tgt_off
+    assert lib.dspark_schedule_capacity(one, one, one, 10, 4, 7, one, null, null, null, one, 16, one, null) == 10
+    assert lib.dspark_schedule_topk(one, one, null, 4, 7, one, one, null, null, one, 1 << 20, one, null) == 1
+    assert lib.dspark_schedule_topk(one, one, one, 4, 17, one, one, null, null, one, 1 << 20, one, null) == 2
+    assert lib.dspark_schedule_threshold(one, one, 0.5, 2, 4, 7, one, one, null, null, one, null) == 2
+    assert lib.dspark_schedule_threshold(one, one, float("nan"), 0, 4, 7, one, one, null, null, one, null) == 9
     vd = ds.Dims(4, 7, 1000, 0, ds.BF16, 0)
     assert lib.dspark_verify_ragged(one, null, one, one, one, one, one, 0, vd, one, one, ctypes.c_void_p(300),
                                     1 << 30, one, null) == 10
