@@ -158,6 +158,30 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
                                          int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Draft with the confidence head's Markov term fused in ("DSpark" S3.2.1;
+ * "Speculative decoding, from zero to DSpark" S8).
+ *
+ * The confidence head is one linear projection of [h_k ; W1[x_{k-1}]] and a
+ * sigmoid.  Its backbone part has no sequential dependence and is an input; its
+ * Markov part needs the token sampled at position k-1, which this call has at
+ * hand, so the head is evaluated inside the draft:
+ *   conf[r, k] = sigmoid(conf_h[r, k] + sum_i conf_w[i] * E[x_{k-1}, i])
+ * (x_0 = anchor[r]), fp32 arithmetic.  Every other argument, output and error is
+ * that of dspark_draft_markov_sample, whose outputs are unchanged.
+ *
+ *   conf_h   [B, K_max] float  the backbone term w_h . h_k + b of the head.
+ *   conf_w   [rank] float      the head's weights on the Markov embedding.
+ *   conf     [B, K_max] float out: c_k for k <= K_r, 0 for k > K_r.
+ * ------------------------------------------------------------------------ */
+dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E, const void *W,
+                                                    const int32_t *anchor, const int32_t *K_r,
+                                                    const float *temperature, uint64_t seed, dspark_dims dims,
+                                                    const float *conf_h, const float *conf_w,
+                                                    int32_t *draft_tok, void *draft_logits, float *draft_lse,
+                                                    float *conf, void *workspace, size_t workspace_bytes,
+                                                    int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Schedule: hardware-aware prefix scheduler ("DSpark" S3.2.2, Algorithm 1;
  * "Speculative decoding, from zero to DSpark" S8).
  *

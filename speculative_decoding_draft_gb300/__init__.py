@@ -43,7 +43,8 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = [
-    "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_draft_packed_projection_bytes",
+    "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_draft_markov_sample_confidence",
+    "dspark_draft_packed_projection_bytes",
     "dspark_draft_pack_projection", "dspark_schedule_workspace_bytes",
     "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_schedule_capacity",
     "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_workspace_bytes",
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
     L.dspark_draft_pack_projection.restype = st
     L.dspark_draft_markov_sample.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
     L.dspark_draft_markov_sample.restype = st
+    L.dspark_draft_markov_sample_confidence.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, P, P, P, sz, P, P]
+    L.dspark_draft_markov_sample_confidence.restype = st
     L.dspark_schedule_workspace_bytes.argtypes = [i64, i64]
     L.dspark_schedule_workspace_bytes.restype = sz
     L.dspark_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, sz, P, P]
@@ -222,7 +225,7 @@ def new_status(device) -> torch.Tensor:
 # ---------------------------------------------------------------------------
 def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
                         want_lse: bool = True, force_simt: bool = False, spare_sm: bool = False,
-                        out: Optional[dict] = None,
+                        conf_h=None, conf_w=None, out: Optional[dict] = None,
                         workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                         stream=None) -> dict:
     """Markov-head draft sampling (C ABI dspark_draft_markov_sample).
@@ -234,6 +237,9 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     [B,K_max] float32 or None, and the status / workspace tensors used.
     spare_sm leaves one SM free of the tensor-core path's persistent kernel, for a
     kernel on another stream (the scheduler) to run beside it.
+    With conf_h [B,K_max] float32 (the backbone term of the confidence head) and
+    conf_w [rank] float32 (its weights on the Markov embedding), the call is
+    dspark_draft_markov_sample_confidence and also returns conf [B,K_max] float32.
     """
     dt = _dtype_code(_dev(U, "U"))
     B, K_max, V = U.shape
@@ -265,11 +271,27 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     nbytes = draft_workspace_bytes(B, K_max, V, rank, dt, flags)
     ws = _workspace(nbytes, dev, workspace)
     dims = Dims(B, K_max, V, rank, dt, flags)
-    code = lib().dspark_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r), _ptr(temperature),
-                                            ctypes.c_uint64(seed), dims, _ptr(tok), _ptr(logits), _ptr(lse),
-                                            _ptr(ws), ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
-    _raise(code, "dspark_draft_markov_sample")
-    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, status=status, workspace=ws)
+    if (conf_h is None) != (conf_w is None):
+        raise ValueError("conf_h and conf_w go together")
+    conf = None
+    if conf_h is None:
+        code = lib().dspark_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r),
+                                                _ptr(temperature), ctypes.c_uint64(seed), dims, _ptr(tok),
+                                                _ptr(logits), _ptr(lse), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                                _ptr(status), _stream(stream))
+        _raise(code, "dspark_draft_markov_sample")
+    else:
+        _dev(conf_h, "conf_h", torch.float32, (B, K_max))
+        _dev(conf_w, "conf_w", torch.float32, (rank,))
+        conf = out.get("conf")
+        if conf is None:
+            conf = torch.empty(B, K_max, dtype=torch.float32, device=dev)
+        code = lib().dspark_draft_markov_sample_confidence(
+            _ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r), _ptr(temperature), ctypes.c_uint64(seed), dims,
+            _ptr(conf_h), _ptr(conf_w), _ptr(tok), _ptr(logits), _ptr(lse), _ptr(conf), _ptr(ws),
+            ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
+        _raise(code, "dspark_draft_markov_sample_confidence")
+    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, conf=conf, status=status, workspace=ws)
 
 
 def schedule_survival(conf, K_r, sps, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,

@@ -134,11 +134,13 @@ dspark_status dspark_draft_pack_projection(const void *W, dspark_dims dims, void
              : DSPARK_ERR_CUDA;
 }
 
-dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
-                                         const int32_t *K_r, const float *temperature, uint64_t seed,
-                                         dspark_dims dims, int32_t *draft_tok, void *draft_logits,
-                                         float *draft_lse, void *workspace, size_t workspace_bytes,
-                                         int32_t *dev_status, void *stream) {
+namespace {
+
+dspark_status draft_call(const void *U, const void *E, const void *W, const int32_t *anchor, const int32_t *K_r,
+                         const float *temperature, uint64_t seed, dspark_dims dims, int32_t *draft_tok,
+                         void *draft_logits, float *draft_lse, const float *conf_h, const float *conf_w,
+                         float *conf, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         void *stream) {
   if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok || !dev_status) return DSPARK_ERR_NULL;
   dspark_status st = check_dims(dims, true);
   if (st != DSPARK_OK) return st;
@@ -165,6 +167,9 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   a.rank = dims.rank;
   a.dtype = dims.dtype;
   a.key = make_philox_key(seed);
+  a.conf_h = conf_h;
+  a.conf_w = conf_w;
+  a.conf_out = conf;
   char *p = (char *)workspace;
   a.perm = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)dims.B);
@@ -199,6 +204,29 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
   const int tc_sms = (dims.flags & DSPARK_FLAG_SPARE_SM) && dev.sms > 1 ? dev.sms - 1 : dev.sms;
   cudaError_t e = use_tc ? launch_draft_tc(a, s, tc_sms) : launch_draft_simt(a, s);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+}  // namespace
+
+dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
+                                         const int32_t *K_r, const float *temperature, uint64_t seed,
+                                         dspark_dims dims, int32_t *draft_tok, void *draft_logits,
+                                         float *draft_lse, void *workspace, size_t workspace_bytes,
+                                         int32_t *dev_status, void *stream) {
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, nullptr,
+                    nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+}
+
+dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E, const void *W,
+                                                    const int32_t *anchor, const int32_t *K_r,
+                                                    const float *temperature, uint64_t seed, dspark_dims dims,
+                                                    const float *conf_h, const float *conf_w,
+                                                    int32_t *draft_tok, void *draft_logits, float *draft_lse,
+                                                    float *conf, void *workspace, size_t workspace_bytes,
+                                                    int32_t *dev_status, void *stream) {
+  if (!conf_h || !conf_w || !conf) return DSPARK_ERR_NULL;
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, conf_h,
+                    conf_w, conf, workspace, workspace_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -45,7 +45,10 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     a.counters[r] = 0;
     for (int k = 0; k < K; ++k) {
       a.best_key[(int64_t)r * K + k] = 0ull;
-      if (k >= kr) a.draft_tok[(int64_t)r * K + k] = -1;
+      if (k >= kr) {
+        a.draft_tok[(int64_t)r * K + k] = -1;
+        if (a.conf_out) a.conf_out[(int64_t)r * K + k] = 0.0f;
+      }
     }
   }
   __syncthreads();
@@ -172,6 +175,11 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_step(const __grid_con
       const Partial *ptr[1] = {a.partials + (int64_t)i * chunks};
       Race tot[1];
       warp_merge_rows<1>(ptr, chunks, tot);
+      if (a.conf_out) {   // the previous token's embedding row is this block's e_s
+        const float c = warp_confidence([&](int q) { return e_s[q]; }, a.conf_w, rank,
+                                        a.conf_h[(int64_t)r * K + k - 1], threadIdx.x);
+        if (threadIdx.x == 0) a.conf_out[(int64_t)r * K + k - 1] = c;
+      }
       if (threadIdx.x == 0) {
         a.draft_tok[(int64_t)r * K + k - 1] = tot[0].idx;
         if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot[0].best : tot[0].m + logf(tot[0].S);

@@ -602,8 +602,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
       }
       k_last = k;
     }
-    // Once every CTA has arrived at the last position: the tokens from the packed maxima
-    // and the normalisers from the CTA partials, one warp per (position, request).
+    // Once every CTA has arrived at the last position: the tokens from the packed maxima,
+    // the normalisers from the CTA partials and, when asked for, the confidence head's
+    // output (its Markov term needs the previous position's token), one warp per
+    // (position, request).
     if (k_last > 0 && !*abort) {
       if (et == 0) {
         const long long t0 = clock64();
@@ -626,6 +628,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm};
           Race tot[1];
           warp_merge_rows<1>(ptr, pl.gm, tot);
+          if (a.conf_out) {
+            const int prev = k == 1 ? a.anchor[r] : key_index(load_key(a.best_key + (int64_t)r * K + k - 2));
+            const __nv_bfloat16 *erow = (const __nv_bfloat16 *)a.E + (int64_t)prev * a.rank;
+            const float c = warp_confidence([&](int q) { return __bfloat162float(erow[q]); }, a.conf_w,
+                                            (int)a.rank, a.conf_h[(int64_t)r * K + k - 1], lane);
+            if (lane == 0) a.conf_out[(int64_t)r * K + k - 1] = c;
+          }
           if (lane == 0) {
             const int64_t at = (int64_t)r * K + k - 1;
             a.draft_tok[at] = key_index(load_key(a.best_key + at));

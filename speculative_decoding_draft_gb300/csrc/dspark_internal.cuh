@@ -521,7 +521,28 @@ struct DraftArgs {
   int32_t *gbar;      // [K_max + 1] grid-barrier arrival counters of the tensor-core path
   Partial *partials;  // [partial_slots]
   int64_t partial_slots;
+  // confidence head with the Markov term (optional): conf_out[r, k] =
+  // sigmoid(conf_h[r, k] + conf_w . E[x_{k-1}])
+  const float *conf_h = nullptr;   // [B, K_max] backbone term w_h . h_k + b
+  const float *conf_w = nullptr;   // [rank] weights of the Markov embedding
+  float *conf_out = nullptr;       // [B, K_max]
 };
+
+// Confidence head ("DSpark" S3.2.1): one linear projection of the backbone state and the
+// previous token's Markov embedding, then a sigmoid.  One warp: e(q) returns entry q of
+// the embedding row; the rank is summed lane-strided, then across the warp.  The sigmoid
+// is evaluated as t / (1 + t), t = exp(s), for s < 0 so that it never overflows.
+template <typename EFn>
+__device__ __forceinline__ float warp_confidence(EFn e, const float *w, int rank, float h, int lane) {
+  float acc = 0.0f;
+  for (int q = lane; q < rank; q += 32) acc = fmaf(e(q), w[q], acc);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+  const float s = h + acc;
+  if (s >= 0.0f) return 1.0f / (1.0f + expf(-s));
+  const float t = expf(s);
+  return t / (1.0f + t);
+}
 
 // Total order key of a perturbed score and its index: larger score first, then the
 // smaller index, so a 64-bit atomicMax merges (score desc, index asc).

@@ -123,6 +123,15 @@ def draft_inputs(cfg: Config, device="cpu") -> dict:
     return dict(U=U, E=E, W=W, **request_params(cfg, device))
 
 
+def confidence_head(cfg: Config, device="cpu") -> dict:
+    """Confidence-head inputs: conf_h [B, K_max] ~ N(1.5, 1), the backbone term (so that the
+    head alone gives confidences like the scheduler inputs'), and conf_w [rank] ~ N(0, 1), the
+    weights on the Markov embedding (with E ~ N(0, ew_std) the Markov term has standard
+    deviation ew_std * sqrt(rank): 0.32 at rank 256, 0.4 for the fp32 case)."""
+    g = _gen(cfg, device, 6)
+    return dict(conf_h=_randn((cfg.B, cfg.K_max), 1.0, g, device) + 1.5, conf_w=_randn((cfg.rank,), 1.0, g, device))
+
+
 # ---------------------------------------------------------------------------
 # scheduler inputs
 # ---------------------------------------------------------------------------
