@@ -17,8 +17,9 @@
 //     instead of one position after another.
 //  2. verify_sample: the residual / bonus two-level draw over the vocabulary,
 //     spread over the whole GPU (request x vocabulary chunk, about two CTAs per
-//     SM in one wave, each thread a run of 32-wide blocks), with the last block of
-//     each request merging the chunk partials.
+//     SM in one wave, each thread a run of 32-wide blocks; for the residual on bf16
+//     rows the next block's loads are in flight while a block is drawn), with the
+//     last block of each request merging the chunk partials.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -27,7 +28,6 @@ namespace {
 constexpr int kRowThreads = 128;
 constexpr int kRowCtasPerSm = 3;
 constexpr int kBatch = 4;          // loads in flight per thread in the accept chain (fp32 / unaligned)
-constexpr int kPkBatch = 16;       // packed bf16 16-byte loads in flight per thread
 constexpr int kRowPk = 12;          // packed bf16 16-byte loads per thread and row item
 constexpr int kRowSlice = kRowThreads * 8 * kRowPk;     // vocabulary slice of one row item
 constexpr int kRowParts = kRowThreads / 32;              // partial statistics per item: one per warp
@@ -119,19 +119,6 @@ __device__ __forceinline__ Stats stats_shfl_down(const Stats &s, int d) {
   o.best = __shfl_down_sync(0xffffffffu, s.best, d);
   o.idx = __shfl_down_sync(0xffffffffu, s.idx, d);
   return o;
-}
-
-// Block reduction; result valid in thread 0.
-__device__ __forceinline__ Stats stats_block_reduce(Stats s, Stats *scratch) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) stats_merge(s, stats_shfl_down(s, d));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) scratch[warp] = s;
-  __syncthreads();
-  if (threadIdx.x == 0)
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) stats_merge(s, scratch[i]);
-  __syncthreads();
-  return s;
 }
 
 __device__ __forceinline__ float pick8(const float (&x)[8], int q) {
@@ -512,6 +499,15 @@ __device__ __forceinline__ void load32(const void *base, int64_t row_off, int v0
   }
 }
 
+// 32 bf16 of a 16-byte aligned row from element v0: four 16-byte loads; 8-element groups
+// at or past `hi` hold bf16 -inf (V and hi are multiples of 8 here).
+__device__ __forceinline__ void issue_block(const void *base, int64_t row_off, int v0, int hi, uint4 (&u)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    u[q] = (v0 + 8 * q + 8 <= hi) ? __ldcs((const uint4 *)((const unsigned short *)base + row_off + v0 + 8 * q))
+                                  : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+
 // Residual weight max(0, p - q) with p = 2^(t a - lt2), q = 2^(d a - ld2).
 __device__ __forceinline__ float resid_weight(float t, float d, float a, float lt2, float ld2) {
   return fmaxf(fast_ex2(fmaf(t, a, -lt2)) - fast_ex2(fmaf(d, a, -ld2)), 0.0f);
@@ -534,6 +530,28 @@ __device__ __forceinline__ void brace_resid_block(BRace &r, float (&t)[kBlockW],
   if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(t, uniform_accept(pick_word()) * L);
 }
 
+// brace_resid_block on packed bf16 rows: the same weights in the same order, unpacked
+// one pair at a time.
+template <class PickWord>
+__device__ __forceinline__ void brace_resid_packed(BRace &r, const uint4 (&tp)[4], const uint4 (&dp)[4], float a,
+                                                   float lt2, float ld2, uint32_t wb, int v0, bool &any_pos,
+                                                   PickWord pick_word) {
+  float w[kBlockW];
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < kBlockW; ++q) {
+    const uint32_t tw = word_of(tp[q >> 3], (q >> 1) & 3), dw = word_of(dp[q >> 3], (q >> 1) & 3);
+    const float t = __uint_as_float((q & 1) ? (tw & 0xffff0000u) : (tw << 16));
+    const float d = __uint_as_float((q & 1) ? (dw & 0xffff0000u) : (dw << 16));
+    w[q] = resid_weight(t, d, a, lt2, ld2);
+    s[q & 3] += w[q];
+  }
+  const float L = (s[0] + s[1]) + (s[2] + s[3]);
+  if (!(L > 0.0f)) return;
+  any_pos = true;
+  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(w, uniform_accept(pick_word()) * L);
+}
+
 // The draw of one request over [lo, hi): residual (mode 1), bonus from the
 // target row (mode 2, also the rounding guard of mode 1), greedy bonus (mode 3).
 template <int DT, bool VEC>
@@ -546,6 +564,27 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
   const PhiloxKey key = a.key;   // round keys in registers for the hot loop
   const float a2 = job.invT * kLog2e;
   const float lt2 = job.lse_t * kLog2e, ld2 = job.lse_q * kLog2e;
+  if (DT == DSPARK_BF16 && VEC && mode == 1) {
+    // residual on packed rows: the next block's target loads are in flight while this block
+    // is drawn, and the draft row's loads go out before the block's noise is generated
+    uint4 tc[4], dc[4], tn[4];
+    int v0 = lo + tid * kBlockW;
+    if (v0 < hi) issue_block(a.tgt, trow, v0, hi, tc);
+    for (; v0 < hi; v0 += nthreads * kBlockW) {
+      const int vn = v0 + nthreads * kBlockW;
+      issue_block(a.D, drow, v0, hi, dc);
+      if (vn < hi) issue_block(a.tgt, trow, vn, hi, tn);
+      // round keys read from the parameter block: registers go to the loads in flight
+      const uint32_t g = (uint32_t)v0 >> 5;
+      const uint32_t wb = word_of(philox(a.key, g >> 2, (uint32_t)job.pos, (uint32_t)r, kTagResid), (int)(g & 3u));
+      brace_resid_packed(rc, tc, dc, a2, lt2, ld2, wb, v0, any_pos, [&] {
+        return word_of(philox(a.key, g >> 2, (uint32_t)job.pos, (uint32_t)r, kTagResidPick), (int)(g & 3u));
+      });
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc[q] = tn[q];
+    }
+    return;
+  }
   for (int v0 = lo + tid * kBlockW; v0 < hi; v0 += nthreads * kBlockW) {
     float t[kBlockW];
     load32<DT, VEC>(a.tgt, trow, v0, hi, t);
@@ -569,7 +608,7 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSampleThreads) verify_sample(const __grid_constant__ VerifyArgs a) {
+__global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_constant__ VerifyArgs a) {
   __shared__ Race red[kSampleThreads / 32];
   __shared__ int s_any[kSampleThreads / 32];
   __shared__ int s_last, s_tok;
