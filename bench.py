@@ -397,7 +397,7 @@ def main(argv=None):
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     ds.lib()          # fails loudly when the CUDA library is missing
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.replica(wl.CONFIGS[args.config], rank)   # each replica drafts its own batch
     w = make_workload(cfg, dev, args.sps)
     # The scheduler depends on the confidences only, not on the drafted tokens, so by
     # default it runs on a second stream beside the draft, which leaves it one SM.

@@ -40,14 +40,15 @@ class Config:
     noise_std: float = 1.0
     sps_kind: str = "tiny"
     sps_len: int = 65
+    batch: int = 0               # which batch of requests (one per replica under torchrun)
 
     @property
     def philox_seed(self) -> int:
-        return self.index
+        return self.index + (self.batch << 32)
 
     @property
     def data_seed(self) -> int:
-        return 1234 + self.index
+        return 1234 + self.index + 1000 * self.batch
 
     @property
     def torch_dtype(self):
@@ -74,6 +75,12 @@ WORKLOAD_TEXT = {
     "dsv4": "DeepSeek-V4-shaped: B=1024, K=5, V=129280, rank 256, bf16",
     "ragged": "ragged mixed: B=2048, K in 1..7, V=151936, rank 256, bf16, 30% greedy",
 }
+
+
+def replica(cfg: Config, rank: int) -> Config:
+    """The batch of requests that replica `rank` processes: the same recipe with its own data
+    and random-stream seeds (rank 0 is the configuration itself)."""
+    return replace(cfg, batch=rank)
 
 
 def small_config(name: str = "qwen", **kw) -> Config:
