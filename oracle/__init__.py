@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.dso_draft_markov_sample.argtypes = [P, P, P, i32, P, P, P, P, u64, i64, i64, i64, i64,
                                               P, P, P, P, P, i32]
         L.dso_draft_markov_sample.restype = i32
+        L.dso_draft_rnn_sample.argtypes = [P, P, P, P, i32, P, P, P, P, P, u64, i64, i64, i64, i64,
+                                           P, P, P, P, P, P, i32]
+        L.dso_draft_rnn_sample.restype = i32
         L.dso_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P, P, P, P]
         L.dso_schedule_survival.restype = i32
         L.dso_draft_confidence.argtypes = [P, i32, i64, i64, P, P, P, P, P, i64, i64, P]
@@ -226,6 +229,45 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed, req_id=None, wa
     if st:
         raise OracleError(st)
     return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags)
+
+
+def draft_rnn_sample(U, E, W, Wc, cx, anchor, K_r, temperature, seed, req_id=None, want_logits=True,
+                     want_feat=False, nthreads=0):
+    """RNN-head draft sampling.  U [B,K_max,V]; E [V,rank]; W [rank,V]; Wc [3 rank, 2 rank] (one dtype);
+    cx [B,K_max,3 rank] float32 (the backbone term of the cell).
+
+    Returns the draft_markov_sample dict plus feat [B,K_max,rank] f64 (the head's feature) when asked.
+    """
+    U, dt = _logits(U)
+    E, dtE = _logits(E)
+    W, dtW = _logits(W)
+    Wc, dtC = _logits(Wc)
+    if not (dt == dtE == dtW == dtC):
+        raise TypeError("U, E, W, Wc must share one dtype")
+    B, K_max, V = U.shape
+    rank = E.shape[1]
+    if E.shape[0] != V or W.shape != (rank, V) or Wc.shape != (3 * rank, 2 * rank):
+        raise ValueError("shape mismatch")
+    cx = _c(cx, np.float32)
+    if cx.shape != (B, K_max, 3 * rank):
+        raise ValueError("cx shape mismatch")
+    anchor = _c(anchor, np.int32)
+    K_r = _c(K_r, np.int32)
+    temperature = _c(temperature, np.float32)
+    rid = None if req_id is None else _c(req_id, np.int64)
+    tok = np.zeros((B, K_max), np.int32)
+    logits = np.zeros_like(U) if want_logits else None
+    lse = np.zeros((B, K_max), np.float64)
+    margin = np.zeros((B, K_max), np.float64)
+    flags = np.zeros((B, K_max), np.uint8)
+    feat = np.zeros((B, K_max, rank), np.float64) if want_feat else None
+    st = lib().dso_draft_rnn_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(Wc), dt, _ptr(cx), _ptr(anchor), _ptr(K_r),
+                                    _ptr(temperature), _ptr(rid), int(seed), B, K_max, V, rank, _ptr(tok),
+                                    _ptr(logits), _ptr(lse), _ptr(margin), _ptr(flags), _ptr(feat),
+                                    _threads(nthreads))
+    if st:
+        raise OracleError(st)
+    return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags, feat=feat)
 
 
 def draft_confidence(E, anchor, draft_tok, K_r, conf_h, conf_w):

@@ -334,6 +334,77 @@ static double row_lse_scaled(const double *z, int64_t V, double T) {
   return m + log(S);
 }
 
+/* One draft position of request rid: z = U row + bias, rounded to the storage dtype     */
+/* (stored when draft_logits is given), then the draw (T > 0) or the argmax (T = 0) with   */
+/* its normaliser, margin and near-tie flags.  Shared by the Markov and the RNN heads.      */
+static int64_t draft_position(const void *U, int dtype, int64_t ubase, const double *bias, int64_t V, double T,
+                              uint64_t seed, int64_t k, uint32_t rid, void *draft_logits, double *z, double *lw,
+                              double *le, double *l_out, double *mg_out, uint8_t *f_out) {
+  for (int64_t v = 0; v < V; ++v) {
+    double exact = load_elem(U, dtype, ubase + v) + bias[v];
+    z[v] = (dtype == ORC_F32) ? (double)(float)exact : round_bf16(exact);
+  }
+  if (draft_logits) for (int64_t v = 0; v < V; ++v) store_elem(draft_logits, dtype, ubase + v, z[v]);
+  int64_t best;
+  double l, mg;
+  uint8_t f = 0;
+  if (T > 0.0) {
+    /* two-level sampler on the weights exp(z / T); a bf16 rounding ambiguity */
+    /* enters as the uncertainty |exp(alt / T) - exp(z / T)| of its weight.  */
+    int amb = 0;
+    for (int64_t v = 0; v < V; ++v) {
+      lw[v] = z[v] / T;
+      le[v] = -INFINITY;
+      if (dtype == ORC_BF16) {
+        double alt;
+        if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) {
+          le[v] = lw[v] + log(fabs(expm1((alt - z[v]) / T)));
+          amb = 1;
+        }
+      }
+    }
+    race_t rc = block_race(lw, amb ? le : NULL, V, seed, (uint32_t)k, rid, TAG_DRAFT, TAG_DRAFT_PICK);
+    best = rc.pick;
+    mg = rc.margin;
+    if (rc.near_block) f |= 1;
+    if (rc.near_pick) f |= 8;
+    if (rc.near_err && !(f & 9)) f |= 2;
+    l = row_lse_scaled(z, V, T);
+    if (dtype == ORC_BF16) {
+      double lse_shift = 0.0;
+      for (int64_t v = 0; v < V; ++v) {
+        double alt;
+        if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt))
+          lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
+      }
+      if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
+    }
+  } else {
+    /* greedy: largest logit, smallest index on ties */
+    int64_t second = -1;
+    best = 0;
+    for (int64_t v = 1; v < V; ++v) {
+      if (z[v] > z[best]) { second = best; best = v; }
+      else if (second < 0 || z[v] > z[second]) second = v;
+    }
+    mg = z[best] - z[second];
+    l = z[best];
+    if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE) f |= 1;
+    if (dtype == ORC_BF16) {
+      for (int64_t v = 0; v < V; ++v) {
+        double alt;
+        if (!bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) continue;
+        if (v == best) { if (alt <= z[second] + ORC_SAMPLE_TIE) f |= 2; }
+        else if (alt >= z[best] - ORC_SAMPLE_TIE) f |= 2;
+      }
+    }
+  }
+  *l_out = l;
+  *mg_out = mg;
+  *f_out = f;
+  return best;
+}
+
 int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dtype,
                             const int32_t *anchor, const int32_t *K_r, const float *temperature,
                             const int64_t *req_id, uint64_t seed,
@@ -369,65 +440,9 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
         for (int64_t v = 0; v < V; ++v) bias[v] += e * load_elem(W, dtype, i * V + v);
       }
       const int64_t ubase = slot * V;
-      for (int64_t v = 0; v < V; ++v) {
-        double exact = load_elem(U, dtype, ubase + v) + bias[v];
-        z[v] = (dtype == ORC_F32) ? (double)(float)exact : round_bf16(exact);
-      }
-      if (draft_logits) for (int64_t v = 0; v < V; ++v) store_elem(draft_logits, dtype, ubase + v, z[v]);
-      int64_t best;
       double l, mg;
       uint8_t f = 0;
-      if (T > 0.0) {
-        /* two-level sampler on the weights exp(z / T); a bf16 rounding ambiguity */
-        /* enters as the uncertainty |exp(alt / T) - exp(z / T)| of its weight.  */
-        int amb = 0;
-        for (int64_t v = 0; v < V; ++v) {
-          lw[v] = z[v] / T;
-          le[v] = -INFINITY;
-          if (dtype == ORC_BF16) {
-            double alt;
-            if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) {
-              le[v] = lw[v] + log(fabs(expm1((alt - z[v]) / T)));
-              amb = 1;
-            }
-          }
-        }
-        race_t rc = block_race(lw, amb ? le : NULL, V, seed, (uint32_t)k, rid, TAG_DRAFT, TAG_DRAFT_PICK);
-        best = rc.pick;
-        mg = rc.margin;
-        if (rc.near_block) f |= 1;
-        if (rc.near_pick) f |= 8;
-        if (rc.near_err && !(f & 9)) f |= 2;
-        l = row_lse_scaled(z, V, T);
-        if (dtype == ORC_BF16) {
-          double lse_shift = 0.0;
-          for (int64_t v = 0; v < V; ++v) {
-            double alt;
-            if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt))
-              lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
-          }
-          if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
-        }
-      } else {
-        /* greedy: largest logit, smallest index on ties */
-        int64_t second = -1;
-        best = 0;
-        for (int64_t v = 1; v < V; ++v) {
-          if (z[v] > z[best]) { second = best; best = v; }
-          else if (second < 0 || z[v] > z[second]) second = v;
-        }
-        mg = z[best] - z[second];
-        l = z[best];
-        if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE) f |= 1;
-        if (dtype == ORC_BF16) {
-          for (int64_t v = 0; v < V; ++v) {
-            double alt;
-            if (!bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) continue;
-            if (v == best) { if (alt <= z[second] + ORC_SAMPLE_TIE) f |= 2; }
-            else if (alt >= z[best] - ORC_SAMPLE_TIE) f |= 2;
-          }
-        }
-      }
+      const int64_t best = draft_position(U, dtype, ubase, bias, V, T, seed, k, rid, draft_logits, z, lw, le, &l, &mg, &f);
       draft_tok[slot] = (int32_t)best;
       if (lse) lse[slot] = l;
       if (margin) margin[slot] = mg;
@@ -438,6 +453,102 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
     free(z);
     free(lw);
     free(le);
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Draft with the RNN head [DSP S3.1, RNN head]: a recurrent state s_k of    */
+/* size r carries the whole prefix within the block.  Per position, one      */
+/* linear projection of z_k = [s_{k-1}; W1[x_{k-1}]; h_k] is split into gate, */
+/* candidate and output components (W_g, W_c, W_o, jointly one projection),  */
+/* s_0 = 0.  The backbone part W_{.,h} h_k + b has no sequential dependence   */
+/* and is an input: cx [B, K_max, 3r]; the sequential part is Wc [3r, 2r]    */
+/* (columns 0..r-1 act on s_{k-1}, r..2r-1 on W1[x_{k-1}]; rows 0..r-1 gate,  */
+/* r..2r-1 candidate, 2r..3r-1 output).                                      */
+/* Readings (the update equation is missing from the paper's page; the text  */
+/* names its inputs, its three components and the zero initial state):       */
+/*   g = sigmoid(a_g), c = tanh(a_c), o = sigmoid(a_o),                       */
+/*   s_k = g * s_{k-1} + (1 - g) * c       (a gated convex update),           */
+/*   f_k = o * s_k                          (the output component gates the   */
+/*                                           state),                          */
+/*   bias_k = f_k . W2                      (the head's feature takes the place*/
+/*                                           of the Markov head's W1 row).    */
+/* fp64 throughout; the biased logits are rounded and sampled exactly as for  */
+/* the Markov head.  feat (optional) returns f_k [B, K_max, r].              */
+/* Pins: a closed output gate gives independent drafting; saturated gates    */
+/* with an identity candidate block give the Markov head on tanh(W1);        */
+/* constant pre-activations give the closed form s_k = c (1 - g^k); the       */
+/* feature at position k depends on tokens before k - 1 (memory).            */
+/* ---------------------------------------------------------------------- */
+static double sigmoid_d(double a) { return 1.0 / (1.0 + exp(-a)); }
+
+int dso_draft_rnn_sample(const void *U, const void *E, const void *W, const void *Wc, int dtype, const float *cx,
+                         const int32_t *anchor, const int32_t *K_r, const float *temperature,
+                         const int64_t *req_id, uint64_t seed,
+                         int64_t B, int64_t K_max, int64_t V, int64_t rank,
+                         int32_t *draft_tok, void *draft_logits, double *lse,
+                         double *margin, uint8_t *flags, double *feat, int nthreads) {
+  if (!U || !E || !W || !Wc || !cx || !anchor || !K_r || !temperature || !draft_tok) return ORC_ERR_NULL;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
+  if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2 || rank < 1) return ORC_ERR_DIMS;
+  for (int64_t b = 0; b < B; ++b) {
+    if (K_r[b] < 1 || K_r[b] > K_max) return ORC_ERR_LENGTHS;
+    if (anchor[b] < 0 || anchor[b] >= V) return ORC_ERR_TOKEN_RANGE;
+    if (!temperature_ok(temperature[b])) return ORC_ERR_TEMPERATURE;
+  }
+  set_threads(nthreads);
+  int64_t b;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    double *bias = (double *)malloc(sizeof(double) * (size_t)V);
+    double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    double *lw = (double *)malloc(sizeof(double) * (size_t)V);
+    double *le = (double *)malloc(sizeof(double) * (size_t)V);
+    double *st = (double *)calloc((size_t)rank, sizeof(double));        /* s_0 = 0 */
+    double *ft = (double *)malloc(sizeof(double) * (size_t)rank);
+    double *pre = (double *)malloc(sizeof(double) * (size_t)(3 * rank));
+    uint32_t rid = (uint32_t)(req_id ? req_id[b] : b);
+    int32_t x_prev = anchor[b];
+    double T = (double)temperature[b];
+    for (int64_t k = 1; k <= K_max; ++k) {
+      int64_t slot = b * K_max + (k - 1);
+      if (k > K_r[b]) { draft_tok[slot] = -1; continue; }
+      /* the cell: pre-activations of gate, candidate and output */
+      for (int64_t j = 0; j < 3 * rank; ++j) {
+        double a = (double)cx[slot * 3 * rank + j];
+        for (int64_t i = 0; i < rank; ++i) a += load_elem(Wc, dtype, j * 2 * rank + i) * st[i];
+        for (int64_t i = 0; i < rank; ++i)
+          a += load_elem(Wc, dtype, j * 2 * rank + rank + i) * load_elem(E, dtype, (int64_t)x_prev * rank + i);
+        pre[j] = a;
+      }
+      for (int64_t i = 0; i < rank; ++i) {
+        const double g = sigmoid_d(pre[i]), c = tanh(pre[rank + i]), o = sigmoid_d(pre[2 * rank + i]);
+        st[i] = g * st[i] + (1.0 - g) * c;
+        ft[i] = o * st[i];
+        if (feat) feat[slot * rank + i] = ft[i];
+      }
+      /* transition bias: the head's feature times the projection */
+      for (int64_t v = 0; v < V; ++v) bias[v] = 0.0;
+      for (int64_t i = 0; i < rank; ++i)
+        for (int64_t v = 0; v < V; ++v) bias[v] += ft[i] * load_elem(W, dtype, i * V + v);
+      double l, mg;
+      uint8_t f = 0;
+      const int64_t best = draft_position(U, dtype, slot * V, bias, V, T, seed, k, rid, draft_logits, z, lw, le, &l,
+                                          &mg, &f);
+      draft_tok[slot] = (int32_t)best;
+      if (lse) lse[slot] = l;
+      if (margin) margin[slot] = mg;
+      if (flags) flags[slot] = f;
+      x_prev = (int32_t)best;
+    }
+    free(bias);
+    free(z);
+    free(lw);
+    free(le);
+    free(st);
+    free(ft);
+    free(pre);
   }
   return ORC_OK;
 }
