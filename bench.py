@@ -55,6 +55,8 @@ def parse_args(argv=None):
                    help="launch the three calls directly instead of replaying captured CUDA graphs")
     p.add_argument("--serial", action="store_true",
                    help="run the scheduler after the draft instead of beside it on a second stream")
+    p.add_argument("--head", choices=["markov", "rnn"], default="markov",
+                   help="the draft's sequential head: the Markov head (default) or the RNN head")
     return p.parse_args(argv)
 
 
@@ -149,7 +151,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def make_workload(cfg, dev, sps_variant):
+def make_workload(cfg, dev, sps_variant, head="markov"):
     import torch
 
     import speculative_decoding_draft_gb300 as ds
@@ -166,7 +168,8 @@ def make_workload(cfg, dev, sps_variant):
     tgt, off = wl.flatten_targets(tgt_dense, ell)
     del tgt_dense
     torch.cuda.empty_cache()
-    return dict(inp=inp, conf=conf, sps=sps, ell=ell, tgt=tgt.contiguous(), off=off.to(dev))
+    return dict(inp=inp, conf=conf, sps=sps, ell=ell, tgt=tgt.contiguous(), off=off.to(dev),
+                rnn=wl.rnn_head(cfg, dev) if head == "rnn" else None)
 
 
 class Step:
@@ -196,8 +199,9 @@ class Step:
         # tensor-core draft path: W2 is a fixed weight, packed once at load time (timed here,
         # outside the step); the CUDA-core path reads it as it is
         cap = torch.cuda.get_device_capability(dev)
-        self.tensor_core = (cap == (10, 3) and cfg.dtype == "bf16" and cfg.rank % 64 == 0 and cfg.rank <= 256
-                            and V % 8 == 0)
+        self.rnn = w.get("rnn")                 # RNN head: the CUDA-core path with its cell per position
+        self.tensor_core = (self.rnn is None and cap == (10, 3) and cfg.dtype == "bf16" and cfg.rank % 64 == 0
+                            and cfg.rank <= 256 and V % 8 == 0)
         self.W = inp["W"]
         self.pack_ms = None
         flags = 0
@@ -212,18 +216,24 @@ class Step:
             self.pack_ms = e0.elapsed_time(e1)
             flags = ds.FLAG_W_PACKED
         dt = ds.BF16 if cfg.dtype == "bf16" else ds.F32
-        self.ws_d = torch.empty(ds.draft_workspace_bytes(B, K, V, cfg.rank, dt, flags), dtype=torch.uint8,
-                                device=dev)
+        ws_bytes = (ds.lib().dspark_draft_rnn_workspace_bytes(ds.Dims(B, K, V, cfg.rank, dt, 0)) if self.rnn
+                    else ds.draft_workspace_bytes(B, K, V, cfg.rank, dt, flags))
+        self.ws_d = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.ws_s = torch.empty(ds.schedule_workspace_bytes(B, K), dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(ds.verify_workspace_bytes(B, V), dtype=torch.uint8, device=dev)
         # draft: prologue + persistent kernel (tensor cores) or prologue + one
         # launch per position (CUDA cores); schedule: 1; verify: row statistics + sample
-        self.draft_launches = 2 if self.tensor_core else 1 + K
+        self.draft_launches = 2 if self.tensor_core else (1 + 2 * K if self.rnn else 1 + K)
         self.launches_per_step = self.draft_launches + 1 + 2
 
     def draft(self, inp=None):
         inp = self.w["inp"] if inp is None else inp
         W = self.W if inp["W"] is self.w["inp"]["W"] else inp["W"]   # resident weights: the packed copy
+        if self.rnn is not None:
+            self.ds.draft_rnn_sample(inp["U"], inp["E"], W, self.rnn["rnn_W"], inp.get("rnn_x", self.rnn["rnn_x"]),
+                                     inp["anchor"], inp["K_r"], inp["temperature"], self.cfg.philox_seed,
+                                     out=self.draft_out, workspace=self.ws_d, status=self.status)
+            return
         self.ds.draft_markov_sample(inp["U"], inp["E"], W, inp["anchor"], inp["K_r"], inp["temperature"],
                                     self.cfg.philox_seed, out=self.draft_out, workspace=self.ws_d,
                                     status=self.status, spare_sm=self.spare_sm)
@@ -243,13 +253,16 @@ class Step:
                               out=self.ver_out, workspace=self.ws_v, status=self.status)
 
 
-def algorithmic(cfg, K_r, ell, n_acc, temperature):
+def algorithmic(cfg, K_r, ell, n_acc, temperature, head="markov"):
     """Algorithmic bytes / flops of each operation for one step (bf16 = 2 bytes)."""
     esz = 2 if cfg.dtype == "bf16" else 4
     V, r = cfg.V, cfg.rank
     sumK = int(K_r.sum())
     draft_bytes = sumK * V * esz + r * V * esz + sumK * r * esz
     draft_flops = 2.0 * sumK * r * V
+    if head == "rnn":   # the cell: its weights once, the backbone term per position, 3r x 2r per position
+        draft_bytes += 6 * r * r * esz + sumK * 3 * r * 4
+        draft_flops += 2.0 * sumK * 3 * r * 2 * r
     # verify, with the draft normalisers known: target rows up to the deciding row, plus the
     # draft row at a rejection (T > 0) for the residual
     ver_rows = 0
@@ -321,8 +334,13 @@ def cpu_baseline(cfg, w, sample_requests):
     tgt_rows = wl.bf16_bits(w["tgt"][: int(off_all[sample_requests])])
     nthreads = os.cpu_count() or 1
     t0 = time.perf_counter()
-    d = oracle.draft_markov_sample(U, E, W, anchor, K_r, T, cfg.philox_seed, req_id=rows.astype(np.int64),
-                                   nthreads=nthreads)
+    if w.get("rnn") is not None:
+        d = oracle.draft_rnn_sample(U, E, W, wl.bf16_bits(w["rnn"]["rnn_W"]),
+                                    w["rnn"]["rnn_x"][:sample_requests].cpu().numpy(), anchor, K_r, T,
+                                    cfg.philox_seed, req_id=rows.astype(np.int64), nthreads=nthreads)
+    else:
+        d = oracle.draft_markov_sample(U, E, W, anchor, K_r, T, cfg.philox_seed, req_id=rows.astype(np.int64),
+                                       nthreads=nthreads)
     s = oracle.schedule_survival(conf, K_all, sps)
     ell = s["ell"][:sample_requests]
     off = s["tgt_off"][: sample_requests + 1]
@@ -398,7 +416,7 @@ def main(argv=None):
     dist_init(world, "nccl")
     ds.lib()          # fails loudly when the CUDA library is missing
     cfg = wl.replica(wl.CONFIGS[args.config], rank)   # each replica drafts its own batch
-    w = make_workload(cfg, dev, args.sps)
+    w = make_workload(cfg, dev, args.sps, args.head)
     # The scheduler depends on the confidences only, not on the drafted tokens, so by
     # default it runs on a second stream beside the draft, which leaves it one SM.
     overlap = not args.serial
@@ -417,7 +435,7 @@ def main(argv=None):
         raise SystemExit(f"device status {st}")
     n_acc = step.ver_out["n_acc"].cpu()
     alg = algorithmic(cfg, w["inp"]["K_r"].cpu(), step.sched_out["ell"].cpu(), n_acc,
-                      w["inp"]["temperature"].cpu())
+                      w["inp"]["temperature"].cpu(), args.head)
 
     # The step's three C-ABI calls are captured once into CUDA graphs (one per call, so the
     # events between them still time each part) and replayed: the same kernels on the same
@@ -493,7 +511,8 @@ def main(argv=None):
     kernels = {
         "draft": {"ms": t_draft, "alg_bytes": alg["draft_bytes"], "GB/s": draft_gbs, "hbm_frac": draft_gbs / hbm,
                   "TFLOP/s": draft_tflops, "tensor_frac": draft_tflops / tf, "launches": step.draft_launches,
-                  "path": "tensor-core" if step.tensor_core else "cuda-core"},
+                  "path": "tensor-core" if step.tensor_core else ("cuda-core, RNN cell per position" if step.rnn
+                                                                   else "cuda-core")},
         "schedule": ({"ms": t_sched, "launches": 1} if not overlap else
                      {"ms": t_sched, "launches": 1,
                       "note": "runs beside the draft on a second stream; ms is the wait after the draft"}),
@@ -518,7 +537,7 @@ def main(argv=None):
                        "l2": "flushed between timed steps (256 MB write, untimed)",
                        "w2_layout": (f"packed once at load time ({step.pack_ms:.3f} ms, outside the step)"
                                      if step.tensor_core else "as given"),
-                       "parallelism": f"replicas x{world}", "launch": launch_mode,
+                       "parallelism": f"replicas x{world}", "launch": launch_mode, "head": args.head,
                        "scheduler": ("beside the draft on a second stream (the draft leaves it one SM)"
                                      if overlap else "after the draft")},
             "roofline": roofline, "kernels": kernels, "gpu_launches": step.launches_per_step * args.steps,
@@ -550,6 +569,8 @@ def e2e_measure(cfg, w, step, dev, args, alg):
     h = {k: inp[k].cpu().pin_memory() for k in ("U", "anchor", "K_r", "temperature")}
     h["conf"] = w["conf"].cpu().pin_memory()
     h["tgt"] = w["tgt"].cpu().pin_memory()
+    if w.get("rnn") is not None:
+        h["rnn_x"] = w["rnn"]["rnn_x"].cpu().pin_memory()   # the RNN cell's backbone term is per-step input
     dbuf = [{k: torch.empty_like(v, device=dev) for k, v in h.items()} for _ in range(2)]
     out_tok = torch.empty(cfg.B, cfg.K_max + 1, dtype=torch.int32).pin_memory()
     n_acc = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
@@ -569,8 +590,9 @@ def e2e_measure(cfg, w, step, dev, args, alg):
             cs.wait_event(done[b])          # the step that last read this buffer has finished
         with torch.cuda.stream(copy[0]):
             d["U"].copy_(h["U"], non_blocking=True)
-            for k in ("anchor", "K_r", "temperature", "conf"):
-                d[k].copy_(h[k], non_blocking=True)
+            for k in ("anchor", "K_r", "temperature", "conf", "rnn_x"):
+                if k in h:
+                    d[k].copy_(h[k], non_blocking=True)
         with torch.cuda.stream(copy[1]):
             d["tgt"].copy_(h["tgt"], non_blocking=True)
         copy[1].wait_stream(copy[0])
@@ -581,6 +603,8 @@ def e2e_measure(cfg, w, step, dev, args, alg):
         stream.wait_event(copied[b])
         dinp = dict(inp)
         dinp.update(U=d["U"], anchor=d["anchor"], K_r=d["K_r"], temperature=d["temperature"])
+        if "rnn_x" in d:
+            dinp["rnn_x"] = d["rnn_x"]
         step.draft(dinp)
         step.schedule(d["conf"], d["K_r"])
         step.verify(d["tgt"], d["temperature"])

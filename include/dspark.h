@@ -182,6 +182,37 @@ dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E
                                                     int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Draft with the RNN head ("DSpark" S3.1, RNN head).
+ *
+ * The Markov head's W1 row is replaced by the output of a gated recurrent cell
+ * whose state s_k (size rank, s_0 = 0) carries the whole prefix of the block.
+ * The paper's update equation is not printed; this library's reading: one
+ * linear projection of [s_{k-1}; W1[x_{k-1}]; h_k], split into gate, candidate
+ * and output parts,
+ *   pre = rnn_x[r, k] + rnn_W [s_{k-1}; E[x_{k-1}]]       (3 rank values)
+ *   g = sigmoid(pre[0:r]), c = tanh(pre[r:2r]), o = sigmoid(pre[2r:3r])
+ *   s_k = g * s_{k-1} + (1 - g) * c,   f_k = o * s_k
+ *   z_k(v) = U[r, k-1, v] + sum_i f_k[i] * W[i, v], then the draw as for the
+ *   Markov head (same random streams), fp32 arithmetic.
+ *
+ *   rnn_W   [3 rank, 2 rank]   call dtype; rows: gate, candidate, output; columns
+ *           0..rank-1 act on the state, rank..2 rank-1 on E[x_{k-1}].
+ *   rnn_x   [B, K_max, 3 rank] float: the backbone term W_h h_k + b (no
+ *           sequential dependence, computed with the backbone).
+ *   workspace >= dspark_draft_rnn_workspace_bytes(dims), 256-byte aligned.
+ * Every other argument is that of dspark_draft_markov_sample.  The call runs on
+ * the CUDA-core path (W as given, rank <= 4096); DSPARK_FLAG_W_PACKED returns
+ * DSPARK_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------ */
+size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims);
+
+dspark_status dspark_draft_rnn_sample(const void *U, const void *E, const void *W, const void *rnn_W,
+                                      const float *rnn_x, const int32_t *anchor, const int32_t *K_r,
+                                      const float *temperature, uint64_t seed, dspark_dims dims,
+                                      int32_t *draft_tok, void *draft_logits, float *draft_lse, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Schedule: hardware-aware prefix scheduler ("DSpark" S3.2.2, Algorithm 1;
  * "Speculative decoding, from zero to DSpark" S8).
  *

@@ -44,7 +44,7 @@ STATUS_NAMES = {
 
 EXPORTED_SYMBOLS = [
     "dspark_draft_workspace_bytes", "dspark_draft_markov_sample", "dspark_draft_markov_sample_confidence",
-    "dspark_draft_packed_projection_bytes",
+    "dspark_draft_rnn_workspace_bytes", "dspark_draft_rnn_sample", "dspark_draft_packed_projection_bytes",
     "dspark_draft_pack_projection", "dspark_schedule_workspace_bytes",
     "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_schedule_capacity",
     "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_workspace_bytes",
@@ -96,6 +96,10 @@ def lib() -> ctypes.CDLL:
     L.dspark_draft_markov_sample.restype = st
     L.dspark_draft_markov_sample_confidence.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, P, P, P, sz, P, P]
     L.dspark_draft_markov_sample_confidence.restype = st
+    L.dspark_draft_rnn_workspace_bytes.argtypes = [Dims]
+    L.dspark_draft_rnn_workspace_bytes.restype = sz
+    L.dspark_draft_rnn_sample.argtypes = [P, P, P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
+    L.dspark_draft_rnn_sample.restype = st
     L.dspark_schedule_workspace_bytes.argtypes = [i64, i64]
     L.dspark_schedule_workspace_bytes.restype = sz
     L.dspark_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, sz, P, P]
@@ -292,6 +296,42 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
             ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
         _raise(code, "dspark_draft_markov_sample_confidence")
     return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, conf=conf, status=status, workspace=ws)
+
+
+def draft_rnn_sample(U, E, W, rnn_W, rnn_x, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
+                     want_lse: bool = True, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """RNN-head draft sampling (C ABI dspark_draft_rnn_sample).
+
+    U [B,K_max,V], E [V,rank], W [rank,V], rnn_W [3 rank, 2 rank] (one dtype); rnn_x
+    [B,K_max,3 rank] float32; anchor, K_r [B] int32; temperature [B] float32.  Returns
+    draft_tok, draft_logits, draft_lse as draft_markov_sample does.
+    """
+    dt = _dtype_code(_dev(U, "U"))
+    B, K_max, V = U.shape
+    rank = E.shape[1]
+    _dev(E, "E", U.dtype, (V, rank))
+    _dev(W, "W", U.dtype, (rank, V))
+    _dev(rnn_W, "rnn_W", U.dtype, (3 * rank, 2 * rank))
+    _dev(rnn_x, "rnn_x", torch.float32, (B, K_max, 3 * rank))
+    _dev(anchor, "anchor", torch.int32, (B,))
+    _dev(K_r, "K_r", torch.int32, (B,))
+    _dev(temperature, "temperature", torch.float32, (B,))
+    dev = U.device
+    out = {} if out is None else out
+    tok = _out(out, "draft_tok", (B, K_max), torch.int32, dev)
+    logits = (out.get("draft_logits") if out.get("draft_logits") is not None else torch.empty_like(U)) \
+        if want_logits else None
+    lse = _out(out, "draft_lse", (B, K_max), torch.float32, dev) if want_lse else None
+    status = new_status(dev) if status is None else status
+    dims = Dims(B, K_max, V, rank, dt, 0)
+    ws = _workspace(lib().dspark_draft_rnn_workspace_bytes(dims), dev, workspace)
+    code = lib().dspark_draft_rnn_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(rnn_W), _ptr(rnn_x), _ptr(anchor),
+                                         _ptr(K_r), _ptr(temperature), ctypes.c_uint64(seed), dims, _ptr(tok),
+                                         _ptr(logits), _ptr(lse), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                         _ptr(status), _stream(stream))
+    _raise(code, "dspark_draft_rnn_sample")
+    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, status=status, workspace=ws)
 
 
 def schedule_survival(conf, K_r, sps, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,

@@ -12,6 +12,7 @@ namespace {
 constexpr int64_t kMaxB = 1 << 20;
 constexpr int64_t kMaxV = (int64_t)1 << 30;
 constexpr int64_t kMaxRank = 8192;
+constexpr int64_t kMaxRnnRank = 4096;   // the RNN cell keeps 5 rank floats in shared memory
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -57,7 +58,7 @@ dspark_status check_dims(const dspark_dims &d, bool need_rank) {
 
 extern "C" {
 
-int dspark_version(void) { return 101; }
+int dspark_version(void) { return 102; }
 
 const char *dspark_status_string(dspark_status s) {
   switch (s) {
@@ -136,16 +137,24 @@ dspark_status dspark_draft_pack_projection(const void *W, dspark_dims dims, void
 
 namespace {
 
+// The RNN head's part of a draft call (null for the Markov head).
+struct RnnHead {
+  const void *W;    // [3 rank, 2 rank], call dtype
+  const float *x;   // [B, K_max, 3 rank]
+};
+
+size_t rnn_state_bytes(const dspark_dims &d) { return al256(sizeof(float) * (size_t)(d.B * d.rank)); }
+
 dspark_status draft_call(const void *U, const void *E, const void *W, const int32_t *anchor, const int32_t *K_r,
                          const float *temperature, uint64_t seed, dspark_dims dims, int32_t *draft_tok,
                          void *draft_logits, float *draft_lse, const float *conf_h, const float *conf_w,
-                         float *conf, void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                         void *stream) {
+                         float *conf, const RnnHead *rnn, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, void *stream) {
   if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok || !dev_status) return DSPARK_ERR_NULL;
   dspark_status st = check_dims(dims, true);
   if (st != DSPARK_OK) return st;
-  if (!workspace || !aligned256(workspace) || workspace_bytes < dspark_draft_workspace_bytes(dims))
-    return DSPARK_ERR_WORKSPACE;
+  const size_t need = rnn ? dspark_draft_rnn_workspace_bytes(dims) : dspark_draft_workspace_bytes(dims);
+  if (!workspace || !aligned256(workspace) || workspace_bytes < need) return DSPARK_ERR_WORKSPACE;
   DeviceInfo dev;
   if (!device_info(&dev)) return DSPARK_ERR_CUDA;
   const bool packed_in = (dims.flags & DSPARK_FLAG_W_PACKED) != 0;
@@ -186,6 +195,14 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   p += al256(sizeof(Partial) * (size_t)a.partial_slots);
+  if (rnn) {   // the CUDA-core path only: the workspace holds no packed W2, then the state / feature
+    a.rnn_W = rnn->W;
+    a.rnn_x = rnn->x;
+    a.rnn_state = (float *)p;
+    p += rnn_state_bytes(dims);
+    a.rnn_feat = (float *)p;
+    p += rnn_state_bytes(dims);
+  }
   const bool use_tc = !(dims.flags & DSPARK_FLAG_FORCE_SIMT) && dev.major == 10 && dev.minor == 3 &&
                       draft_tc_shape_ok(a);
   if (packed_in) {
@@ -214,7 +231,27 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
                                          float *draft_lse, void *workspace, size_t workspace_bytes,
                                          int32_t *dev_status, void *stream) {
   return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, nullptr,
-                    nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+                    nullptr, nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+}
+
+size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims) {
+  if ((dims.flags & DSPARK_FLAG_W_PACKED) || check_dims(dims, true) != DSPARK_OK) return 0;
+  dims.flags |= DSPARK_FLAG_FORCE_SIMT;
+  return dspark_draft_workspace_bytes(dims) + 2 * rnn_state_bytes(dims);
+}
+
+dspark_status dspark_draft_rnn_sample(const void *U, const void *E, const void *W, const void *rnn_W,
+                                      const float *rnn_x, const int32_t *anchor, const int32_t *K_r,
+                                      const float *temperature, uint64_t seed, dspark_dims dims,
+                                      int32_t *draft_tok, void *draft_logits, float *draft_lse, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (!rnn_W || !rnn_x) return DSPARK_ERR_NULL;
+  if (dims.flags & DSPARK_FLAG_W_PACKED) return DSPARK_ERR_UNSUPPORTED;
+  if (dims.rank > kMaxRnnRank) return DSPARK_ERR_DIMS;
+  dims.flags |= DSPARK_FLAG_FORCE_SIMT;   // the cell feeds the CUDA-core bias path
+  const RnnHead rnn{rnn_W, rnn_x};
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, nullptr,
+                    nullptr, nullptr, &rnn, workspace, workspace_bytes, dev_status, stream);
 }
 
 dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E, const void *W,
@@ -226,7 +263,7 @@ dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E
                                                     int32_t *dev_status, void *stream) {
   if (!conf_h || !conf_w || !conf) return DSPARK_ERR_NULL;
   return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, conf_h,
-                    conf_w, conf, workspace, workspace_bytes, dev_status, stream);
+                    conf_w, conf, nullptr, workspace, workspace_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

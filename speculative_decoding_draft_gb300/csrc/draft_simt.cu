@@ -105,6 +105,48 @@ __device__ __forceinline__ void st_logit(void *p, int64_t i, float z) {
   else ((__nv_bfloat16 *)p)[i] = __float2bfloat16_rn(z);
 }
 
+// RNN head cell ("DSpark" S3.1, RNN head) for position k, one block per active request:
+// pre = x_k + W [s_{k-1}; W1[x_{k-1}]] (gate, candidate, output: rows 0..r-1, r..2r-1,
+// 2r..3r-1), s_k = g s_{k-1} + (1 - g) tanh(candidate), feature = o s_k, with g and o the
+// sigmoids of their pre-activations and s_0 = 0.  One warp per output row, lane-strided
+// dot products.
+template <int DT>
+__global__ void __launch_bounds__(kSimtThreads) rnn_cell(const __grid_constant__ DraftArgs a, int k) {
+  extern __shared__ float cell_s[];     // [2 rank] input, then [3 rank] pre-activations
+  if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max, rank = (int)a.rank;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = kSimtThreads / 32;
+  float *zin = cell_s, *pre = cell_s + 2 * rank;
+  const int n_k = a.nact[k];
+  for (int i = blockIdx.x; i < n_k; i += gridDim.x) {
+    const int r = a.perm[i];
+    const int prev = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
+    __syncthreads();
+    for (int q = threadIdx.x; q < rank; q += kSimtThreads) {
+      zin[q] = (k == 1) ? 0.0f : a.rnn_state[(int64_t)r * rank + q];
+      zin[rank + q] = ld<DT>(a.E, (int64_t)prev * rank + q);
+    }
+    __syncthreads();
+    const float *xk = a.rnn_x + ((int64_t)r * K + (k - 1)) * 3 * rank;
+    for (int j = warp; j < 3 * rank; j += nwarps) {
+      float acc = 0.0f;
+      for (int q = lane; q < 2 * rank; q += 32) acc = fmaf(ld<DT>(a.rnn_W, (int64_t)j * 2 * rank + q), zin[q], acc);
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+      if (lane == 0) pre[j] = xk[j] + acc;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < rank; q += kSimtThreads) {
+      const float g = 1.0f / (1.0f + expf(-pre[q]));
+      const float c = tanhf(pre[rank + q]);
+      const float o = 1.0f / (1.0f + expf(-pre[2 * rank + q]));
+      const float st = g * zin[q] + (1.0f - g) * c;
+      a.rnn_state[(int64_t)r * rank + q] = st;
+      a.rnn_feat[(int64_t)r * rank + q] = o * st;
+    }
+  }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kSimtThreads) draft_simt_step(const __grid_constant__ DraftArgs a, int k,
                                                                  int chunks) {
@@ -119,7 +161,9 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_step(const __grid_con
     const int r = a.perm[i];
     const int prev = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
     __syncthreads();
-    for (int q = threadIdx.x; q < rank; q += kSimtThreads) e_s[q] = ld<DT>(a.E, (int64_t)prev * rank + q);
+    // the head's feature: the previous token's W1 row (Markov head) or the RNN cell's output
+    for (int q = threadIdx.x; q < rank; q += kSimtThreads)
+      e_s[q] = a.rnn_feat ? a.rnn_feat[(int64_t)r * rank + q] : ld<DT>(a.E, (int64_t)prev * rank + q);
     __syncthreads();
     const float T = a.temperature[r];
     const bool greedy = (T == 0.0f);
@@ -207,7 +251,23 @@ cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s) {
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  const size_t cell_smem = sizeof(float) * 5 * (size_t)a.rank;
+  if (a.rnn_feat && cell_smem > 48 * 1024) {
+    cudaError_t e = a.dtype == DSPARK_F32
+                        ? cudaFuncSetAttribute(rnn_cell<DSPARK_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)cell_smem)
+                        : cudaFuncSetAttribute(rnn_cell<DSPARK_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)cell_smem);
+    if (e != cudaSuccess) return e;
+  }
   for (int k = 1; k <= (int)a.K_max; ++k) {
+    if (a.rnn_feat) {
+      const unsigned cg = (unsigned)(a.B < 65535 ? a.B : 65535);
+      if (a.dtype == DSPARK_F32) rnn_cell<DSPARK_F32><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
+      else rnn_cell<DSPARK_BF16><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     dim3 grid(chunks, (unsigned)(a.B < 65535 ? a.B : 65535));
     if (a.dtype == DSPARK_F32) draft_simt_step<DSPARK_F32><<<grid, kSimtThreads, smem, s>>>(a, k, chunks);
     else draft_simt_step<DSPARK_BF16><<<grid, kSimtThreads, smem, s>>>(a, k, chunks);

@@ -139,6 +139,18 @@ def confidence_head(cfg: Config, device="cpu") -> dict:
     return dict(conf_h=_randn((cfg.B, cfg.K_max), 1.0, g, device) + 1.5, conf_w=_randn((cfg.rank,), 1.0, g, device))
 
 
+def rnn_head(cfg: Config, device="cpu") -> dict:
+    """RNN-head inputs: rnn_W [3 rank, 2 rank] ~ N(0, 1 / sqrt(2 rank)) in the storage dtype (unit-scale
+    pre-activations from unit-scale inputs), rnn_x [B, K_max, 3 rank] ~ N(0, 1) float32 (the backbone term),
+    and a feature scale: with the state in (-1, 1) the feature times W2 (~N(0, ew_std)) gives a bias of the
+    Markov head's size when W2 is the configuration's."""
+    g = _gen(cfg, device, 7)
+    r = cfg.rank
+    Wc = _randn((3 * r, 2 * r), 1.0 / math.sqrt(2 * r), g, device).to(cfg.torch_dtype)
+    x = _randn((cfg.B, cfg.K_max, 3 * r), 1.0, g, device)
+    return dict(rnn_W=Wc, rnn_x=x)
+
+
 # ---------------------------------------------------------------------------
 # scheduler inputs
 # ---------------------------------------------------------------------------

@@ -30,7 +30,7 @@ def oracle_draft(inp, seed, req_id=None, rows=None):
                                       req_id=req_id)
 
 
-def compare_draft(gpu, orc, K_r, dtype, rows=None, check_logits=True):
+def compare_draft(gpu, orc, K_r, dtype, rows=None, check_logits=True, f32_atol=2e-6):
     """Compare stored logits, log-sum-exp and tokens; returns the number of compared tokens.
 
     Logits and the normaliser of position k depend only on earlier tokens, so they are
@@ -68,7 +68,7 @@ def compare_draft(gpu, orc, K_r, dtype, rows=None, check_logits=True):
                         assert (np.abs(d[bad] - o[bad]) <= step).all(), (b, k)
                     mism_logits += int(bad.sum())
                 else:
-                    np.testing.assert_allclose(d, o, rtol=2e-6, atol=2e-6)
+                    np.testing.assert_allclose(d, o, rtol=2e-6, atol=f32_atol)
                 total_logits += d.size
             if lse is not None and not (f & 4):
                 assert abs(lse[b, k] - orc["lse"][i, k]) <= LSE_RTOL * max(1.0, abs(orc["lse"][i, k])), \

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     import speculative_decoding_draft_gb300 as ds
-    assert lib.dspark_version() == 101
+    assert lib.dspark_version() == 102
     for code, name in ds.STATUS_NAMES.items():
         assert ds.status_string(code) == name
 
@@ -87,6 +87,15 @@ def test_host_validation_needs_no_device(lib):
                                           null) == 10
     assert lib.dspark_schedule_survival(one, one, one, 10, 4, 0, one, one, null, null, null, one, 1 << 20, one,
                                         null) == 2
+    # RNN head: null cell inputs, a packed projection, the workspace query
+    rd = ds.Dims(4, 7, 1000, 16, ds.F32, 0)
+    assert lib.dspark_draft_rnn_sample(one, one, one, null, one, one, one, one, 0, rd, one, null, null, one, 1 << 20,
+                                       one, null) == 1
+    assert lib.dspark_draft_rnn_sample(one, one, one, one, one, one, one, one, 0,
+                                       ds.Dims(4, 7, 1000, 16, ds.BF16, ds.FLAG_W_PACKED), one, null, null, one,
+                                       1 << 20, one, null) == 13
+    assert lib.dspark_draft_rnn_workspace_bytes(rd) >= lib.dspark_draft_workspace_bytes(rd) + 2 * 4 * 4 * 16
+    assert lib.dspark_draft_rnn_workspace_bytes(ds.Dims(4, 7, 1000, 16, ds.BF16, ds.FLAG_W_PACKED)) == 0
     # scheduler variants
     assert lib.dspark_schedule_capacity(one, one, one, 10, 4, 7, null, null, null, null, one, 1 << 20, one,
                                         null) == 1
