@@ -276,7 +276,7 @@ def test_verify_output_law_on_gpu():
 # ---------------------------------------------------------------------------
 # full-size benchmark configurations on sampled requests
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("name", ["qwen", "ragged", "dsv4"])
+@pytest.mark.parametrize("name", ["qwen", "highc", "ragged", "dsv4"])
 def test_draft_full_size_sampled(name):
     cfg = wl.CONFIGS[name]
     g = wl.draft_inputs(cfg, DEV)
@@ -298,7 +298,7 @@ def test_draft_full_size_sampled(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["qwen", "ragged"])
+@pytest.mark.parametrize("name", ["qwen", "highc", "ragged", "dsv4"])
 def test_verify_full_size_sampled(name):
     cfg = wl.CONFIGS[name]
     g = wl.draft_inputs(cfg, DEV)
