@@ -80,6 +80,11 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 #define DSPARK_FLAG_W_PACKED 2u   /* draft: W is the packed projection of dspark_draft_pack_projection */
 #define DSPARK_FLAG_SPARE_SM 4u   /* draft: the tensor-core path leaves one SM free, so that a kernel on
                                      another stream (the scheduler) runs beside it */
+#define DSPARK_FLAG_TEST_BARRIER_TIMEOUT 8u /* draft, tensor-core path, for testing the failure path only:
+                                     the grid barrier before position 2 waits for one arrival more than
+                                     the grid gives, so the bounded wait runs out (about 2 s), the kernel
+                                     drains what it issued, frees its tensor memory and the call reports
+                                     DSPARK_ERR_DEVICE_TIMEOUT through the device status word */
 
 typedef struct {
   int64_t B;      /* requests in the call                                  */

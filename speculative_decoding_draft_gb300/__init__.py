@@ -33,6 +33,7 @@ F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_W_PACKED = 2
 FLAG_SPARE_SM = 4
+FLAG_TEST_BARRIER_TIMEOUT = 8   # failure-path test hook of the tensor-core draft (see include/dspark.h)
 
 STATUS_NAMES = {
     0: "DSPARK_OK", 1: "DSPARK_ERR_NULL", 2: "DSPARK_ERR_DIMS", 3: "DSPARK_ERR_DTYPE",

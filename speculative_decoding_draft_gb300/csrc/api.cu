@@ -176,6 +176,7 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.rank = dims.rank;
   a.dtype = dims.dtype;
   a.key = make_philox_key(seed);
+  a.gbar_extra = (dims.flags & DSPARK_FLAG_TEST_BARRIER_TIMEOUT) ? 1 : 0;
   a.conf_h = conf_h;
   a.conf_w = conf_w;
   a.conf_out = conf;

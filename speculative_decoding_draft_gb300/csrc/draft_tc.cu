@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           // every CTA has folded its position k-1 maxima into the packed keys
           if (et == 0) {
             const long long t0 = clock64();
-            while (ld_acquire(a.gbar + (k - 1)) < G) {
+            while (ld_acquire(a.gbar + (k - 1)) < G + (k == 2 ? a.gbar_extra : 0)) {
               __nanosleep(100);        // back off: many pollers slow the CTAs still working
               if (*abort) break;
               if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }

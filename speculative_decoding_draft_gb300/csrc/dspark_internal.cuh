@@ -529,6 +529,9 @@ struct DraftArgs {
   // RNN head (optional, CUDA-core path): the cell's sequential weights [3 rank, 2 rank] in
   // the call dtype, its backbone term [B, K_max, 3 rank], and per-request state / feature
   // [B, rank] in the workspace; the feature replaces the W1 row in the bias
+  // failure-path test hook (DSPARK_FLAG_TEST_BARRIER_TIMEOUT): arrivals the barrier before
+  // position 2 waits for beyond the grid, which never come, so that bounded wait runs out
+  int gbar_extra = 0;
   const void *rnn_W = nullptr;
   const float *rnn_x = nullptr;
   float *rnn_state = nullptr;
