@@ -33,7 +33,7 @@ constexpr uint32_t kTagResid = 2;
 constexpr uint32_t kTagDraftPick = 3;
 constexpr uint32_t kTagResidPick = 4;
 constexpr int kBlockW = 32;   // indices per block of the two-level draw
-constexpr int kDraftSimtChunk = 8192;   // vocabulary columns per CTA of the CUDA-core draft step
+constexpr int kDraftSimtChunk = 256;   // vocabulary columns per tile of the CUDA-core draft step
 constexpr int kMaxK = 16;
 constexpr float kMinPositiveT = 1e-3f;
 constexpr float kLog2e = 1.4426950408889634f;
