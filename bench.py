@@ -298,15 +298,18 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(kernel: str):
-    """DRAM bytes per call recorded by ncu in profiles/, if the kernel sources are unchanged."""
+def profiled_traffic(kernel: str, workload: str, path: str):
+    """DRAM bytes per call recorded by ncu in profiles/, if the record was taken on this
+    workload and kernel path and the kernel sources are unchanged since."""
     summ = os.path.join(ROOT, "profiles", f"traffic_{kernel}.md")
     if kernel not in KERNEL_SOURCES or not os.path.exists(summ):
         return None
     text = open(summ).read()
     m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"dram_bytes_per_launch_scaled:\s*([0-9.eE+]+)", text)
-    if not m or not t:
+    wk = re.search(r"workload:\s*(\S+)", text)
+    pa = re.search(r"path:\s*(\S+)", text)
+    if not m or not t or not wk or not pa or wk.group(1) != workload or pa.group(1) != path:
         return None
     return float(t.group(1)) if kernel_source_hash(kernel) == m.group(1) else None
 
@@ -521,7 +524,9 @@ def main(argv=None):
                    "hbm_frac_dense": alg["verify_bytes_dense"] / (t_ver * 1e-3) / 1e9 / hbm, "launches": 2},
     }
     dom = "draft" if t_draft >= t_ver else "verify"
-    traffic = profiled_traffic(dom)
+    dom_path = ("tensor-core" if step.tensor_core else ("cuda-core-rnn" if step.rnn else "cuda-core")) \
+        if dom == "draft" else "verify"
+    traffic = profiled_traffic(dom, args.config, dom_path)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": hbm, "unit": "GB/s",
                 "frac": kernels[dom]["hbm_frac"], "traffic": traffic,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,

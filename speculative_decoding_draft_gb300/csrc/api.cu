@@ -12,7 +12,7 @@ namespace {
 constexpr int64_t kMaxB = 1 << 20;
 constexpr int64_t kMaxV = (int64_t)1 << 30;
 constexpr int64_t kMaxRank = 8192;
-constexpr int64_t kMaxRnnRank = 4096;   // the RNN cell keeps 5 rank floats in shared memory
+constexpr int64_t kMaxRnnRank = 4096;   // the RNN entry point's documented rank limit
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -196,11 +196,12 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   p += al256(sizeof(Partial) * (size_t)a.partial_slots);
-  if (rnn) {   // the CUDA-core path only: the workspace holds no packed W2, then the state / feature
+  if (rnn) {   // the CUDA-core path only: the workspace holds no packed W2, then two state
+               // buffers (the cell alternates between them by position) and the feature
     a.rnn_W = rnn->W;
     a.rnn_x = rnn->x;
     a.rnn_state = (float *)p;
-    p += rnn_state_bytes(dims);
+    p += 2 * rnn_state_bytes(dims);
     a.rnn_feat = (float *)p;
     p += rnn_state_bytes(dims);
   }
@@ -238,7 +239,7 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
 size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims) {
   if ((dims.flags & DSPARK_FLAG_W_PACKED) || check_dims(dims, true) != DSPARK_OK) return 0;
   dims.flags |= DSPARK_FLAG_FORCE_SIMT;
-  return dspark_draft_workspace_bytes(dims) + 2 * rnn_state_bytes(dims);
+  return dspark_draft_workspace_bytes(dims) + 3 * rnn_state_bytes(dims);
 }
 
 dspark_status dspark_draft_rnn_sample(const void *U, const void *E, const void *W, const void *rnn_W,

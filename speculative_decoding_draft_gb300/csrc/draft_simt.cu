@@ -106,89 +106,119 @@ __device__ __forceinline__ void st_logit(void *p, int64_t i, float z) {
   else ((__nv_bfloat16 *)p)[i] = __float2bfloat16_rn(z);
 }
 
-// RNN head cell ("DSpark" S3.1, RNN head) for position k, one block per active request:
+// RNN head cell ("DSpark" S3.1, RNN head) for position k:
 // pre = x_k + W [s_{k-1}; W1[x_{k-1}]] (gate, candidate, output: rows 0..r-1, r..2r-1,
 // 2r..3r-1), s_k = g s_{k-1} + (1 - g) tanh(candidate), feature = o s_k, with g and o the
-// sigmoids of their pre-activations and s_0 = 0.  Each warp takes four output rows at a
-// time; with 16-byte aligned weight rows (VEC) every lane reads eight consecutive weights of
-// each row per 16-byte load, all four rows' loads in flight together, otherwise lane-strided
-// scalar loads.
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSimtThreads) rnn_cell(const __grid_constant__ DraftArgs a, int k) {
-  extern __shared__ float cell_s[];     // [2 rank] input, then [3 rank] pre-activations
+// sigmoids of their pre-activations and s_0 = 0.  One block per tile of kCellUnits hidden
+// units x kCellReq active requests: lane j of a warp owns request j of the tile, and the
+// kCellSplit warps of a unit each take one contiguous part of every staged input chunk,
+// accumulating the unit's three pre-activations in ascending input order; the parts' sums
+// are added in part order at the end.  The tile's inputs ([input][request], padded) and its
+// 3 kCellUnits weight rows are staged kCellChunk inputs at a time, every thread holding one
+// input column of all of them, all loads in flight together (the next chunk's while the
+// current one is reduced), so every weight row is read once per request tile.  Tiles of
+// other units read s_{k-1} of the same requests while this one writes s_k, so the state
+// alternates between two buffers by the parity of k.
+constexpr int kCellUnits = 4;
+constexpr int kCellReq = 32;
+constexpr int kCellSplit = 4;
+constexpr int kCellThreads = 32 * kCellUnits * kCellSplit;   // 512
+constexpr int kCellChunk = kCellThreads;                     // one staged input column per thread
+constexpr int kCellPart = kCellChunk / kCellSplit;           // inputs per warp and chunk
+constexpr size_t kCellSmem = sizeof(float) * ((size_t)kCellChunk * (kCellReq + 1) + 3 * kCellUnits * kCellChunk);
+static_assert(kCellSplit * 3 * kCellUnits * kCellReq <= 3 * kCellUnits * kCellChunk,
+              "the partial sums reuse the weight buffer");
+
+template <int DT>
+__global__ void __launch_bounds__(kCellThreads) rnn_cell_tile(const __grid_constant__ DraftArgs a, int k) {
+  extern __shared__ float cell_s[];
+  float(*z_s)[kCellReq + 1] = reinterpret_cast<float(*)[kCellReq + 1]>(cell_s);    // [input][request]
+  float *w_s = cell_s + (size_t)kCellChunk * (kCellReq + 1);                         // [gate][unit][input]
+  __shared__ int s_row_r[kCellReq], s_row_prev[kCellReq];
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, rank = (int)a.rank;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = kSimtThreads / 32;
-  float *zin = cell_s, *pre = cell_s + 2 * rank;
   const int n_k = a.nact[k];
-  for (int i = blockIdx.x; i < n_k; i += gridDim.x) {
-    const int r = a.perm[i];
-    const int prev = (k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2];
-    __syncthreads();
-    for (int q = threadIdx.x; q < rank; q += kSimtThreads) {
-      zin[q] = (k == 1) ? 0.0f : a.rnn_state[(int64_t)r * rank + q];
-      zin[rank + q] = ld<DT>(a.E, (int64_t)prev * rank + q);
-    }
-    __syncthreads();
-    const float *xk = a.rnn_x + ((int64_t)r * K + (k - 1)) * 3 * rank;
-    const int n_in = 2 * rank, n_out = 3 * rank;
-    for (int j0 = warp * 4; j0 < n_out; j0 += nwarps * 4) {
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (VEC) {
-        constexpr int kPer = 16 / (DT == DSPARK_F32 ? 4 : 2);     // weights per 16-byte load
-        for (int q = lane * 8; q < n_in; q += 32 * 8) {            // eight inputs per lane and step
-          uint4 w[4][8 / kPer];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int h = 0; h < 8 / kPer; ++h)
-              w[u][h] = (j0 + u < n_out)
-                            ? __ldg((const uint4 *)((const char *)a.rnn_W +
-                                                    ((int64_t)(j0 + u) * n_in + q + h * kPer) * (DT == DSPARK_F32 ? 4 : 2)))
-                            : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float wv[8];
-#pragma unroll
-            for (int h = 0; h < 8 / kPer; ++h) {
-              const uint32_t w4[4] = {w[u][h].x, w[u][h].y, w[u][h].z, w[u][h].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                if (DT == DSPARK_F32) {
-                  wv[h * 4 + e] = __uint_as_float(w4[e]);
-                } else {
-                  wv[2 * e] = __uint_as_float(w4[e] << 16);
-                  wv[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-                }
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[u] = fmaf(wv[e], zin[q + e], acc[u]);
-          }
-        }
-      } else {
-        for (int q = lane; q < n_in; q += 32)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (j0 + u < n_out) acc[u] = fmaf(ld<DT>(a.rnn_W, (int64_t)(j0 + u) * n_in + q), zin[q], acc[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], d);
-        if (lane == 0 && j0 + u < n_out) pre[j0 + u] = xk[j0 + u] + acc[u];
-      }
-    }
-    __syncthreads();
-    for (int q = threadIdx.x; q < rank; q += kSimtThreads) {
-      const float g = 1.0f / (1.0f + expf(-pre[q]));
-      const float c = tanhf(pre[rank + q]);
-      const float o = 1.0f / (1.0f + expf(-pre[2 * rank + q]));
-      const float st = g * zin[q] + (1.0f - g) * c;
-      a.rnn_state[(int64_t)r * rank + q] = st;
-      a.rnn_feat[(int64_t)r * rank + q] = o * st;
-    }
+  const int i0 = blockIdx.y * kCellReq;
+  if (i0 >= n_k) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int unit = warp % kCellUnits, part = warp / kCellUnits;
+  const int q0 = blockIdx.x * kCellUnits;               // first hidden unit of the tile
+  const size_t plane = (size_t)a.B * (size_t)rank;
+  const float *s_prev = a.rnn_state + (size_t)((k + 1) & 1) * plane;   // s_{k-1}
+  float *s_next = a.rnn_state + (size_t)(k & 1) * plane;               // s_k
+  if (tid < kCellReq) {
+    const int i = i0 + tid;
+    const int r = i < n_k ? a.perm[i] : -1;
+    s_row_r[tid] = r;
+    s_row_prev[tid] = r < 0 ? 0 : ((k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2]);
   }
+  __syncthreads();
+  const int n_in = 2 * rank;
+  float acc[3] = {0.0f, 0.0f, 0.0f};
+  float zr[kCellReq], wr[3 * kCellUnits];
+  auto fetch = [&](int c0) {
+    const int in = c0 + tid;
+    const bool live = in < n_in;
+#pragma unroll
+    for (int j = 0; j < kCellReq; ++j) {
+      const int r = s_row_r[j];
+      float z = 0.0f;
+      if (r >= 0 && live) {
+        if (in < rank) z = (k == 1) ? 0.0f : s_prev[(int64_t)r * rank + in];
+        else z = ld<DT>(a.E, (int64_t)s_row_prev[j] * rank + (in - rank));
+      }
+      zr[j] = z;
+    }
+#pragma unroll
+    for (int gu = 0; gu < 3 * kCellUnits; ++gu) {
+      const int g = gu / kCellUnits, q = q0 + gu % kCellUnits;
+      wr[gu] = (q < rank && live) ? ld<DT>(a.rnn_W, ((int64_t)g * rank + q) * n_in + in) : 0.0f;
+    }
+  };
+  fetch(0);
+  for (int c0 = 0; c0 < n_in; c0 += kCellChunk) {
+#pragma unroll
+    for (int j = 0; j < kCellReq; ++j) z_s[tid][j] = zr[j];
+#pragma unroll
+    for (int gu = 0; gu < 3 * kCellUnits; ++gu) w_s[gu * kCellChunk + tid] = wr[gu];
+    __syncthreads();
+    if (c0 + kCellChunk < n_in) fetch(c0 + kCellChunk);
+    const int c_lo = part * kCellPart, c_hi = min(c_lo + kCellPart, n_in - c0);
+    const float *wg = w_s + unit * kCellChunk;
+#pragma unroll 8
+    for (int c = c_lo; c < c_hi; ++c) {
+      const float z = z_s[c][lane];
+      acc[0] = fmaf(wg[c], z, acc[0]);
+      acc[1] = fmaf(wg[kCellUnits * kCellChunk + c], z, acc[1]);
+      acc[2] = fmaf(wg[2 * kCellUnits * kCellChunk + c], z, acc[2]);
+    }
+    __syncthreads();
+  }
+  // the parts' sums, added in part order by the warps of part 0
+  float *red = w_s;   // [part][gate][unit][request]
+#pragma unroll
+  for (int g = 0; g < 3; ++g) red[((part * 3 + g) * kCellUnits + unit) * kCellReq + lane] = acc[g];
+  __syncthreads();
+  if (part != 0) return;
+  float pre[3];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    float t = red[(g * kCellUnits + unit) * kCellReq + lane];
+#pragma unroll
+    for (int p = 1; p < kCellSplit; ++p) t += red[((p * 3 + g) * kCellUnits + unit) * kCellReq + lane];
+    pre[g] = t;
+  }
+  const int r = s_row_r[lane];
+  const int q = q0 + unit;
+  if (r < 0 || q >= rank) return;
+  const float *xk = a.rnn_x + ((int64_t)r * K + (k - 1)) * 3 * rank;
+  const float g = 1.0f / (1.0f + expf(-(xk[q] + pre[0])));
+  const float c = tanhf(xk[rank + q] + pre[1]);
+  const float o = 1.0f / (1.0f + expf(-(xk[2 * rank + q] + pre[2])));
+  const float sp = (k == 1) ? 0.0f : s_prev[(int64_t)r * rank + q];
+  const float st = g * sp + (1.0f - g) * c;
+  s_next[(int64_t)r * rank + q] = st;
+  a.rnn_feat[(int64_t)r * rank + q] = o * st;
 }
 
 // CUDA-core step for position k: one block per tile of kTileRows active rows x kTileCols
@@ -215,11 +245,11 @@ __device__ __forceinline__ int wsw(int q, int col) {
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSimtThreads) draft_simt_tile(const __grid_constant__ DraftArgs a, int k,
+__global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_constant__ DraftArgs a, int k,
                                                                  int col_tiles) {
-  // GEMM layout: thread (ty, tx) accumulates rows 4 ty .. 4 ty + 3 x columns 8 tx .. 8 tx + 7
-  // (three 16-byte shared loads per 32 FMAs); the tile then goes through shared memory
-  // (swizzled like the W2 chunks) to the epilogue layout, one 32-wide block per thread.
+  // GEMM layout: thread (ty, tx) accumulates rows 4 ty .. 4 ty + 3 x columns 4 tx .. 4 tx + 3
+  // and 128 + 4 tx .. 128 + 4 tx + 3 (three 16-byte shared loads per 32 FMAs); the tile then
+  // goes through shared memory (swizzled) to the epilogue layout, one 32-wide block per thread.
   __shared__ __align__(16) float w_s[kRankChunk * kTileCols];   // W2 chunk, later the bias tile
   __shared__ __align__(16) float f_s[kRankChunk][kTileRows];     // feature chunk, [rank][row]
   __shared__ int s_row_r[kTileRows], s_row_prev[kTileRows];
@@ -248,56 +278,21 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_tile(const __grid_con
   for (int y = 0; y < 4; ++y)
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[y][x] = 0.0f;
-  for (int q0 = 0; q0 < rank; q0 += kRankChunk) {
-    const int qn = min(kRankChunk, rank - q0);
-    // the rows' features for this rank chunk
-    for (int e = tid; e < kTileRows * kRankChunk; e += kSimtThreads) {
-      const int row = e / kRankChunk, qq = e % kRankChunk;
-      const int rr = s_row_r[row];
-      float f = 0.0f;
-      if (rr >= 0 && qq < qn)
-        f = a.rnn_feat ? a.rnn_feat[(int64_t)rr * rank + q0 + qq] : ld<DT>(a.E, (int64_t)s_row_prev[row] * rank + q0 + qq);
-      f_s[qq][row] = f;
-    }
-    // W2 rows q0 .. q0 + qn - 1, columns c0 .. c0 + kTileCols - 1 (zero past V), row-major
-    if (VEC) {
-      constexpr int kPer = 16 / (DT == DSPARK_F32 ? 4 : 2);   // elements per 16-byte load
-      for (int e = tid; e < kRankChunk * kTileCols / kPer; e += kSimtThreads) {
-        const int qq = e / (kTileCols / kPer), col = (e % (kTileCols / kPer)) * kPer;
-        float v[kPer];
-        if (qq < qn && c0 + col + kPer <= V) {
-          const int64_t at = (int64_t)(q0 + qq) * V + c0 + col;
-          const uint4 u = __ldg((const uint4 *)((const char *)a.W + at * (DT == DSPARK_F32 ? 4 : 2)));
-          if (DT == DSPARK_F32) {
-            v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
-            v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
-          } else {
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              v[2 * h] = __uint_as_float(w4[h] << 16);
-              v[2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < kPer; ++h)
-            v[h] = (qq < qn && c0 + col + h < V) ? ld<DT>(a.W, (int64_t)(q0 + qq) * V + c0 + col + h) : 0.0f;
-        }
-#pragma unroll
-        for (int h = 0; h < kPer; ++h) w_s[qq * kTileCols + col + h] = v[h];
-      }
-    } else {
-      for (int e = tid; e < kRankChunk * kTileCols; e += kSimtThreads) {
-        const int qq = e / kTileCols, col = e % kTileCols;
-        w_s[e] = (qq < qn && c0 + col < V) ? ld<DT>(a.W, (int64_t)(q0 + qq) * V + c0 + col) : 0.0f;
-      }
-    }
-    __syncthreads();
+  // the rows' feature for rank value q (the previous token's W1 row, or the RNN cell's output)
+  auto feature = [&](int row, int q) -> float {
+    const int rr = s_row_r[row];
+    if (rr < 0) return 0.0f;
+    return a.rnn_feat ? a.rnn_feat[(int64_t)rr * rank + q] : ld<DT>(a.E, (int64_t)s_row_prev[row] * rank + q);
+  };
+  // one staged rank chunk: rows 4 ty .. 4 ty + 3 x columns 4 tx .. 4 tx + 3 and
+  // kTileCols / 2 + 4 tx .. + 3, ascending rank (each 16-byte W2 load of a warp covers 512
+  // contiguous bytes: four shared-memory wavefronts)
+  auto gemm_chunk = [&](int qn) {
+#pragma unroll 4
     for (int qq = 0; qq < qn; ++qq) {
       const float4 f4 = *reinterpret_cast<const float4 *>(&f_s[qq][4 * ty]);
-      const float4 wa = *reinterpret_cast<const float4 *>(&w_s[qq * kTileCols + 8 * tx]);
-      const float4 wb = *reinterpret_cast<const float4 *>(&w_s[qq * kTileCols + 8 * tx + 4]);
+      const float4 wa = *reinterpret_cast<const float4 *>(&w_s[qq * kTileCols + 4 * tx]);
+      const float4 wb = *reinterpret_cast<const float4 *>(&w_s[qq * kTileCols + kTileCols / 2 + 4 * tx]);
       const float fy[4] = {f4.x, f4.y, f4.z, f4.w};
       const float wx[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
@@ -305,13 +300,89 @@ __global__ void __launch_bounds__(kSimtThreads) draft_simt_tile(const __grid_con
 #pragma unroll
         for (int x = 0; x < 8; ++x) acc[y][x] = fmaf(fy[y], wx[x], acc[y][x]);
     }
-    __syncthreads();
+  };
+  if (VEC) {
+    // V and the rows are 16-byte aligned: a 16-byte unit of a W2 row is either wholly inside
+    // V or wholly past it.  The next chunk's W2 units and features are loaded into registers
+    // while the current chunk's FMAs run, then stored to shared memory after the barrier.
+    constexpr int kPer = 16 / (DT == DSPARK_F32 ? 4 : 2);                 // elements per unit
+    constexpr int kUnitsPerRow = kTileCols / kPer;
+    constexpr int kWLoads = kRankChunk * kUnitsPerRow / kSimtThreads;     // units per thread
+    constexpr int kFLoads = kTileRows * kRankChunk / kSimtThreads;        // features per thread
+    static_assert(kRankChunk * kUnitsPerRow % kSimtThreads == 0 && kTileRows * kRankChunk % kSimtThreads == 0,
+                  "staging splits evenly over the block");
+    uint4 wreg[kWLoads];
+    float freg[kFLoads];
+    auto fetch = [&](int q0) {
+      const int qn = min(kRankChunk, rank - q0);
+#pragma unroll
+      for (int u = 0; u < kFLoads; ++u) {
+        const int e = tid + u * kSimtThreads;
+        const int row = e / kRankChunk, qq = e % kRankChunk;
+        freg[u] = qq < qn ? feature(row, q0 + qq) : 0.0f;
+      }
+#pragma unroll
+      for (int h = 0; h < kWLoads; ++h) {
+        const int e = tid + h * kSimtThreads;
+        const int qq = e / kUnitsPerRow, col = (e % kUnitsPerRow) * kPer;
+        wreg[h] = (qq < qn && c0 + col < V)
+                      ? __ldg((const uint4 *)((const char *)a.W +
+                                              ((int64_t)(q0 + qq) * V + c0 + col) * (DT == DSPARK_F32 ? 4 : 2)))
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    auto stage = [&]() {
+#pragma unroll
+      for (int u = 0; u < kFLoads; ++u) {
+        const int e = tid + u * kSimtThreads;
+        f_s[e % kRankChunk][e / kRankChunk] = freg[u];
+      }
+#pragma unroll
+      for (int h = 0; h < kWLoads; ++h) {
+        const int e = tid + h * kSimtThreads;
+        const int qq = e / kUnitsPerRow, col = (e % kUnitsPerRow) * kPer;
+        float4 *dst = reinterpret_cast<float4 *>(&w_s[qq * kTileCols + col]);
+        const uint4 w = wreg[h];
+        if (DT == DSPARK_F32) {
+          dst[0] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
+        } else {
+          dst[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                               __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+          dst[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                               __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+        }
+      }
+    };
+    fetch(0);
+    for (int q0 = 0; q0 < rank; q0 += kRankChunk) {
+      stage();
+      __syncthreads();
+      if (q0 + kRankChunk < rank) fetch(q0 + kRankChunk);
+      gemm_chunk(min(kRankChunk, rank - q0));
+      __syncthreads();
+    }
+  } else {
+    for (int q0 = 0; q0 < rank; q0 += kRankChunk) {
+      const int qn = min(kRankChunk, rank - q0);
+      for (int e = tid; e < kTileRows * kRankChunk; e += kSimtThreads) {
+        const int row = e / kRankChunk, qq = e % kRankChunk;
+        f_s[qq][row] = qq < qn ? feature(row, q0 + qq) : 0.0f;
+      }
+      // W2 rows q0 .. q0 + qn - 1, columns c0 .. c0 + kTileCols - 1 (zero past V), row-major
+      for (int e = tid; e < kRankChunk * kTileCols; e += kSimtThreads) {
+        const int qq = e / kTileCols, col = e % kTileCols;
+        w_s[e] = (qq < qn && c0 + col < V) ? ld<DT>(a.W, (int64_t)(q0 + qq) * V + c0 + col) : 0.0f;
+      }
+      __syncthreads();
+      gemm_chunk(qn);
+      __syncthreads();
+    }
   }
   // the bias tile to shared memory (swizzled), then each thread takes its 32-wide block
 #pragma unroll
   for (int y = 0; y < 4; ++y)
 #pragma unroll
-    for (int x = 0; x < 8; ++x) w_s[wsw(4 * ty + y, 8 * tx + x)] = acc[y][x];
+    for (int x = 0; x < 8; ++x) w_s[wsw(4 * ty + y, (x < 4 ? 0 : kTileCols / 2 - 4) + 4 * tx + x)] = acc[y][x];
   __syncthreads();
   float z[kBlockW];
   {
@@ -476,29 +547,22 @@ cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s) {
   const int esz = a.dtype == DSPARK_F32 ? 4 : 2;
   const bool vec = ((a.V * esz) % 16 == 0) && (((uintptr_t)a.U | (uintptr_t)a.W) % 16 == 0) &&
                    ((uintptr_t)a.draft_logits % 16 == 0);
-  const size_t cell_smem = sizeof(float) * 5 * (size_t)a.rank;
-  // 16-byte weight rows: 2 rank elements, a multiple of 8 (the vector step of the cell)
-  const bool cell_vec = ((2 * a.rank) % 8 == 0) && ((uintptr_t)a.rnn_W % 16 == 0);
-  if (a.rnn_feat && cell_smem > 48 * 1024) {
-    void *fns[4] = {(void *)rnn_cell<DSPARK_F32, false>, (void *)rnn_cell<DSPARK_F32, true>,
-                    (void *)rnn_cell<DSPARK_BF16, false>, (void *)rnn_cell<DSPARK_BF16, true>};
-    for (void *fn : fns) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cell_smem);
-      if (e != cudaSuccess) return e;
-    }
-  }
   const int64_t row_tiles = (a.B + kTileRows - 1) / kTileRows;
   const dim3 grid((unsigned)col_tiles, (unsigned)(row_tiles < 65535 ? row_tiles : 65535));
   for (int k = 1; k <= (int)a.K_max; ++k) {
     if (a.rnn_feat) {
-      const unsigned cg = (unsigned)(a.B < 65535 ? a.B : 65535);
-      if (a.dtype == DSPARK_F32) {
-        if (cell_vec) rnn_cell<DSPARK_F32, true><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
-        else rnn_cell<DSPARK_F32, false><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
-      } else {
-        if (cell_vec) rnn_cell<DSPARK_BF16, true><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
-        else rnn_cell<DSPARK_BF16, false><<<cg, kSimtThreads, cell_smem, s>>>(a, k);
+      static bool cell_attr = false;
+      if (!cell_attr) {
+        for (void *fn : {(void *)rnn_cell_tile<DSPARK_F32>, (void *)rnn_cell_tile<DSPARK_BF16>}) {
+          cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCellSmem);
+          if (e != cudaSuccess) return e;
+        }
+        cell_attr = true;
       }
+      const dim3 cg((unsigned)((a.rank + kCellUnits - 1) / kCellUnits),
+                    (unsigned)((a.B + kCellReq - 1) / kCellReq));
+      if (a.dtype == DSPARK_F32) rnn_cell_tile<DSPARK_F32><<<cg, kCellThreads, kCellSmem, s>>>(a, k);
+      else rnn_cell_tile<DSPARK_BF16><<<cg, kCellThreads, kCellSmem, s>>>(a, k);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
