@@ -523,14 +523,31 @@ def main(argv=None):
                    "GB/s": ver_gbs, "hbm_frac": ver_gbs / hbm,
                    "hbm_frac_dense": alg["verify_bytes_dense"] / (t_ver * 1e-3) / 1e9 / hbm, "launches": 2},
     }
+    # the CUDA-core draft is bound by its fp32 FMAs (2 r V flops per position against a few
+    # hundred bytes): its peak is the SMs' fp32 lanes at the maximum SM clock
+    clk = clocks.summary()
+    max_mhz = clk.get("sm_max_mhz") or 2070.0
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = n_sms * 128 * 2 * max_mhz * 1e6 / 1e12
+    if not step.tensor_core:
+        kernels["draft"]["fp32_TFLOP/s_peak"] = fp32_peak
+        kernels["draft"]["fp32_frac"] = draft_tflops / fp32_peak
     dom = "draft" if t_draft >= t_ver else "verify"
     dom_path = ("tensor-core" if step.tensor_core else ("cuda-core-rnn" if step.rnn else "cuda-core")) \
         if dom == "draft" else "verify"
     traffic = profiled_traffic(dom, args.config, dom_path)
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": hbm, "unit": "GB/s",
-                "frac": kernels[dom]["hbm_frac"], "traffic": traffic,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "per": "one call (all positions of the step)"}
+    if dom == "draft" and not step.tensor_core:
+        roofline = {"kernel": dom, "bound": "alu", "achieved": draft_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": draft_tflops / fp32_peak, "traffic": traffic,
+                    "peak_source": f"derived: {n_sms} SMs x 128 fp32 lanes x 2 flops x {max_mhz:.0f} MHz "
+                                   "(maximum SM clock)",
+                    "per": "one call (all positions of the step)"}
+    else:
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": hbm, "unit": "GB/s",
+                    "frac": kernels[dom]["hbm_frac"], "traffic": traffic,
+                    "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                                    else peak_kind),
+                    "per": "one call (all positions of the step)"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -546,7 +563,7 @@ def main(argv=None):
                        "scheduler": ("beside the draft on a second stream (the draft leaves it one SM)"
                                      if overlap else "after the draft")},
             "roofline": roofline, "kernels": kernels, "gpu_launches": step.launches_per_step * args.steps,
-            "clocks": clocks.summary()}
+            "clocks": clk}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(cfg, w, step, dev, args, alg)

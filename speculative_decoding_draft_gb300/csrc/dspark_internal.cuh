@@ -526,12 +526,13 @@ struct DraftArgs {
   const float *conf_h = nullptr;   // [B, K_max] backbone term w_h . h_k + b
   const float *conf_w = nullptr;   // [rank] weights of the Markov embedding
   float *conf_out = nullptr;       // [B, K_max]
-  // RNN head (optional, CUDA-core path): the cell's sequential weights [3 rank, 2 rank] in
-  // the call dtype, its backbone term [B, K_max, 3 rank], and per-request state / feature
-  // [B, rank] in the workspace; the feature replaces the W1 row in the bias
   // failure-path test hook (DSPARK_FLAG_TEST_BARRIER_TIMEOUT): arrivals the barrier before
   // position 2 waits for beyond the grid, which never come, so that bounded wait runs out
   int gbar_extra = 0;
+  // RNN head (optional, CUDA-core path): the cell's sequential weights [3 rank, 2 rank] in
+  // the call dtype, its backbone term [B, K_max, 3 rank], and in the workspace the state
+  // [2, B, rank] (position k writes buffer k & 1) and the feature [B, rank]; the feature
+  // replaces the W1 row in the bias
   const void *rnn_W = nullptr;
   const float *rnn_x = nullptr;
   float *rnn_state = nullptr;
