@@ -35,3 +35,23 @@ def test_traffic_dropped_once_the_sources_change(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 64)
     assert bench.profiled_traffic("draft", workload, path) is None
     assert bench.profiled_traffic("schedule", workload, path) is None   # no record at all
+
+
+def test_algorithmic_work_of_a_hand_worked_step():
+    # B = 2 requests, V = 10, r = 4, bf16 (2 bytes); K_r = (2, 3); request 0 drafts 2 and
+    # accepts 1 at T = 1 (rejection: its draft row is read for the residual), request 1 drafts 1
+    # and accepts it at T = 0 (bonus row only)
+    import numpy as np
+
+    from speculative_decoding_draft_gb300 import workloads as wl
+    cfg = wl.small_config("qwen", B=2, V=10, rank=4, dtype="bf16")
+    K_r, ell, n_acc, T = np.array([2, 3]), np.array([2, 1]), np.array([1, 1]), np.array([1.0, 0.0])
+    alg = bench.algorithmic(cfg, K_r, ell, n_acc, T)
+    V, r, e = 10, cfg.rank, 2
+    assert alg["draft_bytes"] == 5 * V * e + r * V * e + 5 * r * e       # U rows, W2 once, W1 rows
+    assert alg["draft_flops"] == 2.0 * 5 * r * V
+    assert alg["verify_bytes"] == (2 + 1 + 2) * V * e                     # rows to the decision (+ residual)
+    assert alg["verify_bytes_dense"] == (5 + 3) * V * e                   # every row 2 l + 1
+    assert (alg["positions"], alg["draft_positions"], alg["verify_positions"]) == (10, 5, 5)
+    rnn = bench.algorithmic(cfg, K_r, ell, n_acc, T, head="rnn")
+    assert rnn["draft_flops"] - alg["draft_flops"] == 2.0 * 5 * 3 * r * 2 * r   # the cell per position
