@@ -1,5 +1,7 @@
 // Markov-head draft sampling ("DSpark", S3.1; "Speculative decoding, from zero
-// to DSpark", S6): prologue and the CUDA-core step kernel.
+// to DSpark", S6): prologue, the RNN head's recurrent cell and the CUDA-core step
+// kernel.  With the RNN head, the cell of position k runs before that position's
+// step kernel and hands it the feature that replaces the W1 row.
 //
 // For position k the active requests (K_r >= k) form a prefix of the
 // permutation `perm`, which orders requests by K_r descending; the prologue
