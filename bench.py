@@ -363,8 +363,10 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = wl.CONFIGS[args.config]
+    workload = wl.WORKLOAD_TEXT.get(args.config, args.config)
     if not torch.cuda.is_available():          # no GPU machine: a reduced copy keeps the run short
         cfg = wl.small_config(args.config, B=8, V=4096)
+        workload += f" -- reduced copy without a GPU: B={cfg.B}, V={cfg.V}"
     import oracle
     oracle.build()
     w = make_workload_cpu(cfg, args.sps)       # inputs and layout from the oracle only
@@ -379,7 +381,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config),
+            "data": "synthetic", "config": {"workload": workload,
                                              "sample": f"{sample} of {cfg.B} requests per step"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"draft + verify of {sample} requests, full schedule, per step"},

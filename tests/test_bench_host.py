@@ -55,3 +55,22 @@ def test_algorithmic_work_of_a_hand_worked_step():
     assert (alg["positions"], alg["draft_positions"], alg["verify_positions"]) == (10, 5, 5)
     rnn = bench.algorithmic(cfg, K_r, ell, n_acc, T, head="rnn")
     assert rnn["draft_flops"] - alg["draft_flops"] == 2.0 * 5 * 3 * r * 2 * r   # the cell per position
+
+
+def test_reference_arm_line_on_the_host(capsys, monkeypatch):
+    # the oracle on the host cores; on a machine without a GPU it runs a reduced copy of the
+    # workload and says so in the line
+    import json
+
+    import torch
+    for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(v, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    if not torch.cuda.is_available():
+        assert "reduced copy without a GPU" in line["config"]["workload"]
