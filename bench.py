@@ -9,7 +9,8 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   verify   dspark_verify_ragged        (rejection sampling over the flattened rows)
 Metric: draft + verify positions per second (sum K_r + sum (ell_r + 1) per step).
 
-Default workload: the Qwen3-4B-shaped step (B=64, K=7, V=151936, rank 256, bf16).
+Default workload: the ragged mixed step, the largest single-GPU configuration (B=2048,
+per-request K in 1..7, V=151936, rank 256, bf16, 30% greedy requests).
 The L2 is flushed (256 MB write, untimed) between timed steps.  Under torchrun
 each rank runs an independent replica of the step on its own GPU (weak scaling);
 the reported value is all ranks' positions over the slowest rank's time.
@@ -47,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="qwen")
+    p.add_argument("--config", default="ragged")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sps", choices=["literal", "step"], default="literal")
@@ -314,44 +315,90 @@ def profiled_traffic(kernel: str, workload: str, path: str):
     return float(t.group(1)) if kernel_source_hash(kernel) == m.group(1) else None
 
 
-def cpu_baseline(cfg, w, sample_requests):
-    """The oracle, as it stands, on the host cores, on `sample_requests` requests of the step."""
+CPU_SAMPLE_ALL = 128      # requests of the step the oracle runs on all host cores
+CPU_SAMPLE_ONE = 16       # requests it runs on one core
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model", "hardware")):
+                return line.split(":", 1)[1].strip()
+        parts = {}
+        for line in open("/proc/cpuinfo"):      # Arm: implementer / part codes
+            if ":" in line:
+                k, v = line.split(":", 1)
+                parts.setdefault(k.strip(), v.strip())
+        if "CPU implementer" in parts:
+            return f"implementer {parts['CPU implementer']} part {parts.get('CPU part', '?')}"
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(cfg, w, sample_requests, nthreads=None):
+    """The oracle, as it stands, on the host cores, on `sample_requests` requests of the step
+    (their draft and verification) plus the full schedule.  Returns (positions/s, seconds,
+    threads, positions)."""
     import numpy as np
 
     import oracle
     from speculative_decoding_draft_gb300 import workloads as wl
 
     inp = w["inp"]
-    rows = np.arange(sample_requests)
-    U = wl.bf16_bits(inp["U"][:sample_requests])
+    n = min(sample_requests, cfg.B)
+    rows = np.arange(n)
+    U = wl.bf16_bits(inp["U"][:n])
     E = wl.bf16_bits(inp["E"])
     W = wl.bf16_bits(inp["W"])
-    anchor = inp["anchor"][:sample_requests].cpu().numpy()
-    K_r = inp["K_r"][:sample_requests].cpu().numpy()
-    T = inp["temperature"][:sample_requests].cpu().numpy()
+    anchor = inp["anchor"][:n].cpu().numpy()
+    K_r = inp["K_r"][:n].cpu().numpy()
+    T = inp["temperature"][:n].cpu().numpy()
     conf = w["conf"].cpu().numpy()
     K_all = inp["K_r"].cpu().numpy()
     sps = w["sps"].cpu().numpy()
-    ell_all = w["ell"].cpu().numpy()
     off_all = w["off"].cpu().numpy()
-    tgt_rows = wl.bf16_bits(w["tgt"][: int(off_all[sample_requests])])
-    nthreads = os.cpu_count() or 1
+    tgt_rows = wl.bf16_bits(w["tgt"][: int(off_all[n])])
+    nthreads = nthreads or (os.cpu_count() or 1)
     t0 = time.perf_counter()
     if w.get("rnn") is not None:
         d = oracle.draft_rnn_sample(U, E, W, wl.bf16_bits(w["rnn"]["rnn_W"]),
-                                    w["rnn"]["rnn_x"][:sample_requests].cpu().numpy(), anchor, K_r, T,
+                                    w["rnn"]["rnn_x"][:n].cpu().numpy(), anchor, K_r, T,
                                     cfg.philox_seed, req_id=rows.astype(np.int64), nthreads=nthreads)
     else:
         d = oracle.draft_markov_sample(U, E, W, anchor, K_r, T, cfg.philox_seed, req_id=rows.astype(np.int64),
                                        nthreads=nthreads)
     s = oracle.schedule_survival(conf, K_all, sps)
-    ell = s["ell"][:sample_requests]
-    off = s["tgt_off"][: sample_requests + 1]
-    v = oracle.verify_ragged(d["draft_logits"], tgt_rows, off, ell, d["draft_tok"], T, cfg.philox_seed + 7919,
-                             req_id=rows.astype(np.int64), nthreads=nthreads)
+    ell = s["ell"][:n]
+    off = s["tgt_off"][: n + 1]
+    oracle.verify_ragged(d["draft_logits"], tgt_rows, off, ell, d["draft_tok"], T, cfg.philox_seed + 7919,
+                         req_id=rows.astype(np.int64), nthreads=nthreads)
     dt = time.perf_counter() - t0
     positions = int(K_r.sum()) + int((ell + 1).sum())
     return positions / dt, dt, nthreads, positions
+
+
+def cpu_baseline_report(cfg, w):
+    """The oracle on all host cores and on one core (each on a bounded sample of the step)."""
+    v_all, dt_all, cores, pos_all = cpu_baseline(cfg, w, CPU_SAMPLE_ALL)
+    v_one, dt_one, _, pos_one = cpu_baseline(cfg, w, CPU_SAMPLE_ONE, nthreads=1)
+    n_all, n_one = min(CPU_SAMPLE_ALL, cfg.B), min(CPU_SAMPLE_ONE, cfg.B)
+    return {"value": v_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"draft + verify of {n_all} of {cfg.B} requests ({pos_all} positions) and the full "
+                      f"schedule, {dt_all:.2f} s on {cores} threads",
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+            "single_thread": {"value": v_one, "unit": UNIT, "cores": 1,
+                              "sample": f"draft + verify of {n_one} of {cfg.B} requests ({pos_one} positions) "
+                                        f"and the full schedule, {dt_one:.2f} s"}}
+
+
+def line_config(args, cfg):
+    """The `config` object of the JSON line, shared by both arms."""
+    from speculative_decoding_draft_gb300 import workloads as wl
+    return {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config), "B": cfg.B, "K": cfg.K_max, "V": cfg.V,
+            "rank": cfg.rank, "sps": args.sps, "head": args.head,
+            "l2": "flushed between timed steps (256 MB write, untimed)"}
 
 
 def run_reference(args):
@@ -363,17 +410,18 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = wl.CONFIGS[args.config]
-    workload = wl.WORKLOAD_TEXT.get(args.config, args.config)
+    config = line_config(args, cfg)
     if not torch.cuda.is_available():          # no GPU machine: a reduced copy keeps the run short
         cfg = wl.small_config(args.config, B=8, V=4096)
-        workload += f" -- reduced copy without a GPU: B={cfg.B}, V={cfg.V}"
+        config = line_config(args, cfg)
+        config["workload"] += f" -- reduced copy without a GPU: B={cfg.B}, V={cfg.V}"
     import oracle
     oracle.build()
     w = make_workload_cpu(cfg, args.sps)       # inputs and layout from the oracle only
-    sample = min(cfg.B, 4)
+    sample = min(cfg.B, CPU_SAMPLE_ALL)
     for _ in range(args.warmup):
         cpu_baseline(cfg, w, sample)
-    times, pos = [], 0
+    times, pos, cores = [], 0, 1
     for _ in range(args.steps):
         _, dt, cores, pos = cpu_baseline(cfg, w, sample)
         times.append(dt)
@@ -381,10 +429,11 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": workload,
-                                             "sample": f"{sample} of {cfg.B} requests per step"},
+            "data": "synthetic", "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"draft + verify of {sample} requests, full schedule, per step"},
+                             "sample": f"draft + verify of {sample} of {cfg.B} requests ({pos} positions) and "
+                                       f"the full schedule, per step",
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -554,26 +603,21 @@ def main(argv=None):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config), "B": cfg.B, "K": cfg.K_max,
-                       "V": cfg.V, "rank": cfg.rank, "sps": args.sps,
-                       "positions_per_step": alg["positions"], "draft_positions": alg["draft_positions"],
-                       "verify_positions": alg["verify_positions"],
-                       "l2": "flushed between timed steps (256 MB write, untimed)",
-                       "w2_layout": (f"packed once at load time ({step.pack_ms:.3f} ms, outside the step)"
-                                     if step.tensor_core else "as given"),
-                       "parallelism": f"replicas x{world}", "launch": launch_mode, "head": args.head,
-                       "scheduler": ("beside the draft on a second stream (the draft leaves it one SM)"
-                                     if overlap else "after the draft")},
+            "config": line_config(args, cfg),
+            "step": {"positions_per_step": alg["positions"], "draft_positions": alg["draft_positions"],
+                     "verify_positions": alg["verify_positions"],
+                     "w2_layout": (f"packed once at load time ({step.pack_ms:.3f} ms, outside the step)"
+                                   if step.tensor_core else "as given"),
+                     "parallelism": f"replicas x{world}", "launch": launch_mode,
+                     "scheduler": ("beside the draft on a second stream (the draft leaves it one SM)"
+                                   if overlap else "after the draft")},
             "roofline": roofline, "kernels": kernels, "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clk}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(cfg, w, step, dev, args, alg)
     if rank == 0 and not args.no_cpu_baseline:
-        v_cpu, dt, cores, pos = cpu_baseline(cfg, w, min(cfg.B, 8))
-        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"draft + verify of {min(cfg.B, 8)} of {cfg.B} requests "
-                                          f"({pos} positions) and the full schedule, {dt:.2f} s"}
+        line["cpu_baseline"] = cpu_baseline_report(cfg, w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

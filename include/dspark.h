@@ -120,6 +120,12 @@ typedef struct {
  *   draft_lse    [B, K_max] float out, optional: log sum_v exp(z_k(v) / T_r), the
  *                draft distribution's normaliser (for T_r = 0: max_v z_k(v));
  *                entries k > K_r are not written.
+ *   draft_tok_logit [B, K_max] float out, optional: z_k(x_k), the stored-dtype logit
+ *                of the drawn token (exact, as a float); entries k > K_r are not
+ *                written.  With draft_lse it gives log q_k(x_k) = z_k(x_k) / T_r -
+ *                lse, all that verification needs of a draft row except at a
+ *                rejection, so draft_logits can stay NULL (no B x K x V logits go
+ *                back to memory; see dspark_verify_markov).
  *   workspace    >= dspark_draft_workspace_bytes(dims) bytes (the same dims and
  *                flags as the call), 256-byte aligned.
  * The tensor-core path is used when dtype = DSPARK_BF16, rank is a multiple of
@@ -159,7 +165,7 @@ dspark_status dspark_draft_markov_sample(const void *U, const void *E, const voi
                                          const int32_t *anchor, const int32_t *K_r,
                                          const float *temperature, uint64_t seed, dspark_dims dims,
                                          int32_t *draft_tok, void *draft_logits, float *draft_lse,
-                                         void *workspace, size_t workspace_bytes,
+                                         float *draft_tok_logit, void *workspace, size_t workspace_bytes,
                                          int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
@@ -183,8 +189,8 @@ dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E
                                                     const float *temperature, uint64_t seed, dspark_dims dims,
                                                     const float *conf_h, const float *conf_w,
                                                     int32_t *draft_tok, void *draft_logits, float *draft_lse,
-                                                    float *conf, void *workspace, size_t workspace_bytes,
-                                                    int32_t *dev_status, void *stream);
+                                                    float *draft_tok_logit, float *conf, void *workspace,
+                                                    size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Draft with the RNN head ("DSpark" S3.1, RNN head).
@@ -214,8 +220,9 @@ size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims);
 dspark_status dspark_draft_rnn_sample(const void *U, const void *E, const void *W, const void *rnn_W,
                                       const float *rnn_x, const int32_t *anchor, const int32_t *K_r,
                                       const float *temperature, uint64_t seed, dspark_dims dims,
-                                      int32_t *draft_tok, void *draft_logits, float *draft_lse, void *workspace,
-                                      size_t workspace_bytes, int32_t *dev_status, void *stream);
+                                      int32_t *draft_tok, void *draft_logits, float *draft_lse,
+                                      float *draft_tok_logit, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Schedule: hardware-aware prefix scheduler ("DSpark" S3.2.2, Algorithm 1;
@@ -399,7 +406,8 @@ const char *dspark_status_string(dspark_status s);
  * return it.  Returns DSPARK_ERR_CUDA when the copy or the synchronisation fails. */
 dspark_status dspark_check(int32_t *dev_status, void *stream);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 200 added draft_tok_logit to the
+ * draft entry points. */
 int dspark_version(void);
 
 #ifdef __cplusplus

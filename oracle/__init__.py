@@ -92,10 +92,10 @@ def lib() -> ctypes.CDLL:
         L.dso_round_bf16.argtypes = [ctypes.c_double]
         L.dso_round_bf16.restype = ctypes.c_double
         L.dso_draft_markov_sample.argtypes = [P, P, P, i32, P, P, P, P, u64, i64, i64, i64, i64,
-                                              P, P, P, P, P, i32]
+                                              P, P, P, P, P, P, i32]
         L.dso_draft_markov_sample.restype = i32
         L.dso_draft_rnn_sample.argtypes = [P, P, P, P, i32, P, P, P, P, P, u64, i64, i64, i64, i64,
-                                           P, P, P, P, P, P, i32]
+                                           P, P, P, P, P, P, P, i32]
         L.dso_draft_rnn_sample.restype = i32
         L.dso_schedule_survival.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, P, P, P, P]
         L.dso_schedule_survival.restype = i32
@@ -108,7 +108,7 @@ def lib() -> ctypes.CDLL:
         L.dso_schedule_threshold.argtypes = [P, P, i64, i64, ctypes.c_float, i32, P, P, P]
         L.dso_schedule_threshold.restype = i32
         L.dso_verify_ragged.argtypes = [P, P, i32, P, P, P, P, P, u64, i64, i64, i64,
-                                        P, P, P, P, P, i32]
+                                        P, P, P, P, P, P, i32]
         L.dso_verify_ragged.restype = i32
         L.dso_row_lse.argtypes = [P, i32, i64, i64, P, P]
         L.dso_row_lse.restype = i32
@@ -198,11 +198,15 @@ def block_race(log_w, seed, position, request, tag_block, tag_pick, log_err=None
 # hot-path operations
 # ---------------------------------------------------------------------------
 def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed, req_id=None, want_logits=True,
-                        nthreads=0):
+                        want_spread=False, nthreads=0):
     """Markov-head draft sampling.  U: [B, K_max, V]; E: [V, rank]; W: [rank, V].
 
     Returns dict(draft_tok [B,K_max] int32, draft_logits (same dtype as U) or None,
-    lse [B,K_max] f64, margin [B,K_max] f64, flags [B,K_max] u8).
+    lse [B,K_max] f64, margin [B,K_max] f64, flags [B,K_max] u8, spread).  With want_spread
+    (bf16), spread [B,K_max,V] f32 bounds, per stored logit, how far another fp32 evaluation
+    of U + bias may move it: 0 where none can change it, one bf16 step where the exact value
+    sits within the fp32 error bound of a rounding midpoint, more where the sum cancels to
+    near zero; else None.
     """
     U, dt = _logits(U)
     E, dtE = _logits(E)
@@ -222,21 +226,24 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed, req_id=None, wa
     lse = np.zeros((B, K_max), np.float64)
     margin = np.zeros((B, K_max), np.float64)
     flags = np.zeros((B, K_max), np.uint8)
+    spread = np.zeros((B, K_max, V), np.float32) if want_spread else None
     st = lib().dso_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), dt, _ptr(anchor), _ptr(K_r),
                                        _ptr(temperature), _ptr(rid), int(seed), B, K_max, V, rank,
                                        _ptr(tok), _ptr(logits), _ptr(lse), _ptr(margin), _ptr(flags),
-                                       _threads(nthreads))
+                                       _ptr(spread), _threads(nthreads))
     if st:
         raise OracleError(st)
-    return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags)
+    return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags, spread=spread)
 
 
 def draft_rnn_sample(U, E, W, Wc, cx, anchor, K_r, temperature, seed, req_id=None, want_logits=True,
-                     want_feat=False, nthreads=0):
+                     want_feat=False, want_spread=False, nthreads=0):
     """RNN-head draft sampling.  U [B,K_max,V]; E [V,rank]; W [rank,V]; Wc [3 rank, 2 rank] (one dtype);
     cx [B,K_max,3 rank] float32 (the backbone term of the cell).
 
     Returns the draft_markov_sample dict plus feat [B,K_max,rank] f64 (the head's feature) when asked.
+    The spread's error bound adds the feature's own fp32 error (at most 1e-5 per component) to
+    the Markov head's summation bound.
     """
     U, dt = _logits(U)
     E, dtE = _logits(E)
@@ -261,13 +268,14 @@ def draft_rnn_sample(U, E, W, Wc, cx, anchor, K_r, temperature, seed, req_id=Non
     margin = np.zeros((B, K_max), np.float64)
     flags = np.zeros((B, K_max), np.uint8)
     feat = np.zeros((B, K_max, rank), np.float64) if want_feat else None
+    spread = np.zeros((B, K_max, V), np.float32) if want_spread else None
     st = lib().dso_draft_rnn_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(Wc), dt, _ptr(cx), _ptr(anchor), _ptr(K_r),
                                     _ptr(temperature), _ptr(rid), int(seed), B, K_max, V, rank, _ptr(tok),
-                                    _ptr(logits), _ptr(lse), _ptr(margin), _ptr(flags), _ptr(feat),
+                                    _ptr(logits), _ptr(lse), _ptr(margin), _ptr(flags), _ptr(feat), _ptr(spread),
                                     _threads(nthreads))
     if st:
         raise OracleError(st)
-    return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags, feat=feat)
+    return dict(draft_tok=tok, draft_logits=logits, lse=lse, margin=margin, flags=flags, feat=feat, spread=spread)
 
 
 def draft_confidence(E, anchor, draft_tok, K_r, conf_h, conf_w):
@@ -378,10 +386,13 @@ def schedule_threshold(conf, K_r, theta, mode=THRESHOLD_CONFIDENCE):
 
 
 def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature, seed, req_id=None,
-                  nthreads=0):
+                  draft_spread=None, nthreads=0):
     """Ragged rejection-sampling verification.
 
     draft_logits [B, K_max, V]; tgt_logits [sum(ell+1), V] flattened; tgt_off [B+1].
+    draft_spread (optional) [B, K_max, V] f32: the draft's spreads (draft_markov_sample's
+    spread); decisions that another fp32 evaluation of the draft logits could move are
+    flagged.
     Returns dict(n_acc [B], out_tok [B, K_max+1], flags [B], flag_pos [B], sample_margin [B]).
     """
     D, dt = _logits(draft_logits)
@@ -399,8 +410,13 @@ def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature
     flags = np.zeros(B, np.uint8)
     fpos = np.zeros(B, np.int32)
     mg = np.zeros(B, np.float64)
+    amb = None
+    if draft_spread is not None:
+        amb = _c(draft_spread, np.float32)
+        if amb.shape != D.shape:
+            raise ValueError("draft_spread must have the draft logits' shape")
     st = lib().dso_verify_ragged(_ptr(D), _ptr(Tg), dt, _ptr(tgt_off), _ptr(ell), _ptr(draft_tok),
-                                 _ptr(temperature), _ptr(rid), int(seed), B, K_max, V,
+                                 _ptr(temperature), _ptr(rid), int(seed), B, K_max, V, _ptr(amb),
                                  _ptr(n_acc), _ptr(out), _ptr(flags), _ptr(fpos), _ptr(mg),
                                  _threads(nthreads))
     if st:

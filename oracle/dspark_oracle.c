@@ -84,6 +84,7 @@ enum { TAG_DRAFT = 0, TAG_ACCEPT = 1, TAG_RESID = 2, TAG_DRAFT_PICK = 3, TAG_RES
 #define ORC_ACCEPT_TIE 1e-5 /* |u - min(1, p/q)| near-tie margin        */
 #define ORC_PICK_TIE 1e-5   /* |u' - cumulative fraction| near-tie margin */
 #define ORC_BLOCK 32        /* block width of the two-level sampler       */
+#define ORC_RNN_FEAT_ERR 1e-5 /* bound on the fp32 error of one RNN feature component */
 
 /* ---------------------------------------------------------------------- */
 /* Philox4x32-10 [PRX S4].                                                 */
@@ -160,22 +161,37 @@ static uint16_t double_to_bf16_bits(double x) {
   return (uint16_t)(bits >> 16);
 }
 
-/* Is x so close to a bf16 rounding midpoint that an fp32 evaluation of it   */
-/* (a few fp32 ulps of error) could round the other way?  Returns the other  */
-/* candidate bf16 value in *alt when it is.                                  */
-static int bf16_ambiguous(double x, double *alt) {
-  if (x == 0.0 || !isfinite(x)) return 0;
-  double q = bf16_quantum(x);
-  double t = x / q;
-  double fl = floor(t);
-  double frac = t - fl;
-  if (fabs(frac - 0.5) < 0x1p-14) {
-    double r = round_bf16(x);
-    double lo = fl * q, hi = (fl + 1.0) * q;
-    *alt = (r == lo) ? hi : lo;
-    return 1;
-  }
-  return 0;
+/* Which bf16 values may an fp32 evaluation of the exact value x store?  The     */
+/* evaluation lies within delta of x (delta: an absolute bound on its error, for    */
+/* instance the fp32 summation bound of the bias), and never closer to a rounding   */
+/* midpoint than 2^-14 of a bf16 step is treated as safe.  With d = max(delta,      */
+/* 2^-14 q(x)), rounding is monotone, so every stored value lies in                 */
+/* [round(x - d), round(x + d)]; those are returned in *lo / *hi.  Returns 0 when    */
+/* the two are equal (the stored value is unambiguous), 1 when they are the two     */
+/* neighbours of one midpoint, 2 when the error spans more than one rounding        */
+/* interval (a sum that cancels to near zero).                                      */
+static int bf16_ambiguity(double x, double delta, double *lo, double *hi) {
+  *lo = *hi = round_bf16(x);
+  if (!isfinite(x)) return 0;
+  double d = (x == 0.0) ? delta : fmax(delta, bf16_quantum(x) * 0x1p-14);
+  if (!(d > 0.0)) return 0;
+  *lo = round_bf16(x - d);
+  *hi = round_bf16(x + d);
+  if (*lo == *hi) return 0;
+  /* one step apart: the quantum of the lower one, or (across a power of two) of the upper */
+  if (*hi - *lo <= fmax(bf16_quantum(*lo), bf16_quantum(*hi))) return 1;
+  return 2;
+}
+
+/* Largest distance between the value x rounds to and any value an fp32 evaluation */
+/* within delta may store (0 when unambiguous); the code in *code when given.       */
+static double bf16_spread(double x, double delta, int *code) {
+  double lo, hi;
+  const int c = bf16_ambiguity(x, delta, &lo, &hi);
+  if (code) *code = c;
+  if (!c) return 0.0;
+  const double r = round_bf16(x);
+  return fmax(hi - r, r - lo);
 }
 
 static double load_elem(const void *p, int dtype, int64_t i) {
@@ -337,48 +353,53 @@ static double row_lse_scaled(const double *z, int64_t V, double T) {
 /* One draft position of request rid: z = U row + bias, rounded to the storage dtype     */
 /* (stored when draft_logits is given), then the draw (T > 0) or the argmax (T = 0) with   */
 /* its normaliser, margin and near-tie flags.  Shared by the Markov and the RNN heads.      */
-static int64_t draft_position(const void *U, int dtype, int64_t ubase, const double *bias, int64_t V, double T,
-                              uint64_t seed, int64_t k, uint32_t rid, void *draft_logits, double *z, double *lw,
-                              double *le, double *l_out, double *mg_out, uint8_t *f_out) {
+/* err[v] (bf16 only): an absolute bound on the error of an fp32 evaluation of U + bias    */
+/* at element v; an element whose stored value that error could change is ambiguous, and   */
+/* spread_out (optional, [V]) receives, per element, the largest distance between the      */
+/* stored value and any value such an evaluation may store (0: unambiguous).               */
+static int64_t draft_position(const void *U, int dtype, int64_t ubase, const double *bias, const double *err,
+                              int64_t V, double T, uint64_t seed, int64_t k, uint32_t rid, void *draft_logits,
+                              double *z, double *lw, double *le, double *l_out, double *mg_out, uint8_t *f_out,
+                              float *spread_out) {
   for (int64_t v = 0; v < V; ++v) {
     double exact = load_elem(U, dtype, ubase + v) + bias[v];
     z[v] = (dtype == ORC_F32) ? (double)(float)exact : round_bf16(exact);
   }
   if (draft_logits) for (int64_t v = 0; v < V; ++v) store_elem(draft_logits, dtype, ubase + v, z[v]);
+  /* spread[v]: how far the stored value may move (0 = unambiguous); kept in le's slot  */
+  /* until the weights are formed                                                      */
+  double *spread = le;
+  int amb_any = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    spread[v] = 0.0;
+    int code = 0;
+    if (dtype == ORC_BF16) spread[v] = bf16_spread(load_elem(U, dtype, ubase + v) + bias[v], err[v], &code);
+    if (spread_out) spread_out[v] = (float)spread[v];
+    if (code) amb_any = 1;
+  }
   int64_t best;
   double l, mg;
   uint8_t f = 0;
   if (T > 0.0) {
-    /* two-level sampler on the weights exp(z / T); a bf16 rounding ambiguity */
-    /* enters as the uncertainty |exp(alt / T) - exp(z / T)| of its weight.  */
-    int amb = 0;
+    l = row_lse_scaled(z, V, T);
+    /* lse moves by at most sum_v p_v |dz_v| / T when stored values move by dz_v */
+    double lse_shift = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+      if (spread[v] > 0.0) lse_shift += exp(z[v] / T - l) * spread[v] / T;
+    if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
+    /* two-level sampler on the weights exp(z / T); an ambiguous element enters as the  */
+    /* uncertainty exp(z / T) (exp(spread / T) - 1) of its weight                        */
     for (int64_t v = 0; v < V; ++v) {
+      const double sp = spread[v];
       lw[v] = z[v] / T;
-      le[v] = -INFINITY;
-      if (dtype == ORC_BF16) {
-        double alt;
-        if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) {
-          le[v] = lw[v] + log(fabs(expm1((alt - z[v]) / T)));
-          amb = 1;
-        }
-      }
+      le[v] = (sp > 0.0) ? lw[v] + log(expm1(sp / T)) : -INFINITY;
     }
-    race_t rc = block_race(lw, amb ? le : NULL, V, seed, (uint32_t)k, rid, TAG_DRAFT, TAG_DRAFT_PICK);
+    race_t rc = block_race(lw, amb_any ? le : NULL, V, seed, (uint32_t)k, rid, TAG_DRAFT, TAG_DRAFT_PICK);
     best = rc.pick;
     mg = rc.margin;
     if (rc.near_block) f |= 1;
     if (rc.near_pick) f |= 8;
     if (rc.near_err && !(f & 9)) f |= 2;
-    l = row_lse_scaled(z, V, T);
-    if (dtype == ORC_BF16) {
-      double lse_shift = 0.0;
-      for (int64_t v = 0; v < V; ++v) {
-        double alt;
-        if (bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt))
-          lse_shift += exp(z[v] / T - l) * fabs(alt - z[v]) / T;
-      }
-      if (lse_shift > 1e-6 * fmax(1.0, fabs(l))) f |= 4;
-    }
   } else {
     /* greedy: largest logit, smallest index on ties */
     int64_t second = -1;
@@ -392,10 +413,11 @@ static int64_t draft_position(const void *U, int dtype, int64_t ubase, const dou
     if (dtype == ORC_F32 && mg < ORC_SAMPLE_TIE) f |= 1;
     if (dtype == ORC_BF16) {
       for (int64_t v = 0; v < V; ++v) {
-        double alt;
-        if (!bf16_ambiguous(load_elem(U, dtype, ubase + v) + bias[v], &alt)) continue;
-        if (v == best) { if (alt <= z[second] + ORC_SAMPLE_TIE) f |= 2; }
-        else if (alt >= z[best] - ORC_SAMPLE_TIE) f |= 2;
+        if (!(spread[v] > 0.0)) continue;
+        double lo, hi;
+        bf16_ambiguity(load_elem(U, dtype, ubase + v) + bias[v], err[v], &lo, &hi);
+        if (v == best) { if (lo <= z[second] + ORC_SAMPLE_TIE) f |= 2; }
+        else if (hi >= z[best] - ORC_SAMPLE_TIE) f |= 2;
       }
     }
   }
@@ -410,7 +432,7 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
                             const int64_t *req_id, uint64_t seed,
                             int64_t B, int64_t K_max, int64_t V, int64_t rank,
                             int32_t *draft_tok, void *draft_logits, double *lse,
-                            double *margin, uint8_t *flags, int nthreads) {
+                            double *margin, uint8_t *flags, float *spread, int nthreads) {
   if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok) return ORC_ERR_NULL;
   if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
   if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2 || rank < 1) return ORC_ERR_DIMS;
@@ -427,22 +449,33 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *lw = (double *)malloc(sizeof(double) * (size_t)V);
     double *le = (double *)malloc(sizeof(double) * (size_t)V);
+    double *err = (double *)malloc(sizeof(double) * (size_t)V);
     uint32_t rid = (uint32_t)(req_id ? req_id[b] : b);
     int32_t x_prev = anchor[b];
     double T = (double)temperature[b];
     for (int64_t k = 1; k <= K_max; ++k) {
       int64_t slot = b * K_max + (k - 1);
       if (k > K_r[b]) { draft_tok[slot] = -1; continue; }
-      /* transition bias: one row of the lookup table times the projection */
-      for (int64_t v = 0; v < V; ++v) bias[v] = 0.0;
+      /* transition bias: one row of the lookup table times the projection; err first */
+      /* collects sum_i |E_i W_iv|                                                     */
+      for (int64_t v = 0; v < V; ++v) bias[v] = err[v] = 0.0;
       for (int64_t i = 0; i < rank; ++i) {
         double e = load_elem(E, dtype, (int64_t)x_prev * rank + i);
-        for (int64_t v = 0; v < V; ++v) bias[v] += e * load_elem(W, dtype, i * V + v);
+        for (int64_t v = 0; v < V; ++v) {
+          const double t = e * load_elem(W, dtype, i * V + v);
+          bias[v] += t;
+          err[v] += fabs(t);
+        }
       }
       const int64_t ubase = slot * V;
+      /* fp32 evaluation error of U + bias: the summation bound rank * u * sum |terms| */
+      /* (doubled, for an accumulator that may truncate) plus the final rounding, u = 2^-24 */
+      for (int64_t v = 0; v < V; ++v)
+        err[v] = 0x1p-23 * ((double)rank * err[v] + fabs(load_elem(U, dtype, ubase + v) + bias[v]));
       double l, mg;
       uint8_t f = 0;
-      const int64_t best = draft_position(U, dtype, ubase, bias, V, T, seed, k, rid, draft_logits, z, lw, le, &l, &mg, &f);
+      const int64_t best = draft_position(U, dtype, ubase, bias, err, V, T, seed, k, rid, draft_logits, z, lw, le,
+                                          &l, &mg, &f, spread ? spread + ubase : NULL);
       draft_tok[slot] = (int32_t)best;
       if (lse) lse[slot] = l;
       if (margin) margin[slot] = mg;
@@ -453,6 +486,7 @@ int dso_draft_markov_sample(const void *U, const void *E, const void *W, int dty
     free(z);
     free(lw);
     free(le);
+    free(err);
   }
   return ORC_OK;
 }
@@ -488,7 +522,7 @@ int dso_draft_rnn_sample(const void *U, const void *E, const void *W, const void
                          const int64_t *req_id, uint64_t seed,
                          int64_t B, int64_t K_max, int64_t V, int64_t rank,
                          int32_t *draft_tok, void *draft_logits, double *lse,
-                         double *margin, uint8_t *flags, double *feat, int nthreads) {
+                         double *margin, uint8_t *flags, double *feat, float *spread, int nthreads) {
   if (!U || !E || !W || !Wc || !cx || !anchor || !K_r || !temperature || !draft_tok) return ORC_ERR_NULL;
   if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_ERR_DTYPE;
   if (B < 1 || K_max < 1 || K_max > ORC_MAX_K || V < 2 || rank < 1) return ORC_ERR_DIMS;
@@ -508,6 +542,10 @@ int dso_draft_rnn_sample(const void *U, const void *E, const void *W, const void
     double *st = (double *)calloc((size_t)rank, sizeof(double));        /* s_0 = 0 */
     double *ft = (double *)malloc(sizeof(double) * (size_t)rank);
     double *pre = (double *)malloc(sizeof(double) * (size_t)(3 * rank));
+    double *err = (double *)malloc(sizeof(double) * (size_t)V);
+    double *wabs = (double *)calloc((size_t)V, sizeof(double));   /* sum_i |W_iv| */
+    for (int64_t i = 0; i < rank; ++i)
+      for (int64_t v = 0; v < V; ++v) wabs[v] += fabs(load_elem(W, dtype, i * V + v));
     uint32_t rid = (uint32_t)(req_id ? req_id[b] : b);
     int32_t x_prev = anchor[b];
     double T = (double)temperature[b];
@@ -529,13 +567,23 @@ int dso_draft_rnn_sample(const void *U, const void *E, const void *W, const void
         if (feat) feat[slot * rank + i] = ft[i];
       }
       /* transition bias: the head's feature times the projection */
-      for (int64_t v = 0; v < V; ++v) bias[v] = 0.0;
+      for (int64_t v = 0; v < V; ++v) bias[v] = err[v] = 0.0;
       for (int64_t i = 0; i < rank; ++i)
-        for (int64_t v = 0; v < V; ++v) bias[v] += ft[i] * load_elem(W, dtype, i * V + v);
+        for (int64_t v = 0; v < V; ++v) {
+          const double t = ft[i] * load_elem(W, dtype, i * V + v);
+          bias[v] += t;
+          err[v] += fabs(t);
+        }
+      /* fp32 evaluation error: the summation and rounding bound of the Markov head plus */
+      /* the feature's own fp32 error (sigmoid, tanh and the recurrence), taken as at     */
+      /* most ORC_RNN_FEAT_ERR per component                                               */
+      for (int64_t v = 0; v < V; ++v)
+        err[v] = 0x1p-23 * ((double)rank * err[v] + fabs(load_elem(U, dtype, slot * V + v) + bias[v])) +
+                 ORC_RNN_FEAT_ERR * wabs[v];
       double l, mg;
       uint8_t f = 0;
-      const int64_t best = draft_position(U, dtype, slot * V, bias, V, T, seed, k, rid, draft_logits, z, lw, le, &l,
-                                          &mg, &f);
+      const int64_t best = draft_position(U, dtype, slot * V, bias, err, V, T, seed, k, rid, draft_logits, z, lw, le,
+                                          &l, &mg, &f, spread ? spread + slot * V : NULL);
       draft_tok[slot] = (int32_t)best;
       if (lse) lse[slot] = l;
       if (margin) margin[slot] = mg;
@@ -549,6 +597,8 @@ int dso_draft_rnn_sample(const void *U, const void *E, const void *W, const void
     free(st);
     free(ft);
     free(pre);
+    free(err);
+    free(wabs);
   }
   return ORC_OK;
 }
@@ -834,6 +884,10 @@ int dso_schedule_threshold(const float *conf, const int32_t *K_r, int64_t B, int
 /* element has p_v > q_v in floating point the correction is drawn from p    */
 /* instead (rounding guard); the bonus is the two-level sampler on exp(z/T)  */
 /* of the next target row, streams (seed, ell+1, request, RESID / RESID_PICK).*/
+/* draft_spread (optional, [B, K_max, V], the draft's spreads): a draft logit */
+/* may be any value within its spread that an fp32 evaluation of the draft   */
+/* could store; the accept tolerance and the residual weights' uncertainties */
+/* widen by what those changes can do.                                      */
 /* Flags per request: bit0 an accept decision with |u - min(1, p/q)| < 1e-5,  */
 /* bit1 the correction/bonus draw is within rounding of another outcome     */
 /* (block scores, in-block boundary, or the fp32 error of p - q), bit2 the   */
@@ -874,6 +928,7 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
                       const int32_t *tgt_off, const int32_t *ell, const int32_t *draft_tok,
                       const float *temperature, const int64_t *req_id, uint64_t seed,
                       int64_t B, int64_t K_max, int64_t V,
+                      const float *draft_spread,
                       int32_t *n_acc, int32_t *out_tok, uint8_t *flags, int32_t *flag_pos,
                       double *sample_margin, int nthreads) {
   if (!draft_logits || !tgt_logits || !tgt_off || !ell || !draft_tok || !temperature || !n_acc || !out_tok)
@@ -909,14 +964,24 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
       int32_t x = draft_tok[r * K_max + j - 1];
       row_scaled(tgt_logits, dtype, (int64_t)tgt_off[r] + j - 1, V, T, st);
       int accept;
+      /* draft logits that another fp32 evaluation may store differently move log q_v  */
+      /* by at most dz_v / T (dz: their spread); log q(x) moves by at most dlq          */
+      const float *am = draft_spread ? draft_spread + (r * K_max + j - 1) * V : NULL;
+      double dlse = 0.0, dlq = 0.0;
       if (T > 0.0) {
         row_scaled(draft_logits, dtype, r * K_max + j - 1, V, T, sd);
         double lp = st[x] - row_lse(st, V);
         double lq = sd[x] - row_lse(sd, V);
+        if (am) {
+          const double ld = row_lse(sd, V);
+          for (int64_t v = 0; v < V; ++v)
+            if (am[v] > 0.0f) dlse += exp(sd[v] - ld) * (double)am[v] / T;
+          dlq = dlse + (double)am[x] / T;
+        }
         double rho = exp(lp - lq);
         double thr = rho < 1.0 ? rho : 1.0;
         double u = dso_uniform_accept(dso_stream_word(seed, 0, (uint32_t)j, rid, TAG_ACCEPT));
-        if (fabs(u - thr) < ORC_ACCEPT_TIE && !fpos) { f |= 1; fpos = (int32_t)j; }
+        if (fabs(u - thr) < ORC_ACCEPT_TIE + thr * expm1(dlq) && !fpos) { f |= 1; fpos = (int32_t)j; }
         accept = u < thr;
       } else {
         double amg;
@@ -936,6 +1001,9 @@ int dso_verify_ragged(const void *draft_logits, const void *tgt_logits, int dtyp
             double p = exp(st[v] - lt), q = exp(sd[v] - ld);
             double res = p - q;
             double err = 4e-6 * (p + q) + 6e-8 * (fabs(st[v] - lt) * p + fabs(sd[v] - ld) * q);
+            if (am) {      /* q_v moves by at most a factor exp(spread_v / T + dlse) */
+              err += q * expm1((double)am[v] / T + dlse);
+            }
             lw[v] = res > 0.0 ? log(res) : -INFINITY;
             le[v] = err > 0.0 ? log(err) : -INFINITY;
             if (res > 0.0) { mass += res; any = 1; }

@@ -93,13 +93,14 @@ def lib() -> ctypes.CDLL:
     L.dspark_draft_packed_projection_bytes.restype = sz
     L.dspark_draft_pack_projection.argtypes = [P, Dims, P, sz, P]
     L.dspark_draft_pack_projection.restype = st
-    L.dspark_draft_markov_sample.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
+    L.dspark_draft_markov_sample.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, P, sz, P, P]
     L.dspark_draft_markov_sample.restype = st
-    L.dspark_draft_markov_sample_confidence.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, P, P, P, sz, P, P]
+    L.dspark_draft_markov_sample_confidence.argtypes = [P, P, P, P, P, P, u64, Dims, P, P, P, P, P, P, P, P, sz, P,
+                                                         P]
     L.dspark_draft_markov_sample_confidence.restype = st
     L.dspark_draft_rnn_workspace_bytes.argtypes = [Dims]
     L.dspark_draft_rnn_workspace_bytes.restype = sz
-    L.dspark_draft_rnn_sample.argtypes = [P, P, P, P, P, P, P, P, u64, Dims, P, P, P, P, sz, P, P]
+    L.dspark_draft_rnn_sample.argtypes = [P, P, P, P, P, P, P, P, u64, Dims, P, P, P, P, P, sz, P, P]
     L.dspark_draft_rnn_sample.restype = st
     L.dspark_schedule_workspace_bytes.argtypes = [i64, i64]
     L.dspark_schedule_workspace_bytes.restype = sz
@@ -229,7 +230,8 @@ def new_status(device) -> torch.Tensor:
 # entry points
 # ---------------------------------------------------------------------------
 def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
-                        want_lse: bool = True, force_simt: bool = False, spare_sm: bool = False,
+                        want_lse: bool = True, want_tok_logit: bool = True, force_simt: bool = False,
+                        spare_sm: bool = False,
                         conf_h=None, conf_w=None, out: Optional[dict] = None,
                         workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                         stream=None) -> dict:
@@ -239,7 +241,8 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     PackedProjection of W (bfloat16, tensor-core path);
     anchor, K_r [B] int32; temperature [B] float32.  Returns a dict with
     draft_tok [B,K_max] int32, draft_logits (U's dtype) or None, draft_lse
-    [B,K_max] float32 or None, and the status / workspace tensors used.
+    [B,K_max] float32 or None, draft_tok_logit [B,K_max] float32 (the drawn tokens'
+    logits) or None, and the status / workspace tensors used.
     spare_sm leaves one SM free of the tensor-core path's persistent kernel, for a
     kernel on another stream (the scheduler) to run beside it.
     With conf_h [B,K_max] float32 (the backbone term of the confidence head) and
@@ -272,6 +275,9 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     lse = out.get("draft_lse") if want_lse else None
     if want_lse and lse is None:
         lse = torch.empty(B, K_max, dtype=torch.float32, device=dev)
+    zx = out.get("draft_tok_logit") if want_tok_logit else None
+    if want_tok_logit and zx is None:
+        zx = torch.empty(B, K_max, dtype=torch.float32, device=dev)
     status = new_status(dev) if status is None else status
     nbytes = draft_workspace_bytes(B, K_max, V, rank, dt, flags)
     ws = _workspace(nbytes, dev, workspace)
@@ -282,8 +288,8 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
     if conf_h is None:
         code = lib().dspark_draft_markov_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r),
                                                 _ptr(temperature), ctypes.c_uint64(seed), dims, _ptr(tok),
-                                                _ptr(logits), _ptr(lse), _ptr(ws), ctypes.c_size_t(ws.numel()),
-                                                _ptr(status), _stream(stream))
+                                                _ptr(logits), _ptr(lse), _ptr(zx), _ptr(ws),
+                                                ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
         _raise(code, "dspark_draft_markov_sample")
     else:
         _dev(conf_h, "conf_h", torch.float32, (B, K_max))
@@ -293,20 +299,22 @@ def draft_markov_sample(U, E, W, anchor, K_r, temperature, seed: int, *, want_lo
             conf = torch.empty(B, K_max, dtype=torch.float32, device=dev)
         code = lib().dspark_draft_markov_sample_confidence(
             _ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(K_r), _ptr(temperature), ctypes.c_uint64(seed), dims,
-            _ptr(conf_h), _ptr(conf_w), _ptr(tok), _ptr(logits), _ptr(lse), _ptr(conf), _ptr(ws),
+            _ptr(conf_h), _ptr(conf_w), _ptr(tok), _ptr(logits), _ptr(lse), _ptr(zx), _ptr(conf), _ptr(ws),
             ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
         _raise(code, "dspark_draft_markov_sample_confidence")
-    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, conf=conf, status=status, workspace=ws)
+    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, draft_tok_logit=zx, conf=conf, status=status,
+                workspace=ws)
 
 
 def draft_rnn_sample(U, E, W, rnn_W, rnn_x, anchor, K_r, temperature, seed: int, *, want_logits: bool = True,
-                     want_lse: bool = True, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
-                     status: Optional[torch.Tensor] = None, stream=None) -> dict:
+                     want_lse: bool = True, want_tok_logit: bool = True, out: Optional[dict] = None,
+                     workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                     stream=None) -> dict:
     """RNN-head draft sampling (C ABI dspark_draft_rnn_sample).
 
     U [B,K_max,V], E [V,rank], W [rank,V], rnn_W [3 rank, 2 rank] (one dtype); rnn_x
     [B,K_max,3 rank] float32; anchor, K_r [B] int32; temperature [B] float32.  Returns
-    draft_tok, draft_logits, draft_lse as draft_markov_sample does.
+    draft_tok, draft_logits, draft_lse, draft_tok_logit as draft_markov_sample does.
     """
     dt = _dtype_code(_dev(U, "U"))
     B, K_max, V = U.shape
@@ -324,15 +332,16 @@ def draft_rnn_sample(U, E, W, rnn_W, rnn_x, anchor, K_r, temperature, seed: int,
     logits = (out.get("draft_logits") if out.get("draft_logits") is not None else torch.empty_like(U)) \
         if want_logits else None
     lse = _out(out, "draft_lse", (B, K_max), torch.float32, dev) if want_lse else None
+    zx = _out(out, "draft_tok_logit", (B, K_max), torch.float32, dev) if want_tok_logit else None
     status = new_status(dev) if status is None else status
     dims = Dims(B, K_max, V, rank, dt, 0)
     ws = _workspace(lib().dspark_draft_rnn_workspace_bytes(dims), dev, workspace)
     code = lib().dspark_draft_rnn_sample(_ptr(U), _ptr(E), _ptr(W), _ptr(rnn_W), _ptr(rnn_x), _ptr(anchor),
                                          _ptr(K_r), _ptr(temperature), ctypes.c_uint64(seed), dims, _ptr(tok),
-                                         _ptr(logits), _ptr(lse), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                         _ptr(logits), _ptr(lse), _ptr(zx), _ptr(ws), ctypes.c_size_t(ws.numel()),
                                          _ptr(status), _stream(stream))
     _raise(code, "dspark_draft_rnn_sample")
-    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, status=status, workspace=ws)
+    return dict(draft_tok=tok, draft_logits=logits, draft_lse=lse, draft_tok_logit=zx, status=status, workspace=ws)
 
 
 def schedule_survival(conf, K_r, sps, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,

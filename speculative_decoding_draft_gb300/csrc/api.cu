@@ -58,7 +58,7 @@ dspark_status check_dims(const dspark_dims &d, bool need_rank) {
 
 extern "C" {
 
-int dspark_version(void) { return 102; }
+int dspark_version(void) { return 200; }
 
 const char *dspark_status_string(dspark_status s) {
   switch (s) {
@@ -107,7 +107,8 @@ static bool draft_packs_into_workspace(const dspark_dims &d) {
 static size_t draft_ws_base(int64_t B, int64_t K_max, int64_t V) {
   return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
          al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
-         al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V));
+         al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V)) +
+         al256(sizeof(float) * (size_t)draft_partial_slots(B, K_max, V));
 }
 
 size_t dspark_draft_workspace_bytes(dspark_dims dims) {
@@ -147,7 +148,8 @@ size_t rnn_state_bytes(const dspark_dims &d) { return al256(sizeof(float) * (siz
 
 dspark_status draft_call(const void *U, const void *E, const void *W, const int32_t *anchor, const int32_t *K_r,
                          const float *temperature, uint64_t seed, dspark_dims dims, int32_t *draft_tok,
-                         void *draft_logits, float *draft_lse, const float *conf_h, const float *conf_w,
+                         void *draft_logits, float *draft_lse, float *draft_zx, const float *conf_h,
+                         const float *conf_w,
                          float *conf, const RnnHead *rnn, void *workspace, size_t workspace_bytes,
                          int32_t *dev_status, void *stream) {
   if (!U || !E || !W || !anchor || !K_r || !temperature || !draft_tok || !dev_status) return DSPARK_ERR_NULL;
@@ -169,6 +171,7 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.draft_tok = draft_tok;
   a.draft_logits = draft_logits;
   a.draft_lse = draft_lse;
+  a.draft_zx = draft_zx;
   a.dev_status = dev_status;
   a.B = dims.B;
   a.K_max = dims.K_max;
@@ -196,6 +199,8 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   p += al256(sizeof(Partial) * (size_t)a.partial_slots);
+  a.zx_part = (float *)p;
+  p += al256(sizeof(float) * (size_t)a.partial_slots);
   if (rnn) {   // the CUDA-core path only: the workspace holds no packed W2, then two state
                // buffers (the cell alternates between them by position) and the feature
     a.rnn_W = rnn->W;
@@ -230,10 +235,11 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
 dspark_status dspark_draft_markov_sample(const void *U, const void *E, const void *W, const int32_t *anchor,
                                          const int32_t *K_r, const float *temperature, uint64_t seed,
                                          dspark_dims dims, int32_t *draft_tok, void *draft_logits,
-                                         float *draft_lse, void *workspace, size_t workspace_bytes,
-                                         int32_t *dev_status, void *stream) {
-  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, nullptr,
-                    nullptr, nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+                                         float *draft_lse, float *draft_tok_logit, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse,
+                    draft_tok_logit, nullptr, nullptr, nullptr, nullptr, workspace, workspace_bytes, dev_status,
+                    stream);
 }
 
 size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims) {
@@ -245,15 +251,17 @@ size_t dspark_draft_rnn_workspace_bytes(dspark_dims dims) {
 dspark_status dspark_draft_rnn_sample(const void *U, const void *E, const void *W, const void *rnn_W,
                                       const float *rnn_x, const int32_t *anchor, const int32_t *K_r,
                                       const float *temperature, uint64_t seed, dspark_dims dims,
-                                      int32_t *draft_tok, void *draft_logits, float *draft_lse, void *workspace,
-                                      size_t workspace_bytes, int32_t *dev_status, void *stream) {
+                                      int32_t *draft_tok, void *draft_logits, float *draft_lse,
+                                      float *draft_tok_logit, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, void *stream) {
   if (!rnn_W || !rnn_x) return DSPARK_ERR_NULL;
   if (dims.flags & DSPARK_FLAG_W_PACKED) return DSPARK_ERR_UNSUPPORTED;
   if (dims.rank > kMaxRnnRank) return DSPARK_ERR_DIMS;
   dims.flags |= DSPARK_FLAG_FORCE_SIMT;   // the cell feeds the CUDA-core bias path
   const RnnHead rnn{rnn_W, rnn_x};
-  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, nullptr,
-                    nullptr, nullptr, &rnn, workspace, workspace_bytes, dev_status, stream);
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse,
+                    draft_tok_logit, nullptr, nullptr, nullptr, &rnn, workspace, workspace_bytes, dev_status,
+                    stream);
 }
 
 dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E, const void *W,
@@ -261,11 +269,11 @@ dspark_status dspark_draft_markov_sample_confidence(const void *U, const void *E
                                                     const float *temperature, uint64_t seed, dspark_dims dims,
                                                     const float *conf_h, const float *conf_w,
                                                     int32_t *draft_tok, void *draft_logits, float *draft_lse,
-                                                    float *conf, void *workspace, size_t workspace_bytes,
-                                                    int32_t *dev_status, void *stream) {
+                                                    float *draft_tok_logit, float *conf, void *workspace,
+                                                    size_t workspace_bytes, int32_t *dev_status, void *stream) {
   if (!conf_h || !conf_w || !conf) return DSPARK_ERR_NULL;
-  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse, conf_h,
-                    conf_w, conf, nullptr, workspace, workspace_bytes, dev_status, stream);
+  return draft_call(U, E, W, anchor, K_r, temperature, seed, dims, draft_tok, draft_logits, draft_lse,
+                    draft_tok_logit, conf_h, conf_w, conf, nullptr, workspace, workspace_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

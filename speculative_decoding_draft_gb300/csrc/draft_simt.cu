@@ -465,24 +465,35 @@ __global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_
       } else {
         const uint32_t g = (uint32_t)(v0 / kBlockW);
         const uint32_t wb = word_of(philox(a.key, g >> 2, (uint32_t)k, (uint32_t)r, kTagDraft), (int)(g & 3u));
-        brace_softmax_block(br, z, mz, a2, wb, v0, [&] {
-          return word_of(philox(a.key, g >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(g & 3u));
-        });
+        brace_softmax_block(
+            br, z, mz, a2, wb, v0,
+            [&] { return word_of(philox(a.key, g >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(g & 3u)); },
+            [&](int q) {   // the drawn element's logit, recomputed exactly as above from U and the bias tile
+              float zz = ld<DT>(a.U, urow + v0 + q) + w_s[tr * kTileCols + tb * 32 + (((q >> 2) ^ (tb & 7)) << 2) + (q & 3)];
+              if (DT == DSPARK_BF16) zz = round_to_bf16(zz);
+              return zz;
+            });
       }
     }
   }
   // the row's eight blocks (lanes 8m .. 8m + 7 of the warp), merged by shuffles
   Race st = from_partial(to_partial(br));
+  float zx = br.zx;   // the logit at st.idx
 #pragma unroll
   for (int d = kBlocksPerRow / 2; d > 0; d >>= 1) {
     Race o = race_shfl_down(st, d);
-    if (tb + d < kBlocksPerRow) race_merge(st, o);
+    const float ozx = __shfl_down_sync(0xffffffffu, zx, d);
+    if (tb + d < kBlocksPerRow) {
+      if (race_takes(st, o)) zx = ozx;
+      race_merge(st, o);
+    }
   }
   const int leader = lane & ~(kBlocksPerRow - 1);
   const int i = i0 + tr;
   int last = 0;
   if (valid && tb == 0) {
     a.partials[(int64_t)i * col_tiles + blockIdx.x] = to_partial(st);
+    a.zx_part[(int64_t)i * col_tiles + blockIdx.x] = zx;
     __threadfence();
     last = (atomicAdd(&a.counters[i], 1) == col_tiles - 1);
   }
@@ -532,6 +543,9 @@ __global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_
   if (tb == 0) {
     a.draft_tok[(int64_t)r * K + k - 1] = tot.idx;
     if (a.draft_lse) a.draft_lse[(int64_t)r * K + k - 1] = greedy ? tot.best : tot.m + logf(tot.S);
+    // the token's logit: the partial of the column tile that holds the token carries it
+    if (a.draft_zx && tot.idx >= 0)
+      a.draft_zx[(int64_t)r * K + k - 1] = load_f32_relaxed(a.zx_part + (int64_t)i * col_tiles + tot.idx / kTileCols);
     if (a.conf_out) a.conf_out[(int64_t)r * K + k - 1] = conf;
     a.counters[i] = 0;
   }

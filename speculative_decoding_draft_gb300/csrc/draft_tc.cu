@@ -39,7 +39,7 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kBlkN = 64;                        // vocabulary columns per packed block
 constexpr int kMaxBlk = 4;                       // blocks per MMA tile (N <= 256)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kAccBufs = 2;
 constexpr int kAccCols = kBlkN * kMaxBlk;        // 256
 constexpr int kTmemCols = kAccBufs * kAccCols;   // 512
@@ -50,9 +50,12 @@ constexpr int kAChunk = kTileM * 128;            // 16 KB: 128 rows x 64 rank va
 constexpr int kASize = 4 * kAChunk;              // rank <= 256
 constexpr int kPiece = kBlkN * 128;              // 8 KB: one packed block, 64 rank rows
 constexpr int kStageBytes = kMaxBlk * kPiece;    // 32 KB
+constexpr int kUDepth = 3;                       // U blocks each epilogue warp stages ahead
+constexpr int kUSlot = 32 * 64;                  // one 32-wide block of a warp's 32 rows (2 KB)
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
-constexpr int kOffSh = kOffW + kStages * kStageBytes;
+constexpr int kOffU = kOffW + kStages * kStageBytes;
+constexpr int kOffSh = kOffU + kEpiWarps * kUDepth * kUSlot;
 constexpr long long kTimeoutCycles = 4000000000LL;
 
 struct TcShared {
@@ -70,6 +73,7 @@ struct TcShared {
   int row_prev[kTileM];
   float row_invT[kTileM];
   Partial part[kWpq * kTileM];   // per-row partials: [column worker][row of the replica group]
+  float part_zx[kWpq * kTileM];  // the logit at each partial's index
 };
 
 constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
@@ -208,6 +212,21 @@ __device__ __forceinline__ void st_u8_hint(void *ptr, uint4 lo, uint4 hi, uint64
                "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w), "l"(policy)
                : "memory");
 }
+// 16-byte global -> shared asynchronous copy (L1 bypassed) with an L2 policy; its
+// completion is tracked by the thread's commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ int ld_acquire(const int32_t *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -230,16 +249,6 @@ __device__ __forceinline__ __nv_bfloat162 bf162_of(uint32_t w) { return *reinter
 
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-}
-
-// U row segment of one epilogue thread for one 32-wide block: 32 bf16 at column c0
-// of its row (16-byte loads; columns past V are not read).
-__device__ __forceinline__ void load_u32(const unsigned short *row, int c0, int V, uint4 (&u)[4], uint64_t pol) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (c0 + 8 * q < V) u[q] = ld_u4_hint(row + c0 + 8 * q, pol);
-    else u[q] = make_uint4(0u, 0u, 0u, 0u);
-  }
 }
 
 // Work split of one draft position: M-tiles of 128 active rows, each shared by gm CTAs
@@ -448,11 +457,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const float a2 = invT * kLog2e;           // scaled logits in log2 units
         const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
         const unsigned short *uptr = (const unsigned short *)a.U + urow;
-        uint4 ucur[4], unext[4];
         // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles; worker wk
-        // takes blocks wk, wk + nwk, ...
+        // takes blocks wk, wk + nwk, ...  Its i-th block's U (each lane its row's 64 bytes) is
+        // staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by cp.async; 16-byte
+        // unit q of lane l sits at l * 64 + ((q ^ ((l >> 1) & 3)) << 4), which keeps the quarter-warp
+        // reads and writes free of bank conflicts.  Every lane commits one group per block, so
+        // wait_group(kUDepth - 1) means the oldest staged block has landed.
         const int nsub_u = 2 * (b1 - b0);
-        if (valid && wk < nsub_u) load_u32(uptr, b0 * kBlkN + wk * 32, V, ucur, pol_stream);   // before the barrier
+        const uint32_t uring = sb + kOffU + (uint32_t)(eq * kUDepth * kUSlot) + (uint32_t)(lane * 64);
+        const int usw = (lane >> 1) & 3;
+        auto stage_u = [&](int i) {
+          const int gsb = wk + i * nwk;
+          if (valid && gsb < nsub_u) {
+            const int c0 = b0 * kBlkN + gsb * 32;
+            const uint32_t dst = uring + (uint32_t)((i % kUDepth) * kUSlot);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (c0 + 8 * q < V) cp_async16(dst + ((q ^ usw) << 4), uptr + c0 + 8 * q, pol_stream);
+          }
+          cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kUDepth; ++i) stage_u(i);   // before the barrier: U does not depend on the tokens
+        int ui = 0;                                    // this worker's blocks consumed in the unit
         if (!waited) {
           // every CTA has folded its position k-1 maxima into the packed keys
           if (et == 0) {
@@ -509,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             continue;
           }
-          for (; gs < s1; gs += nwk) {
+          for (; gs < s1; gs += nwk, ++ui) {
             uint32_t acc[32];
             tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kAccCols + (gs - s0) * 32), acc);
             tmem_wait_ld();
@@ -518,8 +545,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             }
-            if (!valid) continue;
-            if (gs + nwk < nsub_u) load_u32(uptr, b0 * kBlkN + (gs + nwk) * 32, V, unext, pol_stream);   // prefetch
+            cp_async_wait<kUDepth - 1>();           // block ui's U has landed (this lane's copies)
+            uint4 ucur[4];
+            {
+              const uint32_t src = uring + (uint32_t)((ui % kUDepth) * kUSlot);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) ucur[q] = ld_shared_u4(src + ((q ^ usw) << 4));
+            }
             const int c0 = b0 * kBlkN + gs * 32;      // this thread's 32-wide block of the two-level draw
             uint32_t packed[16];
 #pragma unroll
@@ -530,6 +562,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
             }
+            stage_u(ui + kUDepth);                   // the slot is free again: refill it
+            if (!valid) continue;
             if (a.draft_logits) {
               unsigned short *drow = (unsigned short *)a.draft_logits + urow;
               if (wide_s) {                           // whole sectors: 32-byte stores
@@ -576,21 +610,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
                 return word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(gblk & 3u));
               });
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ucur[q] = unext[q];
           }
         }
+        cp_async_wait<0>();                         // nothing of this unit stays in flight
         // merge the 2F worker partials of each row; the row's home thread folds its maximum
         // into the packed (score, index) key of the position with one 64-bit atomicMax -- all
         // the next position needs -- and keeps its softmax partial for the merge after the last position
         sh.part[wk * rpg + row] = to_partial(st);
+        sh.part_zx[wk * rpg + row] = st.zx;
         named_sync_epi();
         if (wk == 0 && valid) {
           Race tot = from_partial(sh.part[row]);
-          for (int q = 1; q < nwk; ++q) race_merge(tot, from_partial(sh.part[q * rpg + row]));
+          float zx = sh.part_zx[row];
+          for (int q = 1; q < nwk; ++q) {
+            const Race o = from_partial(sh.part[q * rpg + row]);
+            if (o.best > tot.best || (o.best == tot.best && o.idx >= 0 && (tot.idx < 0 || o.idx < tot.idx)))
+              zx = sh.part_zx[q * rpg + row];      // race_merge takes o's index
+            race_merge(tot, o);
+          }
           if (tot.idx >= 0) atomicMax(&a.best_key[(int64_t)r * K + k - 1], score_key(tot.best, tot.idx));
-          a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j] =
-              to_partial(tot);
+          // the CTA's partial for the final merge: the logit at its index (for greedy rows that is
+          // the CTA's maximum), the index, the softmax pair
+          Partial pp = to_partial(tot);
+          pp.best = zx;
+          a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j] = pp;
         }
       }
       // this CTA is done with position k (every CTA arrives, with or without work): the
@@ -625,20 +668,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           const StepPlan pl = plan_step(sh.nact, k, G, nb);
           if (i >= pl.n_k) continue;
           const int r = a.perm[i];
-          const Partial *ptr[1] = {a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm};
-          Race tot[1];
-          warp_merge_rows<1>(ptr, pl.gm, tot);
+          const int64_t at = (int64_t)r * K + k - 1;
+          const int x = key_index(load_key(a.best_key + at));
+          // the gm CTA partials of the row: softmax pair, greedy maximum (the largest logit
+          // field) and the logit of the token x, carried by the one partial whose index is x
+          const Partial *pr = a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm;
+          Race tot;
+          race_init(tot);
+          float zx = 0.0f;
+          bool found = false;
+          for (int q = lane; q < pl.gm; q += 32) {
+            const Partial p = load_partial(pr + q);
+            if (p.idx == x) { zx = p.best; found = true; }
+            race_merge(tot, from_partial(p));
+          }
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) race_merge(tot, race_shfl_down(tot, d));
+          const unsigned fb = __ballot_sync(0xffffffffu, found);
+          zx = __shfl_sync(0xffffffffu, zx, fb ? __ffs(fb) - 1 : 0);
           if (a.conf_out) {
-            const int prev = k == 1 ? a.anchor[r] : key_index(load_key(a.best_key + (int64_t)r * K + k - 2));
+            const int prev = k == 1 ? a.anchor[r] : key_index(load_key(a.best_key + at - 1));
             const __nv_bfloat16 *erow = (const __nv_bfloat16 *)a.E + (int64_t)prev * a.rank;
             const float c = warp_confidence([&](int q) { return __bfloat162float(erow[q]); }, a.conf_w,
                                             (int)a.rank, a.conf_h[(int64_t)r * K + k - 1], lane);
             if (lane == 0) a.conf_out[(int64_t)r * K + k - 1] = c;
           }
           if (lane == 0) {
-            const int64_t at = (int64_t)r * K + k - 1;
-            a.draft_tok[at] = key_index(load_key(a.best_key + at));
-            if (a.draft_lse) a.draft_lse[at] = a.temperature[r] == 0.0f ? tot[0].best : tot[0].m + logf(tot[0].S);
+            a.draft_tok[at] = x;
+            if (a.draft_lse) a.draft_lse[at] = a.temperature[r] == 0.0f ? tot.best : tot.m + logf(tot.S);
+            if (a.draft_zx) a.draft_zx[at] = zx;
           }
         }
       }
@@ -665,6 +723,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
       }
     }
   }
+  if (warp >= 2) cp_async_wait<0>();   // U copies still in flight after an abort
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

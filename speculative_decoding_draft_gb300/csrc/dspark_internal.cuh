@@ -207,9 +207,14 @@ __device__ __forceinline__ void argmax_update(Race &r, const float (&s)[N], int 
     if (s[q] > r.best) { r.best = s[q]; r.idx = v0 + q; }
 }
 
+// Does merging b into a take b's index (score desc, index asc)?
+__device__ __forceinline__ bool race_takes(const Race &a, const Race &b) {
+  return b.best > a.best || (b.best == a.best && b.idx >= 0 && (a.idx < 0 || b.idx < a.idx));
+}
+
 // Merge b into a: best by (score desc, index asc); softmax (m, S).
 __device__ __forceinline__ void race_merge(Race &a, const Race &b) {
-  if (b.best > a.best || (b.best == a.best && b.idx >= 0 && (a.idx < 0 || b.idx < a.idx))) {
+  if (race_takes(a, b)) {
     a.best = b.best;
     a.idx = b.idx;
   }
@@ -299,6 +304,7 @@ struct BRace {
   int idx;     // index drawn inside that block
   float M2;    // running max of the scaled logits, log2 units
   float S;     // sum of 2^(y - M2) over the scaled logits y seen
+  float zx;    // the (stored-dtype) logit at idx
 };
 
 __device__ __forceinline__ void brace_init(BRace &r) {
@@ -306,6 +312,7 @@ __device__ __forceinline__ void brace_init(BRace &r) {
   r.idx = -1;
   r.M2 = -INFINITY;
   r.S = 0.0f;
+  r.zx = 0.0f;
 }
 
 __device__ __forceinline__ Partial to_partial(const BRace &r) {
@@ -356,9 +363,11 @@ __device__ __forceinline__ int pick_in_block(const float (&w)[N], float target) 
 // Returns true when the block took the lead.
 // Folds a block with scaled maximum Mb (log2 units) and weights w (sum Sb) into the
 // running softmax, enters the race and, when the block leads, draws the index.
-template <int N, class PickWord>
+// zfn(q) returns the logit of the block's element q; it is evaluated only for a block that
+// takes the lead, to record the logit of the drawn index.
+template <int N, class PickWord, class ZFn>
 __device__ __forceinline__ bool brace_fold_block(BRace &r, const float (&w)[N], float Mb, float Sb, uint32_t wb,
-                                                 int v0, PickWord pick_word) {
+                                                 int v0, PickWord pick_word, ZFn zfn) {
   if (Mb > r.M2) {
     r.S = r.S * fast_ex2(r.M2 - Mb) + Sb;
     r.M2 = Mb;
@@ -367,13 +376,16 @@ __device__ __forceinline__ bool brace_fold_block(BRace &r, const float (&w)[N], 
   }
   const float ell = (Mb + fast_lg2(Sb)) * kLn2;
   if (!brace_enter(r, ell, wb)) return false;
-  r.idx = v0 + pick_in_block(w, uniform_accept(pick_word()) * Sb);
+  const int q = pick_in_block(w, uniform_accept(pick_word()) * Sb);
+  r.idx = v0 + q;
+  r.zx = zfn(q);
   return true;
 }
 
-template <int N, class PickWord>
+// The block's weights overwrite z; zfn(q) must recover the logit of element q elsewhere.
+template <int N, class PickWord, class ZFn>
 __device__ __forceinline__ bool brace_softmax_block(BRace &r, float (&z)[N], float mz, float a, uint32_t wb,
-                                                    int v0, PickWord pick_word) {
+                                                    int v0, PickWord pick_word, ZFn zfn) {
   if (mz == -INFINITY) return false;
   const float Mb = mz * a;
   float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -382,8 +394,13 @@ __device__ __forceinline__ bool brace_softmax_block(BRace &r, float (&z)[N], flo
     z[q] = fast_ex2(fmaf(z[q], a, -Mb));
     s[q & 3] += z[q];
   }
-  return brace_fold_block(r, z, Mb, (s[0] + s[1]) + (s[2] + s[3]), wb, v0, pick_word);
+  return brace_fold_block(r, z, Mb, (s[0] + s[1]) + (s[2] + s[3]), wb, v0, pick_word, zfn);
 }
+
+// Logits that are not needed after the draw (the bonus draw of verification).
+struct NoLogit {
+  __device__ __forceinline__ float operator()(int) const { return 0.0f; }
+};
 
 // ---- paired fp32 arithmetic: one sm_100 instruction for two independent lanes, each
 // rounded exactly like the scalar operation ----
@@ -436,7 +453,20 @@ __device__ __forceinline__ bool brace_softmax_bf16x32(BRace &r, const uint32_t (
   float s0, s1, s2, s3;
   f2_unpack(s01, s0, s1);
   f2_unpack(s23, s2, s3);
-  return brace_fold_block(r, w, Mb, (s0 + s1) + (s2 + s3), wb, v0, pick_word);
+  if (!brace_fold_block(r, w, Mb, (s0 + s1) + (s2 + s3), wb, v0, pick_word, NoLogit{})) return false;
+  const int q = r.idx - v0;          // the drawn element: its logit from the packed words
+  // select word q >> 1 by a tree on its bits (register selects, no indexed access)
+  uint32_t t8[8], t4[4], t2[2];
+  const uint32_t h = (uint32_t)q >> 1;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t8[j] = (h & 1u) ? pk[2 * j + 1] : pk[2 * j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t4[j] = (h & 2u) ? t8[2 * j + 1] : t8[2 * j];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) t2[j] = (h & 4u) ? t4[2 * j + 1] : t4[2 * j];
+  const uint32_t wq = (h & 8u) ? t2[1] : t2[0];
+  r.zx = __uint_as_float((q & 1) ? (wq & 0xffff0000u) : (wq << 16));
+  return true;
 }
 
 // Greedy block: running maximum, smallest index on ties.
@@ -444,6 +474,7 @@ template <int N>
 __device__ __forceinline__ void brace_argmax_block(BRace &r, const float (&z)[N], float mz, int v0) {
   if (!(mz > r.best)) return;
   r.best = mz;
+  r.zx = mz;
   int q0 = N - 1;
 #pragma unroll
   for (int q = N - 1; q >= 0; --q)
@@ -508,6 +539,7 @@ struct DraftArgs {
   int32_t *draft_tok;
   void *draft_logits;
   float *draft_lse;
+  float *draft_zx;    // [B, K_max] the logit of each drawn token (optional)
   int32_t *dev_status;
   int64_t B, K_max, V, rank;
   int dtype;
@@ -520,6 +552,7 @@ struct DraftArgs {
   unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path
   int32_t *gbar;      // [K_max + 1] grid-barrier arrival counters of the tensor-core path
   Partial *partials;  // [partial_slots]
+  float *zx_part;     // [partial_slots] CUDA-core path: the logit at each partial's index
   int64_t partial_slots;
   // confidence head with the Markov term (optional): conf_out[r, k] =
   // sigmoid(conf_h[r, k] + conf_w . E[x_{k-1}])
@@ -562,6 +595,13 @@ __device__ __forceinline__ unsigned long long score_key(float s, int idx) {
   const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
+// A float written by another CTA (gpu-scope relaxed load; see load_partial).
+__device__ __forceinline__ float load_f32_relaxed(const float *p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Packed key written by other CTAs: a gpu-scope relaxed load (after an acquire that
 // observed the writers' release it sees their values).
 __device__ __forceinline__ unsigned long long load_key(const unsigned long long *p) {

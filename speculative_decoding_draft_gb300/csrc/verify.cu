@@ -598,7 +598,7 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
       return word_of(philox(key, g >> 2, (uint32_t)job.pos, (uint32_t)r, kTagResidPick), (int)(g & 3u));
     };
     if (mode == 2) {
-      brace_softmax_block(rc, t, block_max(t), a2, wb, v0, pick_word);
+      brace_softmax_block(rc, t, block_max(t), a2, wb, v0, pick_word, NoLogit{});
       continue;
     }
     float d[kBlockW];

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     import speculative_decoding_draft_gb300 as ds
-    assert lib.dspark_version() == 102
+    assert lib.dspark_version() == 200
     for code, name in ds.STATUS_NAMES.items():
         assert ds.status_string(code) == name
 
@@ -68,32 +68,32 @@ def test_host_validation_needs_no_device(lib):
     import speculative_decoding_draft_gb300 as ds
     dims = ds.Dims(4, 7, 1000, 16, ds.F32, 0)
     null = None
-    assert lib.dspark_draft_markov_sample(null, null, null, null, null, null, 0, dims, null, null, null, null, 0,
-                                          null, null) == 1
+    assert lib.dspark_draft_markov_sample(null, null, null, null, null, null, 0, dims, null, null, null, null, null,
+                                          0, null, null) == 1
     one = ctypes.c_void_p(256)
     bad = ds.Dims(4, 17, 1000, 16, ds.F32, 0)
-    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, one, 1 << 20, one,
-                                          null) == 2
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, null, one, 1 << 20,
+                                          one, null) == 2
     bad = ds.Dims(4, 7, 1000, 16, 7, 0)
-    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, one, 1 << 20, one,
-                                          null) == 3
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, bad, one, null, null, null, one, 1 << 20,
+                                          one, null) == 3
     # packing: null pointers, unsupported shapes and dtypes, short output
     pdims = ds.Dims(1, 1, 1024, 256, ds.BF16, 0)
     assert lib.dspark_draft_pack_projection(null, pdims, one, 1 << 30, null) == 1
     assert lib.dspark_draft_pack_projection(one, ds.Dims(1, 1, 1024, 96, ds.BF16, 0), one, 1 << 30, null) == 13
     assert lib.dspark_draft_pack_projection(one, ds.Dims(1, 1, 1024, 256, ds.F32, 0), one, 1 << 30, null) == 13
     assert lib.dspark_draft_pack_projection(one, pdims, one, 1024, null) == 10
-    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, dims, one, null, null, one, 16, one,
-                                          null) == 10
+    assert lib.dspark_draft_markov_sample(one, one, one, one, one, one, 0, dims, one, null, null, null, one, 16,
+                                          one, null) == 10
     assert lib.dspark_schedule_survival(one, one, one, 10, 4, 0, one, one, null, null, null, one, 1 << 20, one,
                                         null) == 2
     # RNN head: null cell inputs, a packed projection, the workspace query
     rd = ds.Dims(4, 7, 1000, 16, ds.F32, 0)
-    assert lib.dspark_draft_rnn_sample(one, one, one, null, one, one, one, one, 0, rd, one, null, null, one, 1 << 20,
-                                       one, null) == 1
+    assert lib.dspark_draft_rnn_sample(one, one, one, null, one, one, one, one, 0, rd, one, null, null, null, one,
+                                       1 << 20, one, null) == 1
     assert lib.dspark_draft_rnn_sample(one, one, one, one, one, one, one, one, 0,
-                                       ds.Dims(4, 7, 1000, 16, ds.BF16, ds.FLAG_W_PACKED), one, null, null, one,
-                                       1 << 20, one, null) == 13
+                                       ds.Dims(4, 7, 1000, 16, ds.BF16, ds.FLAG_W_PACKED), one, null, null, null,
+                                       one, 1 << 20, one, null) == 13
     assert lib.dspark_draft_rnn_workspace_bytes(rd) >= lib.dspark_draft_workspace_bytes(rd) + 2 * 4 * 4 * 16
     assert lib.dspark_draft_rnn_workspace_bytes(ds.Dims(4, 7, 1000, 16, ds.BF16, ds.FLAG_W_PACKED)) == 0
     # scheduler variants

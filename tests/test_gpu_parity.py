@@ -15,7 +15,7 @@ import oracle
 import speculative_decoding_draft_gb300 as ds
 from speculative_decoding_draft_gb300 import workloads as wl
 
-from parity_helpers import compare_draft, compare_verify, host, oracle_draft
+from parity_helpers import comparable, compare_draft, compare_verify, host, oracle_draft, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -118,6 +118,7 @@ def test_draft_parity(case):
     gpu = _run_draft(_to(inp), cfg.philox_seed, force_simt=simt)
     orc = oracle_draft(inp, cfg.philox_seed)
     n = compare_draft(gpu, orc, inp["K_r"].numpy(), cfg.dtype)
+    assert n == comparable(orc["flags"], inp["K_r"].numpy())
     assert n >= 0.9 * int(inp["K_r"].sum())
 
 
@@ -286,14 +287,13 @@ def test_draft_full_size_sampled(name):
         assert ds.check(gpu["status"]) == "DSPARK_OK"
     else:
         gpu = _run_draft(g, cfg.philox_seed)
-    rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(cfg.B, size=4, replace=False))
-    rows[0] = 0
-    rows[-1] = cfg.B - 1
+    rows = sample_rows(cfg, 16)
     sub = {k: (v[torch.from_numpy(rows).to(DEV)] if k not in ("E", "W") else v) for k, v in g.items()}
     orc = oracle_draft(sub, cfg.philox_seed, req_id=rows.astype(np.int64))
-    n = compare_draft(gpu, orc, sub["K_r"].cpu().numpy(), cfg.dtype, rows=rows)
-    assert n > 0
+    st = {}
+    n = compare_draft(gpu, orc, sub["K_r"].cpu().numpy(), cfg.dtype, rows=rows, stats=st)
+    assert n == comparable(orc["flags"], sub["K_r"].cpu().numpy()), (n, st)
+    assert n >= 0.8 * int(sub["K_r"].sum()), (n, st)
     del g, gpu
     torch.cuda.empty_cache()
 
@@ -396,5 +396,27 @@ def test_host_errors():
     tok = torch.empty(4, 3, dtype=torch.int32, device=DEV)
     p = lambda t: __import__("ctypes").c_void_p(t.data_ptr())
     code = L.dspark_draft_markov_sample(p(g["U"]), p(g["E"]), p(g["W"]), p(g["anchor"]), p(g["K_r"]),
-                                        p(g["temperature"]), 0, dims, p(tok), None, None, p(small), 256, p(st), None)
+                                        p(g["temperature"]), 0, dims, p(tok), None, None, None, p(small), 256, p(st),
+                                        None)
     assert ds.STATUS_NAMES[code] == "DSPARK_ERR_WORKSPACE"
+
+
+@pytest.mark.parametrize("case,simt", [("bf16-tc", False), ("bf16-simt", True), ("fp32-simt", False)])
+def test_draft_tok_logit_is_the_stored_logit(case, simt):
+    # the drawn token's logit output equals the stored logit row at that token, bit for bit,
+    # on both kernel paths and for greedy rows; and it is the same with no logits stored
+    kw = dict(name="ragged", B=150, K_max=4, V=4104) if case.startswith("bf16") else dict(name="tiny", B=9)
+    cfg = wl.small_config(**kw)
+    g = _to(wl.draft_inputs(cfg, "cpu"))
+    d = _run_draft(g, 21, force_simt=simt)
+    tok = d["draft_tok"].long()
+    K_r = g["K_r"].cpu()
+    live = torch.arange(cfg.K_max, device=DEV)[None, :] < g["K_r"][:, None].long()
+    at = torch.gather(d["draft_logits"].float(), 2, tok.clamp(min=0)[..., None])[..., 0]
+    assert torch.equal(at[live], d["draft_tok_logit"][live])
+    assert int(K_r.sum()) == int(live.sum())
+    n = ds.draft_markov_sample(g["U"], g["E"], g["W"], g["anchor"], g["K_r"], g["temperature"], 21,
+                               want_logits=False, force_simt=simt)
+    assert ds.check(n["status"]) == "DSPARK_OK"
+    assert torch.equal(n["draft_tok"], d["draft_tok"])
+    assert torch.equal(n["draft_tok_logit"][live], d["draft_tok_logit"][live])

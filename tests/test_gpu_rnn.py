@@ -14,7 +14,7 @@ import oracle
 import speculative_decoding_draft_gb300 as ds
 from speculative_decoding_draft_gb300 import workloads as wl
 
-from parity_helpers import TOKEN_FLAGS, compare_draft, host
+from parity_helpers import comparable, compare_draft, host
 
 pytestmark = pytest.mark.gpu
 
@@ -32,22 +32,7 @@ def _oracle_rnn(inp, head, seed, rows=None, req_id=None):
     return oracle.draft_rnn_sample(host(inp["U"][sel]), host(inp["E"]), host(inp["W"]), host(head["rnn_W"]),
                                    head["rnn_x"][sel].cpu().numpy(), inp["anchor"][sel].cpu().numpy(),
                                    inp["K_r"][sel].cpu().numpy(), inp["temperature"][sel].cpu().numpy(), seed,
-                                   req_id=req_id)
-
-
-def _comparable(flags, K_r):
-    """Positions compare_draft compares: each request up to its first flagged position, whose
-    token is compared unless the flag says the token itself may differ."""
-    n = 0
-    for b, kr in enumerate(K_r):
-        for k in range(int(kr)):
-            f = int(flags[b, k])
-            if f & TOKEN_FLAGS:
-                break
-            n += 1
-            if f:
-                break
-    return n
+                                   req_id=req_id, want_spread=inp["U"].dtype == torch.bfloat16)
 
 
 CASES = {
@@ -70,7 +55,7 @@ def test_rnn_draft_parity(case):
     assert ds.check(out["status"]) == "DSPARK_OK"
     orc = _oracle_rnn(inp, head, cfg.philox_seed)
     n = compare_draft(out, orc, inp["K_r"].numpy(), cfg.dtype, f32_atol=2e-5)
-    assert n == _comparable(orc["flags"], inp["K_r"].numpy())
+    assert n == comparable(orc["flags"], inp["K_r"].numpy())
 
 
 def test_rnn_draft_full_size_qwen_sampled():
@@ -80,13 +65,13 @@ def test_rnn_draft_full_size_qwen_sampled():
     out = ds.draft_rnn_sample(g["U"], g["E"], g["W"], h["rnn_W"], h["rnn_x"], g["anchor"], g["K_r"],
                               g["temperature"], cfg.philox_seed)
     assert ds.check(out["status"]) == "DSPARK_OK"
-    rows = np.array([0, 31, cfg.B - 1])
+    rows = np.array([0, 17, 31, 48, cfg.B - 1])
     idx = torch.from_numpy(rows).to(DEV)
     sub = {k: (v[idx] if k not in ("E", "W") else v) for k, v in g.items()}
     hsub = dict(rnn_W=h["rnn_W"], rnn_x=h["rnn_x"][idx])
     orc = _oracle_rnn(sub, hsub, cfg.philox_seed, req_id=rows.astype(np.int64))
     n = compare_draft(out, orc, sub["K_r"].cpu().numpy(), cfg.dtype, rows=rows)
-    assert n > 0
+    assert n == comparable(orc["flags"], sub["K_r"].cpu().numpy())
     del g, out
     torch.cuda.empty_cache()
 

@@ -45,7 +45,8 @@ def test_barrier_wait_runs_out_and_the_context_stays_usable():
     t0 = time.perf_counter()
     code = ds.lib().dspark_draft_markov_sample(_p(g["U"]), _p(g["E"]), _p(g["W"]), _p(g["anchor"]), _p(g["K_r"]),
                                                _p(g["temperature"]), ctypes.c_uint64(cfg.philox_seed), dims, _p(tok),
-                                               _p(None), _p(None), _p(ws), ctypes.c_size_t(ws.numel()), _p(status),
+                                               _p(None), _p(None), _p(None), _p(ws), ctypes.c_size_t(ws.numel()),
+                                               _p(status),
                                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert ds.STATUS_NAMES[code] == "DSPARK_OK"          # host-side validation passed
     assert ds.check(status) == "DSPARK_ERR_DEVICE_TIMEOUT"

@@ -10,6 +10,7 @@ import itertools
 import math
 
 import numpy as np
+import torch
 import pytest
 from scipy import stats
 
@@ -217,3 +218,62 @@ def test_argument_errors():
         with pytest.raises(oracle.OracleError) as e:
             oracle.draft_markov_sample(U, E, W, **args)
         assert e.value.name == name
+
+
+def _bf16_bits_from_f32(x):
+    # round-to-nearest-even fp32 -> bf16 by torch (a library routine, not the oracle's rounding)
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+
+
+def _f32_of_bits(b):
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def test_ambiguity_covers_fp32_evaluations():
+    # Every bf16 logit an fp32 evaluation of U + W1[x] . W2 stores, whatever the summation order,
+    # lies within the oracle's spread of the oracle's value (so equals it where the spread is 0);
+    # forced cancellations (U = -bias) get spreads of several bf16 steps.
+    rng = np.random.default_rng(5)
+    V, rank, K = 8192, 256, 2
+    bits = lambda a: _bf16_bits_from_f32(a.astype(np.float32))
+    E = bits(rng.normal(0, 0.02, (V, rank)))
+    W = bits(rng.normal(0, 0.02, (rank, V)))
+    U = bits(rng.normal(0, 3.0, (1, K, V)))
+    anchor = 17
+    Ef, Wf = _f32_of_bits(E).astype(np.float64), _f32_of_bits(W).astype(np.float64)
+    cancel = rng.choice(V, 64, replace=False)
+    U[0, 0, cancel] = bits(-(Ef[anchor] @ Wf)[cancel])          # U + bias cancels to near zero
+    out = oracle.draft_markov_sample(U, E, W, [anchor], [K], [0.0], seed=0, want_spread=True)
+    spread = out["spread"].astype(np.float64)
+    stored = _f32_of_bits(out["draft_logits"]).astype(np.float64)
+    steps = np.abs(stored) * 2.0 ** -8       # at least one bf16 step is below this
+    assert (spread[0, 0, cancel] > 2 * steps[0, 0, cancel]).mean() > 0.9
+    prev = [anchor, int(out["draft_tok"][0, 0])]
+    Uf = _f32_of_bits(U)
+    W32 = _f32_of_bits(W)
+    mism = 0
+    for k in range(K):
+        e = _f32_of_bits(E[prev[k]])
+        terms = e[:, None] * W32                                # exact in fp32 (bf16 x bf16)
+        orders = [np.arange(rank), np.arange(rank)[::-1], rng.permutation(rank)]
+        sums = []
+        for order in orders:                                    # sequential fp32 accumulation
+            acc = np.zeros(V, np.float32)
+            for i in order:
+                acc = (acc + terms[i]).astype(np.float32)
+            sums.append(acc)
+        # chunks of 16 summed pairwise, then the chunk sums in order (a tensor-core-like order)
+        chunk = terms.reshape(rank // 16, 16, V).sum(axis=1, dtype=np.float32)
+        acc = np.zeros(V, np.float32)
+        for c in chunk:
+            acc = (acc + c).astype(np.float32)
+        sums.append(acc)
+        for s in sums:
+            z = (Uf[0, k] + s).astype(np.float32)
+            got = _f32_of_bits(_bf16_bits_from_f32(z)).astype(np.float64)
+            diff = np.abs(got - stored[0, k])
+            assert (diff <= spread[0, k]).all(), np.nonzero(diff > spread[0, k])[0][:8]
+            mism += int((diff > 0).sum())
+    assert mism > 0                                   # the check is not vacuous
+    assert (spread > 0).mean() < 0.02                 # and the marks stay rare

@@ -199,3 +199,61 @@ def test_errors():
         with pytest.raises(oracle.OracleError) as e:
             oracle.verify_ragged(**args)
         assert e.value.name == name
+
+
+def _bits(x):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _vals(b):
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def _step(b, direction):
+    # the bf16 neighbour of each value in the given direction (+1 / -1), exact in bit space
+    v = _vals(b).astype(np.float64)
+    up = (direction > 0) == (v >= 0)
+    nb = np.where(up, b.astype(np.int32) + 1, b.astype(np.int32) - 1)
+    nb = np.where(b == 0, np.where(direction > 0, 1, 0x8001), nb)
+    return nb.astype(np.uint16)
+
+
+def test_draft_ambiguity_marks_cover_one_step_changes():
+    # Soundness of the draft_spread input: moving marked draft logits by one bf16 step (either
+    # way, any subset) never changes the outcome of a request the marked run leaves unflagged
+    # when the spread covers that step, the marks themselves never change the outcome, and
+    # with dense marks some requests are flagged (the check is not vacuous).
+    rng = np.random.default_rng(11)
+    B, K, V = 96, 3, 256
+    D = _bits(rng.normal(0, 2.0, (B, K, V)))
+    tgt_dense = _vals(D).astype(np.float64)
+    tgt = np.concatenate([tgt_dense + rng.normal(0, 0.7, (B, K, V)),
+                          rng.normal(0, 2.0, (B, 1, V))], axis=1)
+    flat = _bits(tgt.reshape(B * (K + 1), V))
+    ell = np.full(B, K, np.int32)
+    off = np.arange(B + 1, dtype=np.int32) * (K + 1)
+    T = np.ones(B, np.float32)
+    tok = np.zeros((B, K), np.int32)
+    for b in range(B):                         # plausible drafts: argmax-ish tokens of their rows
+        for k in range(K):
+            tok[b, k] = int(rng.choice(np.argsort(_vals(D[b, k]))[-8:]))
+    amb = (rng.uniform(size=D.shape) < 0.2).astype(np.uint8)
+    # spread: the larger of the two bf16 steps around each marked value
+    v = np.abs(_vals(D).astype(np.float64))
+    spread = (amb * np.maximum(v * 2.0 ** -7, 2.0 ** -133)).astype(np.float32)
+    base = oracle.verify_ragged(D, flat, off, ell, tok, T, seed=3)
+    marked = oracle.verify_ragged(D, flat, off, ell, tok, T, seed=3, draft_spread=spread)
+    np.testing.assert_array_equal(base["n_acc"], marked["n_acc"])
+    np.testing.assert_array_equal(base["out_tok"], marked["out_tok"])
+    clean = marked["flags"] == 0
+    assert 0 < clean.sum() < B
+    assert (marked["flags"] & ~base["flags"]).any()      # the marks add flags
+    for trial in range(6):
+        sel = (amb == 1) & (rng.uniform(size=D.shape) < 0.7)
+        direction = np.where(rng.uniform(size=D.shape) < 0.5, 1, -1)
+        Dp = np.where(sel, _step(D, direction), D).astype(np.uint16)
+        pert = oracle.verify_ragged(Dp, flat, off, ell, tok, T, seed=3)
+        np.testing.assert_array_equal(pert["n_acc"][clean], marked["n_acc"][clean])
+        np.testing.assert_array_equal(pert["out_tok"][clean], marked["out_tok"][clean])
