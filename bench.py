@@ -2,11 +2,14 @@
 """Benchmark of the DSpark per-step hot path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-  draft    dspark_draft_markov_sample  (Markov-head bias GEMM + Gumbel-max sampling,
-                                        writes tokens, draft logits and normalisers)
+  draft    dspark_draft_markov_sample  (Markov-head bias GEMM + two-level sampling; writes
+                                        tokens, normalisers and the drawn tokens' logits, no
+                                        B x K x V logits)
   schedule dspark_schedule_survival    (survival products, global rank, greedy
                                         admission with early stop)
-  verify   dspark_verify_ragged        (rejection sampling over the flattened rows)
+  verify   dspark_verify_markov        (rejection sampling over the flattened rows; the draft
+                                        rows of rejections are recomputed on the tensor cores)
+With --stored-logits the draft stores its logits and dspark_verify_ragged reads them.
 Metric: draft + verify positions per second (sum K_r + sum (ell_r + 1) per step).
 
 Default workload: the ragged mixed step, the largest single-GPU configuration (B=2048,
@@ -58,6 +61,9 @@ def parse_args(argv=None):
                    help="run the scheduler after the draft instead of beside it on a second stream")
     p.add_argument("--head", choices=["markov", "rnn"], default="markov",
                    help="the draft's sequential head: the Markov head (default) or the RNN head")
+    p.add_argument("--stored-logits", action="store_true",
+                   help="the draft stores its logits and verification reads them (dspark_verify_ragged) "
+                        "instead of recomputing the rejecting rows (dspark_verify_markov)")
     return p.parse_args(argv)
 
 
@@ -176,7 +182,7 @@ def make_workload(cfg, dev, sps_variant, head="markov"):
 class Step:
     """Preallocated buffers and the three C-ABI calls of one step."""
 
-    def __init__(self, cfg, w, dev, spare_sm=False):
+    def __init__(self, cfg, w, dev, spare_sm=False, stored_logits=False):
         import torch
 
         import speculative_decoding_draft_gb300 as ds
@@ -188,8 +194,8 @@ class Step:
         inp = w["inp"]
         self.status = ds.new_status(dev)
         self.draft_out = dict(draft_tok=torch.empty(B, K, dtype=torch.int32, device=dev),
-                              draft_logits=torch.empty_like(inp["U"]),
-                              draft_lse=torch.empty(B, K, dtype=torch.float32, device=dev))
+                              draft_lse=torch.empty(B, K, dtype=torch.float32, device=dev),
+                              draft_tok_logit=torch.empty(B, K, dtype=torch.float32, device=dev))
         self.sched_out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
                               tgt_off=torch.empty(B + 1, dtype=torch.int32, device=dev),
                               theta_best=torch.empty(1, dtype=torch.float64, device=dev),
@@ -221,11 +227,18 @@ class Step:
                     else ds.draft_workspace_bytes(B, K, V, cfg.rank, dt, flags))
         self.ws_d = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.ws_s = torch.empty(ds.schedule_workspace_bytes(B, K), dtype=torch.uint8, device=dev)
-        self.ws_v = torch.empty(ds.verify_workspace_bytes(B, V), dtype=torch.uint8, device=dev)
-        # draft: prologue + persistent kernel (tensor cores) or prologue + one
-        # launch per position (CUDA cores); schedule: 1; verify: row statistics + sample
+        # recompute verification (the default on the tensor-core path): no draft logits stored
+        self.recompute = self.tensor_core and not stored_logits
+        if not self.recompute:
+            self.draft_out["draft_logits"] = torch.empty_like(inp["U"])
+        self.ws_v = torch.empty(ds.verify_markov_workspace_bytes(B, K, V, cfg.rank) if self.recompute
+                                else ds.verify_workspace_bytes(B, V), dtype=torch.uint8, device=dev)
+        # draft: prologue + persistent kernel (tensor cores) or prologue + one launch per
+        # position (CUDA cores); schedule: 1; verify: plan, scan, sample (+ the residual jobs and
+        # the tensor-core residual pass when it recomputes)
         self.draft_launches = 2 if self.tensor_core else (1 + 2 * K if self.rnn else 1 + K)
-        self.launches_per_step = self.draft_launches + 1 + 2
+        self.verify_launches = 5 if self.recompute else 3
+        self.launches_per_step = self.draft_launches + 1 + self.verify_launches
 
     def draft(self, inp=None):
         inp = self.w["inp"] if inp is None else inp
@@ -236,8 +249,8 @@ class Step:
                                      out=self.draft_out, workspace=self.ws_d, status=self.status)
             return
         self.ds.draft_markov_sample(inp["U"], inp["E"], W, inp["anchor"], inp["K_r"], inp["temperature"],
-                                    self.cfg.philox_seed, out=self.draft_out, workspace=self.ws_d,
-                                    status=self.status, spare_sm=self.spare_sm)
+                                    self.cfg.philox_seed, want_logits=not self.recompute, out=self.draft_out,
+                                    workspace=self.ws_d, status=self.status, spare_sm=self.spare_sm)
 
     def schedule(self, conf=None, K_r=None):
         conf = self.w["conf"] if conf is None else conf
@@ -245,17 +258,27 @@ class Step:
         self.ds.schedule_survival(conf, K_r, self.w["sps"], out=self.sched_out, workspace=self.ws_s,
                                   status=self.status)
 
-    def verify(self, tgt=None, temperature=None):
+    def verify(self, tgt=None, temperature=None, inp=None):
         tgt = self.w["tgt"] if tgt is None else tgt
         temperature = self.w["inp"]["temperature"] if temperature is None else temperature
+        inp = self.w["inp"] if inp is None else inp
+        if self.recompute:
+            self.ds.verify_markov(inp["U"], inp["E"], self.W, inp["anchor"], self.draft_out["draft_lse"],
+                                  self.draft_out["draft_tok_logit"], tgt, self.sched_out["tgt_off"],
+                                  self.sched_out["ell"], self.draft_out["draft_tok"], temperature,
+                                  self.cfg.philox_seed + 7919, out=self.ver_out, workspace=self.ws_v,
+                                  status=self.status)
+            return
         self.ds.verify_ragged(self.draft_out["draft_logits"], tgt, self.sched_out["tgt_off"],
                               self.sched_out["ell"], self.draft_out["draft_tok"], temperature,
                               self.cfg.philox_seed + 7919, draft_lse=self.draft_out["draft_lse"],
                               out=self.ver_out, workspace=self.ws_v, status=self.status)
 
 
-def algorithmic(cfg, K_r, ell, n_acc, temperature, head="markov"):
-    """Algorithmic bytes / flops of each operation for one step (bf16 = 2 bytes)."""
+def algorithmic(cfg, K_r, ell, n_acc, temperature, head="markov", recompute=False):
+    """Algorithmic bytes / flops of each operation for one step (bf16 = 2 bytes).  With the
+    recompute verification, a rejection's draft row costs its base-logit row and W1 row, and
+    the call reads W2 once (instead of one stored draft row per rejection)."""
     esz = 2 if cfg.dtype == "bf16" else 4
     V, r = cfg.V, cfg.rank
     sumK = int(K_r.sum())
@@ -268,13 +291,18 @@ def algorithmic(cfg, K_r, ell, n_acc, temperature, head="markov"):
     # draft row at a rejection (T > 0) for the residual
     ver_rows = 0
     ver_rows_dense = 0
+    rejections = 0
     for b in range(cfg.B):
         l, n = int(ell[b]), int(n_acc[b])
         ver_rows += n + 1
         if n < l and float(temperature[b]) > 0:
             ver_rows += 1
+            rejections += 1
         ver_rows_dense += 2 * l + 1
-    return dict(draft_bytes=draft_bytes, draft_flops=draft_flops, verify_bytes=ver_rows * V * esz,
+    verify_bytes = ver_rows * V * esz
+    if recompute and rejections:
+        verify_bytes += rejections * r * esz + r * V * esz
+    return dict(draft_bytes=draft_bytes, draft_flops=draft_flops, verify_bytes=verify_bytes,
                 verify_bytes_dense=ver_rows_dense * V * esz, positions=sumK + int((ell + 1).sum()),
                 draft_positions=sumK, verify_positions=int((ell + 1).sum()))
 
@@ -474,7 +502,7 @@ def main(argv=None):
     # The scheduler depends on the confidences only, not on the drafted tokens, so by
     # default it runs on a second stream beside the draft, which leaves it one SM.
     overlap = not args.serial
-    step = Step(cfg, w, dev, spare_sm=overlap)
+    step = Step(cfg, w, dev, spare_sm=overlap, stored_logits=args.stored_logits)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     def one_step():
@@ -489,7 +517,7 @@ def main(argv=None):
         raise SystemExit(f"device status {st}")
     n_acc = step.ver_out["n_acc"].cpu()
     alg = algorithmic(cfg, w["inp"]["K_r"].cpu(), step.sched_out["ell"].cpu(), n_acc,
-                      w["inp"]["temperature"].cpu(), args.head)
+                      w["inp"]["temperature"].cpu(), args.head, step.recompute)
 
     # The step's three C-ABI calls are captured once into CUDA graphs (one per call, so the
     # events between them still time each part) and replayed: the same kernels on the same
@@ -572,7 +600,9 @@ def main(argv=None):
                       "note": "runs beside the draft on a second stream; ms is the wait after the draft"}),
         "verify": {"ms": t_ver, "alg_bytes": alg["verify_bytes"], "dense_bytes": alg["verify_bytes_dense"],
                    "GB/s": ver_gbs, "hbm_frac": ver_gbs / hbm,
-                   "hbm_frac_dense": alg["verify_bytes_dense"] / (t_ver * 1e-3) / 1e9 / hbm, "launches": 2},
+                   "hbm_frac_dense": alg["verify_bytes_dense"] / (t_ver * 1e-3) / 1e9 / hbm,
+                   "launches": step.verify_launches,
+                   "path": "recompute (dspark_verify_markov)" if step.recompute else "stored rows (dspark_verify_ragged)"},
     }
     # the CUDA-core draft is bound by its fp32 FMAs (2 r V flops per position against a few
     # hundred bytes): its peak is the SMs' fp32 lanes at the maximum SM clock
@@ -675,7 +705,7 @@ def e2e_measure(cfg, w, step, dev, args, alg):
             dinp["rnn_x"] = d["rnn_x"]
         step.draft(dinp)
         step.schedule(d["conf"], d["K_r"])
-        step.verify(d["tgt"], d["temperature"])
+        step.verify(d["tgt"], d["temperature"], dinp)
         out_tok.copy_(step.ver_out["out_tok"], non_blocking=True)
         n_acc.copy_(step.ver_out["n_acc"], non_blocking=True)
         drafts.copy_(step.draft_out["draft_tok"], non_blocking=True)

@@ -124,8 +124,9 @@ typedef struct {
  *                of the drawn token (exact, as a float); entries k > K_r are not
  *                written.  With draft_lse it gives log q_k(x_k) = z_k(x_k) / T_r -
  *                lse, all that verification needs of a draft row except at a
- *                rejection, so draft_logits can stay NULL (no B x K x V logits go
- *                back to memory; see dspark_verify_markov).
+ *                rejection, so draft_logits can stay NULL: no B x K x V logits go
+ *                back to memory, and dspark_verify_markov recomputes the rejecting
+ *                rows.
  *   workspace    >= dspark_draft_workspace_bytes(dims) bytes (the same dims and
  *                flags as the call), 256-byte aligned.
  * The tensor-core path is used when dtype = DSPARK_BF16, rank is a multiple of
@@ -375,8 +376,10 @@ dspark_status dspark_schedule_survival_noalloc(const float *conf, const int32_t 
  *                (as written by dspark_draft_markov_sample).  When given, draft rows
  *                are read only at the rejecting position; when NULL they are
  *                streamed at every verified position.
- * The target rows j <= ell_r of every request are streamed at once (one pass over
- * all of them, in parallel), so rows past a request's first rejection are read too.
+ * The target rows are read position by position (every request's row j before any
+ * row j + 1), and each row is decided as soon as its statistics are complete; rows
+ * past a request's first rejection are skipped once that rejection is known (rows
+ * already in flight are read anyway).
  *   tgt_logits   [tgt_off[B], V]  flattened target logits, ell_r + 1 rows per request.
  *   tgt_off      [B+1] int32      row offsets; tgt_off[r+1] - tgt_off[r] = ell_r + 1.
  *   ell          [B] int32        verification lengths, 0..K_max.
@@ -395,6 +398,40 @@ dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_
                                    dspark_dims dims, int32_t *n_acc, int32_t *out_tok,
                                    void *workspace, size_t workspace_bytes,
                                    int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Verify with the draft rows recomputed ("DSpark" S2.1 and S3.1; "Speculative
+ * decoding, from zero to DSpark" S2 and S6).
+ *
+ * The same verification as dspark_verify_ragged (same accept rule, random
+ * streams and outputs) for drafts of the Markov head whose logits were not
+ * stored: the accept test at position j needs only log q_j(x_j) =
+ * draft_tok_logit / T - draft_lse, and the draft row of a rejecting position j
+ * (T > 0) is recomputed for the residual as z = U[r, j-1] + E[x_{j-1}] . W,
+ * rounded to bf16 exactly as the draft formed it (x_0 = anchor), by the
+ * tensor-core path, so the residual is drawn from the very q that was sampled.
+ * All rejections of a call share one pass over W.
+ *
+ *   U, E, W, anchor   as passed to dspark_draft_markov_sample (W as given, or
+ *                     packed with DSPARK_FLAG_W_PACKED in dims.flags).
+ *   draft_lse, draft_tok_logit  [B, K_max] float: the draft's outputs.
+ *   tgt_logits, tgt_off, ell, draft_tok, temperature, seed, n_acc, out_tok
+ *                     as for dspark_verify_ragged.
+ *   dims              B, K_max, V and rank of the draft; dtype DSPARK_BF16.
+ *   workspace         >= dspark_verify_markov_workspace_bytes(dims), 256-byte aligned.
+ * Needs the tensor-core shape (bf16, rank a multiple of 64 up to 256, V a
+ * multiple of 8, 16-byte aligned U, E, W and tgt_logits, an sm_103 device);
+ * otherwise DSPARK_ERR_UNSUPPORTED (the workspace query returns 0), and
+ * dspark_verify_ragged with stored draft logits serves the call.
+ * ------------------------------------------------------------------------ */
+size_t dspark_verify_markov_workspace_bytes(dspark_dims dims);
+
+dspark_status dspark_verify_markov(const void *U, const void *E, const void *W, const int32_t *anchor,
+                                   const float *draft_lse, const float *draft_tok_logit,
+                                   const void *tgt_logits, const int32_t *tgt_off, const int32_t *ell,
+                                   const int32_t *draft_tok, const float *temperature, uint64_t seed,
+                                   dspark_dims dims, int32_t *n_acc, int32_t *out_tok, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Status helpers.

@@ -23,7 +23,8 @@ __all__ = [
     "DsparkError", "DsparkUnavailable", "lib", "library_path", "draft_markov_sample", "schedule_survival",
     "verify_ragged", "check", "status_string", "draft_workspace_bytes", "schedule_workspace_bytes",
     "verify_workspace_bytes", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_W_PACKED", "FLAG_SPARE_SM", "STATUS_NAMES", "Dims",
-    "PackedProjection", "pack_projection", "packed_projection_bytes",
+    "PackedProjection", "pack_projection", "packed_projection_bytes", "verify_markov",
+    "verify_markov_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -49,7 +50,7 @@ EXPORTED_SYMBOLS = [
     "dspark_draft_pack_projection", "dspark_schedule_workspace_bytes",
     "dspark_schedule_survival", "dspark_schedule_survival_noalloc", "dspark_schedule_capacity",
     "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_workspace_bytes",
-    "dspark_verify_ragged",
+    "dspark_verify_ragged", "dspark_verify_markov_workspace_bytes", "dspark_verify_markov",
     "dspark_status_string", "dspark_check", "dspark_version",
 ]
 
@@ -118,6 +119,10 @@ def lib() -> ctypes.CDLL:
     L.dspark_verify_workspace_bytes.restype = sz
     L.dspark_verify_ragged.argtypes = [P, P, P, P, P, P, P, u64, Dims, P, P, P, sz, P, P]
     L.dspark_verify_ragged.restype = st
+    L.dspark_verify_markov_workspace_bytes.argtypes = [Dims]
+    L.dspark_verify_markov_workspace_bytes.restype = sz
+    L.dspark_verify_markov.argtypes = [P, P, P, P, P, P, P, P, P, P, P, u64, Dims, P, P, P, sz, P, P]
+    L.dspark_verify_markov.restype = st
     L.dspark_status_string.argtypes = [st]
     L.dspark_status_string.restype = ctypes.c_char_p
     L.dspark_check.argtypes = [P, P]
@@ -484,4 +489,59 @@ def verify_ragged(draft_logits, tgt_logits, tgt_off, ell, draft_tok, temperature
                                       _ptr(n_acc), _ptr(out_tok), _ptr(ws), ctypes.c_size_t(ws.numel()),
                                       _ptr(status), _stream(stream))
     _raise(code, "dspark_verify_ragged")
+    return dict(n_acc=n_acc, out_tok=out_tok, status=status, workspace=ws)
+
+
+def verify_markov_workspace_bytes(B: int, K_max: int, V: int, rank: int, packed: bool = True) -> int:
+    return int(lib().dspark_verify_markov_workspace_bytes(Dims(B, K_max, V, rank, BF16,
+                                                                FLAG_W_PACKED if packed else 0)))
+
+
+def verify_markov(U, E, W, anchor, draft_lse, draft_tok_logit, tgt_logits, tgt_off, ell, draft_tok, temperature,
+                  seed: int, *, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Verification with the rejecting draft rows recomputed (C ABI dspark_verify_markov).
+
+    U [B,K_max,V], E [V,rank] bf16 and W [rank,V] bf16 or a PackedProjection of it, anchor [B]
+    int32 -- the draft's inputs -- and its draft_lse, draft_tok_logit [B,K_max] float32 outputs;
+    the rest as for verify_ragged.  Returns n_acc [B] and out_tok [B,K_max+1] (int32).
+    """
+    _dev(U, "U", torch.bfloat16)
+    B, K_max, V = U.shape
+    rank = E.shape[1]
+    _dev(E, "E", torch.bfloat16, (V, rank))
+    flags = 0
+    if isinstance(W, PackedProjection):
+        if (W.rank, W.V) != (rank, V) or W.device != U.device:
+            raise ValueError(f"packed projection of shape ({W.rank}, {W.V}) does not fit U/E")
+        flags |= FLAG_W_PACKED
+        W = W.data
+    else:
+        _dev(W, "W", torch.bfloat16, (rank, V))
+    _dev(anchor, "anchor", torch.int32, (B,))
+    _dev(draft_lse, "draft_lse", torch.float32, (B, K_max))
+    _dev(draft_tok_logit, "draft_tok_logit", torch.float32, (B, K_max))
+    _dev(tgt_logits, "tgt_logits", torch.bfloat16)
+    if tgt_logits.dim() != 2 or tgt_logits.shape[1] != V:
+        raise ValueError("tgt_logits must be [rows, V]")
+    _dev(tgt_off, "tgt_off", torch.int32, (B + 1,))
+    _dev(ell, "ell", torch.int32, (B,))
+    _dev(draft_tok, "draft_tok", torch.int32, (B, K_max))
+    _dev(temperature, "temperature", torch.float32, (B,))
+    dev = U.device
+    out = {} if out is None else out
+    n_acc = out.get("n_acc") if out.get("n_acc") is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    out_tok = out.get("out_tok") if out.get("out_tok") is not None else torch.empty(B, K_max + 1, dtype=torch.int32,
+                                                                                    device=dev)
+    status = new_status(dev) if status is None else status
+    dims = Dims(B, K_max, V, rank, BF16, flags)
+    nbytes = int(lib().dspark_verify_markov_workspace_bytes(dims))
+    if nbytes == 0:
+        _raise(13, "dspark_verify_markov")
+    ws = _workspace(nbytes, dev, workspace)
+    code = lib().dspark_verify_markov(_ptr(U), _ptr(E), _ptr(W), _ptr(anchor), _ptr(draft_lse), _ptr(draft_tok_logit),
+                                      _ptr(tgt_logits), _ptr(tgt_off), _ptr(ell), _ptr(draft_tok), _ptr(temperature),
+                                      ctypes.c_uint64(seed), dims, _ptr(n_acc), _ptr(out_tok), _ptr(ws),
+                                      ctypes.c_size_t(ws.numel()), _ptr(status), _stream(stream))
+    _raise(code, "dspark_verify_markov")
     return dict(n_acc=n_acc, out_tok=out_tok, status=status, workspace=ws)

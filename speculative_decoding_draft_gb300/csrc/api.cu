@@ -2,6 +2,9 @@
 // workspace carving, kernel-path selection and the status helpers.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <map>
+#include <utility>
 
 #include "schedule.cuh"
 
@@ -26,8 +29,10 @@ struct DeviceInfo {
 bool device_info(DeviceInfo *out) {
   static DeviceInfo cache[64];
   static bool have[64] = {false};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
   if (!have[dev]) {
     DeviceInfo d;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
@@ -55,6 +60,22 @@ dspark_status check_dims(const dspark_dims &d, bool need_rank) {
 }
 
 }  // namespace
+
+namespace dspark {
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, int> set_to;   // the size each (device, kernel) allows
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = set_to.find({dev, fn});
+  if (it != set_to.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) set_to[{dev, fn}] = bytes;
+  return e;
+}
+}  // namespace dspark
 
 extern "C" {
 
@@ -107,7 +128,8 @@ static bool draft_packs_into_workspace(const dspark_dims &d) {
 static size_t draft_ws_base(int64_t B, int64_t K_max, int64_t V) {
   return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
          al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
-         al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V)) +
+         al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(int32_t) * (size_t)(B * K_max)) +
+         al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V)) +
          al256(sizeof(float) * (size_t)draft_partial_slots(B, K_max, V));
 }
 
@@ -196,6 +218,8 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   p += al256(8 * (size_t)(dims.B * dims.K_max));
   a.gbar = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 1));
+  a.act = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)(dims.B * dims.K_max));
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   p += al256(sizeof(Partial) * (size_t)a.partial_slots);
@@ -429,6 +453,108 @@ dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_
   a.key = make_philox_key(seed);
   verify_carve(a, workspace);
   return launch_verify(a, (cudaStream_t)stream, dev.sms) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// Recompute entry point: the verify workspace, then the residual pass's jobs [B], keys [B],
+// flags [B], active counts [3], barrier counters [2], and the packed W2 when the caller
+// passes W as given.
+static size_t verify_markov_extra(const dspark_dims &d) {
+  size_t n = al256(sizeof(VJob) * (size_t)d.B) + al256(8 * (size_t)d.B) + al256(sizeof(int32_t) * (size_t)d.B) +
+             al256(sizeof(int32_t) * 3) + al256(sizeof(int32_t) * 2);
+  if (!(d.flags & DSPARK_FLAG_W_PACKED)) n += al256(draft_packed_bytes(d.rank, d.V));
+  return n;
+}
+
+size_t dspark_verify_markov_workspace_bytes(dspark_dims dims) {
+  if (check_dims(dims, true) != DSPARK_OK) return 0;
+  if (dims.dtype != DSPARK_BF16 || dims.rank % 64 != 0 || dims.rank > 256 || dims.V % 8 != 0) return 0;
+  return verify_ws_bytes(dims.B, dims.V, nullptr) + verify_markov_extra(dims);
+}
+
+dspark_status dspark_verify_markov(const void *U, const void *E, const void *W, const int32_t *anchor,
+                                   const float *draft_lse, const float *draft_tok_logit, const void *tgt_logits,
+                                   const int32_t *tgt_off, const int32_t *ell, const int32_t *draft_tok,
+                                   const float *temperature, uint64_t seed, dspark_dims dims, int32_t *n_acc,
+                                   int32_t *out_tok, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                   void *stream) {
+  if (!U || !E || !W || !anchor || !draft_lse || !draft_tok_logit || !tgt_logits || !tgt_off || !ell ||
+      !draft_tok || !temperature || !n_acc || !out_tok || !dev_status)
+    return DSPARK_ERR_NULL;
+  dspark_status st = check_dims(dims, true);
+  if (st != DSPARK_OK) return st;
+  const size_t need = dspark_verify_markov_workspace_bytes(dims);
+  if (need == 0 || (((uintptr_t)U | (uintptr_t)E | (uintptr_t)W | (uintptr_t)tgt_logits) & 15u))
+    return DSPARK_ERR_UNSUPPORTED;   // the recompute runs on the tensor-core path only
+  if (!workspace || !aligned256(workspace) || workspace_bytes < need) return DSPARK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return DSPARK_ERR_CUDA;
+  if (dev.major != 10 || dev.minor != 3) return DSPARK_ERR_UNSUPPORTED;
+  VerifyArgs a;
+  a.D = nullptr;
+  a.D_lse = draft_lse;
+  a.D_zx = draft_tok_logit;
+  a.tgt = tgt_logits;
+  a.tgt_off = tgt_off;
+  a.ell = ell;
+  a.draft_tok = draft_tok;
+  a.temperature = temperature;
+  a.n_acc = n_acc;
+  a.out_tok = out_tok;
+  a.dev_status = dev_status;
+  a.B = dims.B;
+  a.K_max = dims.K_max;
+  a.V = dims.V;
+  a.dtype = dims.dtype;
+  a.key = make_philox_key(seed);
+  verify_carve(a, workspace);
+  char *p = (char *)workspace + verify_ws_bytes(dims.B, dims.V, nullptr);
+  a.anchor = anchor;
+  a.jobs = (VJob *)p;
+  p += al256(sizeof(VJob) * (size_t)dims.B);
+  a.key_out = (unsigned long long *)p;
+  a.resid_key = a.key_out;
+  p += al256(8 * (size_t)dims.B);
+  a.any_out = (int32_t *)p;
+  a.resid_any = a.any_out;
+  p += al256(sizeof(int32_t) * (size_t)dims.B);
+  a.jobs_nact = (int32_t *)p;
+  p += al256(sizeof(int32_t) * 3);
+  a.jobs_gbar = (int32_t *)p;
+  p += al256(sizeof(int32_t) * 2);
+  // the residual pass: the draft kernel's residual mode over the jobs
+  DraftArgs r;
+  r.U = U;
+  r.E = E;
+  r.W = W;
+  r.Wp = (dims.flags & DSPARK_FLAG_W_PACKED) ? W : (const void *)p;
+  r.anchor = anchor;
+  r.K_r = nullptr;
+  r.temperature = temperature;
+  r.draft_tok = nullptr;
+  r.draft_logits = nullptr;
+  r.draft_lse = nullptr;
+  r.draft_zx = nullptr;
+  r.dev_status = dev_status;
+  r.B = dims.B;
+  r.K_max = 1;
+  r.V = dims.V;
+  r.rank = dims.rank;
+  r.dtype = dims.dtype;
+  r.key = a.key;
+  r.perm = r.iperm = r.counters = r.act = nullptr;
+  r.nact = a.jobs_nact;
+  r.best_key = a.key_out;
+  r.gbar = a.jobs_gbar;
+  r.partials = nullptr;
+  r.zx_part = nullptr;
+  r.partial_slots = 0;
+  r.jobs = a.jobs;
+  r.tgt = tgt_logits;
+  r.resid_any = a.any_out;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!(dims.flags & DSPARK_FLAG_W_PACKED) && launch_pack_projection(W, dims.rank, dims.V, (void *)r.Wp, s) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return launch_verify(a, s, dev.sms, &r) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -5,7 +5,8 @@
 //
 // For position k the active requests (K_r >= k) form a prefix of the
 // permutation `perm`, which orders requests by K_r descending; the prologue
-// builds it together with the active counts nact[k].
+// builds it together with the active counts nact[k], and the lists act[k - 1] of the
+// active requests in request order that the tensor-core path tiles.
 //
 // CUDA-core step: grid (vocabulary tile, tile of active rows); each block forms
 // z = U + feature . W2 for its rows and columns with fp32 FMAs (the feature is the
@@ -28,12 +29,16 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
   __shared__ int cnt[kMaxK + 2];          // requests per length value
   __shared__ int base[kMaxK + 2];         // next free slot per length value
   __shared__ int wc[kPrologueThreads / 32][kMaxK + 2];
+  __shared__ int carry[kMaxK + 2];        // act: listed requests per position so far
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_skip = read_status(a.dev_status);
     s_err = 0;
   }
-  if (tid < kMaxK + 2) cnt[tid] = 0;
+  if (tid < kMaxK + 2) {
+    cnt[tid] = 0;
+    carry[tid] = 0;
+  }
   __syncthreads();
   if (s_skip) return;
   if (tid <= a.K_max) a.gbar[tid] = 0;
@@ -91,6 +96,33 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
       int tot = 0;
       for (int w2 = 0; w2 < kPrologueThreads / 32; ++w2) tot += wc[w2][tid];
       base[tid] += tot;
+    }
+    __syncthreads();
+  }
+  // act[k - 1]: the requests with K_r >= k in request order (a ballot prefix per position)
+  for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
+    const int r = c0 + tid;
+    const int v = r < B ? a.K_r[r] : 0;
+    for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
+    __syncthreads();
+    for (int k = 1; k <= K; ++k) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, v >= k);
+      if (lane == 0) wc[warp][k] = __popc(bal);
+    }
+    __syncthreads();
+    for (int k = 1; k <= K; ++k) {          // every lane runs every k: the ballots are warp-wide
+      const uint32_t bal = __ballot_sync(0xffffffffu, v >= k);
+      if (v >= k) {
+        int before = carry[k];
+        for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][k];
+        a.act[(int64_t)(k - 1) * B + before + __popc(bal & ((1u << lane) - 1u))] = r;
+      }
+    }
+    __syncthreads();
+    if (tid >= 1 && tid <= K) {
+      int tot = 0;
+      for (int w2 = 0; w2 < kPrologueThreads / 32; ++w2) tot += wc[w2][tid];
+      carry[tid] += tot;
     }
     __syncthreads();
   }
@@ -567,13 +599,9 @@ cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s) {
   const dim3 grid((unsigned)col_tiles, (unsigned)(row_tiles < 65535 ? row_tiles : 65535));
   for (int k = 1; k <= (int)a.K_max; ++k) {
     if (a.rnn_feat) {
-      static bool cell_attr = false;
-      if (!cell_attr) {
-        for (void *fn : {(void *)rnn_cell_tile<DSPARK_F32>, (void *)rnn_cell_tile<DSPARK_BF16>}) {
-          cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCellSmem);
-          if (e != cudaSuccess) return e;
-        }
-        cell_attr = true;
+      for (const void *fn : {(const void *)rnn_cell_tile<DSPARK_F32>, (const void *)rnn_cell_tile<DSPARK_BF16>}) {
+        cudaError_t e = ensure_dynamic_smem(fn, (int)kCellSmem);
+        if (e != cudaSuccess) return e;
       }
       const dim3 cg((unsigned)((a.rank + kCellUnits - 1) / kCellUnits),
                     (unsigned)((a.B + kCellReq - 1) / kCellReq));

@@ -4,8 +4,9 @@
 // "Speculative decoding, from zero to DSpark" S6 (p_k = softmax(U_k + B_k)).
 //
 // One persistent cooperative launch walks every draft position k = 1..K_max.  The
-// active requests at position k (K_r >= k) are the first n_k entries of `perm`;
-// they are cut into M-tiles of 128 rows, and every M-tile is shared by gm CTAs that
+// active requests at position k (K_r >= k), listed in request order in act[k - 1] (so
+// that a tile's rows sit as close together in U as the active set allows: rows scattered
+// over the whole of U made each tile three times slower), are cut into M-tiles of 128 rows, and every M-tile is shared by gm CTAs that
 // own contiguous ranges of 64-wide vocabulary blocks.  A CTA stages the gathered
 // operand W1[x_{k-1}] (128 x r) once per range and streams W2 through it.
 //
@@ -56,7 +57,6 @@ constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
 constexpr int kOffU = kOffW + kStages * kStageBytes;
 constexpr int kOffSh = kOffU + kEpiWarps * kUDepth * kUSlot;
-constexpr long long kTimeoutCycles = 4000000000LL;
 
 struct TcShared {
   uint64_t full[kStages];
@@ -73,56 +73,17 @@ struct TcShared {
   int row_prev[kTileM];
   float row_invT[kTileM];
   Partial part[kWpq * kTileM];   // per-row partials: [column worker][row of the replica group]
-  float part_zx[kWpq * kTileM];  // the logit at each partial's index
+  float part_zx[kWpq * kTileM];  // the logit at each partial's index (residual mode: "some p > q")
+  // residual mode: per row the rejecting position, the base-logit and target rows, and the
+  // log2-scaled normalisers of p and q
+  int row_j[kTileM], row_urow[kTileM], row_trow[kTileM];
+  float row_lt2[kTileM], row_lq2[kTileM];
 };
 
 constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// ---- PTX wrappers ---------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
-}
-// One bounded probe of a barrier phase: the thread sleeps until the phase completes or
-// about 20 us pass, so waiting roles do not spin on the issue slots of the epilogue.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(20000)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on a barrier phase.  Returns false (and raises the CTA abort
-// flag) when the wait gave up or another role already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  const long long t0 = clock64();
-  while (!mbar_try(bar, parity)) {
-    if (*abort) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
-      *abort = 1;
-      return false;
-    }
-  }
-  return true;
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+// ---- PTX wrappers (the mbarrier and bulk-copy ones are in dspark_internal.cuh) ----
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -164,35 +125,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Contiguous global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// L2 policies: the projection W2 is re-read at every draft position and should stay in
-// L2; the base logits U and the stored draft logits are touched once.
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint4 ld_u4_hint(const void *ptr, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(policy));
-  return v;
-}
+// 16-byte streaming load of bf16 data read once.
+__device__ __forceinline__ uint4 ld_stream_u4(const unsigned short *p) { return __ldcs((const uint4 *)p); }
 __device__ __forceinline__ void st_u4_hint(void *ptr, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(policy)
@@ -221,11 +155,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
 
 __device__ __forceinline__ int ld_acquire(const int32_t *p) {
   int v;
@@ -267,7 +196,12 @@ __device__ __forceinline__ StepPlan plan_step(const int *nact, int k, int G, int
 __device__ __forceinline__ int range_lo(int j, int nb, int gm) { return (int)((int64_t)j * nb / gm); }
 
 // ---------------------------------------------------------------------------
-template <int RCH>   // rank / 64
+// RESID: the residual mode of the recompute verification -- one position whose rows are the
+// jobs; per row z = U + W1[x_{j-1}] W2 is formed exactly as the draft formed it, and the
+// two-level draw runs over max(0, p - q) (streams of the verification's seed, position j, tags
+// 2 and 4) instead of softmax(z / T); the winner goes into the request's packed key and a
+// positive residual anywhere into its flag.
+template <int RCH, bool RESID>   // rank / 64
 __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __grid_constant__ DraftArgs a) {
   constexpr int kRank = RCH * 64;
   constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
@@ -411,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
     const bool wide_s = (V % 16 == 0) && ((uintptr_t)a.draft_logits % 32 == 0);
     uint32_t tt = 0;
     int unit_no = 0;
-    int tab_m = -1;                     // M-tile whose rows sh.row_req / sh.row_invT hold
+    int tab_m = -1;                     // (position, M-tile) whose rows sh.row_req / sh.row_invT hold
     int k_last = 0;                     // last position this CTA arrived at
     for (int k = 1; k <= K && !*abort; ++k) {
       const StepPlan pl = plan_step(sh.nact, k, G, nb);
@@ -426,14 +360,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // of the rows, and the F replica groups split each tile's columns
         const int F = nrows <= 32 ? 4 : (nrows <= 64 ? 2 : 1);
         const int rpg = kTileM / F;
-        if (m != tab_m) {                // the same decision in every epilogue thread
-          // rows of M-tile m (perm order) and their 1/T: fixed for the whole call, so
-          // loaded only when this CTA moves to another M-tile
+        if (k * 65536 + m != tab_m) {    // the same decision in every epilogue thread
+          // rows of M-tile m at position k (a run of the position's active list, in request
+          // order) and their 1/T
           named_sync_epi();           // readers of the previous table are done
           if (et < kTileM) {
             const int i = et;
-            if (row0 + i < (int)a.B) {
-              const int r = a.perm[row0 + i];
+            if (RESID && row0 + i < pl.n_k) {
+              const VJob jb = a.jobs[row0 + i];
+              sh.row_req[i] = jb.r;
+              sh.row_invT[i] = jb.invT;
+              sh.row_j[i] = jb.j;
+              sh.row_urow[i] = jb.urow;
+              sh.row_trow[i] = jb.trow;
+              sh.row_lt2[i] = jb.lse_t * kLog2e;
+              sh.row_lq2[i] = jb.lse_q * kLog2e;
+            } else if (row0 + i < pl.n_k) {
+              const int r = a.act[(int64_t)(k - 1) * a.B + row0 + i];
               sh.row_req[i] = r;
               const float T = a.temperature[r];
               sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
@@ -443,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             }
           }
           named_sync_epi();
-          tab_m = m;
+          tab_m = k * 65536 + m;
         }
         const int arow = quad * 32 + lane;        // TMEM lane = M-row
         const int grp = arow / rpg;               // replica group (warp-uniform: rpg >= 32)
@@ -455,8 +398,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const float invT = sh.row_invT[row];
         const bool greedy = (invT == 0.0f);
         const float a2 = invT * kLog2e;           // scaled logits in log2 units
-        const int64_t urow = ((int64_t)r * K + (k - 1)) * (int64_t)V;
+        const int64_t urow = RESID ? (int64_t)(valid ? sh.row_urow[row] : 0) * V : ((int64_t)r * K + (k - 1)) * (int64_t)V;
         const unsigned short *uptr = (const unsigned short *)a.U + urow;
+        // residual mode: the target row, its stream position and the normalisers
+        const unsigned short *tptr =
+            RESID ? (const unsigned short *)a.tgt + (int64_t)(valid ? sh.row_trow[row] : 0) * V : nullptr;
+        const uint32_t rpos = RESID ? (uint32_t)(valid ? sh.row_j[row] : 0) : (uint32_t)k;
+        const float lt2 = RESID ? sh.row_lt2[row] : 0.0f, lq2 = RESID ? sh.row_lq2[row] : 0.0f;
+        bool any_pos = false;
         // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles; worker wk
         // takes blocks wk, wk + nwk, ...  Its i-th block's U (each lane its row's 64 bytes) is
         // staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by cp.async; 16-byte
@@ -496,7 +445,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         }
         if (et < kTileM && et < nrows) {
           const int rq = sh.row_req[et];
-          sh.row_prev[et] = (k == 1) ? a.anchor[rq] : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2));
+          sh.row_prev[et] = RESID ? a.jobs[row0 + et].prev
+                                  : ((k == 1) ? a.anchor[rq] : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2)));
         }
         named_sync_epi();
         // gather the A operand with asynchronous 16-byte copies, all in flight at once: request
@@ -522,6 +472,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
 
         BRace st;
         brace_init(st);
+        // residual mode: the target block of this worker's next 32 columns, one block ahead in
+        // registers (units past V read as -inf, so their weights are 0)
+        uint4 tcur[4], tnext[4];
+        auto load_t = [&](int gsb, uint4 (&t)[4]) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = b0 * kBlkN + gsb * 32 + 8 * q;
+            t[q] = (valid && gsb < nsub_u && c + 8 <= V) ? ld_stream_u4(tptr + c)
+                                                         : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+          }
+        };
+        if (RESID) load_t(wk, tcur);
         for (int bt = b0; bt < b1; bt += kMaxBlk, ++tt) {
           const int mt = min(kMaxBlk, b1 - bt);
           const int b = (int)(tt % kAccBufs);
@@ -563,6 +525,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
             }
             stage_u(ui + kUDepth);                   // the slot is free again: refill it
+            if (RESID) load_t(gs + nwk, tnext);
             if (!valid) continue;
             if (a.draft_logits) {
               unsigned short *drow = (unsigned short *)a.draft_logits + urow;
@@ -587,6 +550,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 if (c0 + 2 * e >= V) packed[e] = 0xFF80FF80u;   // two bf16 -inf
+            }
+            if (RESID) {
+              // residual weights max(0, p - q) of the block against the target row
+              const uint4 dp[4] = {make_uint4(packed[0], packed[1], packed[2], packed[3]),
+                                   make_uint4(packed[4], packed[5], packed[6], packed[7]),
+                                   make_uint4(packed[8], packed[9], packed[10], packed[11]),
+                                   make_uint4(packed[12], packed[13], packed[14], packed[15])};
+              const uint32_t gblk = (uint32_t)c0 >> 5;
+              const uint32_t wb = word_of(philox(a.key, gblk >> 2, rpos, (uint32_t)r, kTagResid), (int)(gblk & 3u));
+              brace_resid_packed(st, tcur, dp, a2, lt2, lq2, wb, c0, any_pos, [&] {
+                return word_of(philox(a.key, gblk >> 2, rpos, (uint32_t)r, kTagResidPick), (int)(gblk & 3u));
+              });
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tcur[q] = tnext[q];
+              continue;
             }
             // block maximum on bf16 pairs (exact), then across the pair
             __nv_bfloat162 m2[4] = {bf162_of(packed[0]), bf162_of(packed[1]), bf162_of(packed[2]), bf162_of(packed[3])};
@@ -617,9 +595,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // into the packed (score, index) key of the position with one 64-bit atomicMax -- all
         // the next position needs -- and keeps its softmax partial for the merge after the last position
         sh.part[wk * rpg + row] = to_partial(st);
-        sh.part_zx[wk * rpg + row] = st.zx;
+        sh.part_zx[wk * rpg + row] = RESID ? (any_pos ? 1.0f : 0.0f) : st.zx;
         named_sync_epi();
-        if (wk == 0 && valid) {
+        if (RESID && wk == 0 && valid) {
+          // the row's residual draw: the CTA's winner into the request's key, its flag
+          Race tot = from_partial(sh.part[row]);
+          bool any = sh.part_zx[row] != 0.0f;
+          for (int q = 1; q < nwk; ++q) {
+            race_merge(tot, from_partial(sh.part[q * rpg + row]));
+            any = any || sh.part_zx[q * rpg + row] != 0.0f;
+          }
+          if (tot.idx >= 0) atomicMax(&a.best_key[r], score_key(tot.best, tot.idx));
+          if (any) atomicOr(a.resid_any + r, 1);
+        } else if (!RESID && wk == 0 && valid) {
           Race tot = from_partial(sh.part[row]);
           float zx = sh.part_zx[row];
           for (int q = 1; q < nwk; ++q) {
@@ -649,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
     // the normalisers from the CTA partials and, when asked for, the confidence head's
     // output (its Markov term needs the previous position's token), one warp per
     // (position, request).
-    if (k_last > 0 && !*abort) {
+    if (!RESID && k_last > 0 && !*abort) {
       if (et == 0) {
         const long long t0 = clock64();
         while (ld_acquire(a.gbar + k_last) < G) {
@@ -667,7 +655,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           if (k > k_last) break;
           const StepPlan pl = plan_step(sh.nact, k, G, nb);
           if (i >= pl.n_k) continue;
-          const int r = a.perm[i];
+          const int r = a.act[(int64_t)(k - 1) * B + i];
           const int64_t at = (int64_t)r * K + k - 1;
           const int x = key_index(load_key(a.best_key + at));
           // the gm CTA partials of the row: softmax pair, greedy maximum (the largest logit
@@ -778,21 +766,21 @@ cudaError_t launch_pack_projection(const void *W, int64_t rank, int64_t V, void 
   return cudaGetLastError();
 }
 
-cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
+namespace {
+template <bool RESID>
+cudaError_t launch_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
   if (!a.Wp || ((uintptr_t)a.Wp & 15u)) return cudaErrorInvalidValue;
-  static bool attr_set[5] = {false, false, false, false, false};
   const int rch = (int)(a.rank / 64);
   void *fn = nullptr;
   switch (rch) {
-    case 1: fn = (void *)draft_tc_persistent<1>; break;
-    case 2: fn = (void *)draft_tc_persistent<2>; break;
-    case 3: fn = (void *)draft_tc_persistent<3>; break;
-    default: fn = (void *)draft_tc_persistent<4>; break;
+    case 1: fn = (void *)draft_tc_persistent<1, RESID>; break;
+    case 2: fn = (void *)draft_tc_persistent<2, RESID>; break;
+    case 3: fn = (void *)draft_tc_persistent<3, RESID>; break;
+    default: fn = (void *)draft_tc_persistent<4, RESID>; break;
   }
-  if (!attr_set[rch]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  {
+    cudaError_t e = ensure_dynamic_smem(fn, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[rch] = true;
   }
   const int grid = num_sms > 1024 ? 1024 : num_sms;
   // cooperative launch: all CTAs are co-resident, so the bounded grid barrier between
@@ -810,5 +798,9 @@ cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
   void *args[1] = {(void *)&a};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
+}  // namespace
+
+cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms) { return launch_tc<false>(a, s, num_sms); }
+cudaError_t launch_resid_tc(const DraftArgs &a, cudaStream_t s, int num_sms) { return launch_tc<true>(a, s, num_sms); }
 
 }  // namespace dspark

@@ -129,6 +129,84 @@ __device__ __forceinline__ bool temperature_ok(float t) {
 }
 
 // -------------------------------------------------------------------------
+// mbarrier, bulk copy and L2-policy wrappers (inline PTX).
+// -------------------------------------------------------------------------
+constexpr long long kTimeoutCycles = 4000000000LL;   // budget of every bounded wait (about 2 s)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+}
+// One bounded probe of a barrier phase: the thread sleeps until the phase completes or
+// about 20 us pass, so waiting roles do not spin on the issue slots of the epilogue.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(20000)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier phase.  Returns false (and raises the CTA abort
+// flag) when the wait gave up or another role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Contiguous global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: the projection W2 is re-read at every draft position and should stay in
+// L2; the base logits U and the stored draft logits are touched once.
+// 16-byte shared-memory load.
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// -------------------------------------------------------------------------
 // Gumbel race state (one per thread; merged across threads and blocks).
 // -------------------------------------------------------------------------
 struct Race {
@@ -469,6 +547,35 @@ __device__ __forceinline__ bool brace_softmax_bf16x32(BRace &r, const uint32_t (
   return true;
 }
 
+// Residual weight max(0, p - q) with p = 2^(t a - lt2), q = 2^(d a - ld2).
+__device__ __forceinline__ float resid_weight(float t, float d, float a, float lt2, float ld2) {
+  return fmaxf(fast_ex2(fmaf(t, a, -lt2)) - fast_ex2(fmaf(d, a, -ld2)), 0.0f);
+}
+
+// One block of residual weights max(0, p - q) on packed bf16 rows (tp: target, dp: draft; pair e
+// of the block in word (e & 3) of unit e >> 2), in the two-level draw; any_pos records a positive
+// weight.  The verification's stored-row pass and the tensor-core recompute pass share it, so
+// both draw the same token.
+template <class PickWord>
+__device__ __forceinline__ void brace_resid_packed(BRace &r, const uint4 (&tp)[4], const uint4 (&dp)[4], float a,
+                                                   float lt2, float ld2, uint32_t wb, int v0, bool &any_pos,
+                                                   PickWord pick_word) {
+  float w[kBlockW];
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < kBlockW; ++q) {
+    const uint32_t tw = word_of(tp[q >> 3], (q >> 1) & 3), dw = word_of(dp[q >> 3], (q >> 1) & 3);
+    const float t = __uint_as_float((q & 1) ? (tw & 0xffff0000u) : (tw << 16));
+    const float d = __uint_as_float((q & 1) ? (dw & 0xffff0000u) : (dw << 16));
+    w[q] = resid_weight(t, d, a, lt2, ld2);
+    s[q & 3] += w[q];
+  }
+  const float L = (s[0] + s[1]) + (s[2] + s[3]);
+  if (!(L > 0.0f)) return;
+  any_pos = true;
+  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(w, uniform_accept(pick_word()) * L);
+}
+
 // Greedy block: running maximum, smallest index on ties.
 template <int N>
 __device__ __forceinline__ void brace_argmax_block(BRace &r, const float (&z)[N], float mz, int v0) {
@@ -531,6 +638,15 @@ __device__ __forceinline__ void warp_merge_rows(const Partial *const (&p)[R], in
 // -------------------------------------------------------------------------
 // Host-side launchers (defined in the kernel translation units).
 // -------------------------------------------------------------------------
+// One residual draw of the recompute verification: request r rejected its draft token at
+// position j (T > 0); the draft row (r, j) is recomputed from the base logits and W1[x_{j-1}] W2.
+struct VJob {
+  int r, j, prev;   // request, rejecting position, x_{j-1} (the anchor for j = 1)
+  int urow;         // base-logit row r K_max + j - 1
+  int trow;         // flattened target row tgt_off[r] + j - 1
+  float lse_t, lse_q, invT;
+};
+
 struct DraftArgs {
   const void *U, *E, *W;
   const void *Wp;     // W2 in the packed tensor-core layout (tensor-core path only)
@@ -547,6 +663,9 @@ struct DraftArgs {
   // workspace carve-out
   int32_t *perm;      // [B] requests ordered by K_r descending
   int32_t *iperm;     // [B] position of each request in perm
+  int32_t *act;       // [K_max, B] row k-1: the requests with K_r >= k in request order (the
+                      // tensor-core path's M-tiles take consecutive runs of it, so a tile's rows
+                      // lie as close together in U as the active set allows)
   int32_t *nact;      // [K_max + 2] active requests per position
   int32_t *counters;  // [B] per-row arrival counters (zero between steps)
   unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path
@@ -570,6 +689,11 @@ struct DraftArgs {
   const float *rnn_x = nullptr;
   float *rnn_state = nullptr;
   float *rnn_feat = nullptr;
+  // residual mode of the tensor-core kernel (the recompute verification): one position whose
+  // rows are jobs[0 .. nact[1]); key and flag per request in best_key / resid_any
+  const VJob *jobs = nullptr;
+  const void *tgt = nullptr;
+  int32_t *resid_any = nullptr;
 };
 
 // Confidence head ("DSpark" S3.2.1): one linear projection of the backbone state and the
@@ -617,6 +741,7 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms);
+cudaError_t launch_resid_tc(const DraftArgs &a, cudaStream_t s, int num_sms);   // residual mode
 constexpr int64_t kTcPartialsPerStep = 128 * 1024;   // slots per draft position on the tensor-core path
 bool draft_tc_shape_ok(const DraftArgs &a);
 size_t draft_packed_bytes(int64_t rank, int64_t V);  // 0 when rank is not a positive multiple of 64
@@ -624,7 +749,8 @@ cudaError_t launch_pack_projection(const void *W, int64_t rank, int64_t V, void 
 
 
 struct VerifyJob {
-  int mode;      // 0 none, 1 residual (T > 0), 2 bonus (T > 0), 3 bonus (greedy)
+  int mode;      // 0 none, 1 residual (T > 0), 2 bonus (T > 0), 3 bonus (greedy),
+                 // 4 residual drawn by the tensor-core recompute pass (token or rounding guard)
   int pos;       // stream position (j, or ell + 1 for the bonus)
   int64_t trow;  // target row
   int64_t drow;  // draft row (residual only)
@@ -632,17 +758,33 @@ struct VerifyJob {
   int out_slot;  // index into out_tok
 };
 
-// Merged statistics of one drafted row: lse_t = log sum exp(target / T) (the maximum for
-// T = 0), amax its argmax, zx_t the scaled target logit at the draft token, and the
-// same two for the draft row when no draft normaliser is given.
-struct RowRes {
-  float lse_t, zx_t, lse_q, zx_d;
+constexpr int kNoReject = 127;   // dead[r] of a request with no rejected position
+
+// One verified drafted row (request r, position j <= ell_r) of the statistics pass; the plan
+// kernel lists them position-major (every request's position 1, then position 2, ...).
+struct VRow {
+  int r, j, x;     // request, position, draft token x_j
+  int trow;        // row of the flattened target logits: tgt_off[r] + j - 1
+  float invT;      // 1 / T (1 for greedy)
+  float lqx;       // log q_j(x_j), T > 0 with a known draft normaliser
+  int kind;        // 1 softmax statistics of the target row, 2 its argmax (T = 0), 3 softmax
+                   // statistics of the target and of the draft row (no draft normaliser)
+  int drow;        // draft row r K_max + j - 1
+};
+
+// Statistics of a completed row: log-sum-exp of target / T (the maximum for T = 0), the
+// argmax, the scaled target logit at x_j and (kind 3) the draft row's log-sum-exp.
+struct VRowRes {
+  float lse_t;
   int amax;
+  float zx_t;
+  float lse_q;
 };
 
 struct VerifyArgs {
-  const void *D;
-  const float *D_lse;
+  const void *D;        // stored draft logits [B, K_max, V]; NULL for the recompute entry point
+  const float *D_lse;   // draft normalisers [B, K_max] (optional with stored logits)
+  const float *D_zx = nullptr;    // drawn tokens' logits [B, K_max] (recompute entry point)
   const void *tgt;
   const int32_t *tgt_off, *ell, *draft_tok;
   const float *temperature;
@@ -650,18 +792,39 @@ struct VerifyArgs {
   int64_t B, K_max, V;
   int dtype;
   PhiloxKey key;
-  int32_t *counters;   // [B] chunk arrivals of the sampling pass, zeroed per call
+  // workspace
+  VRow *rows;           // [B * kMaxK] the verified rows, position-major
+  int32_t *nrows;       // [1] how many
+  int32_t *dead;        // [B] first rejecting position (kNoReject: none)
+  int32_t *arrive;      // [B * kMaxK] warp arrivals per listed row
+  VRowRes *rres;        // [B * kMaxK] request-major: r K_max + j - 1
+  Partial *row_t, *row_d;   // [B * kMaxK * row_slices * 4] per listed row, slice and warp
+  float *zx_t, *zx_d;       // [B * kMaxK] per listed row: scaled logits at the draft token
+  int row_slices;           // vocabulary slices per row of the statistics pass
+  int32_t *counters;   // [B] chunk arrivals of the sampling pass (reset by the plan kernel)
   Partial *partials;   // [B * chunks]
   int chunks;          // vocabulary chunks of the sampling pass (at most the workspace's)
   int chunk_len;       // columns per chunk, a multiple of 32
-  Partial *row_t, *row_d;   // [B * kMaxK * row_slices * 4] target / draft statistics per slice and warp
-  float *zx_t, *zx_d;       // [B * kMaxK] scaled logits at the draft tokens
-  int row_slices;           // vocabulary slices per row of the statistics pass
+  // recompute entry point: the residual draws of the tensor-core pass
+  const unsigned long long *resid_key = nullptr;   // [B] packed (score, index) maximum per request
+  const int32_t *resid_any = nullptr;              // [B] non-zero when some p_v > q_v
+  // recompute entry point, the job pass: lists the T > 0 rejections for the tensor-core pass
+  const int32_t *anchor = nullptr;      // [B] x_0 (the previous token of a rejection at j = 1)
+  VJob *jobs = nullptr;                 // [B]
+  int32_t *jobs_nact = nullptr;         // [3] active counts of the residual pass: {B, #jobs, 0}
+  int32_t *jobs_gbar = nullptr;         // [2] its grid-barrier counters
+  unsigned long long *key_out = nullptr;   // = resid_key, reset per call
+  int32_t *any_out = nullptr;              // = resid_any, reset per call
 };
 
 int verify_row_slices(int64_t V);
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks);
-void verify_carve(VerifyArgs &a, void *workspace);   // jobs, counters, partials, row statistics
-cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms);
+void verify_carve(VerifyArgs &a, void *workspace);
+// resid: the residual pass's arguments for the recompute entry point (nullptr: stored rows)
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms, const DraftArgs *resid = nullptr);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) applies to the current device: set once per
+// (device, kernel), under a lock so that host threads and several devices are safe.
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
 
 }  // namespace dspark

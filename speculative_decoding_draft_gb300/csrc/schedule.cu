@@ -334,13 +334,8 @@ cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
   const size_t pool_bytes = schedule_ws_bytes(a.B, a.K_max);
   const bool in_smem = pool_bytes <= kSmemPoolMax;
   if (in_smem) {
-    static size_t attr_bytes = 0;
-    if (pool_bytes > attr_bytes) {
-      cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemPoolMax);
-      if (e != cudaSuccess) return e;
-      attr_bytes = kSmemPoolMax;
-    }
+    cudaError_t e = ensure_dynamic_smem((const void *)schedule_kernel, (int)kSmemPoolMax);
+    if (e != cudaSuccess) return e;
   }
   schedule_kernel<<<1, kThreads, in_smem ? pool_bytes : 0, s>>>(a, in_smem ? 1 : 0);
   return cudaGetLastError();

@@ -1,25 +1,27 @@
 // Ragged rejection-sampling verification ("DSpark", S2.1; "Speculative
 // decoding, from zero to DSpark", S2 and Appendix A1).
 //
-// Two kernels (after a reset of the per-request arrival counters):
-//  1. verify_rows: one CTA per (drafted row, vocabulary slice) for every position
-//     j = 1..ell_r of every request at once.  Each CTA streams its slice of target
-//     row j (and of the draft row when no draft normaliser is given) with 16-byte
-//     loads, reduces the online-softmax statistics (max, sum of exponentials) of
-//     z/T -- the argmax for T = 0 -- and stores them with the scaled logit at the
-//     draft token.  The last CTA of a request merges the slices of each row in a
-//     fixed order and walks the positions, one lane per position: the first j with
-//     u_j >= min(1, p(x_j)/q(x_j)) (or x_j != argmax for T = 0) ends the walk.  The
-//     walk also produces the sampling job of the request: the residual at the
-//     rejecting position, the bonus row when every position is accepted, or
-//     nothing for greedy rejections (their correction is the argmax already found).
-//     Rows past the first rejection are read too: all rows stream in parallel
-//     instead of one position after another.
-//  2. verify_sample: the residual / bonus two-level draw over the vocabulary,
-//     spread over the whole GPU (request x vocabulary chunk, about two CTAs per
-//     SM in one wave, each thread a run of 32-wide blocks; for the residual on bf16
-//     rows the next block's loads are in flight while a block is drawn), with the
-//     last block of each request merging the chunk partials.
+// Three kernels:
+//  1. verify_plan (one CTA): validates every request, resets its state and lists the
+//     verified rows (r, j <= ell_r) position-major -- every request's position 1, then
+//     position 2, ... -- with the draft side of each accept test precomputed (log q(x_j)
+//     when the draft normaliser is known).
+//  2. verify_scan (persistent): walks (row, vocabulary slice) items in that order.  A
+//     producer warp stages each item's target slice (and the draft slice when no draft
+//     normaliser is given) into a shared-memory ring by bulk copy; four warps reduce the
+//     online-softmax statistics of z/T (the argmax for T = 0) and publish per-warp
+//     partials.  The warp whose arrival completes a row merges its slices in a fixed
+//     order and decides the row at once: accept x_j iff u_j < min(1, p(x_j)/q(x_j)) (x_j
+//     the target argmax for T = 0); a rejection lowers the request's first-rejection word
+//     by atomicMin.  Before staging an item the producer reads that word and skips rows
+//     past an already-known rejection, so the rows read are the ones up to each request's
+//     deciding row, except where a decision is not yet known.  The bulk copies are in the
+//     async proxy: the release fence before a warp's arrival does not wait for them.
+//  3. verify_sample: per request the outcome -- n_acc = (first rejection) - 1 or ell_r,
+//     the accepted tokens -- and the draw: the residual norm(max(0, p - q)) at a
+//     rejection (T > 0), the argmax of the rejecting row (T = 0, known from the scan), or
+//     the bonus from the next target row; spread over (request x vocabulary chunk) CTAs
+//     with the last chunk merging.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -165,50 +167,6 @@ struct RowItem {
   int64_t trow;          // first element of the target row
 };
 
-// Metadata of item `item` (row-major over rows, then slices), the same in every thread.
-// An invalid request raises the status word once (slice 0 of row 1, or of the row with
-// the bad token) and streams nothing.
-__device__ __forceinline__ RowItem row_item(const VerifyArgs &a, int item, int tid) {
-  const int K = (int)a.K_max, V = (int)a.V, S = a.row_slices;
-  RowItem it;
-  it.rowi = item / S;
-  const int sl = item % S;
-  const int r = it.rowi / K, j = it.rowi % K + 1;
-  it.kind = 0;
-  // every value is requested before any is used: one round trip
-  const int l = a.ell[r];
-  const float T = a.temperature[r];
-  const int x = a.draft_tok[it.rowi];
-  const int64_t o0 = a.tgt_off[r], o1 = a.tgt_off[r + 1], of = a.tgt_off[0];
-  const int err = request_error(K, r, l, T, o0, o1, of);
-  if (err) {
-    if (sl == 0 && j == 1 && tid == 0) set_status(a.dev_status, err);
-    return it;
-  }
-  if (j > l) return it;
-  if (x < 0 || x >= V) {
-    if (sl == 0 && tid == 0) set_status(a.dev_status, DSPARK_ERR_TOKEN_RANGE);
-    return it;
-  }
-  it.x = x;
-  it.kind = (T == 0.0f) ? 2 : 1;
-  it.invT = (T == 0.0f) ? 1.0f : 1.0f / T;
-  it.trow = (o0 + j - 1) * (int64_t)V;
-  it.lo = min(V, sl * kRowSlice);
-  it.hi = min(V, it.lo + kRowSlice);
-  return it;
-}
-
-// bf16 rows, 16-byte aligned: the item's kRowPk packed loads per thread.
-__device__ __forceinline__ void row_issue(const VerifyArgs &a, const RowItem &it, int tid, uint4 (&pk)[kRowPk]) {
-#pragma unroll
-  for (int uu = 0; uu < kRowPk; ++uu) {
-    const int v0 = it.lo + (uu * kRowThreads + tid) * 8;
-    pk[uu] = (it.kind && v0 + 8 <= it.hi) ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + it.trow + v0))
-                                          : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 // The item's statistics from its packed loads: the thread's maximum over its 8 kRowPk
 // values first (bf16 pairs, exact), then one pass of exponentials against it, two lanes per
 // fp32 instruction; slots past the slice hold -inf.
@@ -305,35 +263,6 @@ __device__ __forceinline__ void row_generic(const VerifyArgs &a, const RowItem &
   }
 }
 
-// Merge of the slice statistics of drafted row rowi (one warp, lanes over slices, then a
-// fixed shuffle tree: the result does not depend on which CTA streamed which slice).
-// Valid in lane 0.
-__device__ __forceinline__ RowRes row_merge(const VerifyArgs &a, int64_t rowi, bool greedy, bool stream_d, int lane) {
-  const int S = a.row_slices;
-  const bool sd_on = !greedy && stream_d;
-  Stats ct, cd;
-  stats_init(ct);
-  stats_init(cd);
-  const float zt = greedy ? 0.0f : __ldcg(a.zx_t + rowi);
-  const float zd = sd_on ? __ldcg(a.zx_d + rowi) : 0.0f;
-  for (int q = lane; q < S * kRowParts; q += 32) {
-    stats_merge(ct, partial_to_stats(load_partial(a.row_t + rowi * S * kRowParts + q)));
-    if (sd_on) stats_merge(cd, partial_to_stats(load_partial(a.row_d + rowi * S * kRowParts + q)));
-  }
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) {
-    stats_merge(ct, stats_shfl_down(ct, d));
-    if (sd_on) stats_merge(cd, stats_shfl_down(cd, d));
-  }
-  RowRes rr;
-  rr.amax = ct.idx;
-  rr.lse_t = greedy ? ct.best : ct.m + logf(ct.S);
-  rr.zx_t = zt;
-  rr.lse_q = sd_on ? cd.m + logf(cd.S) : 0.0f;
-  rr.zx_d = zd;
-  return rr;
-}
-
 // Warp reduction of one item's statistics, valid in lane 0: the softmax pair (m, S) for
 // T > 0 (a branch-free merge), the (maximum, smallest index) pair for T = 0.
 __device__ __forceinline__ Stats warp_reduce_row(Stats s, int kind) {
@@ -361,130 +290,6 @@ __device__ __forceinline__ Stats warp_reduce_row(Stats s, int kind) {
   return s;
 }
 
-// Statistics pass: persistent CTAs walk the row items (every drafted row of every request,
-// cut into vocabulary slices) with the next item's loads in flight while the current one is
-// reduced.  Per item: the online-softmax statistics (max, sum of exponentials) of the
-// slice of target row j / T -- its argmax for T = 0 -- and of the draft row when no draft
-// normaliser is given, and the scaled logits at the draft token in the slice that holds it.
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows(const __grid_constant__ VerifyArgs a) {
-  constexpr bool kPacked = (DT == DSPARK_BF16) && VEC;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (read_status(a.dev_status)) return;
-  const int S = a.row_slices;
-  const int total = (int)(a.B * a.K_max) * S;
-  const bool stream_d = (a.D_lse == nullptr);
-  int item = blockIdx.x;
-  if (item >= total) return;
-  RowItem cur = row_item(a, item, tid);
-  uint4 pc[kRowPk];
-  if (kPacked) row_issue(a, cur, tid, pc);
-  for (; item < total; item += gridDim.x) {
-    const int nitem = item + gridDim.x;
-    RowItem nxt;
-    nxt.kind = 0;
-    if (nitem < total) nxt = row_item(a, nitem, tid);
-    uint4 pn[kRowPk];
-    if (kPacked) row_issue(a, nxt, tid, pn);   // in flight while this item is reduced
-    if (cur.kind) {
-      const bool sd_on = stream_d && cur.kind == 1;
-      Stats st, sd;
-      stats_init(st);
-      stats_init(sd);
-      // the thread that holds the draft token writes its scaled logits directly
-      if (kPacked && !sd_on) row_consume(cur, pc, tid, st, a.zx_t + cur.rowi);
-      else row_generic<DT, VEC>(a, cur, sd_on, tid, st, sd, a.zx_t + cur.rowi, a.zx_d + cur.rowi);
-      st = warp_reduce_row(st, cur.kind);
-      if (sd_on) sd = warp_reduce_row(sd, 1);
-      if (lane == 0) {
-        const int64_t at = ((int64_t)cur.rowi * S + cur.lo / kRowSlice) * kRowParts + warp;
-        a.row_t[at] = stats_to_partial(st);
-        if (sd_on) a.row_d[at] = stats_to_partial(sd);
-      }
-    }
-    cur = nxt;
-#pragma unroll
-    for (int q = 0; q < kRowPk; ++q) pc[q] = pn[q];
-  }
-}
-
-// The accept walk of request r from its merged rows (one warp; lane j - 1 tests position
-// j, the first rejection ends the walk): the sampling job, and with write_out the
-// accepted tokens, the padding and n_acc.  A greedy rejection's correction (the argmax)
-// is written here too.
-template <int DT>
-__device__ void decide_request(const VerifyArgs &a, int r, int lane, bool write_out, const RowRes *rows,
-                               VerifyJob *out_job) {
-  const int K = (int)a.K_max;
-  const int l = a.ell[r];
-  const float T = a.temperature[r];
-  const bool greedy = (T == 0.0f);
-  const float invT = greedy ? 1.0f : 1.0f / T;
-  const int64_t off = a.tgt_off[r];
-  const int j = lane + 1;
-  bool reject = false;
-  int amax = -1, x = -1;
-  float lt = 0.0f, lq = 0.0f;
-  if (j <= l) {
-    const int64_t rowi = (int64_t)r * K + j - 1;
-    x = a.draft_tok[rowi];
-    const RowRes rr = rows[j - 1];
-    amax = rr.amax;
-    if (greedy) {
-      reject = (x != rr.amax);
-    } else {
-      const float u = uniform_accept(philox(a.key, 0u, (uint32_t)j, (uint32_t)r, kTagAccept).x);
-      lt = rr.lse_t;
-      float lq_x;
-      if (a.D_lse != nullptr) {
-        lq = a.D_lse[rowi];
-        lq_x = load1<DT>(a.D, rowi * a.V + x) * invT - lq;
-      } else {
-        lq = rr.lse_q;
-        lq_x = rr.zx_d - lq;
-      }
-      reject = !(u < expf((rr.zx_t - lt) - lq_x));
-    }
-  }
-  const unsigned rej = __ballot_sync(0xffffffffu, reject);
-  const int n = rej ? __ffs(rej) - 1 : l;                 // accepted drafts
-  const float lt_n = __shfl_sync(0xffffffffu, lt, n & 31);
-  const float lq_n = __shfl_sync(0xffffffffu, lq, n & 31);
-  const int amax_n = __shfl_sync(0xffffffffu, amax, n & 31);
-  if (write_out && lane <= K) {
-    int32_t *out = a.out_tok + (int64_t)r * (K + 1);
-    if (lane < n) out[lane] = x;
-    else if (lane > n) out[lane] = -1;
-  }
-  if (lane == 0) {
-    VerifyJob job;
-    job.mode = 0;
-    job.pos = 0;
-    job.trow = 0;
-    job.drow = 0;
-    job.lse_t = lt_n;
-    job.lse_q = lq_n;
-    job.invT = invT;
-    job.out_slot = r * (K + 1) + n;
-    if (rej) {
-      if (greedy) {
-        if (write_out) a.out_tok[(int64_t)r * (K + 1) + n] = amax_n;
-      } else {
-        job.mode = 1;
-        job.pos = n + 1;
-        job.trow = off + n;
-        job.drow = (int64_t)r * K + n;
-      }
-    } else {
-      job.mode = greedy ? 3 : 2;
-      job.pos = l + 1;
-      job.trow = off + l;
-    }
-    if (write_out) a.n_acc[r] = n;
-    *out_job = job;
-  }
-}
-
 // --------------------------------------------------------------------------
 // residual / bonus sampling
 // --------------------------------------------------------------------------
@@ -508,11 +313,6 @@ __device__ __forceinline__ void issue_block(const void *base, int64_t row_off, i
                                   : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
 }
 
-// Residual weight max(0, p - q) with p = 2^(t a - lt2), q = 2^(d a - ld2).
-__device__ __forceinline__ float resid_weight(float t, float d, float a, float lt2, float ld2) {
-  return fmaxf(fast_ex2(fmaf(t, a, -lt2)) - fast_ex2(fmaf(d, a, -ld2)), 0.0f);
-}
-
 // One block of residual weights in the two-level draw.
 template <class PickWord>
 __device__ __forceinline__ void brace_resid_block(BRace &r, float (&t)[kBlockW], const float (&d)[kBlockW],
@@ -528,28 +328,6 @@ __device__ __forceinline__ void brace_resid_block(BRace &r, float (&t)[kBlockW],
   if (!(L > 0.0f)) return;
   any_pos = true;
   if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(t, uniform_accept(pick_word()) * L);
-}
-
-// brace_resid_block on packed bf16 rows: the same weights in the same order, unpacked
-// one pair at a time.
-template <class PickWord>
-__device__ __forceinline__ void brace_resid_packed(BRace &r, const uint4 (&tp)[4], const uint4 (&dp)[4], float a,
-                                                   float lt2, float ld2, uint32_t wb, int v0, bool &any_pos,
-                                                   PickWord pick_word) {
-  float w[kBlockW];
-  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-  for (int q = 0; q < kBlockW; ++q) {
-    const uint32_t tw = word_of(tp[q >> 3], (q >> 1) & 3), dw = word_of(dp[q >> 3], (q >> 1) & 3);
-    const float t = __uint_as_float((q & 1) ? (tw & 0xffff0000u) : (tw << 16));
-    const float d = __uint_as_float((q & 1) ? (dw & 0xffff0000u) : (dw << 16));
-    w[q] = resid_weight(t, d, a, lt2, ld2);
-    s[q & 3] += w[q];
-  }
-  const float L = (s[0] + s[1]) + (s[2] + s[3]);
-  if (!(L > 0.0f)) return;
-  any_pos = true;
-  if (brace_enter(r, fast_lg2(L) * kLn2, wb)) r.idx = v0 + pick_in_block(w, uniform_accept(pick_word()) * L);
 }
 
 // The draw of one request over [lo, hi): residual (mode 1), bonus from the
@@ -607,35 +385,375 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
   }
 }
 
+// ---------------------------------------------------------------------------
+// 1. plan: validation, per-request reset, the position-major row list
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+// 0 when request r is valid (lengths, offsets, temperature, the draft tokens it verifies),
+// else the status code.
+__device__ __forceinline__ int request_check(const VerifyArgs &a, int r) {
+  const int K = (int)a.K_max, V = (int)a.V;
+  const int l = a.ell[r];
+  const int err = request_error(K, r, l, a.temperature[r], a.tgt_off[r], a.tgt_off[r + 1], a.tgt_off[0]);
+  if (err) return err;
+  for (int j = 1; j <= l; ++j) {
+    const int x = a.draft_tok[(int64_t)r * K + j - 1];
+    if (x < 0 || x >= V) return DSPARK_ERR_TOKEN_RANGE;
+  }
+  return 0;
+}
+
+// One CTA: counts the rows of every position (shared atomics), then lists each valid
+// request's rows j = 1..ell_r at start[j] + (its rank among position j's rows).  The order
+// inside a position is whatever the atomics give; no result depends on it (each row is
+// decided on its own, and its slices merge in slice order).
+template <int DT>
+__global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constant__ VerifyArgs a) {
+  __shared__ int cnt[kMaxK + 2], fill[kMaxK + 2], start[kMaxK + 2];
+  if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x;
+  if (tid < kMaxK + 2) {
+    cnt[tid] = 0;
+    fill[tid] = 0;
+  }
+  __syncthreads();
+  for (int r = tid; r < B; r += kPlanThreads) {
+    a.dead[r] = kNoReject;
+    a.counters[r] = 0;
+    const int err = request_check(a, r);
+    if (err) {
+      set_status(a.dev_status, err);
+      continue;
+    }
+    const int l = a.ell[r];
+    for (int j = 1; j <= l; ++j) atomicAdd(&cnt[j], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    start[1] = 0;
+    for (int j = 1; j <= K; ++j) start[j + 1] = start[j] + cnt[j];
+    *a.nrows = start[K + 1];
+  }
+  __syncthreads();
+  for (int r = tid; r < B; r += kPlanThreads) {
+    if (request_check(a, r)) continue;
+    const int l = a.ell[r];
+    const float T = a.temperature[r];
+    const bool greedy = (T == 0.0f);
+    const float invT = greedy ? 1.0f : 1.0f / T;
+    const int off = a.tgt_off[r];
+    for (int j = 1; j <= l; ++j) {
+      VRow w;
+      w.r = r;
+      w.j = j;
+      w.drow = r * K + j - 1;
+      w.x = a.draft_tok[w.drow];
+      w.trow = off + j - 1;
+      w.invT = invT;
+      w.lqx = 0.0f;
+      if (greedy) {
+        w.kind = 2;
+      } else if (a.D_lse != nullptr) {
+        // log q(x_j) from the draft normaliser and the drawn token's logit (its own output, or
+        // the stored row's element)
+        const float zx = a.D_zx ? a.D_zx[w.drow] : load1<DT>(a.D, (int64_t)w.drow * a.V + w.x);
+        w.lqx = zx * invT - a.D_lse[w.drow];
+        w.kind = 1;
+      } else {
+        w.kind = 3;
+      }
+      const int slot = start[j] + atomicAdd(&fill[j], 1);
+      a.rows[slot] = w;
+      a.arrive[slot] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. scan: staged row statistics with the accept decision at each row's completion
+// ---------------------------------------------------------------------------
+constexpr int kScanWarps = kRowThreads / 32;        // reducing warps; one more warp stages
+constexpr int kScanThreads = kRowThreads + 32;
+constexpr int kScanStages = 3;
+constexpr int kSliceBytes = kRowSlice * 2;          // one bf16 slice (24 KB)
+
+struct ScanMeta {
+  VRow w;
+  int ri, sl, kind;   // listed row, slice, kind (0: skipped)
+};
+
+// Merge of listed row ri's slice partials (one warp: lanes over the partials in a fixed
+// order, then a fixed shuffle tree) and the accept decision; lane 0 stores the row's
+// statistics and lowers the request's first-rejection word on a rejection.
+__device__ void decide_row(const VerifyArgs &a, const VRow &w, int ri, int S, int lane) {
+  const bool greedy = (w.kind == 2), two = (w.kind == 3);
+  Stats ct, cd;
+  stats_init(ct);
+  stats_init(cd);
+  const Partial *pt = a.row_t + (int64_t)ri * S * kRowParts;
+  const Partial *pd = a.row_d + (int64_t)ri * S * kRowParts;
+  for (int q = lane; q < S * kRowParts; q += 32) {
+    stats_merge(ct, partial_to_stats(load_partial(pt + q)));
+    if (two) stats_merge(cd, partial_to_stats(load_partial(pd + q)));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    stats_merge(ct, stats_shfl_down(ct, d));
+    if (two) stats_merge(cd, stats_shfl_down(cd, d));
+  }
+  if (lane != 0) return;
+  VRowRes rr;
+  rr.amax = ct.idx;
+  rr.lse_t = greedy ? ct.best : ct.m + logf(ct.S);
+  rr.zx_t = greedy ? 0.0f : __ldcg(a.zx_t + ri);
+  rr.lse_q = two ? cd.m + logf(cd.S) : 0.0f;
+  bool reject;
+  if (greedy) {
+    reject = (w.x != rr.amax);
+  } else {
+    const float u = uniform_accept(philox(a.key, 0u, (uint32_t)w.j, (uint32_t)w.r, kTagAccept).x);
+    const float lqx = two ? __ldcg(a.zx_d + ri) - rr.lse_q : w.lqx;
+    reject = !(u < expf((rr.zx_t - rr.lse_t) - lqx));
+  }
+  a.rres[(int64_t)w.r * a.K_max + w.j - 1] = rr;
+  if (reject) atomicMin(a.dead + w.r, w.j);
+}
+
+// Persistent CTAs walk the (listed row, slice) items, item = blockIdx.x + t * gridDim.x.
+// BULK (bf16, 16-byte aligned rows): warp kScanWarps stages each item by bulk copy into a
+// kScanStages ring; otherwise the reducing warps load the slice themselves (VEC: 16-byte
+// loads) and the staging warp only prepares the item.
+template <int DT, bool VEC, bool BULK>
+__global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constant__ VerifyArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kScanStages], empty[kScanStages];
+  __shared__ ScanMeta meta[kScanStages];
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (read_status(a.dev_status)) return;
+  const int S = a.row_slices, V = (int)a.V;
+  const int64_t nitems = (int64_t)(*(volatile const int32_t *)a.nrows) * S;
+  const int64_t G = gridDim.x;
+  if ((int64_t)blockIdx.x >= nitems) return;
+  const bool two = (a.D_lse == nullptr);
+  const uint32_t stage_bytes = BULK ? (two ? 2u : 1u) * kSliceBytes : 0u;
+  const uint32_t bar_full = smem_u32(&full[0]), bar_empty = smem_u32(&empty[0]);
+  if (tid == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kScanWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int *abort = &abort_flag;
+
+  if (warp == kScanWarps) {
+    // ---------------- staging warp (lane 0) ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t last_use[kScanStages];
+      bool issued[kScanStages];
+#pragma unroll
+      for (int s = 0; s < kScanStages; ++s) {
+        last_use[s] = 0;
+        issued[s] = false;
+      }
+      int t = 0;
+      for (int64_t item = blockIdx.x; item < nitems; item += G, ++t) {
+        const int s = t % kScanStages;
+        const uint32_t use = (uint32_t)(t / kScanStages);
+        if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
+        ScanMeta m;
+        m.ri = (int)(item / S);
+        m.sl = (int)(item % S);
+        m.w = a.rows[m.ri];
+        // rows past a rejection already found need no statistics
+        m.kind = (*(volatile const int32_t *)(a.dead + m.w.r) < m.w.j) ? 0 : m.w.kind;
+        meta[s] = m;
+        if (!BULK || m.kind == 0) {
+          mbar_arrive(bar_full + 8 * s);
+          continue;
+        }
+        const int lo = m.sl * kRowSlice;
+        const uint32_t bytes = (uint32_t)(min(kRowSlice, V - lo) * 2);
+        const uint32_t dst = smem_u32(ring) + (uint32_t)s * stage_bytes;
+        mbar_arrive_tx(bar_full + 8 * s, bytes * (m.kind == 3 ? 2u : 1u));
+        bulk_g2s(dst, (const unsigned short *)a.tgt + ((int64_t)m.w.trow * V + lo), bytes, bar_full + 8 * s, pol);
+        if (m.kind == 3)
+          bulk_g2s(dst + kSliceBytes, (const unsigned short *)a.D + ((int64_t)m.w.drow * V + lo), bytes,
+                   bar_full + 8 * s, pol);
+#pragma unroll
+        for (int q = 0; q < kScanStages; ++q)
+          if (q == s) {
+            last_use[q] = use;
+            issued[q] = true;
+          }
+      }
+      if (*abort) {   // wait (bounded) until the copies issued into each stage have landed
+#pragma unroll
+        for (int q = 0; q < kScanStages; ++q) {
+          if (!issued[q]) continue;
+          const long long t0 = clock64();
+          while (!mbar_try(bar_full + 8 * q, last_use[q] & 1u) && clock64() - t0 < kTimeoutCycles / 4) {
+          }
+        }
+        set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
+      }
+    }
+    return;
+  }
+
+  // ---------------- reducing warps ----------------
+  int t = 0;
+  for (int64_t item = blockIdx.x; item < nitems; item += G, ++t) {
+    const int s = t % kScanStages;
+    const uint32_t use = (uint32_t)(t / kScanStages);
+    if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
+    const ScanMeta m = meta[s];
+    Stats st, sd;
+    stats_init(st);
+    stats_init(sd);
+    RowItem it;
+    it.rowi = m.w.drow;
+    it.x = m.w.x;
+    it.kind = (m.kind == 2) ? 2 : (m.kind ? 1 : 0);
+    it.invT = m.w.invT;
+    it.trow = (int64_t)m.w.trow * V;
+    it.lo = min(V, m.sl * kRowSlice);
+    it.hi = min(V, it.lo + kRowSlice);
+    float *own_t = a.zx_t + m.ri, *own_d = a.zx_d + m.ri;
+    if (m.kind) {
+      if (BULK) {
+        const uint32_t base = smem_u32(ring) + (uint32_t)s * stage_bytes;
+        uint4 pk[kRowPk];
+#pragma unroll
+        for (int q = 0; q < kRowPk; ++q) pk[q] = ld_shared_u4(base + 16u * (uint32_t)(q * kRowThreads + tid));
+        row_consume(it, pk, tid, st, own_t);
+        if (m.kind == 3) {
+#pragma unroll
+          for (int q = 0; q < kRowPk; ++q)
+            pk[q] = ld_shared_u4(base + kSliceBytes + 16u * (uint32_t)(q * kRowThreads + tid));
+          RowItem itd = it;
+          itd.kind = 1;
+          row_consume(itd, pk, tid, sd, own_d);
+        }
+      } else {
+        row_generic<DT, VEC>(a, it, m.kind == 3, tid, st, sd, own_t, own_d);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the stage is read
+    if (!m.kind) continue;
+    st = warp_reduce_row(st, it.kind);
+    if (m.kind == 3) sd = warp_reduce_row(sd, 1);
+    if (lane == 0) {
+      const int64_t at = ((int64_t)m.ri * S + m.sl) * kRowParts + warp;
+      a.row_t[at] = stats_to_partial(st);
+      if (m.kind == 3) a.row_d[at] = stats_to_partial(sd);
+    }
+    // each lane releases what it wrote (the partial, the logit at the draft token); these
+    // lanes have no global loads in flight, so the fences are short
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = (atomicAdd(a.arrive + m.ri, 1) == S * kRowParts - 1);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      decide_row(a, m.w, m.ri, S, lane);
+    }
+  }
+  if (*abort && tid == 0) set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// 3. sampling: outcome per request and the residual / bonus draw
+// ---------------------------------------------------------------------------
+// Request r's outcome from the scan (one warp): n = (first rejection) - 1, or ell_r when no
+// position was rejected; with write_out the accepted tokens, the padding, n_acc and a greedy
+// rejection's correction (the argmax of the rejecting row) are written.  Returns the draw
+// job in lane 0.
+__device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_out, VerifyJob *out_job) {
+  const int K = (int)a.K_max;
+  const int l = a.ell[r];
+  const float T = a.temperature[r];
+  const bool greedy = (T == 0.0f);
+  const int dead = a.dead[r];
+  const int n = dead <= l ? dead - 1 : l;                  // accepted drafts
+  if (write_out && lane <= K) {
+    int32_t *out = a.out_tok + (int64_t)r * (K + 1);
+    if (lane < n) out[lane] = a.draft_tok[(int64_t)r * K + lane];
+    else if (lane > n) out[lane] = -1;
+  }
+  if (lane != 0) return;
+  const int64_t off = a.tgt_off[r];
+  VerifyJob job;
+  job.mode = 0;
+  job.pos = 0;
+  job.trow = 0;
+  job.drow = 0;
+  job.lse_t = 0.0f;
+  job.lse_q = 0.0f;
+  job.invT = greedy ? 1.0f : 1.0f / T;
+  job.out_slot = r * (K + 1) + n;
+  if (n < l) {                                             // rejected at position n + 1
+    const VRowRes rr = a.rres[(int64_t)r * K + n];
+    if (greedy) {
+      if (write_out) a.out_tok[job.out_slot] = rr.amax;
+    } else {
+      job.mode = a.resid_key ? 4 : 1;
+      job.pos = n + 1;
+      job.trow = off + n;
+      job.drow = (int64_t)r * K + n;
+      job.lse_t = rr.lse_t;
+      job.lse_q = a.D_lse ? a.D_lse[job.drow] : rr.lse_q;
+    }
+  } else {
+    job.mode = greedy ? 3 : 2;
+    job.pos = l + 1;
+    job.trow = off + l;
+  }
+  if (write_out) a.n_acc[r] = n;
+  *out_job = job;
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_constant__ VerifyArgs a) {
   __shared__ Race red[kSampleThreads / 32];
   __shared__ int s_any[kSampleThreads / 32];
   __shared__ int s_last, s_tok;
   __shared__ VerifyJob s_job;
-  __shared__ RowRes s_rows[kMaxK];
   const int cx = blockIdx.x, tid = threadIdx.x;
   if (read_status(a.dev_status)) return;
-  const int K = (int)a.K_max;
+  const int V = (int)a.V;
   for (int r = blockIdx.y; r < (int)a.B; r += gridDim.y) {
-    // every chunk merges the request's row statistics (a warp per row) and walks its
-    // positions -- the same decision everywhere; chunk 0 writes the accepted tokens
-    {
-      const bool greedy = a.temperature[r] == 0.0f;
-      const bool stream_d = (a.D_lse == nullptr);
-      const int l = a.ell[r];
-      for (int jw = tid >> 5; jw < l; jw += kSampleThreads / 32) {
-        const RowRes rr = row_merge(a, (int64_t)r * K + jw, greedy, stream_d, tid & 31);
-        if ((tid & 31) == 0) s_rows[jw] = rr;
-      }
-    }
-    __syncthreads();
-    if (tid < 32) decide_request<DT>(a, r, tid, cx == 0, s_rows, &s_job);
+    // every chunk reads the same outcome; chunk 0 writes the accepted tokens
+    if (tid < 32) job_from_scan(a, r, tid, cx == 0, &s_job);
     __syncthreads();
     const VerifyJob job = s_job;
     __syncthreads();
     if (job.mode == 0) continue;
-    const int V = (int)a.V;
+    if (job.mode == 4) {
+      // the residual was drawn by the tensor-core recompute pass: its token, or (no p > q
+      // survived rounding anywhere) the draw from p on the rejecting row; chunk 0 only
+      if (cx != 0) continue;
+      int tok = -1;
+      if (a.resid_any[r]) {
+        tok = key_index(a.resid_key[r]);
+      } else {
+        BRace bp;
+        brace_init(bp);
+        bool dummy = false;
+        sample_range<DT, VEC>(a, job, r, 0, V, tid, kSampleThreads, bp, dummy, true);
+        tok = race_block_reduce(from_partial(to_partial(bp)), red).idx;
+      }
+      if (tid == 0) a.out_tok[job.out_slot] = tok;
+      __syncthreads();
+      continue;
+    }
     const int lo = min(V, cx * a.chunk_len), hi = min(V, lo + a.chunk_len);
     BRace br;
     brace_init(br);
@@ -683,16 +801,51 @@ __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_
       const Race rp = race_block_reduce(from_partial(to_partial(bp)), red);
       if (tid == 0) s_tok = rp.idx;
     }
-    if (tid == 0) {
-      a.out_tok[job.out_slot] = s_tok;
-      a.counters[r] = 0;
-    }
+    if (tid == 0) a.out_tok[job.out_slot] = s_tok;
     __syncthreads();
   }
 }
 
-template <int DT, bool VEC>
-cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms) {
+// Recompute entry point: the T > 0 rejections become the jobs of the tensor-core residual
+// pass (one CTA; the order of the list is the atomics' and changes no result), and that pass's
+// keys, flags and counters start from zero.
+__global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constant__ VerifyArgs a) {
+  __shared__ int count;
+  if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x;
+  if (tid == 0) count = 0;
+  __syncthreads();
+  for (int r = tid; r < B; r += kPlanThreads) {
+    a.key_out[r] = 0ull;
+    a.any_out[r] = 0;
+    const int l = a.ell[r];
+    const int dead = a.dead[r];
+    const int n = dead <= l ? dead - 1 : l;
+    const float T = a.temperature[r];
+    if (n >= l || T == 0.0f) continue;
+    VJob jb;
+    jb.r = r;
+    jb.j = n + 1;
+    jb.prev = (n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1];
+    jb.urow = r * K + n;
+    jb.trow = a.tgt_off[r] + n;
+    jb.lse_t = a.rres[(int64_t)r * K + n].lse_t;
+    jb.lse_q = a.D_lse[(int64_t)r * K + n];
+    jb.invT = 1.0f / T;
+    a.jobs[atomicAdd(&count, 1)] = jb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.jobs_nact[0] = B;
+    a.jobs_nact[1] = count;
+    a.jobs_nact[2] = 0;
+    a.jobs_gbar[0] = 0;
+    a.jobs_gbar[1] = 0;
+  }
+}
+
+template <int DT, bool VEC, bool BULK>
+cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftArgs *resid) {
   // sampling chunks: about two CTAs per SM over all requests in one wave, each chunk a
   // multiple of 32 columns (the blocks of the two-level draw) and at most a.chunks of them
   {
@@ -702,11 +855,27 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms) {
     a.chunk_len = (int)((per + kBlockW - 1) / kBlockW * kBlockW);
     a.chunks = (int)((a.V + a.chunk_len - 1) / a.chunk_len);
   }
-  const int64_t items = a.B * a.K_max * (int64_t)a.row_slices;
-  const int64_t grid = items < (int64_t)kRowCtasPerSm * num_sms ? items : (int64_t)kRowCtasPerSm * num_sms;
-  if (grid > 0) {
-    verify_rows<DT, VEC><<<(unsigned)grid, kRowThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+  verify_plan<DT><<<1, kPlanThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // scan: a wave of persistent CTAs (3 per SM with single-row stages, 1 with two rows)
+  const bool two = (a.D_lse == nullptr);
+  const int smem = BULK ? kScanStages * kSliceBytes * (two ? 2 : 1) : 0;
+  if (BULK) {
+    e = ensure_dynamic_smem((const void *)verify_scan<DT, VEC, BULK>, smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t max_items = a.B * a.K_max * (int64_t)a.row_slices;
+  const int64_t per_sm = (BULK && two) ? 1 : 3;
+  const int64_t grid = max_items < per_sm * num_sms ? max_items : per_sm * num_sms;
+  verify_scan<DT, VEC, BULK><<<(unsigned)grid, kScanThreads, smem, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (resid) {
+    verify_jobs<<<1, kPlanThreads, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_resid_tc(*resid, s, num_sms);
     if (e != cudaSuccess) return e;
   }
   verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)(a.B < 65535 ? a.B : 65535)), kSampleThreads, 0, s>>>(a);
@@ -717,17 +886,20 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms) {
 
 int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice); }
 
-// Workspace layout (every part 256-byte aligned): chunk counters [B] (zeroed at the start
-// of every call), sampling partials [B * chunks], slice statistics of the target and draft
-// rows [B * kMaxK * slices * warps] each, scaled logits at the draft tokens [B * kMaxK] each.  Rows
-// are sized for kMaxK positions so the size depends on B and V only.
+// Workspace layout (every part 256-byte aligned): sampling counters [B], sampling partials
+// [B * chunks], slice statistics of the target and draft rows [B * kMaxK * slices * warps]
+// each, scaled logits at the draft tokens [B * kMaxK] each, the listed rows [B * kMaxK], their
+// count, the first-rejection words [B], the row arrivals [B * kMaxK], the row results
+// [B * kMaxK].  Rows are sized for kMaxK positions so the size depends on B and V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   const int c = (int)((V + kSampleUnit - 1) / kSampleUnit);   // the most chunks a call uses
   if (chunks) *chunks = c;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)B * (size_t)kMaxK;
   return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) +
-         2 * al(sizeof(Partial) * rows * verify_row_slices(V) * kRowParts) + 2 * al(sizeof(float) * rows);
+         2 * al(sizeof(Partial) * rows * verify_row_slices(V) * kRowParts) + 2 * al(sizeof(float) * rows) +
+         al(sizeof(VRow) * rows) + al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) +
+         al(sizeof(int32_t) * rows) + al(sizeof(VRowRes) * rows);
 }
 
 void verify_carve(VerifyArgs &a, void *workspace) {
@@ -749,17 +921,27 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   a.zx_t = (float *)p;
   p += al(sizeof(float) * rows);
   a.zx_d = (float *)p;
+  p += al(sizeof(float) * rows);
+  a.rows = (VRow *)p;
+  p += al(sizeof(VRow) * rows);
+  a.nrows = (int32_t *)p;
+  p += al(sizeof(int32_t));
+  a.dead = (int32_t *)p;
+  p += al(sizeof(int32_t) * (size_t)a.B);
+  a.arrive = (int32_t *)p;
+  p += al(sizeof(int32_t) * rows);
+  a.rres = (VRowRes *)p;
 }
 
-cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms) {
-  // arrival counters start from zero on every call (the workspace may be fresh)
-  cudaError_t e0 = cudaMemsetAsync(a.counters, 0, sizeof(int32_t) * (size_t)a.B, s);
-  if (e0 != cudaSuccess) return e0;
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms, const DraftArgs *resid) {
   const int esz = a.dtype == DSPARK_F32 ? 4 : 2;
-  const bool vec = ((a.V * esz) % 16 == 0) && ((uintptr_t)a.tgt % 16 == 0) && ((uintptr_t)a.D % 16 == 0);
+  const bool vec = ((a.V * esz) % 16 == 0) && ((uintptr_t)a.tgt % 16 == 0) &&
+                   (a.D == nullptr || (uintptr_t)a.D % 16 == 0);
   if (a.dtype == DSPARK_F32)
-    return vec ? launch_typed<DSPARK_F32, true>(a, s, num_sms) : launch_typed<DSPARK_F32, false>(a, s, num_sms);
-  return vec ? launch_typed<DSPARK_BF16, true>(a, s, num_sms) : launch_typed<DSPARK_BF16, false>(a, s, num_sms);
+    return vec ? launch_typed<DSPARK_F32, true, false>(a, s, num_sms, resid)
+               : launch_typed<DSPARK_F32, false, false>(a, s, num_sms, resid);
+  return vec ? launch_typed<DSPARK_BF16, true, true>(a, s, num_sms, resid)
+             : launch_typed<DSPARK_BF16, false, false>(a, s, num_sms, resid);
 }
 
 }  // namespace dspark

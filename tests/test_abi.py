@@ -109,3 +109,23 @@ def test_host_validation_needs_no_device(lib):
     vd = ds.Dims(4, 7, 1000, 0, ds.BF16, 0)
     assert lib.dspark_verify_ragged(one, null, one, one, one, one, one, 0, vd, one, one, ctypes.c_void_p(300),
                                     1 << 30, one, null) == 10
+
+
+def test_verify_markov_host_validation(lib):
+    # the recompute verification: null pointers, shapes without a tensor-core path, short workspaces
+    import speculative_decoding_draft_gb300 as ds
+    one = ctypes.c_void_p(256)
+    null = None
+    dims = ds.Dims(4, 7, 1024, 256, ds.BF16, ds.FLAG_W_PACKED)
+    args = [one] * 11
+    assert lib.dspark_verify_markov(*([null] + args[1:]), 0, dims, one, one, one, 1 << 30, one, null) == 1
+    assert lib.dspark_verify_markov_workspace_bytes(dims) > lib.dspark_verify_workspace_bytes(4, 1024)
+    assert lib.dspark_verify_markov_workspace_bytes(ds.Dims(4, 7, 1024, 256, ds.F32, 0)) == 0
+    assert lib.dspark_verify_markov_workspace_bytes(ds.Dims(4, 7, 1024, 96, ds.BF16, 0)) == 0
+    assert lib.dspark_verify_markov(*args, 0, ds.Dims(4, 7, 1024, 96, ds.BF16, 0), one, one, one, 1 << 30, one,
+                                    null) == 13
+    assert lib.dspark_verify_markov(*args, 0, dims, one, one, one, 16, one, null) == 10
+    # a W given as is is packed into the workspace, which grows by the packed size
+    unpacked = ds.Dims(4, 7, 1024, 256, ds.BF16, 0)
+    assert (lib.dspark_verify_markov_workspace_bytes(unpacked) - lib.dspark_verify_markov_workspace_bytes(dims)
+            >= lib.dspark_draft_packed_projection_bytes(256, 1024))

@@ -1,8 +1,10 @@
 """The benchmark's step chained through the C ABI, against the oracle's chain.
 
-The GPU step is exactly the one the benchmark times: the draft (W2 packed once) writes
-tokens, logits and normalisers; the scheduler computes the lengths and offsets; verification
-consumes the GPU's own draft outputs and the target rows laid out by the GPU's offsets.  The
+The GPU step is the one the benchmark times: the draft (W2 packed once) writes tokens,
+normalisers and the drawn tokens' logits; the scheduler computes the lengths and offsets;
+verification consumes the GPU's own draft outputs and the target rows laid out by the GPU's
+offsets, recomputing the rejecting draft rows (the same step with stored logits and the
+stored-row verification is checked as well).  The
 oracle runs the same chain on its own: its draft of the compared requests, its schedule of the
 whole batch, its verification of those requests on its own draft.  Schedules are compared
 bit-exactly in full; drafts as in the draft parity tests; verification outcomes (accepted
@@ -34,18 +36,27 @@ def _built():
     __graft_entry__.build()
 
 
-def _gpu_step(cfg, g, sps_variant):
+def _gpu_step(cfg, g, sps_variant, markov=False):
+    """markov: the benchmark's step -- the draft stores no logits and verification recomputes the
+    rejecting rows (dspark_verify_markov); otherwise the draft stores its logits and
+    dspark_verify_ragged reads them."""
     W = ds.pack_projection(g["W"]) if cfg.dtype == "bf16" and cfg.rank % 64 == 0 and cfg.rank <= 256 \
         and cfg.V % 8 == 0 else g["W"]
-    d = ds.draft_markov_sample(g["U"], g["E"], W, g["anchor"], g["K_r"], g["temperature"], cfg.philox_seed)
+    d = ds.draft_markov_sample(g["U"], g["E"], W, g["anchor"], g["K_r"], g["temperature"], cfg.philox_seed,
+                               want_logits=not markov)
     conf = wl.confidences(cfg, "cpu")
     sps = wl.sps_table(cfg, sps_variant)
     s = ds.schedule_survival(conf.to(DEV), g["K_r"], sps.to(DEV), status=d["status"])
     tgt = wl.target_dense(cfg, g["U"], g["K_r"])
     flat, off = wl.flatten_targets(tgt, s["ell"])
     del tgt
-    v = ds.verify_ragged(d["draft_logits"], flat, s["tgt_off"], s["ell"], d["draft_tok"], g["temperature"],
-                         cfg.philox_seed + VERIFY_SEED_OFFSET, draft_lse=d["draft_lse"], status=d["status"])
+    if markov:
+        v = ds.verify_markov(g["U"], g["E"], W, g["anchor"], d["draft_lse"], d["draft_tok_logit"], flat,
+                             s["tgt_off"], s["ell"], d["draft_tok"], g["temperature"],
+                             cfg.philox_seed + VERIFY_SEED_OFFSET, status=d["status"])
+    else:
+        v = ds.verify_ragged(d["draft_logits"], flat, s["tgt_off"], s["ell"], d["draft_tok"], g["temperature"],
+                             cfg.philox_seed + VERIFY_SEED_OFFSET, draft_lse=d["draft_lse"], status=d["status"])
     assert ds.check(d["status"]) == "DSPARK_OK"
     assert torch.equal(off.to(DEV), s["tgt_off"])
     return d, s, v, flat, conf, sps
@@ -98,11 +109,21 @@ def test_step_chain_small(name, kw, sps_variant):
     _check(cfg, g, np.arange(cfg.B), d, s, v, flat, conf, sps)
 
 
+@pytest.mark.parametrize("name,kw", [("ragged", dict(B=150, K_max=5, V=4104)), ("qwen", dict(B=40, K_max=7, V=2056))])
+@pytest.mark.parametrize("sps_variant", ["literal", "step"])
+def test_step_chain_small_recompute(name, kw, sps_variant):
+    cfg = wl.small_config(name, **kw)
+    g = {k: v.to(DEV) for k, v in wl.draft_inputs(cfg, "cpu").items()}
+    d, s, v, flat, conf, sps = _gpu_step(cfg, g, sps_variant, markov=True)
+    _check(cfg, g, np.arange(cfg.B), d, s, v, flat, conf, sps)
+
+
 @pytest.mark.parametrize("name", ["qwen", "ragged"])
-def test_step_chain_full_size(name):
+@pytest.mark.parametrize("markov", [True, False])
+def test_step_chain_full_size(name, markov):
     cfg = wl.CONFIGS[name]
     g = wl.draft_inputs(cfg, DEV)
-    d, s, v, flat, conf, sps = _gpu_step(cfg, g, "literal")
+    d, s, v, flat, conf, sps = _gpu_step(cfg, g, "literal", markov=markov)
     _check(cfg, g, sample_rows(cfg, 16), d, s, v, flat, conf, sps)
     del g, d, s, v, flat
     torch.cuda.empty_cache()
