@@ -55,8 +55,7 @@ constexpr int kUDepth = 3;                       // U blocks each epilogue warp 
 constexpr int kUSlot = 32 * 64;                  // one 32-wide block of a warp's 32 rows (2 KB)
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
-constexpr int kOffU = kOffW + kStages * kStageBytes;
-constexpr int kOffSh = kOffU + kEpiWarps * kUDepth * kUSlot;
+constexpr int kOffSh = kOffW + kStages * kStageBytes + kEpiWarps * kUDepth * kUSlot;
 
 struct TcShared {
   uint64_t full[kStages];
@@ -125,8 +124,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 16-byte streaming load of bf16 data read once.
-__device__ __forceinline__ uint4 ld_stream_u4(const unsigned short *p) { return __ldcs((const uint4 *)p); }
 __device__ __forceinline__ void st_u4_hint(void *ptr, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(policy)
@@ -204,6 +201,9 @@ __device__ __forceinline__ int range_lo(int j, int nb, int gm) { return (int)((i
 template <int RCH, bool RESID>   // rank / 64
 __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __grid_constant__ DraftArgs a) {
   constexpr int kRank = RCH * 64;
+  constexpr int NS = kStages;
+  constexpr int kOffUr = kOffW + NS * kStageBytes;
+  constexpr int kLook = kUDepth;
   constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
   volatile int *abort = &sh.abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         for (int bt = b0; bt < b1 && !*abort; bt += kMaxBlk) {
           const int m = min(kMaxBlk, b1 - bt);
           for (int c = 0; c < RCH; ++c, ++it) {
-            const int s = (int)(it % kStages);
-            const uint32_t use = it / kStages;
+            const int s = (int)(it % NS);
+            const uint32_t use = it / NS;
             if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
             mbar_arrive_tx(bar_full + 8 * s, (uint32_t)(m * kPiece));
             bulk_g2s(sb + kOffW + s * kStageBytes, Wp + ((int64_t)c * nb + bt) * kPiece, (uint32_t)(m * kPiece),
@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             const uint32_t d = tmem + (uint32_t)(b * kAccCols);
             const uint32_t idesc = idesc_n(m * kBlkN);
             for (int c = 0; ok && c < RCH; ++c, ++it) {
-              const int s = (int)(it % kStages);
-              const uint32_t use = it / kStages;
+              const int s = (int)(it % NS);
+              const uint32_t use = it / NS;
               if (!(ok = mbar_wait(bar_full + 8 * s, use & 1u, abort))) break;
               tc_fence_after();
 #pragma unroll
@@ -413,9 +413,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // reads and writes free of bank conflicts.  Every lane commits one group per block, so
         // wait_group(kUDepth - 1) means the oldest staged block has landed.
         const int nsub_u = 2 * (b1 - b0);
-        const uint32_t uring = sb + kOffU + (uint32_t)(eq * kUDepth * kUSlot) + (uint32_t)(lane * 64);
+        const uint32_t uring = sb + kOffUr + (uint32_t)(eq * kUDepth * kUSlot) + (uint32_t)(lane * 64);
         const int usw = (lane >> 1) & 3;
-        auto stage_u = [&](int i) {
+        auto stage_u = [&](int i) {    // U of the worker's i-th block
           const int gsb = wk + i * nwk;
           if (valid && gsb < nsub_u) {
             const int c0 = b0 * kBlkN + gsb * 32;
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           cp_async_commit();
         };
 #pragma unroll
-        for (int i = 0; i < kUDepth; ++i) stage_u(i);   // before the barrier: U does not depend on the tokens
+        for (int i = 0; i < kLook; ++i) stage_u(i);   // before the barrier: U does not depend on the tokens
         int ui = 0;                                    // this worker's blocks consumed in the unit
         if (!waited) {
           // every CTA has folded its position k-1 maxima into the packed keys
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = b0 * kBlkN + gsb * 32 + 8 * q;
-            t[q] = (valid && gsb < nsub_u && c + 8 <= V) ? ld_stream_u4(tptr + c)
+            t[q] = (valid && gsb < nsub_u && c + 8 <= V) ? __ldcs((const uint4 *)(tptr + c))
                                                          : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
           }
         };
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             }
-            cp_async_wait<kUDepth - 1>();           // block ui's U has landed (this lane's copies)
+            cp_async_wait<kLook - 1>();             // block ui's U has landed (this lane's copies)
             uint4 ucur[4];
             {
               const uint32_t src = uring + (uint32_t)((ui % kUDepth) * kUSlot);
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
             }
-            stage_u(ui + kUDepth);                   // the slot is free again: refill it
+            stage_u(ui + kLook);                     // the slot is free again: refill it
             if (RESID) load_t(gs + nwk, tnext);
             if (!valid) continue;
             if (a.draft_logits) {

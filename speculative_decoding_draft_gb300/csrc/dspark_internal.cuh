@@ -768,12 +768,14 @@ struct VRow {
   float invT;      // 1 / T (1 for greedy)
   float lqx;       // log q_j(x_j), T > 0 with a known draft normaliser
   int kind;        // 1 softmax statistics of the target row, 2 its argmax (T = 0), 3 softmax
-                   // statistics of the target and of the draft row (no draft normaliser)
+                   // statistics of the target and of the draft row (no draft normaliser);
+                   // the bonus row j = ell_r + 1: 4 the bonus draw (T > 0), 5 its argmax (T = 0)
   int drow;        // draft row r K_max + j - 1
 };
 
 // Statistics of a completed row: log-sum-exp of target / T (the maximum for T = 0), the
-// argmax, the scaled target logit at x_j and (kind 3) the draft row's log-sum-exp.
+// argmax (for a bonus row: the bonus token), the scaled target logit at x_j and (kind 3) the
+// draft row's log-sum-exp.  Stored per request and position: r (K_max + 1) + j - 1.
 struct VRowRes {
   float lse_t;
   int amax;
@@ -793,14 +795,11 @@ struct VerifyArgs {
   int dtype;
   PhiloxKey key;
   // workspace
-  VRow *rows;           // [B * kMaxK] the verified rows, position-major
+  VRow *rows;           // [B * (kMaxK + 1)] the verified rows and bonus rows, position-major
   int32_t *nrows;       // [1] how many
   int32_t *dead;        // [B] first rejecting position (kNoReject: none)
-  int32_t *arrive;      // [B * kMaxK] warp arrivals per listed row
-  VRowRes *rres;        // [B * kMaxK] request-major: r K_max + j - 1
-  Partial *row_t, *row_d;   // [B * kMaxK * row_slices * 4] per listed row, slice and warp
-  float *zx_t, *zx_d;       // [B * kMaxK] per listed row: scaled logits at the draft token
-  int row_slices;           // vocabulary slices per row of the statistics pass
+  VRowRes *rres;        // [B * (kMaxK + 1)] request-major: r (K_max + 1) + j - 1
+  int row_slices;       // vocabulary slices per row of the statistics pass
   int32_t *counters;   // [B] chunk arrivals of the sampling pass (reset by the plan kernel)
   Partial *partials;   // [B * chunks]
   int chunks;          // vocabulary chunks of the sampling pass (at most the workspace's)

@@ -6,22 +6,23 @@
 //     verified rows (r, j <= ell_r) position-major -- every request's position 1, then
 //     position 2, ... -- with the draft side of each accept test precomputed (log q(x_j)
 //     when the draft normaliser is known).
-//  2. verify_scan (persistent): walks (row, vocabulary slice) items in that order.  A
-//     producer warp stages each item's target slice (and the draft slice when no draft
-//     normaliser is given) into a shared-memory ring by bulk copy; four warps reduce the
-//     online-softmax statistics of z/T (the argmax for T = 0) and publish per-warp
-//     partials.  The warp whose arrival completes a row merges its slices in a fixed
-//     order and decides the row at once: accept x_j iff u_j < min(1, p(x_j)/q(x_j)) (x_j
-//     the target argmax for T = 0); a rejection lowers the request's first-rejection word
-//     by atomicMin.  Before staging an item the producer reads that word and skips rows
-//     past an already-known rejection, so the rows read are the ones up to each request's
-//     deciding row, except where a decision is not yet known.  The bulk copies are in the
-//     async proxy: the release fence before a warp's arrival does not wait for them.
-//  3. verify_sample: per request the outcome -- n_acc = (first rejection) - 1 or ell_r,
-//     the accepted tokens -- and the draw: the residual norm(max(0, p - q)) at a
-//     rejection (T > 0), the argmax of the rejecting row (T = 0, known from the scan), or
-//     the bonus from the next target row; spread over (request x vocabulary chunk) CTAs
-//     with the last chunk merging.
+//  2. verify_scan (persistent): each CTA takes whole listed rows in that order and streams
+//     a row's vocabulary slices through a shared-memory ring (bulk copies issued by a
+//     staging warp; the target slice, and the draft slice when no draft normaliser is
+//     given), folding them into per-thread online-softmax statistics of z/T (the argmax for
+//     T = 0).  At the row's last slice the warps reduce in a fixed order and the row is
+//     decided there: accept x_j iff u_j < min(1, p(x_j)/q(x_j)) (x_j the target argmax for
+//     T = 0); a rejection lowers the request's first-rejection word by atomicMin.  Before
+//     staging a row the staging warp reads that word and skips rows past a known
+//     rejection, so the rows read are the ones up to each request's deciding row, except
+//     where a decision is not known yet.
+//  3. verify_sample: per request the outcome -- n_acc = (first rejection) - 1 or ell_r, the
+//     accepted tokens, then the correction or bonus: the argmax of the rejecting row for T = 0
+//     and the bonus token are the scan's (the bonus row is listed at position ell_r + 1, and
+//     the scan draws it -- the two-level draw over z / T -- or takes its argmax for T = 0,
+//     skipping it once a rejection is known); a T > 0 rejection draws the residual
+//     norm(max(0, p - q)) here, spread over (request x vocabulary chunk) CTAs with the last
+//     chunk merging, or takes the tensor-core recompute pass's draw.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -405,15 +406,15 @@ __device__ __forceinline__ int request_check(const VerifyArgs &a, int r) {
 }
 
 // One CTA: counts the rows of every position (shared atomics), then lists each valid
-// request's rows j = 1..ell_r at start[j] + (its rank among position j's rows).  The order
-// inside a position is whatever the atomics give; no result depends on it (each row is
-// decided on its own, and its slices merge in slice order).
+// request's rows j = 1..ell_r and its bonus row j = ell_r + 1 at start[j] + (its rank among
+// position j's rows).  The order inside a position is whatever the atomics give; no result
+// depends on it (each row is processed by one CTA on its own).
 template <int DT>
 __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constant__ VerifyArgs a) {
-  __shared__ int cnt[kMaxK + 2], fill[kMaxK + 2], start[kMaxK + 2];
+  __shared__ int cnt[kMaxK + 3], fill[kMaxK + 3], start[kMaxK + 3];
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x;
-  if (tid < kMaxK + 2) {
+  if (tid < kMaxK + 3) {
     cnt[tid] = 0;
     fill[tid] = 0;
   }
@@ -427,13 +428,13 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
       continue;
     }
     const int l = a.ell[r];
-    for (int j = 1; j <= l; ++j) atomicAdd(&cnt[j], 1);
+    for (int j = 1; j <= l + 1; ++j) atomicAdd(&cnt[j], 1);
   }
   __syncthreads();
   if (tid == 0) {
     start[1] = 0;
-    for (int j = 1; j <= K; ++j) start[j + 1] = start[j] + cnt[j];
-    *a.nrows = start[K + 1];
+    for (int j = 1; j <= K + 1; ++j) start[j + 1] = start[j] + cnt[j];
+    *a.nrows = start[K + 2];
   }
   __syncthreads();
   for (int r = tid; r < B; r += kPlanThreads) {
@@ -463,79 +464,86 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
       } else {
         w.kind = 3;
       }
-      const int slot = start[j] + atomicAdd(&fill[j], 1);
-      a.rows[slot] = w;
-      a.arrive[slot] = 0;
+      a.rows[start[j] + atomicAdd(&fill[j], 1)] = w;
     }
+    // the bonus row: drawn (or its argmax taken) by the scan, used when every position is accepted
+    VRow w;
+    w.r = r;
+    w.j = l + 1;
+    w.drow = 0;
+    w.x = -1;
+    w.trow = off + l;
+    w.invT = invT;
+    w.lqx = 0.0f;
+    w.kind = greedy ? 5 : 4;
+    a.rows[start[l + 1] + atomicAdd(&fill[l + 1], 1)] = w;
   }
 }
 
 // ---------------------------------------------------------------------------
-// 2. scan: staged row statistics with the accept decision at each row's completion
+// 2. scan: the rows' statistics, each row decided where it completes
 // ---------------------------------------------------------------------------
 constexpr int kScanWarps = kRowThreads / 32;        // reducing warps; one more warp stages
 constexpr int kScanThreads = kRowThreads + 32;
 constexpr int kScanStages = 3;
 constexpr int kSliceBytes = kRowSlice * 2;          // one bf16 slice (24 KB)
 
+// One ring slot: a slice of a listed row, a skipped row (kind 0, one slot) or the end (-1).
 struct ScanMeta {
   VRow w;
-  int ri, sl, kind;   // listed row, slice, kind (0: skipped)
+  int ri, sl, kind;
+  int last;           // the row's last slice
 };
 
-// Merge of listed row ri's slice partials (one warp: lanes over the partials in a fixed
-// order, then a fixed shuffle tree) and the accept decision; lane 0 stores the row's
-// statistics and lowers the request's first-rejection word on a rejection.
-__device__ void decide_row(const VerifyArgs &a, const VRow &w, int ri, int S, int lane) {
+// The accept decision of a completed row from its merged statistics (lane 0 of warp 0):
+// stores the row's results and lowers the request's first-rejection word on a rejection.
+__device__ __forceinline__ void decide_row(const VerifyArgs &a, const VRow &w, const Stats &ct, const Stats &cd,
+                                           float zx_t, float zx_d) {
   const bool greedy = (w.kind == 2), two = (w.kind == 3);
-  Stats ct, cd;
-  stats_init(ct);
-  stats_init(cd);
-  const Partial *pt = a.row_t + (int64_t)ri * S * kRowParts;
-  const Partial *pd = a.row_d + (int64_t)ri * S * kRowParts;
-  for (int q = lane; q < S * kRowParts; q += 32) {
-    stats_merge(ct, partial_to_stats(load_partial(pt + q)));
-    if (two) stats_merge(cd, partial_to_stats(load_partial(pd + q)));
-  }
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) {
-    stats_merge(ct, stats_shfl_down(ct, d));
-    if (two) stats_merge(cd, stats_shfl_down(cd, d));
-  }
-  if (lane != 0) return;
   VRowRes rr;
   rr.amax = ct.idx;
   rr.lse_t = greedy ? ct.best : ct.m + logf(ct.S);
-  rr.zx_t = greedy ? 0.0f : __ldcg(a.zx_t + ri);
+  rr.zx_t = greedy ? 0.0f : zx_t;
   rr.lse_q = two ? cd.m + logf(cd.S) : 0.0f;
   bool reject;
   if (greedy) {
     reject = (w.x != rr.amax);
   } else {
     const float u = uniform_accept(philox(a.key, 0u, (uint32_t)w.j, (uint32_t)w.r, kTagAccept).x);
-    const float lqx = two ? __ldcg(a.zx_d + ri) - rr.lse_q : w.lqx;
+    const float lqx = two ? zx_d - rr.lse_q : w.lqx;
     reject = !(u < expf((rr.zx_t - rr.lse_t) - lqx));
   }
-  a.rres[(int64_t)w.r * a.K_max + w.j - 1] = rr;
+  a.rres[(int64_t)w.r * (a.K_max + 1) + w.j - 1] = rr;
   if (reject) atomicMin(a.dead + w.r, w.j);
 }
 
-// Persistent CTAs walk the (listed row, slice) items, item = blockIdx.x + t * gridDim.x.
-// BULK (bf16, 16-byte aligned rows): warp kScanWarps stages each item by bulk copy into a
-// kScanStages ring; otherwise the reducing warps load the slice themselves (VEC: 16-byte
-// loads) and the staging warp only prepares the item.
+__device__ __forceinline__ void named_sync_scan() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory");
+}
+
+// Persistent CTAs take whole listed rows, ri = blockIdx.x + t * gridDim.x (position-major,
+// so every request's position j comes before any position j + 1), and stream each row's
+// vocabulary slices in order.  BULK (bf16, 16-byte aligned rows): warp kScanWarps stages each
+// slice by bulk copy into a kScanStages ring; otherwise the reducing warps load the slice
+// themselves (VEC: 16-byte loads) and the staging warp only hands out the slices.  A row
+// whose request already has an earlier rejection is skipped before any of it is read.
+// Each thread folds its part of every slice into running statistics; at the row's last
+// slice the four warps reduce in a fixed order and warp 0 decides the row.
 template <int DT, bool VEC, bool BULK>
 __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constant__ VerifyArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kScanStages], empty[kScanStages];
   __shared__ ScanMeta meta[kScanStages];
+  __shared__ Stats s_part[2][2][kScanWarps];   // [row parity][target, draft][warp]
+  __shared__ float s_zx[2][2];                  // [row parity][target, draft]: scaled logits at x
+  __shared__ Race s_race[2][kScanWarps];        // [row parity][warp]: bonus draws
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (read_status(a.dev_status)) return;
   const int S = a.row_slices, V = (int)a.V;
-  const int64_t nitems = (int64_t)(*(volatile const int32_t *)a.nrows) * S;
-  const int64_t G = gridDim.x;
-  if ((int64_t)blockIdx.x >= nitems) return;
+  const int nrows = *(volatile const int32_t *)a.nrows;
+  const int G = gridDim.x;
+  if ((int)blockIdx.x >= nrows) return;
   const bool two = (a.D_lse == nullptr);
   const uint32_t stage_bytes = BULK ? (two ? 2u : 1u) * kSliceBytes : 0u;
   const uint32_t bar_full = smem_u32(&full[0]), bar_empty = smem_u32(&empty[0]);
@@ -561,36 +569,58 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
         last_use[s] = 0;
         issued[s] = false;
       }
-      int t = 0;
-      for (int64_t item = blockIdx.x; item < nitems; item += G, ++t) {
+      int t = 0;   // slots handed out
+      auto slot = [&](const ScanMeta &m) -> bool {   // the next ring slot gets m (and its copies)
         const int s = t % kScanStages;
         const uint32_t use = (uint32_t)(t / kScanStages);
-        if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) break;
-        ScanMeta m;
-        m.ri = (int)(item / S);
-        m.sl = (int)(item % S);
-        m.w = a.rows[m.ri];
-        // rows past a rejection already found need no statistics
-        m.kind = (*(volatile const int32_t *)(a.dead + m.w.r) < m.w.j) ? 0 : m.w.kind;
+        if (!mbar_wait(bar_empty + 8 * s, (use & 1u) ^ 1u, abort)) return false;
         meta[s] = m;
-        if (!BULK || m.kind == 0) {
+        if (!BULK || m.kind <= 0) {
           mbar_arrive(bar_full + 8 * s);
+        } else {
+          const int lo = m.sl * kRowSlice;
+          const uint32_t bytes = (uint32_t)(min(kRowSlice, V - lo) * 2);
+          const uint32_t dst = smem_u32(ring) + (uint32_t)s * stage_bytes;
+          mbar_arrive_tx(bar_full + 8 * s, bytes * (m.kind == 3 ? 2u : 1u));
+          bulk_g2s(dst, (const unsigned short *)a.tgt + ((int64_t)m.w.trow * V + lo), bytes, bar_full + 8 * s, pol);
+          if (m.kind == 3)
+            bulk_g2s(dst + kSliceBytes, (const unsigned short *)a.D + ((int64_t)m.w.drow * V + lo), bytes,
+                     bar_full + 8 * s, pol);
+#pragma unroll
+          for (int q = 0; q < kScanStages; ++q)
+            if (q == s) {
+              last_use[q] = use;
+              issued[q] = true;
+            }
+        }
+        ++t;
+        return true;
+      };
+      bool ok = true;
+      for (int ri = blockIdx.x; ok && ri < nrows; ri += G) {
+        ScanMeta m;
+        m.ri = ri;
+        m.w = a.rows[ri];
+        // rows past a rejection already found need no statistics
+        const bool skip = *(volatile const int32_t *)(a.dead + m.w.r) < m.w.j;
+        if (skip) {
+          m.sl = 0;
+          m.kind = 0;
+          m.last = 1;
+          ok = slot(m);
           continue;
         }
-        const int lo = m.sl * kRowSlice;
-        const uint32_t bytes = (uint32_t)(min(kRowSlice, V - lo) * 2);
-        const uint32_t dst = smem_u32(ring) + (uint32_t)s * stage_bytes;
-        mbar_arrive_tx(bar_full + 8 * s, bytes * (m.kind == 3 ? 2u : 1u));
-        bulk_g2s(dst, (const unsigned short *)a.tgt + ((int64_t)m.w.trow * V + lo), bytes, bar_full + 8 * s, pol);
-        if (m.kind == 3)
-          bulk_g2s(dst + kSliceBytes, (const unsigned short *)a.D + ((int64_t)m.w.drow * V + lo), bytes,
-                   bar_full + 8 * s, pol);
-#pragma unroll
-        for (int q = 0; q < kScanStages; ++q)
-          if (q == s) {
-            last_use[q] = use;
-            issued[q] = true;
-          }
+        m.kind = m.w.kind;
+        for (int sl = 0; ok && sl < S; ++sl) {
+          m.sl = sl;
+          m.last = (sl == S - 1);
+          ok = slot(m);
+        }
+      }
+      if (ok) {
+        ScanMeta m;
+        m.kind = -1;
+        slot(m);
       }
       if (*abort) {   // wait (bounded) until the copies issued into each stage have landed
 #pragma unroll
@@ -607,64 +637,161 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
   }
 
   // ---------------- reducing warps ----------------
-  int t = 0;
-  for (int64_t item = blockIdx.x; item < nitems; item += G, ++t) {
+  Stats rt, rd;            // running statistics of the current row (this thread's share)
+  stats_init(rt);
+  stats_init(rd);
+  BRace rb;                // running bonus draw of the current row (kind 4)
+  brace_init(rb);
+  int rows_done = 0;       // parity of the shared partials
+  for (int t = 0;; ++t) {
     const int s = t % kScanStages;
     const uint32_t use = (uint32_t)(t / kScanStages);
     if (!mbar_wait(bar_full + 8 * s, use & 1u, abort)) break;
     const ScanMeta m = meta[s];
-    Stats st, sd;
-    stats_init(st);
-    stats_init(sd);
-    RowItem it;
-    it.rowi = m.w.drow;
-    it.x = m.w.x;
-    it.kind = (m.kind == 2) ? 2 : (m.kind ? 1 : 0);
-    it.invT = m.w.invT;
-    it.trow = (int64_t)m.w.trow * V;
-    it.lo = min(V, m.sl * kRowSlice);
-    it.hi = min(V, it.lo + kRowSlice);
-    float *own_t = a.zx_t + m.ri, *own_d = a.zx_d + m.ri;
-    if (m.kind) {
+    if (m.kind < 0) break;
+    const int par = rows_done & 1;
+    if (m.kind == 4) {
+      // bonus draw: this thread's 32-wide blocks of the slice (blocks tid, tid + 128, ...), the
+      // two-level draw on z / T with the residual / bonus streams at position ell + 1
+      const int lo = min(V, m.sl * kRowSlice), hi = min(V, lo + kRowSlice);
+      const float a2 = m.w.invT * kLog2e;
+      const uint32_t pos = (uint32_t)m.w.j, rq = (uint32_t)m.w.r;
+#pragma unroll 1
+      for (int q = 0; q < kRowSlice / 32 / kRowThreads; ++q) {
+        const int b = tid + q * kRowThreads;
+        const int v0 = lo + 32 * b;
+        if (v0 >= hi) break;
+        const uint32_t g = (uint32_t)v0 >> 5;
+        const uint32_t wb = word_of(philox(a.key, g >> 2, pos, rq, kTagResid), (int)(g & 3u));
+        auto pick = [&] { return word_of(philox(a.key, g >> 2, pos, rq, kTagResidPick), (int)(g & 3u)); };
+        if (BULK) {
+          const uint32_t base = smem_u32(ring) + (uint32_t)s * stage_bytes + 64u * (uint32_t)b;
+          // the block's four 16-byte units, loaded in an order rotated by (lane >> 1) & 3 so that
+          // the 8 lanes of each quarter warp touch 8 different bank groups, then rotated back
+          const int rot = (lane >> 1) & 3;
+          uint4 u[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) u[h] = ld_shared_u4(base + 16u * (uint32_t)((h + rot) & 3));
+          if (rot & 1) {   // slot h held unit h + rot: rotate right by one, then by two
+            const uint4 t3 = u[3];
+            u[3] = u[2];
+            u[2] = u[1];
+            u[1] = u[0];
+            u[0] = t3;
+          }
+          if (rot & 2) {
+            const uint4 t0 = u[0], t1 = u[1];
+            u[0] = u[2];
+            u[1] = u[3];
+            u[2] = t0;
+            u[3] = t1;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            if (v0 + 8 * h + 8 > hi) u[h] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+            pk[4 * h] = u[h].x;
+            pk[4 * h + 1] = u[h].y;
+            pk[4 * h + 2] = u[h].z;
+            pk[4 * h + 3] = u[h].w;
+          }
+          __nv_bfloat162 m2[4] = {bf162_word(pk[0]), bf162_word(pk[1]), bf162_word(pk[2]), bf162_word(pk[3])};
+#pragma unroll
+          for (int e = 4; e < 16; ++e) m2[e & 3] = __hmax2(m2[e & 3], bf162_word(pk[e]));
+          m2[0] = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
+          brace_softmax_bf16x32(rb, pk, fmaxf(__low2float(m2[0]), __high2float(m2[0])), a2, wb, v0, pick);
+        } else {
+          float t[kBlockW];
+          load32<DT, VEC>(a.tgt, (int64_t)m.w.trow * V, v0, hi, t);
+          brace_softmax_block(rb, t, block_max(t), a2, wb, v0, pick, NoLogit{});
+        }
+      }
+    } else if (m.kind) {
+      RowItem it;
+      it.rowi = m.w.drow;
+      it.x = m.w.x;
+      it.kind = (m.kind == 2 || m.kind == 5) ? 2 : 1;
+      it.invT = m.w.invT;
+      it.trow = (int64_t)m.w.trow * V;
+      it.lo = min(V, m.sl * kRowSlice);
+      it.hi = min(V, it.lo + kRowSlice);
+      Stats st, sd;
+      stats_init(st);
+      stats_init(sd);
       if (BULK) {
         const uint32_t base = smem_u32(ring) + (uint32_t)s * stage_bytes;
         uint4 pk[kRowPk];
 #pragma unroll
         for (int q = 0; q < kRowPk; ++q) pk[q] = ld_shared_u4(base + 16u * (uint32_t)(q * kRowThreads + tid));
-        row_consume(it, pk, tid, st, own_t);
+        row_consume(it, pk, tid, st, &s_zx[par][0]);
         if (m.kind == 3) {
 #pragma unroll
           for (int q = 0; q < kRowPk; ++q)
             pk[q] = ld_shared_u4(base + kSliceBytes + 16u * (uint32_t)(q * kRowThreads + tid));
           RowItem itd = it;
           itd.kind = 1;
-          row_consume(itd, pk, tid, sd, own_d);
+          row_consume(itd, pk, tid, sd, &s_zx[par][1]);
         }
       } else {
-        row_generic<DT, VEC>(a, it, m.kind == 3, tid, st, sd, own_t, own_d);
+        row_generic<DT, VEC>(a, it, m.kind == 3, tid, st, sd, &s_zx[par][0], &s_zx[par][1]);
       }
+      stats_merge(rt, st);
+      if (m.kind == 3) stats_merge(rd, sd);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the stage is read
-    if (!m.kind) continue;
-    st = warp_reduce_row(st, it.kind);
-    if (m.kind == 3) sd = warp_reduce_row(sd, 1);
-    if (lane == 0) {
-      const int64_t at = ((int64_t)m.ri * S + m.sl) * kRowParts + warp;
-      a.row_t[at] = stats_to_partial(st);
-      if (m.kind == 3) a.row_d[at] = stats_to_partial(sd);
+    if (!m.last) continue;
+    if (m.kind == 4) {
+      // the bonus draw of the row: warps reduce their races, warp 0 merges the four in order
+      Race rc = from_partial(to_partial(rb));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) race_merge(rc, race_shfl_down(rc, d));
+      if (lane == 0) s_race[par][warp] = rc;
+      named_sync_scan();
+      if (warp == 0 && lane == 0) {
+        Race tot = s_race[par][0];
+#pragma unroll
+        for (int q = 1; q < kScanWarps; ++q) race_merge(tot, s_race[par][q]);
+        VRowRes rr;
+        rr.lse_t = 0.0f;
+        rr.amax = tot.idx;
+        rr.zx_t = 0.0f;
+        rr.lse_q = 0.0f;
+        a.rres[(int64_t)m.w.r * (a.K_max + 1) + m.w.j - 1] = rr;
+      }
+    } else if (m.kind) {
+      // the row is complete: warps reduce their shares, warp 0 merges the four in order
+      const int kind = (m.kind == 2 || m.kind == 5) ? 2 : 1;
+      Stats wt = warp_reduce_row(rt, kind);
+      Stats wd = (m.kind == 3) ? warp_reduce_row(rd, 1) : rd;
+      if (lane == 0) {
+        s_part[par][0][warp] = wt;
+        s_part[par][1][warp] = wd;
+      }
+      named_sync_scan();
+      if (warp == 0 && lane == 0) {
+        Stats ct = s_part[par][0][0], cd = s_part[par][1][0];
+#pragma unroll
+        for (int q = 1; q < kScanWarps; ++q) {
+          stats_merge(ct, s_part[par][0][q]);
+          if (m.kind == 3) stats_merge(cd, s_part[par][1][q]);
+        }
+        if (m.kind == 5) {        // greedy bonus: the argmax of the row
+          VRowRes rr;
+          rr.lse_t = ct.best;
+          rr.amax = ct.idx;
+          rr.zx_t = 0.0f;
+          rr.lse_q = 0.0f;
+          a.rres[(int64_t)m.w.r * (a.K_max + 1) + m.w.j - 1] = rr;
+        } else {
+          decide_row(a, m.w, ct, cd, s_zx[par][0], s_zx[par][1]);
+        }
+      }
     }
-    // each lane releases what it wrote (the partial, the logit at the draft token); these
-    // lanes have no global loads in flight, so the fences are short
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = (atomicAdd(a.arrive + m.ri, 1) == S * kRowParts - 1);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      decide_row(a, m.w, m.ri, S, lane);
-    }
+    stats_init(rt);
+    stats_init(rd);
+    brace_init(rb);
+    ++rows_done;
   }
   if (*abort && tid == 0) set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
 }
@@ -673,9 +800,9 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
 // 3. sampling: outcome per request and the residual / bonus draw
 // ---------------------------------------------------------------------------
 // Request r's outcome from the scan (one warp): n = (first rejection) - 1, or ell_r when no
-// position was rejected; with write_out the accepted tokens, the padding, n_acc and a greedy
-// rejection's correction (the argmax of the rejecting row) are written.  Returns the draw
-// job in lane 0.
+// position was rejected; with write_out the accepted tokens, the padding, n_acc, a greedy
+// rejection's correction (the argmax of the rejecting row) and the bonus token (drawn by the
+// scan) are written.  Returns in lane 0 the residual job of a T > 0 rejection, if any.
 __device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_out, VerifyJob *out_job) {
   const int K = (int)a.K_max;
   const int l = a.ell[r];
@@ -700,7 +827,7 @@ __device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_o
   job.invT = greedy ? 1.0f : 1.0f / T;
   job.out_slot = r * (K + 1) + n;
   if (n < l) {                                             // rejected at position n + 1
-    const VRowRes rr = a.rres[(int64_t)r * K + n];
+    const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
     if (greedy) {
       if (write_out) a.out_tok[job.out_slot] = rr.amax;
     } else {
@@ -711,10 +838,9 @@ __device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_o
       job.lse_t = rr.lse_t;
       job.lse_q = a.D_lse ? a.D_lse[job.drow] : rr.lse_q;
     }
-  } else {
-    job.mode = greedy ? 3 : 2;
-    job.pos = l + 1;
-    job.trow = off + l;
+  } else if (write_out) {
+    // every position accepted: the bonus token the scan drew (or the argmax for T = 0)
+    a.out_tok[job.out_slot] = a.rres[(int64_t)r * (K + 1) + l].amax;
   }
   if (write_out) a.n_acc[r] = n;
   *out_job = job;
@@ -829,7 +955,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constan
     jb.prev = (n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1];
     jb.urow = r * K + n;
     jb.trow = a.tgt_off[r] + n;
-    jb.lse_t = a.rres[(int64_t)r * K + n].lse_t;
+    jb.lse_t = a.rres[(int64_t)r * (K + 1) + n].lse_t;
     jb.lse_q = a.D_lse[(int64_t)r * K + n];
     jb.invT = 1.0f / T;
     a.jobs[atomicAdd(&count, 1)] = jb;
@@ -865,9 +991,9 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
     e = ensure_dynamic_smem((const void *)verify_scan<DT, VEC, BULK>, smem);
     if (e != cudaSuccess) return e;
   }
-  const int64_t max_items = a.B * a.K_max * (int64_t)a.row_slices;
+  const int64_t max_rows = a.B * (a.K_max + 1);
   const int64_t per_sm = (BULK && two) ? 1 : 3;
-  const int64_t grid = max_items < per_sm * num_sms ? max_items : per_sm * num_sms;
+  const int64_t grid = max_rows < per_sm * num_sms ? max_rows : per_sm * num_sms;
   verify_scan<DT, VEC, BULK><<<(unsigned)grid, kScanThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -887,24 +1013,21 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
 int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice); }
 
 // Workspace layout (every part 256-byte aligned): sampling counters [B], sampling partials
-// [B * chunks], slice statistics of the target and draft rows [B * kMaxK * slices * warps]
-// each, scaled logits at the draft tokens [B * kMaxK] each, the listed rows [B * kMaxK], their
-// count, the first-rejection words [B], the row arrivals [B * kMaxK], the row results
-// [B * kMaxK].  Rows are sized for kMaxK positions so the size depends on B and V only.
+// [B * chunks], the listed rows [B * (kMaxK + 1)], their count, the first-rejection words [B],
+// the row results [B * (kMaxK + 1)].  Sized for kMaxK positions, so the size depends on B and
+// V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   const int c = (int)((V + kSampleUnit - 1) / kSampleUnit);   // the most chunks a call uses
   if (chunks) *chunks = c;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  const size_t rows = (size_t)B * (size_t)kMaxK;
-  return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) +
-         2 * al(sizeof(Partial) * rows * verify_row_slices(V) * kRowParts) + 2 * al(sizeof(float) * rows) +
-         al(sizeof(VRow) * rows) + al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) +
-         al(sizeof(int32_t) * rows) + al(sizeof(VRowRes) * rows);
+  const size_t rows = (size_t)B * (size_t)(kMaxK + 1);
+  return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) + al(sizeof(VRow) * rows) +
+         al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) + al(sizeof(VRowRes) * rows);
 }
 
 void verify_carve(VerifyArgs &a, void *workspace) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  const size_t rows = (size_t)a.B * (size_t)kMaxK;
+  const size_t rows = (size_t)a.B * (size_t)(kMaxK + 1);
   int chunks = 1;
   verify_ws_bytes(a.B, a.V, &chunks);
   a.chunks = chunks;
@@ -914,22 +1037,12 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   p += al(sizeof(int32_t) * (size_t)a.B);
   a.partials = (Partial *)p;
   p += al(sizeof(Partial) * (size_t)a.B * (size_t)chunks);
-  a.row_t = (Partial *)p;
-  p += al(sizeof(Partial) * rows * a.row_slices * kRowParts);
-  a.row_d = (Partial *)p;
-  p += al(sizeof(Partial) * rows * a.row_slices * kRowParts);
-  a.zx_t = (float *)p;
-  p += al(sizeof(float) * rows);
-  a.zx_d = (float *)p;
-  p += al(sizeof(float) * rows);
   a.rows = (VRow *)p;
   p += al(sizeof(VRow) * rows);
   a.nrows = (int32_t *)p;
   p += al(sizeof(int32_t));
   a.dead = (int32_t *)p;
   p += al(sizeof(int32_t) * (size_t)a.B);
-  a.arrive = (int32_t *)p;
-  p += al(sizeof(int32_t) * rows);
   a.rres = (VRowRes *)p;
 }
 
