@@ -6,7 +6,8 @@
 // For position k the active requests (K_r >= k) form a prefix of the
 // permutation `perm`, which orders requests by K_r descending; the prologue
 // builds it together with the active counts nact[k], and the lists act[k - 1] of the
-// active requests in request order that the tensor-core path tiles.
+// active requests that the tensor-core path tiles (T > 0 first, then T = 0, each in
+// request order).
 //
 // CUDA-core step: grid (vocabulary tile, tile of active rows); each block forms
 // z = U + feature . W2 for its rows and columns with fp32 FMAs (the feature is the
@@ -99,10 +100,14 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     }
     __syncthreads();
   }
-  // act[k - 1]: the requests with K_r >= k in request order (a ballot prefix per position)
-  for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
-    const int r = c0 + tid;
-    const int v = r < B ? a.K_r[r] : 0;
+  // act[k - 1]: the requests with K_r >= k, those with T > 0 first and then the greedy ones,
+  // each in request order (a ballot prefix per position).  At most one warp of rows per
+  // position then holds both kinds, so the others run one kind of draw, not both in turn.
+  const int Bp = (B + kPrologueThreads - 1) / kPrologueThreads * kPrologueThreads;
+  for (int c = 0; c < 2 * Bp; c += kPrologueThreads) {
+    const int pass = c >= Bp ? 1 : 0;       // 0: the requests with T > 0, 1: the greedy ones
+    const int r = c - pass * Bp + tid;
+    const int v = (r < B && ((a.temperature[r] == 0.0f) == (pass == 1))) ? a.K_r[r] : 0;
     for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
     __syncthreads();
     for (int k = 1; k <= K; ++k) {

@@ -4,9 +4,9 @@
 // "Speculative decoding, from zero to DSpark" S6 (p_k = softmax(U_k + B_k)).
 //
 // One persistent cooperative launch walks every draft position k = 1..K_max.  The
-// active requests at position k (K_r >= k), listed in request order in act[k - 1] (so
-// that a tile's rows sit as close together in U as the active set allows: rows scattered
-// over the whole of U made each tile three times slower), are cut into M-tiles of 128 rows, and every M-tile is shared by gm CTAs that
+// active requests at position k (K_r >= k), listed in act[k - 1] with the T > 0 requests
+// first and the greedy ones after them, each in request order (warps of one kind of draw;
+// rows close together in U), are cut into M-tiles of 128 rows, and every M-tile is shared by gm CTAs that
 // own contiguous ranges of 64-wide vocabulary blocks.  A CTA stages the gathered
 // operand W1[x_{k-1}] (128 x r) once per range and streams W2 through it.
 //
@@ -73,9 +73,10 @@ struct TcShared {
   float row_invT[kTileM];
   Partial part[kWpq * kTileM];   // per-row partials: [column worker][row of the replica group]
   float part_zx[kWpq * kTileM];  // the logit at each partial's index (residual mode: "some p > q")
-  // residual mode: per row the rejecting position, the base-logit and target rows, and the
-  // log2-scaled normalisers of p and q
-  int row_j[kTileM], row_urow[kTileM], row_trow[kTileM];
+  int row_urow[kTileM];        // the row of U (of the base logits) each M-tile row reads
+  // residual mode: per row the rejecting position, the target row, and the log2-scaled
+  // normalisers of p and q
+  int row_j[kTileM], row_trow[kTileM];
   float row_lt2[kTileM], row_lq2[kTileM];
 };
 
@@ -378,10 +379,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             } else if (row0 + i < pl.n_k) {
               const int r = a.act[(int64_t)(k - 1) * a.B + row0 + i];
               sh.row_req[i] = r;
+              sh.row_urow[i] = r * K + (k - 1);
               const float T = a.temperature[r];
               sh.row_invT[i] = (T == 0.0f) ? 0.0f : 1.0f / T;
             } else {
               sh.row_req[i] = -1;
+              sh.row_urow[i] = 0;
+              if (RESID) sh.row_trow[i] = 0;
               sh.row_invT[i] = 0.0f;
             }
           }
@@ -398,31 +402,50 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const float invT = sh.row_invT[row];
         const bool greedy = (invT == 0.0f);
         const float a2 = invT * kLog2e;           // scaled logits in log2 units
-        const int64_t urow = RESID ? (int64_t)(valid ? sh.row_urow[row] : 0) * V : ((int64_t)r * K + (k - 1)) * (int64_t)V;
-        const unsigned short *uptr = (const unsigned short *)a.U + urow;
-        // residual mode: the target row, its stream position and the normalisers
-        const unsigned short *tptr =
-            RESID ? (const unsigned short *)a.tgt + (int64_t)(valid ? sh.row_trow[row] : 0) * V : nullptr;
+        const int64_t urow = (int64_t)sh.row_urow[row] * V;   // this thread's row of U and of the logits
+        // residual mode: the stream position and the normalisers
         const uint32_t rpos = RESID ? (uint32_t)(valid ? sh.row_j[row] : 0) : (uint32_t)k;
         const float lt2 = RESID ? sh.row_lt2[row] : 0.0f, lq2 = RESID ? sh.row_lq2[row] : 0.0f;
         bool any_pos = false;
         // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles; worker wk
-        // takes blocks wk, wk + nwk, ...  Its i-th block's U (each lane its row's 64 bytes) is
-        // staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by cp.async; 16-byte
-        // unit q of lane l sits at l * 64 + ((q ^ ((l >> 1) & 3)) << 4), which keeps the quarter-warp
-        // reads and writes free of bank conflicts.  Every lane commits one group per block, so
-        // wait_group(kUDepth - 1) means the oldest staged block has landed.
+        // takes blocks wk, wk + nwk, ...  Its i-th block's U (64 bytes of each of the warp's 32
+        // rows) is staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by
+        // cp.async.  Four lanes copy one row's 64 contiguous bytes, so each instruction touches 8
+        // rows: with one row per lane every instruction touched 32 rows far apart in memory, and
+        // the ragged draft (rows of the active requests, scattered) ran 1.5x slower than the same
+        // work on consecutive rows.  16-byte unit q of row l sits at l * 64 + ((q ^ ((l >> 1) & 3))
+        // << 4), which keeps the quarter-warp reads and writes free of bank conflicts.  Every lane
+        // commits one group per block, so wait_group(kUDepth - 1) and a warp barrier mean the
+        // oldest staged block has landed for the whole warp.
         const int nsub_u = 2 * (b1 - b0);
-        const uint32_t uring = sb + kOffUr + (uint32_t)(eq * kUDepth * kUSlot) + (uint32_t)(lane * 64);
+        const uint32_t uring0 = sb + kOffUr + (uint32_t)(eq * kUDepth * kUSlot);
+        const uint32_t uring = uring0 + (uint32_t)(lane * 64);
         const int usw = (lane >> 1) & 3;
+        const int cq = lane & 3;                  // the 16-byte unit this lane copies of each row
+        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+        const int rb = row - lane;                // the warp's first row (rows rb .. rb + 31)
+        // the U rows this lane copies: kept in registers for the unit, except in the residual
+        // mode, whose extra target registers leave no room (there they come from the row table)
+        const unsigned short *uptr_l[4];
+        if constexpr (!RESID) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            uptr_l[p] = (const unsigned short *)a.U + (int64_t)sh.row_urow[rb + p * 8 + (lane >> 2)] * V;
+        }
         auto stage_u = [&](int i) {    // U of the worker's i-th block
           const int gsb = wk + i * nwk;
-          if (valid && gsb < nsub_u) {
-            const int c0 = b0 * kBlkN + gsb * 32;
-            const uint32_t dst = uring + (uint32_t)((i % kUDepth) * kUSlot);
+          if (gsb < nsub_u) {
+            const int c = b0 * kBlkN + gsb * 32 + 8 * cq;
+            const uint32_t slot = uring0 + (uint32_t)((i % kUDepth) * kUSlot);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (c0 + 8 * q < V) cp_async16(dst + ((q ^ usw) << 4), uptr + c0 + 8 * q, pol_stream);
+            for (int p = 0; p < 4; ++p) {
+              const int l = p * 8 + (lane >> 2);
+              const unsigned short *src;
+              if constexpr (RESID) src = (const unsigned short *)a.U + (int64_t)sh.row_urow[rb + l] * V;
+              else src = uptr_l[p];
+              if (((vmask >> l) & 1u) && c < V)
+                cp_async16(slot + (uint32_t)(l * 64) + (uint32_t)((cq ^ ((l >> 1) & 3)) << 4), src + c, pol_stream);
+            }
           }
           cp_async_commit();
         };
@@ -473,17 +496,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         BRace st;
         brace_init(st);
         // residual mode: the target block of this worker's next 32 columns, one block ahead in
-        // registers (units past V read as -inf, so their weights are 0)
-        uint4 tcur[4], tnext[4];
-        auto load_t = [&](int gsb, uint4 (&t)[4]) {
+        // registers (units past V read as -inf, so their weights are 0).  The first block of the
+        // unit is loaded row by row; later blocks are loaded two ahead like U, four lanes per row
+        // (traw: unit cq of rows p * 8 + lane / 4), and passed to their rows' lanes through the
+        // U slot just consumed, before it is refilled.
+        const uint4 kNegInf4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        uint4 tcur[4], tnext[4], traw[4];
+        if (RESID) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int c = b0 * kBlkN + gsb * 32 + 8 * q;
-            t[q] = (valid && gsb < nsub_u && c + 8 <= V) ? __ldcs((const uint4 *)(tptr + c))
-                                                         : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+            const int c = b0 * kBlkN + wk * 32 + 8 * q;
+            tcur[q] = (valid && wk < nsub_u && c + 8 <= V)
+                          ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + ((int64_t)sh.row_trow[row] * V + c)))
+                          : kNegInf4;
+          }
+        }
+        auto load_traw = [&](int gsb) {
+          const int c = b0 * kBlkN + gsb * 32 + 8 * cq;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int l = p * 8 + (lane >> 2);
+            traw[p] = (((vmask >> l) & 1u) && gsb < nsub_u && c + 8 <= V)
+                          ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + ((int64_t)sh.row_trow[rb + l] * V + c)))
+                          : kNegInf4;
           }
         };
-        if (RESID) load_t(wk, tcur);
+        if (RESID) load_traw(wk + nwk);
         for (int bt = b0; bt < b1; bt += kMaxBlk, ++tt) {
           const int mt = min(kMaxBlk, b1 - bt);
           const int b = (int)(tt % kAccBufs);
@@ -508,6 +546,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             }
             cp_async_wait<kLook - 1>();             // block ui's U has landed (this lane's copies)
+            __syncwarp();                           // ... and every lane's
             uint4 ucur[4];
             {
               const uint32_t src = uring + (uint32_t)((ui % kUDepth) * kUSlot);
@@ -524,8 +563,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               const __nv_bfloat162 zb = __floats2bfloat162_rn(z0, z1);   // one rounding of each fp32 sum
               packed[e] = *reinterpret_cast<const uint32_t *>(&zb);
             }
+            __syncwarp();                            // every lane has read the slot
+            if (RESID) {                             // the next block's target rows, through the slot
+              const uint32_t slot = uring0 + (uint32_t)((ui % kUDepth) * kUSlot);
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const int l = p * 8 + (lane >> 2);
+                st_shared_u4(slot + (uint32_t)(l * 64) + (uint32_t)((cq ^ ((l >> 1) & 3)) << 4), traw[p]);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tnext[q] = ld_shared_u4(uring + (uint32_t)((ui % kUDepth) * kUSlot) + ((q ^ usw) << 4));
+              __syncwarp();
+              load_traw(gs + 2 * nwk);
+            }
             stage_u(ui + kLook);                     // the slot is free again: refill it
-            if (RESID) load_t(gs + nwk, tnext);
             if (!valid) continue;
             if (a.draft_logits) {
               unsigned short *drow = (unsigned short *)a.draft_logits + urow;
