@@ -179,7 +179,9 @@ __device__ __forceinline__ void named_sync_epi() {
 }
 
 // Work split of one draft position: M-tiles of 128 active rows, each shared by gm CTAs
-// that own contiguous ranges of 64-wide vocabulary blocks.
+// that own contiguous ranges of 64-wide vocabulary blocks.  The ranges start at even blocks
+// (128 columns), so a range's 32-wide draw blocks fall into the random stream's groups of four
+// (one Philox call each) the same way in every range.
 struct StepPlan {
   int n_k, m_tiles, gm, units;
 };
@@ -187,11 +189,13 @@ __device__ __forceinline__ StepPlan plan_step(const int *nact, int k, int G, int
   StepPlan p;
   p.n_k = nact[k];
   p.m_tiles = (p.n_k + kTileM - 1) / kTileM;
-  p.gm = p.m_tiles ? max(1, min(G / p.m_tiles, nb)) : 1;
+  p.gm = p.m_tiles ? max(1, min(G / p.m_tiles, (nb + 1) / 2)) : 1;
   p.units = p.m_tiles * p.gm;
   return p;
 }
-__device__ __forceinline__ int range_lo(int j, int nb, int gm) { return (int)((int64_t)j * nb / gm); }
+__device__ __forceinline__ int range_lo(int j, int nb, int gm) {
+  return j >= gm ? nb : 2 * (int)((int64_t)j * ((nb + 1) / 2) / gm);
+}
 
 // ---------------------------------------------------------------------------
 // RESID: the residual mode of the recompute verification -- one position whose rows are the
@@ -407,8 +411,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const uint32_t rpos = RESID ? (uint32_t)(valid ? sh.row_j[row] : 0) : (uint32_t)k;
         const float lt2 = RESID ? sh.row_lt2[row] : 0.0f, lq2 = RESID ? sh.row_lq2[row] : 0.0f;
         bool any_pos = false;
-        // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles; worker wk
-        // takes blocks wk, wk + nwk, ...  Its i-th block's U (64 bytes of each of the warp's 32
+        // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles, in groups
+        // of gsz = 8 / nwk (4, 2 or 1) consecutive blocks, so that every tile (8 blocks) gives each
+        // of the nwk workers one group; worker wk takes groups wk, wk + nwk, ...  Four consecutive
+        // blocks from an even 64-wide block share one Philox call, which a worker then computes
+        // once per group.  The worker's i-th block gsb_of(i)'s U (64 bytes of each of the warp's 32
         // rows) is staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by
         // cp.async.  Four lanes copy one row's 64 contiguous bytes, so each instruction touches 8
         // rows: with one row per lane every instruction touched 32 rows far apart in memory, and
@@ -418,6 +425,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // commits one group per block, so wait_group(kUDepth - 1) and a warp barrier mean the
         // oldest staged block has landed for the whole warp.
         const int nsub_u = 2 * (b1 - b0);
+        const int gsh = nwk == 2 ? 2 : (nwk == 4 ? 1 : 0);   // log2 of the group size
+        auto gsb_of = [&](int i) { return (((i >> gsh) * nwk + wk) << gsh) + (i & ((1 << gsh) - 1)); };
         const uint32_t uring0 = sb + kOffUr + (uint32_t)(eq * kUDepth * kUSlot);
         const uint32_t uring = uring0 + (uint32_t)(lane * 64);
         const int usw = (lane >> 1) & 3;
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
             uptr_l[p] = (const unsigned short *)a.U + (int64_t)sh.row_urow[rb + p * 8 + (lane >> 2)] * V;
         }
         auto stage_u = [&](int i) {    // U of the worker's i-th block
-          const int gsb = wk + i * nwk;
+          const int gsb = gsb_of(i);
           if (gsb < nsub_u) {
             const int c = b0 * kBlkN + gsb * 32 + 8 * cq;
             const uint32_t slot = uring0 + (uint32_t)((i % kUDepth) * kUSlot);
@@ -505,8 +514,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         if (RESID) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int c = b0 * kBlkN + wk * 32 + 8 * q;
-            tcur[q] = (valid && wk < nsub_u && c + 8 <= V)
+            const int c = b0 * kBlkN + gsb_of(0) * 32 + 8 * q;
+            tcur[q] = (valid && gsb_of(0) < nsub_u && c + 8 <= V)
                           ? __ldcs((const uint4 *)((const unsigned short *)a.tgt + ((int64_t)sh.row_trow[row] * V + c)))
                           : kNegInf4;
           }
@@ -521,7 +530,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
                           : kNegInf4;
           }
         };
-        if (RESID) load_traw(wk + nwk);
+        if (RESID) load_traw(gsb_of(1));
+        uint4 pw = make_uint4(0u, 0u, 0u, 0u);   // the last Philox output of this thread's row
+        uint32_t pctr = 0xffffffffu;              // ... and its counter (a block group)
         for (int bt = b0; bt < b1; bt += kMaxBlk, ++tt) {
           const int mt = min(kMaxBlk, b1 - bt);
           const int b = (int)(tt % kAccBufs);
@@ -529,18 +540,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           if (!mbar_wait(bar_accf + 8 * b, ause & 1u, abort)) break;
           tc_fence_after();
           const int s0 = 2 * (bt - b0), s1 = s0 + 2 * mt;   // the tile's blocks in unit numbering
-          int gs = s0 + (wk - s0 % nwk + nwk) % nwk;         // this worker's first block in the tile
+          int gs = gsb_of(ui);                               // this worker's first block in the tile
           if (gs >= s1) {                         // nothing for this worker in this tile
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acce + 8 * b);
             continue;
           }
-          for (; gs < s1; gs += nwk, ++ui) {
+          for (; gs < s1; gs = gsb_of(++ui)) {
             uint32_t acc[32];
             tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kAccCols + (gs - s0) * 32), acc);
             tmem_wait_ld();
-            if (gs + nwk >= s1) {                 // this warp's last read of the accumulator
+            if (gsb_of(ui + 1) >= s1) {           // this warp's last read of the accumulator
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_acce + 8 * b);
@@ -575,7 +586,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
 #pragma unroll
               for (int q = 0; q < 4; ++q) tnext[q] = ld_shared_u4(uring + (uint32_t)((ui % kUDepth) * kUSlot) + ((q ^ usw) << 4));
               __syncwarp();
-              load_traw(gs + 2 * nwk);
+              load_traw(gsb_of(ui + 2));
             }
             stage_u(ui + kLook);                     // the slot is free again: refill it
             if (!valid) continue;
@@ -610,7 +621,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
                                    make_uint4(packed[8], packed[9], packed[10], packed[11]),
                                    make_uint4(packed[12], packed[13], packed[14], packed[15])};
               const uint32_t gblk = (uint32_t)c0 >> 5;
-              const uint32_t wb = word_of(philox(a.key, gblk >> 2, rpos, (uint32_t)r, kTagResid), (int)(gblk & 3u));
+              if ((gblk >> 2) != pctr) {
+                pctr = gblk >> 2;
+                pw = philox(a.key, pctr, rpos, (uint32_t)r, kTagResid);
+              }
+              const uint32_t wb = word_of(pw, (int)(gblk & 3u));
               brace_resid_packed(st, tcur, dp, a2, lt2, lq2, wb, c0, any_pos, [&] {
                 return word_of(philox(a.key, gblk >> 2, rpos, (uint32_t)r, kTagResidPick), (int)(gblk & 3u));
               });
@@ -634,8 +649,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               brace_argmax_block(st, z, mz, c0);
             } else {
               const uint32_t gblk = (uint32_t)c0 >> 5;
-              const uint32_t wb =
-                  word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraft), (int)(gblk & 3u));
+              if ((gblk >> 2) != pctr) {
+                pctr = gblk >> 2;
+                pw = philox(a.key, pctr, (uint32_t)k, (uint32_t)r, kTagDraft);
+              }
+              const uint32_t wb = word_of(pw, (int)(gblk & 3u));
               brace_softmax_bf16x32(st, packed, mz, a2, wb, c0, [&] {
                 return word_of(philox(a.key, gblk >> 2, (uint32_t)k, (uint32_t)r, kTagDraftPick), (int)(gblk & 3u));
               });
