@@ -245,7 +245,7 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
     a.Wp = p;   // packed into the workspace by this call
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_draft_prologue(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_draft_prologue(a, s, use_tc) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (use_tc && !packed_in && launch_pack_projection(W, dims.rank, dims.V, (void *)a.Wp, s) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   // with DSPARK_FLAG_SPARE_SM the persistent kernel (one CTA per SM) leaves one SM free

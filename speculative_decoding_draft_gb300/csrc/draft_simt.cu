@@ -25,11 +25,33 @@ namespace {
 constexpr int kPrologueThreads = 1024;
 constexpr int kSimtThreads = 256;
 
-__global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a) {
+// Exclusive prefix over the 32 warps of per-warp counts cnt[w][v] for v = 1..K (warp v - 1
+// scans value v, a lane per warp), into pre[w][v]; tot[v] gets the sum.  K <= 32.
+__device__ __forceinline__ void prologue_warp_prefix(int (*cnt)[kMaxK + 2], int (*pre)[kMaxK + 2], int *tot, int K,
+                                                     int warp, int lane) {
+  if (warp < K) {
+    const int v = warp + 1;
+    const int c = cnt[lane][v];
+    int incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    pre[lane][v] = incl - c;
+    if (lane == 31) tot[v] = incl;
+  }
+}
+
+// lists: 1 = the K_r-descending permutation (the CUDA-core path), 2 = the per-position
+// active lists (the tensor-core path).
+__global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a, int lists) {
   __shared__ int s_err, s_skip;
   __shared__ int cnt[kMaxK + 2];          // requests per length value
   __shared__ int base[kMaxK + 2];         // next free slot per length value
-  __shared__ int wc[kPrologueThreads / 32][kMaxK + 2];
+  __shared__ int wc[kPrologueThreads / 32][kMaxK + 2];    // per-warp counts of one round
+  __shared__ int wp[kPrologueThreads / 32][kMaxK + 2];    // their exclusive prefix over warps
+  __shared__ int wt[kMaxK + 2];                           // their sum
   __shared__ int carry[kMaxK + 2];        // act: listed requests per position so far
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -76,29 +98,29 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     a.nact[K + 1] = 0;
   }
   __syncthreads();
-  // stable scatter, 1024 requests per round: rank among equal lengths by warp match + warp prefix
-  for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
-    const int r = c0 + tid;
-    const int v = r < B ? a.K_r[r] : 0;
-    const uint32_t peers = __match_any_sync(0xffffffffu, v);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
-    __syncthreads();
-    if (lane == __ffs(peers) - 1) wc[warp][v] = __popc(peers);
-    __syncthreads();
-    int before = 0;
-    for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][v];
-    if (r < B) {
-      a.perm[base[v] + before + rank] = r;
-      a.iperm[r] = base[v] + before + rank;
+  if (lists == 1) {
+    // stable scatter, 1024 requests per round: rank among equal lengths by warp match, then
+    // the prefix of the warps' counts
+    for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
+      const int r = c0 + tid;
+      const int v = r < B ? a.K_r[r] : 0;
+      const uint32_t peers = __match_any_sync(0xffffffffu, v);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
+      __syncthreads();
+      if (lane == __ffs(peers) - 1) wc[warp][v] = __popc(peers);
+      __syncthreads();
+      prologue_warp_prefix(wc, wp, wt, K, warp, lane);
+      __syncthreads();
+      if (r < B) {
+        a.perm[base[v] + wp[warp][v] + rank] = r;
+        a.iperm[r] = base[v] + wp[warp][v] + rank;
+      }
+      __syncthreads();
+      if (tid >= 1 && tid <= K) base[tid] += wt[tid];
+      __syncthreads();
     }
-    __syncthreads();
-    if (tid >= 1 && tid <= K) {
-      int tot = 0;
-      for (int w2 = 0; w2 < kPrologueThreads / 32; ++w2) tot += wc[w2][tid];
-      base[tid] += tot;
-    }
-    __syncthreads();
+    return;
   }
   // act[k - 1]: the requests with K_r >= k, those with T > 0 first and then the greedy ones,
   // each in request order (a ballot prefix per position).  At most one warp of rows per
@@ -108,27 +130,19 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     const int pass = c >= Bp ? 1 : 0;       // 0: the requests with T > 0, 1: the greedy ones
     const int r = c - pass * Bp + tid;
     const int v = (r < B && ((a.temperature[r] == 0.0f) == (pass == 1))) ? a.K_r[r] : 0;
-    for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
-    __syncthreads();
     for (int k = 1; k <= K; ++k) {
       const uint32_t bal = __ballot_sync(0xffffffffu, v >= k);
       if (lane == 0) wc[warp][k] = __popc(bal);
     }
     __syncthreads();
+    prologue_warp_prefix(wc, wp, wt, K, warp, lane);
+    __syncthreads();
     for (int k = 1; k <= K; ++k) {          // every lane runs every k: the ballots are warp-wide
       const uint32_t bal = __ballot_sync(0xffffffffu, v >= k);
-      if (v >= k) {
-        int before = carry[k];
-        for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][k];
-        a.act[(int64_t)(k - 1) * B + before + __popc(bal & ((1u << lane) - 1u))] = r;
-      }
+      if (v >= k) a.act[(int64_t)(k - 1) * B + carry[k] + wp[warp][k] + __popc(bal & ((1u << lane) - 1u))] = r;
     }
     __syncthreads();
-    if (tid >= 1 && tid <= K) {
-      int tot = 0;
-      for (int w2 = 0; w2 < kPrologueThreads / 32; ++w2) tot += wc[w2][tid];
-      carry[tid] += tot;
-    }
+    if (tid >= 1 && tid <= K) carry[tid] += wt[tid];
     __syncthreads();
   }
 }
@@ -590,8 +604,8 @@ __global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_
 
 }  // namespace
 
-cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s) {
-  draft_prologue<<<1, kPrologueThreads, 0, s>>>(a);
+cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s, bool tensor_core) {
+  draft_prologue<<<1, kPrologueThreads, 0, s>>>(a, tensor_core ? 2 : 1);
   return cudaGetLastError();
 }
 

@@ -741,7 +741,7 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
 
-cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s);
+cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s, bool tensor_core);
 cudaError_t launch_draft_simt(const DraftArgs &a, cudaStream_t s);
 cudaError_t launch_draft_tc(const DraftArgs &a, cudaStream_t s, int num_sms);
 cudaError_t launch_resid_tc(const DraftArgs &a, cudaStream_t s, int num_sms);   // residual mode
