@@ -40,13 +40,9 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kBlkN = 64;                        // vocabulary columns per packed block
 constexpr int kMaxBlk = 4;                       // blocks per MMA tile (N <= 256)
-constexpr int kStages = 3;
 constexpr int kAccBufs = 2;
 constexpr int kAccCols = kBlkN * kMaxBlk;        // 256
 constexpr int kTmemCols = kAccBufs * kAccCols;   // 512
-constexpr int kEpiWarps = 8;
-constexpr int kWpq = kEpiWarps / 4;             // epilogue warps per TMEM lane quadrant
-constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
 constexpr int kAChunk = kTileM * 128;            // 16 KB: 128 rows x 64 rank values
 constexpr int kASize = 4 * kAChunk;              // rank <= 256
 constexpr int kPiece = kBlkN * 128;              // 8 KB: one packed block, 64 rank rows
@@ -55,11 +51,24 @@ constexpr int kUDepth = 3;                       // U blocks each epilogue warp 
 constexpr int kUSlot = 32 * 64;                  // one 32-wide block of a warp's 32 rows (2 KB)
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
-constexpr int kOffSh = kOffW + kStages * kStageBytes + kEpiWarps * kUDepth * kUSlot;
 
+// Per mode: epilogue warps (three per TMEM lane quadrant for the draft, which fits 128
+// registers a thread; two for the residual mode, which needs 168) and W2 stages (the draft's
+// extra U slots leave room for two; two stages measured as fast as three).
+template <bool RESID>
+struct TcCfg {
+  static constexpr int kEpiWarps = RESID ? 8 : 12;
+  static constexpr int kWpq = kEpiWarps / 4;     // epilogue warps per TMEM lane quadrant
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kStages = RESID ? 3 : 2;
+  static constexpr int kOffUr = kOffW + kStages * kStageBytes;
+  static constexpr int kOffSh = kOffUr + kEpiWarps * kUDepth * kUSlot;
+};
+
+template <int EPI, int NST>
 struct TcShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[NST];
+  uint64_t empty[NST];
   uint64_t accf[kAccBufs];
   uint64_t acce[kAccBufs];
   uint64_t aready;
@@ -71,8 +80,8 @@ struct TcShared {
   int row_req[kTileM];
   int row_prev[kTileM];
   float row_invT[kTileM];
-  Partial part[kWpq * kTileM];   // per-row partials: [column worker][row of the replica group]
-  float part_zx[kWpq * kTileM];  // the logit at each partial's index (residual mode: "some p > q")
+  Partial part[EPI / 4 * kTileM];   // per-row partials: [column worker][row of the replica group]
+  float part_zx[EPI / 4 * kTileM];  // the logit at each partial's index (residual mode: "some p > q")
   int row_urow[kTileM];        // the row of U (of the base logits) each M-tile row reads
   // residual mode: per row the rejecting position, the target row, and the log2-scaled
   // normalisers of p and q
@@ -80,8 +89,11 @@ struct TcShared {
   float row_lt2[kTileM], row_lq2[kTileM];
 };
 
-constexpr int kSmemBytes = kOffSh + (int)sizeof(TcShared) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <bool RESID>
+constexpr int tc_smem_bytes() {
+  return TcCfg<RESID>::kOffSh + (int)sizeof(TcShared<TcCfg<RESID>::kEpiWarps, TcCfg<RESID>::kStages>) + 1024;
+}
+static_assert(tc_smem_bytes<false>() <= 232448 && tc_smem_bytes<true>() <= 232448, "shared memory budget");
 
 // ---- PTX wrappers (the mbarrier and bulk-copy ones are in dspark_internal.cuh) ----
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -174,8 +186,9 @@ __device__ __forceinline__ uint32_t idesc_n(int n) { return kIdescBase | ((uint3
 
 __device__ __forceinline__ __nv_bfloat162 bf162_of(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); }
 
+template <int EPI>
 __device__ __forceinline__ void named_sync_epi() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(EPI * 32) : "memory");
 }
 
 // Work split of one draft position: M-tiles of 128 active rows, each shared by gm CTAs
@@ -204,17 +217,22 @@ __device__ __forceinline__ int range_lo(int j, int nb, int gm) {
 // 2 and 4) instead of softmax(z / T); the winner goes into the request's packed key and a
 // positive residual anywhere into its flag.
 template <int RCH, bool RESID>   // rank / 64
-__global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __grid_constant__ DraftArgs a) {
+__global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent(const __grid_constant__ DraftArgs a) {
   constexpr int kRank = RCH * 64;
+  constexpr int kEpiWarps = TcCfg<RESID>::kEpiWarps;
+  constexpr int kWpq = TcCfg<RESID>::kWpq;
+  constexpr int kStages = TcCfg<RESID>::kStages;
   constexpr int NS = kStages;
-  constexpr int kOffUr = kOffW + NS * kStageBytes;
+  constexpr int kOffUr = TcCfg<RESID>::kOffUr;
+  constexpr int kOffSh = TcCfg<RESID>::kOffSh;
+  using Shared = TcShared<kEpiWarps, kStages>;
   constexpr int kLook = kUDepth;
   constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t *gb = smem_raw + (sb - raw);
-  TcShared &sh = *reinterpret_cast<TcShared *>(gb + kOffSh);
+  Shared &sh = *reinterpret_cast<Shared *>(gb + kOffSh);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) sh.skip = read_status(a.dev_status);
@@ -340,10 +358,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
-    const int eq = warp - 2;            // 0..7
+    const int eq = warp - 2;            // 0 .. kEpiWarps - 1
     const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 are reachable by this warp
     const int wq = eq >> 2;             // this warp's rank among the warps of its quadrant
-    const int et = eq * 32 + lane;      // 0..255
+    const int et = eq * 32 + lane;      // 0 .. 32 kEpiWarps - 1
     const uint64_t pol_stream = policy_evict_first();
     // every lane stores to another row, so the logits go out in whole 32-byte sectors where
     // the rows start on 32-byte boundaries (V % 16 == 0 from a 32-byte aligned base)
@@ -368,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         if (k * 65536 + m != tab_m) {    // the same decision in every epilogue thread
           // rows of M-tile m at position k (a run of the position's active list, in request
           // order) and their 1/T
-          named_sync_epi();           // readers of the previous table are done
+          named_sync_epi<kEpiWarps>();           // readers of the previous table are done
           if (et < kTileM) {
             const int i = et;
             if (RESID && row0 + i < pl.n_k) {
@@ -393,7 +411,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               sh.row_invT[i] = 0.0f;
             }
           }
-          named_sync_epi();
+          named_sync_epi<kEpiWarps>();
           tab_m = k * 65536 + m;
         }
         const int arow = quad * 32 + lane;        // TMEM lane = M-row
@@ -412,10 +430,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         const float lt2 = RESID ? sh.row_lt2[row] : 0.0f, lq2 = RESID ? sh.row_lq2[row] : 0.0f;
         bool any_pos = false;
         // the unit's 32-wide blocks are numbered 0 .. 2 (b1 - b0) - 1 across its tiles, in groups
-        // of gsz = 8 / nwk (4, 2 or 1) consecutive blocks, so that every tile (8 blocks) gives each
-        // of the nwk workers one group; worker wk takes groups wk, wk + nwk, ...  Four consecutive
-        // blocks from an even 64-wide block share one Philox call, which a worker then computes
-        // once per group.  The worker's i-th block gsb_of(i)'s U (64 bytes of each of the warp's 32
+        // of 4 / F consecutive blocks (a tile of 8 blocks holds 2F groups); worker wk takes groups
+        // wk, wk + nwk, ... across the tiles.  Four consecutive blocks from an even 64-wide block
+        // share one Philox call, which a worker then computes once per group.  The worker's i-th block gsb_of(i)'s U (64 bytes of each of the warp's 32
         // rows) is staged into slot i % kUDepth of the warp's ring kUDepth blocks ahead by
         // cp.async.  Four lanes copy one row's 64 contiguous bytes, so each instruction touches 8
         // rows: with one row per lane every instruction touched 32 rows far apart in memory, and
@@ -425,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // commits one group per block, so wait_group(kUDepth - 1) and a warp barrier mean the
         // oldest staged block has landed for the whole warp.
         const int nsub_u = 2 * (b1 - b0);
-        const int gsh = nwk == 2 ? 2 : (nwk == 4 ? 1 : 0);   // log2 of the group size
+        const int gsh = F == 1 ? 2 : (F == 2 ? 1 : 0);      // log2 of the group size
         auto gsb_of = [&](int i) { return (((i >> gsh) * nwk + wk) << gsh) + (i & ((1 << gsh) - 1)); };
         const uint32_t uring0 = sb + kOffUr + (uint32_t)(eq * kUDepth * kUSlot);
         const uint32_t uring = uring0 + (uint32_t)(lane * 64);
@@ -471,7 +488,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
               if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }
             }
           }
-          named_sync_epi();
+          named_sync_epi<kEpiWarps>();
           waited = true;
           if (*abort) break;
         }
@@ -480,7 +497,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           sh.row_prev[et] = RESID ? a.jobs[row0 + et].prev
                                   : ((k == 1) ? a.anchor[rq] : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2)));
         }
-        named_sync_epi();
+        named_sync_epi<kEpiWarps>();
         // gather the A operand with asynchronous 16-byte copies, all in flight at once: request
         // row i's unit c8 of K-chunk c goes to every replica M-row ar = g * rpg + i, chunk c,
         // unit (c8 ^ (ar & 7)) -- the 128-byte swizzle
@@ -666,7 +683,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
         // the next position needs -- and keeps its softmax partial for the merge after the last position
         sh.part[wk * rpg + row] = to_partial(st);
         sh.part_zx[wk * rpg + row] = RESID ? (any_pos ? 1.0f : 0.0f) : st.zx;
-        named_sync_epi();
+        named_sync_epi<kEpiWarps>();
         if (RESID && wk == 0 && valid) {
           // the row's residual draw: the CTA's winner into the request's key, its flag
           Race tot = from_partial(sh.part[row]);
@@ -696,7 +713,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
       }
       // this CTA is done with position k (every CTA arrives, with or without work): the
       // barrier gathers the epilogue's atomics, the arriving thread's fence releases them
-      named_sync_epi();
+      named_sync_epi<kEpiWarps>();
       if (et == 0) {
         __threadfence();
         atomicAdd(a.gbar + k, 1);
@@ -716,7 +733,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) draft_tc_persistent(const __gri
           if (clock64() - t0 > kTimeoutCycles) { *abort = 1; break; }
         }
       }
-      named_sync_epi();
+      named_sync_epi<kEpiWarps>();
       if (!*abort) {
         const int B = (int)a.B;
         const int64_t nw = (int64_t)G * kEpiWarps;
@@ -849,7 +866,7 @@ cudaError_t launch_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
     default: fn = (void *)draft_tc_persistent<4, RESID>; break;
   }
   {
-    cudaError_t e = ensure_dynamic_smem(fn, kSmemBytes);
+    cudaError_t e = ensure_dynamic_smem(fn, tc_smem_bytes<RESID>());
     if (e != cudaSuccess) return e;
   }
   const int grid = num_sms > 1024 ? 1024 : num_sms;
@@ -857,8 +874,8 @@ cudaError_t launch_tc(const DraftArgs &a, cudaStream_t s, int num_sms) {
   // positions can always complete
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreadsTc, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(TcCfg<RESID>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc_smem_bytes<RESID>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
