@@ -70,7 +70,10 @@ typedef enum {
   DSPARK_ERR_WORKSPACE = 10,      /* workspace NULL, too small or not 256-byte aligned   */
   DSPARK_ERR_DEVICE_TIMEOUT = 11, /* device: a bounded wait inside a kernel gave up      */
   DSPARK_ERR_CUDA = 12,           /* a CUDA runtime call failed (launch, query, copy)    */
-  DSPARK_ERR_UNSUPPORTED = 13     /* the current device is not sm_103 / shape unsupported */
+  DSPARK_ERR_UNSUPPORTED = 13,    /* the current device is not sm_103 / shape unsupported */
+  DSPARK_ERR_BOUNDS = 14          /* device, bounds-checked build only: an index the kernels
+                                     computed fell outside its buffer (the access was sent to
+                                     element 0 instead); never returned by the normal build */
 } dspark_status;
 
 typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;

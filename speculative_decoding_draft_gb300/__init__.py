@@ -28,7 +28,8 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libdspark.so")
+# DSPARK_LIBRARY selects another build of the same library (the bounds-checked one in tests)
+_LIB_PATH = os.environ.get("DSPARK_LIBRARY") or os.path.join(_HERE, "libdspark.so")
 
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
@@ -41,7 +42,7 @@ STATUS_NAMES = {
     4: "DSPARK_ERR_TEMPERATURE", 5: "DSPARK_ERR_SPS_TOO_SHORT", 6: "DSPARK_ERR_OFFSETS",
     7: "DSPARK_ERR_TOKEN_RANGE", 8: "DSPARK_ERR_LENGTHS", 9: "DSPARK_ERR_CONFIDENCE",
     10: "DSPARK_ERR_WORKSPACE", 11: "DSPARK_ERR_DEVICE_TIMEOUT", 12: "DSPARK_ERR_CUDA",
-    13: "DSPARK_ERR_UNSUPPORTED",
+    13: "DSPARK_ERR_UNSUPPORTED", 14: "DSPARK_ERR_BOUNDS",
 }
 
 EXPORTED_SYMBOLS = [

@@ -2,6 +2,9 @@
 
 Each translation unit is compiled in parallel, then linked into one shared
 library next to this file.  The only target is sm_103a; the build needs no GPU.
+build(bounds=True) makes the bounds-checked variant, libdspark_bounds.so, compiled
+with -DDSPARK_BOUNDS: every index the kernels compute from data before an access is
+checked against its buffer (DSPARK_ERR_BOUNDS, the access sent to element 0).
 """
 from __future__ import annotations
 
@@ -17,6 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdspark.so")
+BUILD_BOUNDS = os.path.join(HERE, "_build_bounds")
+LIB_BOUNDS = os.path.join(HERE, "libdspark_bounds.so")
 SOURCES = ["api.cu", "schedule.cu", "schedule_noalloc.cu", "verify.cu", "draft_simt.cu", "draft_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -38,15 +43,16 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, bounds: bool = False) -> str:
+    lib, bdir = (LIB_BOUNDS, BUILD_BOUNDS) if bounds else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DDSPARK_BOUNDS"] if bounds else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [cc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,14 +65,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             if err:
                 sys.stderr.write(err)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                bounds="--bounds" in sys.argv))

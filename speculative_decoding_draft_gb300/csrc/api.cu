@@ -97,6 +97,7 @@ const char *dspark_status_string(dspark_status s) {
     case DSPARK_ERR_DEVICE_TIMEOUT: return "DSPARK_ERR_DEVICE_TIMEOUT";
     case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
     case DSPARK_ERR_UNSUPPORTED: return "DSPARK_ERR_UNSUPPORTED";
+    case DSPARK_ERR_BOUNDS: return "DSPARK_ERR_BOUNDS";
   }
   return "DSPARK_ERR_UNKNOWN";
 }
@@ -197,6 +198,7 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   a.dev_status = dev_status;
   a.B = dims.B;
   a.K_max = dims.K_max;
+  a.u_rows = dims.B * dims.K_max;
   a.V = dims.V;
   a.rank = dims.rank;
   a.dtype = dims.dtype;
@@ -537,6 +539,7 @@ dspark_status dspark_verify_markov(const void *U, const void *E, const void *W, 
   r.dev_status = dev_status;
   r.B = dims.B;
   r.K_max = 1;
+  r.u_rows = dims.B * dims.K_max;
   r.V = dims.V;
   r.rank = dims.rank;
   r.dtype = dims.dtype;

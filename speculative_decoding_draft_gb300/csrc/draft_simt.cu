@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
       prologue_warp_prefix(wc, wp, wt, K, warp, lane);
       __syncthreads();
       if (r < B) {
-        a.perm[base[v] + wp[warp][v] + rank] = r;
-        a.iperm[r] = base[v] + wp[warp][v] + rank;
+        const int slot = (int)bchk(base[v] + wp[warp][v] + rank, B, a.dev_status);
+        a.perm[slot] = r;
+        a.iperm[r] = slot;
       }
       __syncthreads();
       if (tid >= 1 && tid <= K) base[tid] += wt[tid];
@@ -139,7 +140,8 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     __syncthreads();
     for (int k = 1; k <= K; ++k) {          // every lane runs every k: the ballots are warp-wide
       const uint32_t bal = __ballot_sync(0xffffffffu, v >= k);
-      if (v >= k) a.act[(int64_t)(k - 1) * B + carry[k] + wp[warp][k] + __popc(bal & ((1u << lane) - 1u))] = r;
+      if (v >= k)
+        a.act[(int64_t)(k - 1) * B + bchk(carry[k] + wp[warp][k] + __popc(bal & ((1u << lane) - 1u)), B, a.dev_status)] = r;
     }
     __syncthreads();
     if (tid >= 1 && tid <= K) carry[tid] += wt[tid];
@@ -201,9 +203,10 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_tile(const __grid_const
   float *s_next = a.rnn_state + (size_t)(k & 1) * plane;               // s_k
   if (tid < kCellReq) {
     const int i = i0 + tid;
-    const int r = i < n_k ? a.perm[i] : -1;
+    const int r = i < n_k ? (int)bchk(a.perm[i], a.B, a.dev_status) : -1;
     s_row_r[tid] = r;
-    s_row_prev[tid] = r < 0 ? 0 : ((k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2]);
+    s_row_prev[tid] =
+        r < 0 ? 0 : (int)bchk((k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2], a.V, a.dev_status);
   }
   __syncthreads();
   const int n_in = 2 * rank;
@@ -319,9 +322,10 @@ __global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_
   const int c0 = blockIdx.x * kTileCols;
   if (tid < kTileRows) {
     const int i = i0 + tid;
-    const int r = i < n_k ? a.perm[i] : -1;
+    const int r = i < n_k ? (int)bchk(a.perm[i], a.B, a.dev_status) : -1;
     s_row_r[tid] = r;
-    s_row_prev[tid] = r < 0 ? 0 : ((k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2]);
+    s_row_prev[tid] =
+        r < 0 ? 0 : (int)bchk((k == 1) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + k - 2], a.V, a.dev_status);
   }
   __syncthreads();
   const int r = s_row_r[tr];

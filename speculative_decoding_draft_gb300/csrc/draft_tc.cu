@@ -391,15 +391,15 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
             const int i = et;
             if (RESID && row0 + i < pl.n_k) {
               const VJob jb = a.jobs[row0 + i];
-              sh.row_req[i] = jb.r;
+              sh.row_req[i] = (int)bchk(jb.r, a.B, a.dev_status);
               sh.row_invT[i] = jb.invT;
               sh.row_j[i] = jb.j;
-              sh.row_urow[i] = jb.urow;
+              sh.row_urow[i] = (int)bchk(jb.urow, a.u_rows, a.dev_status);
               sh.row_trow[i] = jb.trow;
               sh.row_lt2[i] = jb.lse_t * kLog2e;
               sh.row_lq2[i] = jb.lse_q * kLog2e;
             } else if (row0 + i < pl.n_k) {
-              const int r = a.act[(int64_t)(k - 1) * a.B + row0 + i];
+              const int r = (int)bchk(a.act[(int64_t)(k - 1) * a.B + row0 + i], a.B, a.dev_status);
               sh.row_req[i] = r;
               sh.row_urow[i] = r * K + (k - 1);
               const float T = a.temperature[r];
@@ -494,8 +494,10 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
         }
         if (et < kTileM && et < nrows) {
           const int rq = sh.row_req[et];
-          sh.row_prev[et] = RESID ? a.jobs[row0 + et].prev
-                                  : ((k == 1) ? a.anchor[rq] : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2)));
+          sh.row_prev[et] = (int)bchk(RESID ? a.jobs[row0 + et].prev
+                                            : ((k == 1) ? a.anchor[rq]
+                                                        : key_index(load_key(a.best_key + (int64_t)rq * K + k - 2))),
+                                      V, a.dev_status);
         }
         named_sync_epi<kEpiWarps>();
         // gather the A operand with asynchronous 16-byte copies, all in flight at once: request
@@ -708,7 +710,8 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
           // the CTA's maximum), the index, the softmax pair
           Partial pp = to_partial(tot);
           pp.best = zx;
-          a.partials[(int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j] = pp;
+          a.partials[bchk((int64_t)(k - 1) * kTcPartialsPerStep + ((int64_t)m * kTileM + row) * pl.gm + j,
+                          a.partial_slots, a.dev_status)] = pp;
         }
       }
       // this CTA is done with position k (every CTA arrives, with or without work): the
@@ -742,12 +745,13 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
           if (k > k_last) break;
           const StepPlan pl = plan_step(sh.nact, k, G, nb);
           if (i >= pl.n_k) continue;
-          const int r = a.act[(int64_t)(k - 1) * B + i];
+          const int r = (int)bchk(a.act[(int64_t)(k - 1) * B + i], B, a.dev_status);
           const int64_t at = (int64_t)r * K + k - 1;
           const int x = key_index(load_key(a.best_key + at));
           // the gm CTA partials of the row: softmax pair, greedy maximum (the largest logit
           // field) and the logit of the token x, carried by the one partial whose index is x
-          const Partial *pr = a.partials + (int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm;
+          const Partial *pr = a.partials + bchk((int64_t)(k - 1) * kTcPartialsPerStep + (int64_t)i * pl.gm,
+                                                a.partial_slots - pl.gm + 1, a.dev_status);
           Race tot;
           race_init(tot);
           float zx = 0.0f;
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
           const unsigned fb = __ballot_sync(0xffffffffu, found);
           zx = __shfl_sync(0xffffffffu, zx, fb ? __ffs(fb) - 1 : 0);
           if (a.conf_out) {
-            const int prev = k == 1 ? a.anchor[r] : key_index(load_key(a.best_key + at - 1));
+            const int prev = (int)bchk(k == 1 ? a.anchor[r] : key_index(load_key(a.best_key + at - 1)), V, a.dev_status);
             const __nv_bfloat16 *erow = (const __nv_bfloat16 *)a.E + (int64_t)prev * a.rank;
             const float c = warp_confidence([&](int q) { return __bfloat162float(erow[q]); }, a.conf_w,
                                             (int)a.rank, a.conf_h[(int64_t)r * K + k - 1], lane);

@@ -187,6 +187,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// Index check of the bounds-checked build (-DDSPARK_BOUNDS): an index outside [0, n) records
+// DSPARK_ERR_BOUNDS in the status word and comes back as 0, so the access stays inside its
+// buffer and the caller sees the error.  In the normal build the index passes through.
+__device__ __forceinline__ int64_t bchk(int64_t i, int64_t n, int32_t *status) {
+#ifdef DSPARK_BOUNDS
+  if (i < 0 || i >= n) {
+    set_status(status, DSPARK_ERR_BOUNDS);
+    return 0;
+  }
+#else
+  (void)n;
+  (void)status;
+#endif
+  return i;
+}
+
 // 16-byte shared-memory load and store.
 __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
   uint4 v;
@@ -666,9 +682,10 @@ struct DraftArgs {
   // workspace carve-out
   int32_t *perm;      // [B] requests ordered by K_r descending
   int32_t *iperm;     // [B] position of each request in perm
-  int32_t *act;       // [K_max, B] row k-1: the requests with K_r >= k in request order (the
-                      // tensor-core path's M-tiles take consecutive runs of it, so a tile's rows
-                      // lie as close together in U as the active set allows)
+  int32_t *act;       // [K_max, B] row k-1: the requests with K_r >= k, those with T > 0 first
+                      // and then the greedy ones, each in request order (the tensor-core path's
+                      // M-tiles take consecutive runs of it: rows close together in U, and warps
+                      // of one kind of draw but at most one per position)
   int32_t *nact;      // [K_max + 2] active requests per position
   int32_t *counters;  // [B] per-row arrival counters (zero between steps)
   unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path
@@ -676,6 +693,7 @@ struct DraftArgs {
   Partial *partials;  // [partial_slots]
   float *zx_part;     // [partial_slots] CUDA-core path: the logit at each partial's index
   int64_t partial_slots;
+  int64_t u_rows = 0;  // rows of U (B x K_max of the draft; the residual pass runs with K_max = 1)
   // confidence head with the Markov term (optional): conf_out[r, k] =
   // sigmoid(conf_h[r, k] + conf_w . E[x_{k-1}])
   const float *conf_h = nullptr;   // [B, K_max] backbone term w_h . h_k + b

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
         w.trow = off + l;
         w.kind = greedy ? 5 : 4;
       }
-      a.rows[start[j] + slot] = w;
+      a.rows[bchk(start[j] + slot, (int64_t)B * (K + 1), a.dev_status)] = w;
     }
   }
 }
@@ -635,6 +635,12 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
         ScanMeta m;
         m.ri = ri;
         m.w = a.rows[ri];
+#ifdef DSPARK_BOUNDS
+        m.w.r = (int)bchk(m.w.r, a.B, a.dev_status);
+        m.w.j = 1 + (int)bchk(m.w.j - 1, a.K_max + 1, a.dev_status);
+        m.w.trow = (int)bchk(m.w.trow, a.tgt_off[a.B], a.dev_status);
+        m.w.drow = (int)bchk(m.w.drow, a.B * a.K_max, a.dev_status);
+#endif
         // rows past a rejection already found need no statistics
         const bool skip = *(volatile const int32_t *)(a.dead + m.w.r) < m.w.j;
         if (skip) {
@@ -857,7 +863,7 @@ __device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_o
   job.lse_t = 0.0f;
   job.lse_q = 0.0f;
   job.invT = greedy ? 1.0f : 1.0f / T;
-  job.out_slot = r * (K + 1) + n;
+  job.out_slot = (int)bchk(r * (K + 1) + n, a.B * (K + 1), a.dev_status);
   if (n < l) {                                             // rejected at position n + 1
     const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
     if (greedy) {
@@ -1004,7 +1010,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constan
     jb.lse_t = a.rres[(int64_t)r * (K + 1) + n].lse_t;
     jb.lse_q = a.D_lse[(int64_t)r * K + n];
     jb.invT = 1.0f / T;
-    a.jobs[slot] = jb;
+    a.jobs[bchk(slot, B, a.dev_status)] = jb;
   }
   __syncthreads();
   if (tid == 0) {
