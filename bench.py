@@ -52,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="ragged")
+    p.add_argument("--batch", type=int, default=0,
+                   help="requests per step instead of the configuration's B (smaller cases for profiler captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sps", choices=["literal", "step"], default="literal")
@@ -316,7 +318,8 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-KERNEL_SOURCES = {"draft": ("draft_tc.cu", "dspark_internal.cuh"), "verify": ("verify.cu", "dspark_internal.cuh")}
+KERNEL_SOURCES = {"draft": ("draft_tc.cu", "dspark_internal.cuh"),
+                  "verify": ("verify.cu", "draft_tc.cu", "dspark_internal.cuh")}   # + the residual pass
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -424,7 +427,10 @@ def cpu_baseline_report(cfg, w):
 def line_config(args, cfg):
     """The `config` object of the JSON line, shared by both arms."""
     from speculative_decoding_draft_gb300 import workloads as wl
-    return {"workload": wl.WORKLOAD_TEXT.get(args.config, args.config), "B": cfg.B, "K": cfg.K_max, "V": cfg.V,
+    name = wl.WORKLOAD_TEXT.get(args.config, args.config)
+    if getattr(args, "batch", 0) > 0:
+        name += f" -- run at B={cfg.B}"
+    return {"workload": name, "B": cfg.B, "K": cfg.K_max, "V": cfg.V,
             "rank": cfg.rank, "sps": args.sps, "head": args.head,
             "l2": "flushed between timed steps (256 MB write, untimed)"}
 
@@ -498,6 +504,9 @@ def main(argv=None):
     dist_init(world, "nccl")
     ds.lib()          # fails loudly when the CUDA library is missing
     cfg = wl.replica(wl.CONFIGS[args.config], rank)   # each replica drafts its own batch
+    if args.batch > 0:
+        from dataclasses import replace
+        cfg = replace(cfg, B=args.batch)
     w = make_workload(cfg, dev, args.sps, args.head)
     # The scheduler depends on the confidences only, not on the drafted tokens, so by
     # default it runs on a second stream beside the draft, which leaves it one SM.
@@ -615,7 +624,7 @@ def main(argv=None):
         kernels["draft"]["fp32_frac"] = draft_tflops / fp32_peak
     dom = "draft" if t_draft >= t_ver else "verify"
     dom_path = ("tensor-core" if step.tensor_core else ("cuda-core-rnn" if step.rnn else "cuda-core")) \
-        if dom == "draft" else "verify"
+        if dom == "draft" else ("recompute" if step.recompute else "stored")
     traffic = profiled_traffic(dom, args.config, dom_path)
     if dom == "draft" and not step.tensor_core:
         roofline = {"kernel": dom, "bound": "alu", "achieved": draft_tflops, "peak": fp32_peak, "unit": "TFLOP/s",

@@ -18,7 +18,7 @@ def test_records_name_their_workload_and_path():
         workload, path, nbytes, _ = _record(kernel)
         assert workload in ("qwen", "tiny", "highc", "dsv4", "ragged")
         assert nbytes > 0
-        assert path in ("tensor-core", "verify")
+        assert path in ("tensor-core", "recompute", "stored")
 
 
 def test_traffic_only_for_the_captured_workload_and_path(monkeypatch):
