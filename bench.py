@@ -623,7 +623,8 @@ def main(argv=None):
         kernels["draft"]["fp32_TFLOP/s_peak"] = fp32_peak
         kernels["draft"]["fp32_frac"] = draft_tflops / fp32_peak
     dom = "draft" if t_draft >= t_ver else "verify"
-    dom_path = ("tensor-core" if step.tensor_core else ("cuda-core-rnn" if step.rnn else "cuda-core")) \
+    dom_path = (("tensor-core" if step.recompute else "tensor-core-logits") if step.tensor_core
+                else ("cuda-core-rnn" if step.rnn else "cuda-core")) \
         if dom == "draft" else ("recompute" if step.recompute else "stored")
     traffic = profiled_traffic(dom, args.config, dom_path)
     if dom == "draft" and not step.tensor_core:
