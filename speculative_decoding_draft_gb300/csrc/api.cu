@@ -130,6 +130,7 @@ static size_t draft_ws_base(int64_t B, int64_t K_max, int64_t V) {
   return 2 * al256(sizeof(int32_t) * (size_t)B) + al256(sizeof(int32_t) * (size_t)(K_max + 2)) +
          al256(sizeof(int32_t) * (size_t)(B > 4096 ? B : 4096)) + al256(8 * (size_t)(B * K_max)) +
          al256(sizeof(int32_t) * (size_t)(K_max + 1)) + al256(sizeof(int32_t) * (size_t)(B * K_max)) +
+         al256(sizeof(int32_t) * (size_t)(2 * K_max * ((B + 31) / 32))) +
          al256(sizeof(Partial) * (size_t)draft_partial_slots(B, K_max, V)) +
          al256(sizeof(float) * (size_t)draft_partial_slots(B, K_max, V));
 }
@@ -222,6 +223,8 @@ dspark_status draft_call(const void *U, const void *E, const void *W, const int3
   p += al256(sizeof(int32_t) * (size_t)(dims.K_max + 1));
   a.act = (int32_t *)p;
   p += al256(sizeof(int32_t) * (size_t)(dims.B * dims.K_max));
+  a.grp = (int32_t *)p;
+  p += al256(sizeof(int32_t) * (size_t)(2 * dims.K_max * ((dims.B + 31) / 32)));
   a.partials = (Partial *)p;
   a.partial_slots = draft_partial_slots(dims.B, dims.K_max, dims.V);
   p += al256(sizeof(Partial) * (size_t)a.partial_slots);
@@ -544,7 +547,7 @@ dspark_status dspark_verify_markov(const void *U, const void *E, const void *W, 
   r.rank = dims.rank;
   r.dtype = dims.dtype;
   r.key = a.key;
-  r.perm = r.iperm = r.counters = r.act = nullptr;
+  r.perm = r.iperm = r.counters = r.act = r.grp = nullptr;
   r.nact = a.jobs_nact;
   r.best_key = a.key_out;
   r.gbar = a.jobs_gbar;

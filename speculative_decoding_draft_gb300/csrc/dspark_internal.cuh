@@ -682,10 +682,13 @@ struct DraftArgs {
   // workspace carve-out
   int32_t *perm;      // [B] requests ordered by K_r descending
   int32_t *iperm;     // [B] position of each request in perm
-  int32_t *act;       // [K_max, B] row k-1: the requests with K_r >= k, those with T > 0 first
-                      // and then the greedy ones, each in request order (the tensor-core path's
-                      // M-tiles take consecutive runs of it: rows close together in U, and warps
-                      // of one kind of draw but at most one per position)
+  int32_t *act;       // [K_max, B] row k-1: the requests with K_r >= k in groups of 32 of one
+                      // kind (T > 0 or greedy), full groups in the order they complete in
+                      // request order, then the partial ones (the tensor-core path's M-tiles take
+                      // consecutive runs of it: rows close together in U, and warps of one kind
+                      // of draw but at most one per position)
+  int32_t *grp;       // [K_max, 2, ceil(B / 32)] building act: per full group, the other kind's
+                      // full groups completed before it
   int32_t *nact;      // [K_max + 2] active requests per position
   int32_t *counters;  // [B] per-row arrival counters (zero between steps)
   unsigned long long *best_key;  // [B, K_max] packed (score, index) maxima of the tensor-core path

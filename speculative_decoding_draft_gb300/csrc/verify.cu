@@ -696,13 +696,21 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
       const int lo = min(V, m.sl * kRowSlice), hi = min(V, lo + kRowSlice);
       const float a2 = m.w.invT * kLog2e;
       const uint32_t pos = (uint32_t)m.w.j, rq = (uint32_t)m.w.r;
+      // each block's noise word is computed one block ahead, so that its Philox chain runs
+      // beside the previous block's arithmetic
+      auto noise = [&](int v) -> uint32_t {
+        const uint32_t g = (uint32_t)v >> 5;
+        return v < hi ? word_of(philox(a.key, g >> 2, pos, rq, kTagResid), (int)(g & 3u)) : 0u;
+      };
+      uint32_t wb_next = noise(lo + 32 * tid);
 #pragma unroll 1
       for (int q = 0; q < kRowSlice / 32 / kRowThreads; ++q) {
         const int b = tid + q * kRowThreads;
         const int v0 = lo + 32 * b;
         if (v0 >= hi) break;
         const uint32_t g = (uint32_t)v0 >> 5;
-        const uint32_t wb = word_of(philox(a.key, g >> 2, pos, rq, kTagResid), (int)(g & 3u));
+        const uint32_t wb = wb_next;
+        wb_next = noise(v0 + 32 * kRowThreads);
         auto pick = [&] { return word_of(philox(a.key, g >> 2, pos, rq, kTagResidPick), (int)(g & 3u)); };
         if (BULK) {
           const uint32_t base = smem_u32(ring) + (uint32_t)s * stage_bytes + 64u * (uint32_t)b;
