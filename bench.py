@@ -239,7 +239,7 @@ class Step:
         # position (CUDA cores); schedule: 1; verify: plan, scan, sample (+ the residual jobs and
         # the tensor-core residual pass when it recomputes)
         self.draft_launches = 2 if self.tensor_core else (1 + 2 * K if self.rnn else 1 + K)
-        self.verify_launches = 5 if self.recompute else 3
+        self.verify_launches = 6 if self.recompute else 5
         self.launches_per_step = self.draft_launches + 1 + self.verify_launches
 
     def draft(self, inp=None):

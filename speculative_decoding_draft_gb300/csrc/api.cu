@@ -464,8 +464,7 @@ dspark_status dspark_verify_ragged(const void *draft_logits, const float *draft_
 // flags [B], active counts [3], barrier counters [2], and the packed W2 when the caller
 // passes W as given.
 static size_t verify_markov_extra(const dspark_dims &d) {
-  size_t n = al256(sizeof(VJob) * (size_t)d.B) + al256(8 * (size_t)d.B) + al256(sizeof(int32_t) * (size_t)d.B) +
-             al256(sizeof(int32_t) * 3) + al256(sizeof(int32_t) * 2);
+  size_t n = al256(8 * (size_t)d.B) + al256(sizeof(int32_t) * (size_t)d.B) + al256(sizeof(int32_t) * 2);
   if (!(d.flags & DSPARK_FLAG_W_PACKED)) n += al256(draft_packed_bytes(d.rank, d.V));
   return n;
 }
@@ -514,16 +513,12 @@ dspark_status dspark_verify_markov(const void *U, const void *E, const void *W, 
   verify_carve(a, workspace);
   char *p = (char *)workspace + verify_ws_bytes(dims.B, dims.V, nullptr);
   a.anchor = anchor;
-  a.jobs = (VJob *)p;
-  p += al256(sizeof(VJob) * (size_t)dims.B);
   a.key_out = (unsigned long long *)p;
   a.resid_key = a.key_out;
   p += al256(8 * (size_t)dims.B);
   a.any_out = (int32_t *)p;
   a.resid_any = a.any_out;
   p += al256(sizeof(int32_t) * (size_t)dims.B);
-  a.jobs_nact = (int32_t *)p;
-  p += al256(sizeof(int32_t) * 3);
   a.jobs_gbar = (int32_t *)p;
   p += al256(sizeof(int32_t) * 2);
   // the residual pass: the draft kernel's residual mode over the jobs

@@ -1,11 +1,11 @@
 // Ragged rejection-sampling verification ("DSpark", S2.1; "Speculative
 // decoding, from zero to DSpark", S2 and Appendix A1).
 //
-// Three kernels:
-//  1. verify_plan (one CTA): validates every request, resets its state and lists the
-//     verified rows (r, j <= ell_r) position-major -- every request's position 1, then
-//     position 2, ... -- with the draft side of each accept test precomputed (log q(x_j)
-//     when the draft normaliser is known).
+// Three stages:
+//  1. verify_plan_count (one CTA) and verify_plan_fill (a thread per request): validate every
+//     request, reset its state and list the verified rows (r, j <= ell_r) position-major --
+//     every request's position 1, then position 2, ... -- with the draft side of each accept
+//     test precomputed (log q(x_j) when the draft normaliser is known).
 //  2. verify_scan (persistent): each CTA takes whole listed rows in that order and streams
 //     a row's vocabulary slices through a shared-memory ring (bulk copies issued by a
 //     staging warp; the target slice, and the draft slice when no draft normaliser is
@@ -16,13 +16,14 @@
 //     staging a row the staging warp reads that word and skips rows past a known
 //     rejection, so the rows read are the ones up to each request's deciding row, except
 //     where a decision is not known yet.
-//  3. verify_sample: per request the outcome -- n_acc = (first rejection) - 1 or ell_r, the
-//     accepted tokens, then the correction or bonus: the argmax of the rejecting row for T = 0
-//     and the bonus token are the scan's (the bonus row is listed at position ell_r + 1, and
-//     the scan draws it -- the two-level draw over z / T -- or takes its argmax for T = 0,
-//     skipping it once a rejection is known); a T > 0 rejection draws the residual
-//     norm(max(0, p - q)) here, spread over (request x vocabulary chunk) CTAs with the last
-//     chunk merging, or takes the tensor-core recompute pass's draw.
+//  3. verify_jobs (one CTA): per request the outcome -- n_acc = (first rejection) - 1 or
+//     ell_r, the accepted tokens, then the correction or bonus: the argmax of the rejecting row
+//     for T = 0 and the bonus token are the scan's (the bonus row is listed at position
+//     ell_r + 1, and the scan draws it -- the two-level draw over z / T -- or takes its argmax
+//     for T = 0, skipping it once a rejection is known) -- and the list of T > 0 rejections.
+//     verify_sample then draws each rejection's residual norm(max(0, p - q)), spread over
+//     (rejection x vocabulary chunk) CTAs with the last chunk merging, or takes the
+//     tensor-core recompute pass's draw.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -365,51 +366,29 @@ __device__ void sample_range(const VerifyArgs &a, const VerifyJob &job, int r, i
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
 
-// 0 when request r is valid (lengths, offsets, temperature, the draft tokens it verifies),
-// else the status code.
-__device__ __forceinline__ int request_check(const VerifyArgs &a, int r) {
-  const int K = (int)a.K_max, V = (int)a.V;
-  const int l = a.ell[r];
-  const int err = request_error(K, r, l, a.temperature[r], a.tgt_off[r], a.tgt_off[r + 1], a.tgt_off[0]);
-  if (err) return err;
-  for (int j = 1; j <= l; ++j) {
-    const int x = a.draft_tok[(int64_t)r * K + j - 1];
-    if (x < 0 || x >= V) return DSPARK_ERR_TOKEN_RANGE;
-  }
-  return 0;
-}
-
-// One CTA: counts the rows of every position, then lists each valid request's rows
-// j = 1..ell_r and its bonus row j = ell_r + 1 at start[j] + (its rank among position j's
-// rows).  Counts and ranks are taken per warp (one shared atomic per warp and position); the
-// order inside a position is whatever the atomics give, and no result depends on it (each
-// row is processed by one CTA on its own).
-template <int DT>
-__global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constant__ VerifyArgs a) {
-  __shared__ int cnt[kMaxK + 3], fill[kMaxK + 3], start[kMaxK + 3];
-  __shared__ int s_bad;
+// Two kernels.  verify_plan_count (one CTA) resets each request's state, counts the rows of
+// every position (ell_r + 1 rows of a request whose length is in range; the fill pass checks
+// everything else and reports it) and sets each position's first slot.  verify_plan_fill (a
+// thread per request and position) validates the request and lists its rows j = 1..ell_r and
+// its bonus row j = ell_r + 1 at row_start[j] + (a slot taken per warp and position from
+// row_fill[j]).
+// The order inside a position is whatever the atomics give, and no result depends on it
+// (each row is processed by one CTA on its own).  With an invalid request the status word is
+// set and every later kernel returns at once.
+__global__ void __launch_bounds__(kPlanThreads) verify_plan_count(const __grid_constant__ VerifyArgs a) {
+  __shared__ int cnt[kMaxK + 3];
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x, lane = tid & 31;
-  if (tid < kMaxK + 3) {
-    cnt[tid] = 0;
-    fill[tid] = 0;
-  }
-  if (tid == 0) s_bad = 0;
+  if (tid < kMaxK + 3) cnt[tid] = 0;
   __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
   for (int r0 = 0; r0 < B; r0 += kPlanThreads) {   // every thread runs every round: warp-wide ballots
     const int r = r0 + tid;
-    int nr = 0;                                    // rows of request r (ell_r + 1; 0 if none)
+    int nr = 0;                                    // rows of request r
     if (r < B) {
       a.dead[r] = kNoReject;
       a.counters[r] = 0;
-      const int err = request_check(a, r);
-      if (err) {
-        set_status(a.dev_status, err);
-        s_bad = 1;
-      } else {
-        nr = a.ell[r] + 1;
-      }
+      const int l = a.ell[r];
+      nr = (l >= 0 && l <= K) ? l + 1 : 0;
     }
     for (int j = 1; j <= K + 1; ++j) {
       const uint32_t bal = __ballot_sync(0xffffffffu, j <= nr);
@@ -418,29 +397,43 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
     }
   }
   __syncthreads();
-  if (s_bad) return;                               // nothing runs after an invalid request
   if (tid == 0) {
-    start[1] = 0;
-    for (int j = 1; j <= K + 1; ++j) start[j + 1] = start[j] + cnt[j];
-    *a.nrows = start[K + 2];
-  }
-  __syncthreads();
-  for (int r0 = 0; r0 < B; r0 += kPlanThreads) {
-    const int r = r0 + tid;
-    const int l = r < B ? a.ell[r] : -1;
-    const float T = r < B ? a.temperature[r] : 1.0f;
-    const bool greedy = (T == 0.0f);
-    const float invT = greedy ? 1.0f : 1.0f / T;
-    const int off = r < B ? a.tgt_off[r] : 0;
+    int st = 0;
     for (int j = 1; j <= K + 1; ++j) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, j <= l + 1);
-      if (bal == 0u) break;
-      const int leader = __ffs(bal) - 1;
-      int slot = 0;
-      if (lane == leader) slot = atomicAdd(&fill[j], __popc(bal));
-      slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(bal & lt);
-      if (j > l + 1) continue;
-      VRow w;
+      a.row_start[j] = st;
+      a.row_fill[j] = 0;
+      st += cnt[j];
+    }
+    *a.nrows = st;
+  }
+}
+
+constexpr int kFillThreads = 256;
+
+// A thread per (request r, position j), j = 1..K_max + 1: the row if j <= ell_r + 1.  The
+// thread of j = 1 checks the request's length, offsets and temperature, each row's thread its
+// own draft token before using it; a slot is taken per warp and position (the lanes with the
+// same j share one atomic).
+template <int DT>
+__global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_constant__ VerifyArgs a) {
+  if (read_status(a.dev_status)) return;
+  const int K = (int)a.K_max, B = (int)a.B, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kFillThreads + threadIdx.x;
+  const int r = (int)(item / (K + 1)), j = (int)(item % (K + 1)) + 1;
+  bool row = false;
+  VRow w;
+  if (r < B) {
+    const int l = a.ell[r];
+    const float T = a.temperature[r];
+    if (j == 1) {
+      const int err = request_error(K, r, l, T, a.tgt_off[r], a.tgt_off[r + 1], a.tgt_off[0]);
+      if (err) set_status(a.dev_status, err);
+    }
+    if (l >= 0 && l <= K && j <= l + 1) {
+      const bool greedy = (T == 0.0f);
+      const float invT = greedy ? 1.0f : 1.0f / T;
+      const int off = a.tgt_off[r];
+      row = true;
       w.r = r;
       w.j = j;
       w.invT = invT;
@@ -449,7 +442,10 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
         w.drow = r * K + j - 1;
         w.x = a.draft_tok[w.drow];
         w.trow = off + j - 1;
-        if (greedy) {
+        if (w.x < 0 || w.x >= (int)a.V) {
+          set_status(a.dev_status, DSPARK_ERR_TOKEN_RANGE);
+          row = false;
+        } else if (greedy) {
           w.kind = 2;
         } else if (a.D_lse != nullptr) {
           // log q(x_j) from the draft normaliser and the drawn token's logit (its own output,
@@ -468,9 +464,16 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan(const __grid_constan
         w.trow = off + l;
         w.kind = greedy ? 5 : 4;
       }
-      a.rows[bchk(start[j] + slot, (int64_t)B * (K + 1), a.dev_status)] = w;
     }
   }
+  const uint32_t bal = __ballot_sync(0xffffffffu, row);
+  const uint32_t peers = __match_any_sync(0xffffffffu, row ? j : 0) & bal;
+  if (!row) return;
+  const int leader = __ffs(peers) - 1;
+  int slot = 0;
+  if (lane == leader) slot = atomicAdd(&a.row_fill[j], __popc(peers));
+  slot = __shfl_sync(peers, slot, leader) + __popc(peers & ((1u << lane) - 1u));
+  a.rows[bchk(a.row_start[j] + slot, (int64_t)B * (K + 1), a.dev_status)] = w;
 }
 
 // One block of the bonus draw (the two-level draw over z / T) from its 16 bf16 pair words in
@@ -845,69 +848,28 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
 // ---------------------------------------------------------------------------
 // 3. sampling: outcome per request and the residual / bonus draw
 // ---------------------------------------------------------------------------
-// Request r's outcome from the scan (one warp): n = (first rejection) - 1, or ell_r when no
-// position was rejected; with write_out the accepted tokens, the padding, n_acc, a greedy
-// rejection's correction (the argmax of the rejecting row) and the bonus token (drawn by the
-// scan) are written.  Returns in lane 0 the residual job of a T > 0 rejection, if any.
-__device__ void job_from_scan(const VerifyArgs &a, int r, int lane, bool write_out, VerifyJob *out_job) {
-  const int K = (int)a.K_max;
-  const int l = a.ell[r];
-  const float T = a.temperature[r];
-  const bool greedy = (T == 0.0f);
-  const int dead = a.dead[r];
-  const int n = dead <= l ? dead - 1 : l;                  // accepted drafts
-  if (write_out && lane <= K) {
-    int32_t *out = a.out_tok + (int64_t)r * (K + 1);
-    if (lane < n) out[lane] = a.draft_tok[(int64_t)r * K + lane];
-    else if (lane > n) out[lane] = -1;
-  }
-  if (lane != 0) return;
-  const int64_t off = a.tgt_off[r];
-  VerifyJob job;
-  job.mode = 0;
-  job.pos = 0;
-  job.trow = 0;
-  job.drow = 0;
-  job.lse_t = 0.0f;
-  job.lse_q = 0.0f;
-  job.invT = greedy ? 1.0f : 1.0f / T;
-  job.out_slot = (int)bchk(r * (K + 1) + n, a.B * (K + 1), a.dev_status);
-  if (n < l) {                                             // rejected at position n + 1
-    const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
-    if (greedy) {
-      if (write_out) a.out_tok[job.out_slot] = rr.amax;
-    } else {
-      job.mode = a.resid_key ? 4 : 1;
-      job.pos = n + 1;
-      job.trow = off + n;
-      job.drow = (int64_t)r * K + n;
-      job.lse_t = rr.lse_t;
-      job.lse_q = a.D_lse ? a.D_lse[job.drow] : rr.lse_q;
-    }
-  } else if (write_out) {
-    // every position accepted: the bonus token the scan drew (or the argmax for T = 0)
-    a.out_tok[job.out_slot] = a.rres[(int64_t)r * (K + 1) + l].amax;
-  }
-  if (write_out) a.n_acc[r] = n;
-  *out_job = job;
-}
-
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_constant__ VerifyArgs a) {
   __shared__ Race red[kSampleThreads / 32];
   __shared__ int s_any[kSampleThreads / 32];
   __shared__ int s_last, s_tok;
-  __shared__ VerifyJob s_job;
   const int cx = blockIdx.x, tid = threadIdx.x;
   if (read_status(a.dev_status)) return;
-  const int V = (int)a.V;
-  for (int r = blockIdx.y; r < (int)a.B; r += gridDim.y) {
-    // every chunk reads the same outcome; chunk 0 writes the accepted tokens
-    if (tid < 32) job_from_scan(a, r, tid, cx == 0, &s_job);
-    __syncthreads();
-    const VerifyJob job = s_job;
-    __syncthreads();
-    if (job.mode == 0) continue;
+  const int V = (int)a.V, K = (int)a.K_max;
+  const int njobs = *(volatile const int32_t *)(a.jobs_nact + 1);
+  for (int ji = blockIdx.y; ji < njobs; ji += gridDim.y) {
+    // one T > 0 rejection: its residual token (every other output is verify_jobs')
+    const VJob jb = a.jobs[ji];
+    const int r = jb.r;
+    VerifyJob job;
+    job.mode = a.resid_key ? 4 : 1;
+    job.pos = jb.j;
+    job.trow = jb.trow;
+    job.drow = jb.urow;
+    job.lse_t = jb.lse_t;
+    job.lse_q = jb.lse_q;
+    job.invT = jb.invT;
+    job.out_slot = r * (K + 1) + jb.j - 1;
     if (job.mode == 4) {
       // the residual was drawn by the tensor-core recompute pass: its token, or (no p > q
       // survived rounding anywhere) the draw from p on the rejecting row; chunk 0 only
@@ -978,9 +940,13 @@ __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_
   }
 }
 
-// Recompute entry point: the T > 0 rejections become the jobs of the tensor-core residual
-// pass (one CTA; the order of the list is the atomics' and changes no result), and that pass's
-// keys, flags and counters start from zero.
+// Every request's outcome from the scan, and the T > 0 rejections as the jobs of the residual
+// draw (one CTA; the order of the list is the atomics' and changes no result).  n = (first
+// rejection) - 1, or ell_r when every position was accepted; the accepted tokens, the -1
+// padding and at slot n the greedy correction (the rejecting row's argmax) or the bonus token
+// (the scan's draw, or its argmax for T = 0) are written here; a T > 0 rejection's token is
+// the residual draw's.  With the recompute entry point the residual pass's keys and flags
+// start from zero.
 __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constant__ VerifyArgs a) {
   __shared__ int count;
   if (read_status(a.dev_status)) return;
@@ -994,13 +960,24 @@ __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constan
     int n = 0;
     float T = 1.0f;
     if (r < B) {
-      a.key_out[r] = 0ull;
-      a.any_out[r] = 0;
+      if (a.key_out) {
+        a.key_out[r] = 0ull;
+        a.any_out[r] = 0;
+      }
       const int l = a.ell[r];
       const int dead = a.dead[r];
       n = dead <= l ? dead - 1 : l;
       T = a.temperature[r];
-      job = n < l && T != 0.0f;
+      const bool greedy = (T == 0.0f);
+      const int64_t rb = (int64_t)r * (K + 1);
+      for (int i = 0; i <= K; ++i) {
+        int v = -1;
+        if (i < n) v = a.draft_tok[(int64_t)r * K + i];
+        else if (i == n) v = n < l ? (greedy ? a.rres[rb + n].amax : -1) : a.rres[rb + l].amax;
+        a.out_tok[rb + i] = v;
+      }
+      a.n_acc[r] = n;
+      job = n < l && !greedy;
     }
     const uint32_t bal = __ballot_sync(0xffffffffu, job);
     if (bal == 0u) continue;
@@ -1012,11 +989,12 @@ __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constan
     VJob jb;
     jb.r = r;
     jb.j = n + 1;
-    jb.prev = (n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1];
+    jb.prev = a.anchor ? ((n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1]) : 0;
     jb.urow = r * K + n;
     jb.trow = a.tgt_off[r] + n;
-    jb.lse_t = a.rres[(int64_t)r * (K + 1) + n].lse_t;
-    jb.lse_q = a.D_lse[(int64_t)r * K + n];
+    const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
+    jb.lse_t = rr.lse_t;
+    jb.lse_q = a.D_lse ? a.D_lse[(int64_t)r * K + n] : rr.lse_q;
     jb.invT = 1.0f / T;
     a.jobs[bchk(slot, B, a.dev_status)] = jb;
   }
@@ -1025,8 +1003,10 @@ __global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constan
     a.jobs_nact[0] = B;
     a.jobs_nact[1] = count;
     a.jobs_nact[2] = 0;
-    a.jobs_gbar[0] = 0;
-    a.jobs_gbar[1] = 0;
+    if (a.jobs_gbar) {
+      a.jobs_gbar[0] = 0;
+      a.jobs_gbar[1] = 0;
+    }
   }
 }
 
@@ -1041,8 +1021,11 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
     a.chunk_len = (int)((per + kBlockW - 1) / kBlockW * kBlockW);
     a.chunks = (int)((a.V + a.chunk_len - 1) / a.chunk_len);
   }
-  verify_plan<DT><<<1, kPlanThreads, 0, s>>>(a);
+  verify_plan_count<<<1, kPlanThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  verify_plan_fill<DT><<<(unsigned)((a.B * (a.K_max + 1) + kFillThreads - 1) / kFillThreads), kFillThreads, 0, s>>>(a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // scan: a wave of persistent CTAs (4 per SM with single-row stages, 2 with two rows; two
   // stages at four CTAs per SM ran 4 % faster than three stages at three)
@@ -1058,10 +1041,10 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
   verify_scan<DT, VEC, BULK><<<(unsigned)grid, kScanThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  verify_jobs<<<1, kPlanThreads, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   if (resid) {
-    verify_jobs<<<1, kPlanThreads, 0, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     e = launch_resid_tc(*resid, s, num_sms);
     if (e != cudaSuccess) return e;
   }
@@ -1083,7 +1066,8 @@ size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)B * (size_t)(kMaxK + 1);
   return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) + al(sizeof(VRow) * rows) +
-         al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) + al(sizeof(VRowRes) * rows);
+         al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) + al(sizeof(VRowRes) * rows) +
+         al(sizeof(VJob) * (size_t)B) + al(sizeof(int32_t) * 3);
 }
 
 void verify_carve(VerifyArgs &a, void *workspace) {
@@ -1100,11 +1084,18 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   p += al(sizeof(Partial) * (size_t)a.B * (size_t)chunks);
   a.rows = (VRow *)p;
   p += al(sizeof(VRow) * rows);
-  a.nrows = (int32_t *)p;
+  a.nrows = (int32_t *)p;          // one 256-byte block: the count, the starts, the fill counters
+  a.row_start = a.nrows + 4;
+  a.row_fill = a.nrows + 32;
+  static_assert(32 + kMaxK + 3 <= 64, "plan counters fit one 256-byte block");
   p += al(sizeof(int32_t));
   a.dead = (int32_t *)p;
   p += al(sizeof(int32_t) * (size_t)a.B);
   a.rres = (VRowRes *)p;
+  p += al(sizeof(VRowRes) * rows);
+  a.jobs = (VJob *)p;
+  p += al(sizeof(VJob) * (size_t)a.B);
+  a.jobs_nact = (int32_t *)p;
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, int num_sms, const DraftArgs *resid) {
