@@ -4,10 +4,10 @@
 // step kernel and hands it the feature that replaces the W1 row.
 //
 // For position k the active requests (K_r >= k) form a prefix of the
-// permutation `perm`, which orders requests by K_r descending; the prologue
-// builds it together with the active counts nact[k], and the lists act[k - 1] of the
-// active requests that the tensor-core path tiles (T > 0 first, then T = 0, each in
-// request order).
+// permutation `perm`, which orders requests by K_r descending; the CUDA-core path's
+// prologue builds it together with the active counts nact[k].  The tensor-core path's
+// prologue (one CTA per position) builds the lists act[k - 1] that its tiles take
+// instead: the active requests in 32-request groups of one kind (T > 0 or greedy).
 //
 // CUDA-core step: grid (vocabulary tile, tile of active rows); each block forms
 // z = U + feature . W2 for its rows and columns with fp32 FMAs (the feature is the
@@ -43,49 +43,50 @@ __device__ __forceinline__ void prologue_warp_prefix(int (*cnt)[kMaxK + 2], int 
   }
 }
 
-// lists: 1 = the K_r-descending permutation (the CUDA-core path), 2 = the per-position
-// active lists (the tensor-core path).
-__global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a, int lists) {
+// Validation and reset of request r (both paths): its length, anchor and temperature; its
+// packed maxima cleared, the slots past K_r set to -1.  Returns the error code (0: valid).
+__device__ __forceinline__ int prologue_request(const DraftArgs &a, int r) {
+  const int K = (int)a.K_max, V = (int)a.V;
+  const int kr = a.K_r[r];
+  int err = 0;
+  if (kr < 1 || kr > K) err = DSPARK_ERR_LENGTHS;
+  const int x0 = a.anchor[r];
+  if (x0 < 0 || x0 >= V) err = DSPARK_ERR_TOKEN_RANGE;
+  if (!temperature_ok(a.temperature[r])) err = DSPARK_ERR_TEMPERATURE;
+  a.counters[r] = 0;
+  for (int k = 0; k < K; ++k) {
+    a.best_key[(int64_t)r * K + k] = 0ull;
+    if (k >= kr) {
+      a.draft_tok[(int64_t)r * K + k] = -1;
+      if (a.conf_out) a.conf_out[(int64_t)r * K + k] = 0.0f;
+    }
+  }
+  return err;
+}
+
+// The CUDA-core path's prologue (one CTA): validation and reset, the active counts nact[k],
+// and the K_r-descending permutation.
+__global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_constant__ DraftArgs a) {
   __shared__ int s_err, s_skip;
   __shared__ int cnt[kMaxK + 2];          // requests per length value
   __shared__ int base[kMaxK + 2];         // next free slot per length value
   __shared__ int wc[kPrologueThreads / 32][kMaxK + 2];    // per-warp counts of one round
   __shared__ int wp[kPrologueThreads / 32][kMaxK + 2];    // their exclusive prefix over warps
   __shared__ int wt[kMaxK + 2];                           // their sum
-  __shared__ int carry[kMaxK + 2];        // act: T > 0 (perm: all) requests per position so far
-  __shared__ int carry_g[kMaxK + 2];      // act: greedy requests per position so far
-  __shared__ int wc_g[kPrologueThreads / 32][kMaxK + 2];  // the same three for greedy requests
-  __shared__ int wp_g[kPrologueThreads / 32][kMaxK + 2];
-  __shared__ int wt_g[kMaxK + 2];
-  __shared__ int n_s[kMaxK + 2], n_g[kMaxK + 2];           // active T > 0 / greedy per position
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_skip = read_status(a.dev_status);
     s_err = 0;
   }
-  if (tid < kMaxK + 2) {
-    cnt[tid] = 0;
-    carry[tid] = 0;
-  }
+  if (tid < kMaxK + 2) cnt[tid] = 0;
   __syncthreads();
   if (s_skip) return;
   if (tid <= a.K_max) a.gbar[tid] = 0;
-  const int B = (int)a.B, K = (int)a.K_max, V = (int)a.V;
+  const int B = (int)a.B, K = (int)a.K_max;
   for (int r = tid; r < B; r += kPrologueThreads) {
-    const int kr = a.K_r[r];
-    if (kr < 1 || kr > K) atomicCAS(&s_err, 0, (int)DSPARK_ERR_LENGTHS);
-    else atomicAdd(&cnt[kr], 1);
-    const int x0 = a.anchor[r];
-    if (x0 < 0 || x0 >= V) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TOKEN_RANGE);
-    if (!temperature_ok(a.temperature[r])) atomicCAS(&s_err, 0, (int)DSPARK_ERR_TEMPERATURE);
-    a.counters[r] = 0;
-    for (int k = 0; k < K; ++k) {
-      a.best_key[(int64_t)r * K + k] = 0ull;
-      if (k >= kr) {
-        a.draft_tok[(int64_t)r * K + k] = -1;
-        if (a.conf_out) a.conf_out[(int64_t)r * K + k] = 0.0f;
-      }
-    }
+    const int err = prologue_request(a, r);
+    if (err) atomicCAS(&s_err, 0, err);
+    else atomicAdd(&cnt[a.K_r[r]], 1);
   }
   __syncthreads();
   if (s_err) {
@@ -103,100 +104,121 @@ __global__ void __launch_bounds__(kPrologueThreads) draft_prologue(const __grid_
     a.nact[K + 1] = 0;
   }
   __syncthreads();
-  if (lists == 1) {
-    // stable scatter, 1024 requests per round: rank among equal lengths by warp match, then
-    // the prefix of the warps' counts
-    for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
-      const int r = c0 + tid;
-      const int v = r < B ? a.K_r[r] : 0;
-      const uint32_t peers = __match_any_sync(0xffffffffu, v);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
-      __syncthreads();
-      if (lane == __ffs(peers) - 1) wc[warp][v] = __popc(peers);
-      __syncthreads();
-      prologue_warp_prefix(wc, wp, wt, K, warp, lane);
-      __syncthreads();
-      if (r < B) {
-        const int slot = (int)bchk(base[v] + wp[warp][v] + rank, B, a.dev_status);
-        a.perm[slot] = r;
-        a.iperm[r] = slot;
-      }
-      __syncthreads();
-      if (tid >= 1 && tid <= K) base[tid] += wt[tid];
-      __syncthreads();
+  // stable scatter, 1024 requests per round: rank among equal lengths by warp match, then the
+  // prefix of the warps' counts
+  for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
+    const int r = c0 + tid;
+    const int v = r < B ? a.K_r[r] : 0;
+    const uint32_t peers = __match_any_sync(0xffffffffu, v);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    for (int e = tid; e < (kPrologueThreads / 32) * (kMaxK + 2); e += kPrologueThreads) (&wc[0][0])[e] = 0;
+    __syncthreads();
+    if (lane == __ffs(peers) - 1) wc[warp][v] = __popc(peers);
+    __syncthreads();
+    prologue_warp_prefix(wc, wp, wt, K, warp, lane);
+    __syncthreads();
+    if (r < B) {
+      const int slot = (int)bchk(base[v] + wp[warp][v] + rank, B, a.dev_status);
+      a.perm[slot] = r;
+      a.iperm[r] = slot;
     }
-    return;
+    __syncthreads();
+    if (tid >= 1 && tid <= K) base[tid] += wt[tid];
+    __syncthreads();
   }
-  // act[k - 1]: the requests with K_r >= k as groups of 32 of one kind (T > 0 or greedy), each
-  // group 32 consecutive such requests in request order, the full groups in the order they
-  // complete (their last member's index), then the partial group of each kind.  Every warp of
-  // a tile then runs one kind of draw (but at most one per position), and a tile's rows lie
-  // about as close together in U as the active set allows: listing all T > 0 requests before
-  // all greedy ones spread a greedy tile's rows over ~430 requests at 30 % greedy and made the
-  // draft 7 % slower than with the greedy requests in one run.
-  //
-  // A full group of kind c, number g, whose last member has o requests of the other kind
-  // before it, is the (g + floor(o / 32))-th full group in that order (o / 32 full groups of
-  // the other kind completed earlier).  Phase 0 records floor(o / 32) per group (a.grp);
-  // phase 1 writes the lists.
-  const int G32 = (B + 31) / 32;
-  for (int phase = 0; phase < 2; ++phase) {
-    if (tid < kMaxK + 2) {
-      carry[tid] = 0;
-      carry_g[tid] = 0;
+}
+
+// Exclusive prefix over the 32 warps of one count per warp (one warp scans), and the sum.
+__device__ __forceinline__ void block_warp_prefix(const int *cnt, int *pre, int *tot, int lane) {
+  const int c = cnt[lane];
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  pre[lane] = incl - c;
+  if (lane == 31) *tot = incl;
+}
+
+// The tensor-core path's prologue: one CTA per draft position k, since the positions' lists do
+// not depend on one another.  CTA k - 1 validates and resets the requests [B (k-1) / K,
+// B k / K) and builds act[k - 1]: the requests with K_r >= k as groups of 32 of one kind (T > 0
+// or greedy), each group 32 consecutive such requests in request order, the full groups in
+// the order they complete (their last member's index), then the partial group of each kind.
+// Every warp of a tile then runs one kind of draw (but at most one per position), and a
+// tile's rows lie about as close together in U as the active set allows: listing all T > 0
+// requests before all greedy ones spread a greedy tile's rows over ~430 requests at 30 %
+// greedy and made the draft 7 % slower than with the greedy requests in one run.
+//
+// A full group of kind c, number g, whose last member has o requests of the other kind before
+// it, is the (g + floor(o / 32))-th full group in that order (o / 32 full groups of the other
+// kind completed earlier).  Phase 0 records floor(o / 32) per group (a.grp); phase 1 writes the
+// list.  (One CTA building every position's list took 29 us at B = 2048.)
+__global__ void __launch_bounds__(kPrologueThreads) draft_prologue_tc(const __grid_constant__ DraftArgs a) {
+  __shared__ int wc[2][kPrologueThreads / 32], wp[2][kPrologueThreads / 32], wt[2];
+  __shared__ int carry[2], n_kind[2];
+  if (read_status(a.dev_status)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = (int)a.B, K = (int)a.K_max, k = (int)blockIdx.x + 1;
+  if (blockIdx.x == 0) {
+    if (tid <= K) a.gbar[tid] = 0;
+    if (tid == 0) {
+      a.nact[0] = B;
+      a.nact[K + 1] = 0;
     }
+  }
+  {
+    const int r0 = (int)((int64_t)B * blockIdx.x / K), r1 = (int)((int64_t)B * (blockIdx.x + 1) / K);
+    for (int r = r0 + tid; r < r1; r += kPrologueThreads) {
+      const int err = prologue_request(a, r);
+      if (err) set_status(a.dev_status, err);
+    }
+  }
+  const int G32 = (B + 31) / 32;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int phase = 0; phase < 2; ++phase) {
+    if (tid < 2) carry[tid] = 0;
     __syncthreads();
     for (int c0 = 0; c0 < B; c0 += kPrologueThreads) {
       const int r = c0 + tid;
-      const int kr = r < B ? a.K_r[r] : 0;
-      const bool greedy = r < B && a.temperature[r] == 0.0f;
-      const int vs = greedy ? 0 : kr, vg = greedy ? kr : 0;
-      for (int k = 1; k <= K; ++k) {
-        const uint32_t bs = __ballot_sync(0xffffffffu, vs >= k), bg = __ballot_sync(0xffffffffu, vg >= k);
-        if (lane == 0) {
-          wc[warp][k] = __popc(bs);
-          wc_g[warp][k] = __popc(bg);
-        }
+      const bool active = r < B && a.K_r[r] >= k;
+      const int kind = (r < B && a.temperature[r] == 0.0f) ? 1 : 0;   // 1: greedy
+      const uint32_t b0 = __ballot_sync(0xffffffffu, active && kind == 0);
+      const uint32_t b1 = __ballot_sync(0xffffffffu, active && kind == 1);
+      if (lane == 0) {
+        wc[0][warp] = __popc(b0);
+        wc[1][warp] = __popc(b1);
       }
       __syncthreads();
-      prologue_warp_prefix(wc, wp, wt, K, warp, lane);
-      prologue_warp_prefix(wc_g, wp_g, wt_g, K, warp, lane);
+      if (warp < 2) block_warp_prefix(wc[warp], wp[warp], &wt[warp], lane);
       __syncthreads();
-      const uint32_t lt = (1u << lane) - 1u;
-      for (int k = 1; k <= K; ++k) {        // every lane runs every k: the ballots are warp-wide
-        const uint32_t bs = __ballot_sync(0xffffffffu, vs >= k), bg = __ballot_sync(0xffffffffu, vg >= k);
-        if (kr < k) continue;
-        const int before_s = carry[k] + wp[warp][k] + __popc(bs & lt);      // T > 0 actives before r
-        const int before_g = carry_g[k] + wp_g[warp][k] + __popc(bg & lt);  // greedy actives before r
-        const int rank = greedy ? before_g : before_s, other = greedy ? before_s : before_g;
+      if (active) {
+        const int before0 = carry[0] + wp[0][warp] + __popc(b0 & lt);   // T > 0 actives before r
+        const int before1 = carry[1] + wp[1][warp] + __popc(b1 & lt);   // greedy actives before r
+        const int rank = kind ? before1 : before0, other = kind ? before0 : before1;
         const int g = rank >> 5, l = rank & 31;
-        int *grp = a.grp + ((int64_t)(k - 1) * 2 + (greedy ? 1 : 0)) * G32;
+        int *grp = a.grp + ((int64_t)(k - 1) * 2 + kind) * G32;
         if (phase == 0) {
           if (l == 31) grp[bchk(g, G32, a.dev_status)] = other >> 5;
         } else {
-          const int ns = n_s[k], ng = n_g[k];
+          const int ns = n_kind[0], ng = n_kind[1];
           const int full = (ns >> 5) + (ng >> 5);
-          const int pos = (g < ((greedy ? ng : ns) >> 5)) ? 32 * (g + grp[bchk(g, G32, a.dev_status)]) + l
-                                                          : 32 * full + (greedy ? (ns & 31) : 0) + l;
+          const int pos = (g < ((kind ? ng : ns) >> 5)) ? 32 * (g + grp[bchk(g, G32, a.dev_status)]) + l
+                                                        : 32 * full + (kind ? (ns & 31) : 0) + l;
           a.act[(int64_t)(k - 1) * B + bchk(pos, B, a.dev_status)] = r;
         }
       }
       __syncthreads();
-      if (tid >= 1 && tid <= K) {
-        carry[tid] += wt[tid];
-        carry_g[tid] += wt_g[tid];
-      }
+      if (tid < 2) carry[tid] += wt[tid];
       __syncthreads();
     }
     if (phase == 0) {
-      if (tid >= 1 && tid <= K) {
-        n_s[tid] = carry[tid];
-        n_g[tid] = carry_g[tid];
-      }
+      if (tid < 2) n_kind[tid] = carry[tid];
       __syncthreads();
     }
   }
+  if (tid == 0) a.nact[k] = n_kind[0] + n_kind[1];
 }
 
 template <int DT>
@@ -659,7 +681,8 @@ __global__ void __launch_bounds__(kSimtThreads, 3) draft_simt_tile(const __grid_
 }  // namespace
 
 cudaError_t launch_draft_prologue(const DraftArgs &a, cudaStream_t s, bool tensor_core) {
-  draft_prologue<<<1, kPrologueThreads, 0, s>>>(a, tensor_core ? 2 : 1);
+  if (tensor_core) draft_prologue_tc<<<(unsigned)a.K_max, kPrologueThreads, 0, s>>>(a);
+  else draft_prologue<<<1, kPrologueThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

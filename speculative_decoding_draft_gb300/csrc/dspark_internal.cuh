@@ -823,6 +823,7 @@ struct VerifyArgs {
   int32_t *nrows;       // [1] how many
   int32_t *row_start;   // [kMaxK + 3] first list slot of position j's rows
   int32_t *row_fill;    // [kMaxK + 3] position j's rows listed so far
+  int32_t *scan_next;   // [1] the next listed row a scan CTA takes
   int32_t *dead;        // [B] first rejecting position (kNoReject: none)
   VRowRes *rres;        // [B * (kMaxK + 1)] request-major: r (K_max + 1) + j - 1
   int row_slices;       // vocabulary slices per row of the statistics pass

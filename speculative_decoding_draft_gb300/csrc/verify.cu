@@ -405,6 +405,14 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_count(const __grid_c
       st += cnt[j];
     }
     *a.nrows = st;
+    *a.scan_next = 0;
+    a.jobs_nact[0] = B;    // the residual jobs' counts (verify_jobs fills [1])
+    a.jobs_nact[1] = 0;
+    a.jobs_nact[2] = 0;
+    if (a.jobs_gbar) {
+      a.jobs_gbar[0] = 0;
+      a.jobs_gbar[1] = 0;
+    }
   }
 }
 
@@ -558,8 +566,11 @@ __device__ __forceinline__ void named_sync_scan() {
   asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory");
 }
 
-// Persistent CTAs take whole listed rows, ri = blockIdx.x + t * gridDim.x (position-major,
-// so every request's position j comes before any position j + 1), and stream each row's
+// Persistent CTAs take whole listed rows in list order (position-major, so every request's
+// position j is taken before any position j + 1): CTA c first row c, then the next untaken
+// row from a shared counter, so a CTA whose row was cheap (skipped, or statistics only) takes
+// the next one sooner than one drawing a bonus row (19 % off the call at B = 2048; the first
+// row by CTA index keeps the rows of a small batch on different SMs).  Each CTA streams each row's
 // vocabulary slices in order.  BULK (bf16, 16-byte aligned rows): warp kScanWarps stages each
 // slice by bulk copy into a kScanStages ring; otherwise the reducing warps load the slice
 // themselves (VEC: 16-byte loads) and the staging warp only hands out the slices.  A row
@@ -579,7 +590,6 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
   if (read_status(a.dev_status)) return;
   const int S = a.row_slices, V = (int)a.V;
   const int nrows = *(volatile const int32_t *)a.nrows;
-  const int G = gridDim.x;
   if ((int)blockIdx.x >= nrows) return;
   const bool two = (a.D_lse == nullptr);
   const uint32_t stage_bytes = BULK ? (two ? 2u : 1u) * kSliceBytes : 0u;
@@ -634,7 +644,7 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
         return true;
       };
       bool ok = true;
-      for (int ri = blockIdx.x; ok && ri < nrows; ri += G) {
+      for (int ri = blockIdx.x; ok && ri < nrows; ri = (int)gridDim.x + atomicAdd(a.scan_next, 1)) {
         ScanMeta m;
         m.ri = ri;
         m.w = a.rows[ri];
@@ -941,73 +951,54 @@ __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_
 }
 
 // Every request's outcome from the scan, and the T > 0 rejections as the jobs of the residual
-// draw (one CTA; the order of the list is the atomics' and changes no result).  n = (first
-// rejection) - 1, or ell_r when every position was accepted; the accepted tokens, the -1
-// padding and at slot n the greedy correction (the rejecting row's argmax) or the bonus token
-// (the scan's draw, or its argmax for T = 0) are written here; a T > 0 rejection's token is
-// the residual draw's.  With the recompute entry point the residual pass's keys and flags
-// start from zero.
-__global__ void __launch_bounds__(kPlanThreads) verify_jobs(const __grid_constant__ VerifyArgs a) {
-  __shared__ int count;
+// draw (a thread per request; job slots from one global atomic per warp, so the order of the
+// list is the atomics' and changes no result).  n = (first rejection) - 1, or ell_r when every
+// position was accepted; the accepted tokens, the -1 padding and at slot n the greedy
+// correction (the rejecting row's argmax) or the bonus token (the scan's draw, or its argmax
+// for T = 0) are written here; a T > 0 rejection's token is the residual draw's.  With the
+// recompute entry point the residual pass's keys and flags start from zero.
+constexpr int kJobThreads = 256;
+__global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant__ VerifyArgs a) {
   if (read_status(a.dev_status)) return;
-  const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x;
-  if (tid == 0) count = 0;
-  __syncthreads();
-  const int lane = tid & 31;
-  for (int r0 = 0; r0 < B; r0 += kPlanThreads) {   // every thread runs every round: warp-wide ballot
-    const int r = r0 + tid;
-    bool job = false;
-    int n = 0;
-    float T = 1.0f;
-    if (r < B) {
-      if (a.key_out) {
-        a.key_out[r] = 0ull;
-        a.any_out[r] = 0;
-      }
-      const int l = a.ell[r];
-      const int dead = a.dead[r];
-      n = dead <= l ? dead - 1 : l;
-      T = a.temperature[r];
-      const bool greedy = (T == 0.0f);
-      const int64_t rb = (int64_t)r * (K + 1);
-      for (int i = 0; i <= K; ++i) {
-        int v = -1;
-        if (i < n) v = a.draft_tok[(int64_t)r * K + i];
-        else if (i == n) v = n < l ? (greedy ? a.rres[rb + n].amax : -1) : a.rres[rb + l].amax;
-        a.out_tok[rb + i] = v;
-      }
-      a.n_acc[r] = n;
-      job = n < l && !greedy;
+  const int K = (int)a.K_max, B = (int)a.B, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kJobThreads + threadIdx.x;
+  bool job = false;
+  int n = 0;
+  float T = 1.0f;
+  if (r < B) {
+    if (a.key_out) {
+      a.key_out[r] = 0ull;
+      a.any_out[r] = 0;
     }
-    const uint32_t bal = __ballot_sync(0xffffffffu, job);
-    if (bal == 0u) continue;
-    const int leader = __ffs(bal) - 1;
-    int slot = 0;
-    if (lane == leader) slot = atomicAdd(&count, __popc(bal));
-    slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(bal & ((1u << lane) - 1u));
-    if (!job) continue;
-    VJob jb;
-    jb.r = r;
-    jb.j = n + 1;
-    jb.prev = a.anchor ? ((n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1]) : 0;
-    jb.urow = r * K + n;
-    jb.trow = a.tgt_off[r] + n;
-    const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
-    jb.lse_t = rr.lse_t;
-    jb.lse_q = a.D_lse ? a.D_lse[(int64_t)r * K + n] : rr.lse_q;
-    jb.invT = 1.0f / T;
-    a.jobs[bchk(slot, B, a.dev_status)] = jb;
+    const int l = a.ell[r];
+    const int dead = a.dead[r];
+    n = dead <= l ? dead - 1 : l;
+    T = a.temperature[r];
+    const bool greedy = (T == 0.0f);
+    const int64_t rb = (int64_t)r * (K + 1);
+    const int last = n < l ? (greedy ? a.rres[rb + n].amax : -1) : a.rres[rb + l].amax;
+    for (int i = 0; i <= K; ++i) a.out_tok[rb + i] = i < n ? a.draft_tok[(int64_t)r * K + i] : (i == n ? last : -1);
+    a.n_acc[r] = n;
+    job = n < l && !greedy;
   }
-  __syncthreads();
-  if (tid == 0) {
-    a.jobs_nact[0] = B;
-    a.jobs_nact[1] = count;
-    a.jobs_nact[2] = 0;
-    if (a.jobs_gbar) {
-      a.jobs_gbar[0] = 0;
-      a.jobs_gbar[1] = 0;
-    }
-  }
+  const uint32_t bal = __ballot_sync(0xffffffffu, job);
+  if (bal == 0u) return;
+  const int leader = __ffs(bal) - 1;
+  int slot = 0;
+  if (lane == leader) slot = atomicAdd(&a.jobs_nact[1], __popc(bal));
+  slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(bal & ((1u << lane) - 1u));
+  if (!job) return;
+  VJob jb;
+  jb.r = r;
+  jb.j = n + 1;
+  jb.prev = a.anchor ? ((n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1]) : 0;
+  jb.urow = r * K + n;
+  jb.trow = a.tgt_off[r] + n;
+  const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
+  jb.lse_t = rr.lse_t;
+  jb.lse_q = a.D_lse ? a.D_lse[(int64_t)r * K + n] : rr.lse_q;
+  jb.invT = 1.0f / T;
+  a.jobs[bchk(slot, B, a.dev_status)] = jb;
 }
 
 template <int DT, bool VEC, bool BULK>
@@ -1041,7 +1032,7 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
   verify_scan<DT, VEC, BULK><<<(unsigned)grid, kScanThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  verify_jobs<<<1, kPlanThreads, 0, s>>>(a);
+  verify_jobs<<<(unsigned)((a.B + kJobThreads - 1) / kJobThreads), kJobThreads, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (resid) {
@@ -1087,7 +1078,8 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   a.nrows = (int32_t *)p;          // one 256-byte block: the count, the starts, the fill counters
   a.row_start = a.nrows + 4;
   a.row_fill = a.nrows + 32;
-  static_assert(32 + kMaxK + 3 <= 64, "plan counters fit one 256-byte block");
+  a.scan_next = a.nrows + 60;
+  static_assert(32 + kMaxK + 3 <= 60, "plan counters fit one 256-byte block");
   p += al(sizeof(int32_t));
   a.dead = (int32_t *)p;
   p += al(sizeof(int32_t) * (size_t)a.B);
