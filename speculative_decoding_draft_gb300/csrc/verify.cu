@@ -709,21 +709,30 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
       const int lo = min(V, m.sl * kRowSlice), hi = min(V, lo + kRowSlice);
       const float a2 = m.w.invT * kLog2e;
       const uint32_t pos = (uint32_t)m.w.j, rq = (uint32_t)m.w.r;
-      // each block's noise word is computed one block ahead, so that its Philox chain runs
-      // beside the previous block's arithmetic
-      auto noise = [&](int v) -> uint32_t {
-        const uint32_t g = (uint32_t)v >> 5;
-        return v < hi ? word_of(philox(a.key, g >> 2, pos, rq, kTagResid), (int)(g & 3u)) : 0u;
-      };
-      uint32_t wb_next = noise(lo + 32 * tid);
+      // noise words: block b = tid + q * kRowThreads of the slice is block (lo / 32 + b) of the
+      // row, in Philox group lo / 128 + tid / 4 + q * kRowThreads / 4 as word tid & 3.  The four
+      // lanes of a quad share their groups, so lane 4i + c makes the one Philox call of
+      // iteration c for its quad and the quad's lanes take their words from it by shuffles
+      // (all lanes, before any of them leaves the loop at the row's end)
+      static_assert(kRowSlice % 128 == 0 && kRowSlice / 32 / kRowThreads <= 3, "noise groups of a slice");
+      const int cw = lane & 3;
+      const uint4 pw = philox(a.key, ((uint32_t)lo >> 7) + (uint32_t)(tid >> 2) + (uint32_t)(cw * (kRowThreads / 4)),
+                              pos, rq, kTagResid);
+      uint32_t wq[3];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int src = (lane & ~3) | q;
+        const uint32_t x = __shfl_sync(0xffffffffu, pw.x, src), y = __shfl_sync(0xffffffffu, pw.y, src);
+        const uint32_t z = __shfl_sync(0xffffffffu, pw.z, src), w = __shfl_sync(0xffffffffu, pw.w, src);
+        wq[q] = cw == 0 ? x : (cw == 1 ? y : (cw == 2 ? z : w));
+      }
 #pragma unroll 1
       for (int q = 0; q < kRowSlice / 32 / kRowThreads; ++q) {
         const int b = tid + q * kRowThreads;
         const int v0 = lo + 32 * b;
         if (v0 >= hi) break;
         const uint32_t g = (uint32_t)v0 >> 5;
-        const uint32_t wb = wb_next;
-        wb_next = noise(v0 + 32 * kRowThreads);
+        const uint32_t wb = q == 0 ? wq[0] : (q == 1 ? wq[1] : wq[2]);
         auto pick = [&] { return word_of(philox(a.key, g >> 2, pos, rq, kTagResidPick), (int)(g & 3u)); };
         if (BULK) {
           const uint32_t base = smem_u32(ring) + (uint32_t)s * stage_bytes + 64u * (uint32_t)b;
