@@ -124,6 +124,15 @@ __device__ __forceinline__ int read_status(const int32_t *st) {
   return *(volatile const int32_t *)st;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialisation
+// may become resident while the kernel before it in the stream is still running: it calls
+// grid_dep_wait() before its first global memory access, which returns once that kernel has
+// completed and its writes are visible.  grid_dep_launch() lets the next such kernel become
+// resident early (it changes nothing about what that kernel may read).  Both are no-ops
+// when the kernel was launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool temperature_ok(float t) {
   return (t == 0.0f) || (t >= kMinPositiveT && t <= 3.0e38f);
 }

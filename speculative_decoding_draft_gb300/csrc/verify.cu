@@ -377,6 +377,7 @@ constexpr int kPlanThreads = 1024;
 // set and every later kernel returns at once.
 __global__ void __launch_bounds__(kPlanThreads) verify_plan_count(const __grid_constant__ VerifyArgs a) {
   __shared__ int cnt[kMaxK + 3];
+  grid_dep_launch();
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x, lane = tid & 31;
   if (tid < kMaxK + 3) cnt[tid] = 0;
@@ -424,6 +425,8 @@ constexpr int kFillThreads = 256;
 // same j share one atomic).
 template <int DT>
 __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_constant__ VerifyArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kFillThreads + threadIdx.x;
@@ -587,6 +590,8 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
   __shared__ Race s_race[2][kScanWarps];        // [row parity][warp]: bonus draws
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(a.dev_status)) return;
   const int S = a.row_slices, V = (int)a.V;
   const int nrows = *(volatile const int32_t *)a.nrows;
@@ -873,6 +878,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_
   __shared__ int s_any[kSampleThreads / 32];
   __shared__ int s_last, s_tok;
   const int cx = blockIdx.x, tid = threadIdx.x;
+  grid_dep_wait();
   if (read_status(a.dev_status)) return;
   const int V = (int)a.V, K = (int)a.K_max;
   const int njobs = *(volatile const int32_t *)(a.jobs_nact + 1);
@@ -968,6 +974,8 @@ __global__ void __launch_bounds__(kSampleThreads, 2) verify_sample(const __grid_
 // recompute entry point the residual pass's keys and flags start from zero.
 constexpr int kJobThreads = 256;
 __global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant__ VerifyArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kJobThreads + threadIdx.x;
@@ -1010,6 +1018,24 @@ __global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant
   a.jobs[bchk(slot, B, a.dev_status)] = jb;
 }
 
+// Launch with programmatic stream serialisation: the kernel may become resident while the
+// previous kernel in the stream runs, and waits for it in grid_dep_wait().
+template <class... P>
+cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             const VerifyArgs &a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <int DT, bool VEC, bool BULK>
 cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftArgs *resid) {
   // sampling chunks: about two CTAs per SM over all requests in one wave, each chunk a
@@ -1024,8 +1050,8 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
   verify_plan_count<<<1, kPlanThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  verify_plan_fill<DT><<<(unsigned)((a.B * (a.K_max + 1) + kFillThreads - 1) / kFillThreads), kFillThreads, 0, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(verify_plan_fill<DT>, dim3((unsigned)((a.B * (a.K_max + 1) + kFillThreads - 1) / kFillThreads)),
+                       dim3(kFillThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   // scan: a wave of persistent CTAs (4 per SM with single-row stages, 2 with two rows; two
   // stages at four CTAs per SM ran 4 % faster than three stages at three)
@@ -1038,18 +1064,16 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
   const int64_t max_rows = a.B * (a.K_max + 1);
   const int64_t per_sm = (BULK && two) ? 2 : 4;
   const int64_t grid = max_rows < per_sm * num_sms ? max_rows : per_sm * num_sms;
-  verify_scan<DT, VEC, BULK><<<(unsigned)grid, kScanThreads, smem, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(verify_scan<DT, VEC, BULK>, dim3((unsigned)grid), dim3(kScanThreads), (size_t)smem, s, a);
   if (e != cudaSuccess) return e;
-  verify_jobs<<<(unsigned)((a.B + kJobThreads - 1) / kJobThreads), kJobThreads, 0, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(verify_jobs, dim3((unsigned)((a.B + kJobThreads - 1) / kJobThreads)), dim3(kJobThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   if (resid) {
     e = launch_resid_tc(*resid, s, num_sms);
     if (e != cudaSuccess) return e;
   }
-  verify_sample<DT, VEC><<<dim3(a.chunks, (unsigned)(a.B < 65535 ? a.B : 65535)), kSampleThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(verify_sample<DT, VEC>, dim3(a.chunks, (unsigned)(a.B < 65535 ? a.B : 65535)),
+                          dim3(kSampleThreads), 0, s, a);
 }
 
 }  // namespace
