@@ -796,7 +796,8 @@ constexpr int kNoReject = 127;   // dead[r] of a request with no rejected positi
 // One verified drafted row (request r, position j <= ell_r) of the statistics pass; the plan
 // kernel lists them position-major (every request's position 1, then position 2, ...).
 struct VRow {
-  int r, j, x;     // request, position, draft token x_j
+  int r, j, x;     // request, position, draft token x_j; for a bonus draw (kind 4) the part:
+                   // (parts << 8) | part, the part covering slices [part S / parts, (part + 1) S / parts)
   int trow;        // row of the flattened target logits: tgt_off[r] + j - 1
   float invT;      // 1 / T (1 for greedy)
   float lqx;       // log q_j(x_j), T > 0 with a known draft normaliser
@@ -829,11 +830,13 @@ struct VerifyArgs {
   PhiloxKey key;
   // workspace
   VRow *rows;           // [B * (kMaxK + 1)] the verified rows and bonus rows, position-major
-  int32_t *nrows;       // [1] how many
+  int32_t *nrows;       // [2] how many; [1]: parts per bonus draw row
   int32_t *row_start;   // [kMaxK + 3] first list slot of position j's rows
   int32_t *row_fill;    // [kMaxK + 3] position j's rows listed so far
   int32_t *scan_next;   // [1] the next listed row a scan CTA takes
   int32_t *dead;        // [B] first rejecting position (kNoReject: none)
+  unsigned long long *bonus_key;   // [B] packed (score, index) maximum of the bonus draw's parts
+  int scan_cap;         // scan CTAs resident at once (the bonus draws are split only within one wave)
   VRowRes *rres;        // [B * (kMaxK + 1)] request-major: r (K_max + 1) + j - 1
   int row_slices;       // vocabulary slices per row of the statistics pass
   int32_t *counters;   // [B] chunk arrivals of the sampling pass (reset by the plan kernel)

@@ -16,11 +16,13 @@
 //     staging a row the staging warp reads that word and skips rows past a known
 //     rejection, so the rows read are the ones up to each request's deciding row, except
 //     where a decision is not known yet.
-//  3. verify_jobs (one CTA): per request the outcome -- n_acc = (first rejection) - 1 or
+//  3. verify_jobs (a thread per request): the outcome -- n_acc = (first rejection) - 1 or
 //     ell_r, the accepted tokens, then the correction or bonus: the argmax of the rejecting row
 //     for T = 0 and the bonus token are the scan's (the bonus row is listed at position
-//     ell_r + 1, and the scan draws it -- the two-level draw over z / T -- or takes its argmax
-//     for T = 0, skipping it once a rejection is known) -- and the list of T > 0 rejections.
+//     ell_r + 1, and the scan draws it -- the two-level draw over z / T, at small batches in
+//     up to four parts over slice ranges that merge in a packed (score, index) maximum -- or
+//     takes its argmax for T = 0, skipping it once a rejection is known) -- and the list of
+//     T > 0 rejections.
 //     verify_sample then draws each rejection's residual norm(max(0, p - q)), spread over
 //     (rejection x vocabulary chunk) CTAs with the last chunk merging, or takes the
 //     tensor-core recompute pass's draw.
@@ -368,7 +370,10 @@ constexpr int kPlanThreads = 1024;
 
 // Two kernels.  verify_plan_count (one CTA) resets each request's state, counts the rows of
 // every position (ell_r + 1 rows of a request whose length is in range; the fill pass checks
-// everything else and reports it) and sets each position's first slot.  verify_plan_fill (a
+// everything else and reports it) and sets each position's first slot.  When the rows and the
+// T > 0 bonus draws fit one wave of scan CTAs with room to spare, each bonus draw is listed as
+// up to four parts over ranges of its slices (the draw is a maximum over blocks, so the parts
+// merge exactly), which keeps a bonus draw from being the one long row of a small batch.  verify_plan_fill (a
 // thread per request and position) validates the request and lists its rows j = 1..ell_r and
 // its bonus row j = ell_r + 1 at row_start[j] + (a slot taken per warp and position from
 // row_fill[j]).
@@ -376,20 +381,25 @@ constexpr int kPlanThreads = 1024;
 // (each row is processed by one CTA on its own).  With an invalid request the status word is
 // set and every later kernel returns at once.
 __global__ void __launch_bounds__(kPlanThreads) verify_plan_count(const __grid_constant__ VerifyArgs a) {
-  __shared__ int cnt[kMaxK + 3];
+  __shared__ int cnt[kMaxK + 3], cntb[kMaxK + 3];   // rows, T > 0 bonus draws per position
   grid_dep_launch();
   if (read_status(a.dev_status)) return;
   const int K = (int)a.K_max, B = (int)a.B, tid = threadIdx.x, lane = tid & 31;
-  if (tid < kMaxK + 3) cnt[tid] = 0;
+  if (tid < kMaxK + 3) {
+    cnt[tid] = 0;
+    cntb[tid] = 0;
+  }
   __syncthreads();
   for (int r0 = 0; r0 < B; r0 += kPlanThreads) {   // every thread runs every round: warp-wide ballots
     const int r = r0 + tid;
     int nr = 0;                                    // rows of request r
     if (r < B) {
       a.dead[r] = kNoReject;
+      a.bonus_key[r] = 0ull;
       a.counters[r] = 0;
       const int l = a.ell[r];
       nr = (l >= 0 && l <= K) ? l + 1 : 0;
+      if (nr > 0 && a.temperature[r] != 0.0f) atomicAdd(&cntb[l + 1], 1);
     }
     for (int j = 1; j <= K + 1; ++j) {
       const uint32_t bal = __ballot_sync(0xffffffffu, j <= nr);
@@ -399,13 +409,28 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_count(const __grid_c
   }
   __syncthreads();
   if (tid == 0) {
+    int tot = 0, nbt = 0;
+    for (int j = 1; j <= K + 1; ++j) {
+      tot += cnt[j];
+      nbt += cntb[j];
+    }
+    // parts per bonus draw: all listed rows in one wave of the scan, at most one part per
+    // slice, and within the list's capacity B (kMaxK + 1)
+    int P = 1;
+    if (nbt > 0 && tot + nbt <= a.scan_cap) {
+      P = min(4, 1 + (a.scan_cap - tot) / nbt);
+      P = min(P, a.row_slices);
+      P = min(P, 1 + (int)(((int64_t)B * (kMaxK + 1) - tot) / nbt));
+      P = max(P, 1);
+    }
     int st = 0;
     for (int j = 1; j <= K + 1; ++j) {
       a.row_start[j] = st;
       a.row_fill[j] = 0;
-      st += cnt[j];
+      st += cnt[j] + (P - 1) * cntb[j];
     }
-    *a.nrows = st;
+    a.nrows[0] = st;
+    a.nrows[1] = P;
     *a.scan_next = 0;
     a.jobs_nact[0] = B;    // the residual jobs' counts (verify_jobs fills [1])
     a.jobs_nact[1] = 0;
@@ -469,7 +494,7 @@ __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_co
         }
       } else {
         // the bonus row: drawn (or its argmax taken) by the scan, used when every position is
-        // accepted
+        // accepted; a draw is listed as nrows[1] parts (x: parts and part, below)
         w.drow = 0;
         w.x = -1;
         w.trow = off + l;
@@ -477,14 +502,20 @@ __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_co
       }
     }
   }
+  // list slots of this thread's row: the parts of a bonus draw, else one; lanes with the same
+  // position and the same count share one atomic
+  const int np = (row && w.kind == 4) ? a.nrows[1] : 1;
   const uint32_t bal = __ballot_sync(0xffffffffu, row);
-  const uint32_t peers = __match_any_sync(0xffffffffu, row ? j : 0) & bal;
+  const uint32_t peers = __match_any_sync(0xffffffffu, row ? 2 * j + (np > 1 ? 1 : 0) : 0) & bal;
   if (!row) return;
   const int leader = __ffs(peers) - 1;
   int slot = 0;
-  if (lane == leader) slot = atomicAdd(&a.row_fill[j], __popc(peers));
-  slot = __shfl_sync(peers, slot, leader) + __popc(peers & ((1u << lane) - 1u));
-  a.rows[bchk(a.row_start[j] + slot, (int64_t)B * (K + 1), a.dev_status)] = w;
+  if (lane == leader) slot = atomicAdd(&a.row_fill[j], np * __popc(peers));
+  slot = __shfl_sync(peers, slot, leader) + np * __popc(peers & ((1u << lane) - 1u));
+  for (int p = 0; p < np; ++p) {
+    if (w.kind == 4) w.x = (np << 8) | p;
+    a.rows[bchk(a.row_start[j] + slot + p, (int64_t)B * (kMaxK + 1), a.dev_status)] = w;
+  }
 }
 
 // One block of the bonus draw (the two-level draw over z / T) from its 16 bf16 pair words in
@@ -659,8 +690,15 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
         m.w.trow = (int)bchk(m.w.trow, a.tgt_off[a.B], a.dev_status);
         m.w.drow = (int)bchk(m.w.drow, a.B * a.K_max, a.dev_status);
 #endif
+        // the row's slices (a part of a bonus draw: its range of them)
+        int sl0 = 0, sl1 = S;
+        if (m.w.kind == 4) {
+          const int parts = max(1, m.w.x >> 8), part = m.w.x & 255;
+          sl0 = part * S / parts;
+          sl1 = min(S, (part + 1) * S / parts);
+        }
         // rows past a rejection already found need no statistics
-        const bool skip = *(volatile const int32_t *)(a.dead + m.w.r) < m.w.j;
+        const bool skip = *(volatile const int32_t *)(a.dead + m.w.r) < m.w.j || sl0 >= sl1;
         if (skip) {
           m.sl = 0;
           m.kind = 0;
@@ -669,9 +707,9 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
           continue;
         }
         m.kind = m.w.kind;
-        for (int sl = 0; ok && sl < S; ++sl) {
+        for (int sl = sl0; ok && sl < sl1; ++sl) {
           m.sl = sl;
-          m.last = (sl == S - 1);
+          m.last = (sl == sl1 - 1);
           ok = slot(m);
         }
       }
@@ -815,7 +853,9 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the stage is read
     if (!m.last) continue;
     if (m.kind == 4) {
-      // the bonus draw of the row: warps reduce their races, warp 0 merges the four in order
+      // the bonus draw of the row (or of its part): warps reduce their races, warp 0 merges
+      // the four and folds the winner into the request's packed (score, index) key -- the
+      // maximum score, the smallest index on ties, whatever the order the parts arrive in
       Race rc = from_partial(to_partial(rb));
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) race_merge(rc, race_shfl_down(rc, d));
@@ -825,12 +865,7 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
         Race tot = s_race[par][0];
 #pragma unroll
         for (int q = 1; q < kScanWarps; ++q) race_merge(tot, s_race[par][q]);
-        VRowRes rr;
-        rr.lse_t = 0.0f;
-        rr.amax = tot.idx;
-        rr.zx_t = 0.0f;
-        rr.lse_q = 0.0f;
-        a.rres[(int64_t)m.w.r * (a.K_max + 1) + m.w.j - 1] = rr;
+        if (tot.idx >= 0) atomicMax(a.bonus_key + m.w.r, score_key(tot.best, tot.idx));
       }
     } else if (m.kind) {
       // the row is complete: warps reduce their shares, warp 0 merges the four in order
@@ -993,7 +1028,15 @@ __global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant
     T = a.temperature[r];
     const bool greedy = (T == 0.0f);
     const int64_t rb = (int64_t)r * (K + 1);
-    const int last = n < l ? (greedy ? a.rres[rb + n].amax : -1) : a.rres[rb + l].amax;
+    int last = -1;    // the token after the accepted ones: the correction, the bonus token
+    if (n < l) {
+      if (greedy) last = a.rres[rb + n].amax;
+    } else if (greedy) {
+      last = a.rres[rb + l].amax;
+    } else {
+      const unsigned long long bk = a.bonus_key[r];
+      last = bk ? key_index(bk) : -1;
+    }
     for (int i = 0; i <= K; ++i) a.out_tok[rb + i] = i < n ? a.draft_tok[(int64_t)r * K + i] : (i == n ? last : -1);
     a.n_acc[r] = n;
     job = n < l && !greedy;
@@ -1047,23 +1090,24 @@ cudaError_t launch_typed(VerifyArgs a, cudaStream_t s, int num_sms, const DraftA
     a.chunk_len = (int)((per + kBlockW - 1) / kBlockW * kBlockW);
     a.chunks = (int)((a.V + a.chunk_len - 1) / a.chunk_len);
   }
+  // scan: a wave of persistent CTAs (4 per SM with single-row stages, 2 with two rows; two
+  // stages at four CTAs per SM ran 4 % faster than three stages at three)
+  const bool two = (a.D_lse == nullptr);
+  const int64_t per_sm = (BULK && two) ? 2 : 4;
+  a.scan_cap = (int)(per_sm * num_sms);
   verify_plan_count<<<1, kPlanThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_dependent(verify_plan_fill<DT>, dim3((unsigned)((a.B * (a.K_max + 1) + kFillThreads - 1) / kFillThreads)),
                        dim3(kFillThreads), 0, s, a);
   if (e != cudaSuccess) return e;
-  // scan: a wave of persistent CTAs (4 per SM with single-row stages, 2 with two rows; two
-  // stages at four CTAs per SM ran 4 % faster than three stages at three)
-  const bool two = (a.D_lse == nullptr);
   const int smem = BULK ? kScanStages * kSliceBytes * (two ? 2 : 1) : 0;
   if (BULK) {
     e = ensure_dynamic_smem((const void *)verify_scan<DT, VEC, BULK>, smem);
     if (e != cudaSuccess) return e;
   }
-  const int64_t max_rows = a.B * (a.K_max + 1);
-  const int64_t per_sm = (BULK && two) ? 2 : 4;
-  const int64_t grid = max_rows < per_sm * num_sms ? max_rows : per_sm * num_sms;
+  const int64_t max_rows = a.B * (a.K_max + 1) + 3 * a.B;     // with bonus draws in four parts
+  const int64_t grid = max_rows < a.scan_cap ? max_rows : a.scan_cap;
   e = launch_dependent(verify_scan<DT, VEC, BULK>, dim3((unsigned)grid), dim3(kScanThreads), (size_t)smem, s, a);
   if (e != cudaSuccess) return e;
   e = launch_dependent(verify_jobs, dim3((unsigned)((a.B + kJobThreads - 1) / kJobThreads)), dim3(kJobThreads), 0, s, a);
@@ -1082,15 +1126,16 @@ int verify_row_slices(int64_t V) { return (int)((V + kRowSlice - 1) / kRowSlice)
 
 // Workspace layout (every part 256-byte aligned): sampling counters [B], sampling partials
 // [B * chunks], the listed rows [B * (kMaxK + 1)], their count, the first-rejection words [B],
-// the row results [B * (kMaxK + 1)].  Sized for kMaxK positions, so the size depends on B and
-// V only.
+// the bonus draws' keys [B], the row results [B * (kMaxK + 1)].  Sized for kMaxK positions, so
+// the size depends on B and V only.
 size_t verify_ws_bytes(int64_t B, int64_t V, int *chunks) {
   const int c = (int)((V + kSampleUnit - 1) / kSampleUnit);   // the most chunks a call uses
   if (chunks) *chunks = c;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)B * (size_t)(kMaxK + 1);
   return al(sizeof(int32_t) * (size_t)B) + al(sizeof(Partial) * (size_t)B * (size_t)c) + al(sizeof(VRow) * rows) +
-         al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) + al(sizeof(VRowRes) * rows) +
+         al(sizeof(int32_t)) + al(sizeof(int32_t) * (size_t)B) + al(sizeof(unsigned long long) * (size_t)B) +
+         al(sizeof(VRowRes) * rows) +
          al(sizeof(VJob) * (size_t)B) + al(sizeof(int32_t) * 3);
 }
 
@@ -1108,7 +1153,7 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   p += al(sizeof(Partial) * (size_t)a.B * (size_t)chunks);
   a.rows = (VRow *)p;
   p += al(sizeof(VRow) * rows);
-  a.nrows = (int32_t *)p;          // one 256-byte block: the count, the starts, the fill counters
+  a.nrows = (int32_t *)p;          // one 256-byte block: the count and the bonus parts, the starts, the fill counters
   a.row_start = a.nrows + 4;
   a.row_fill = a.nrows + 32;
   a.scan_next = a.nrows + 60;
@@ -1116,6 +1161,8 @@ void verify_carve(VerifyArgs &a, void *workspace) {
   p += al(sizeof(int32_t));
   a.dead = (int32_t *)p;
   p += al(sizeof(int32_t) * (size_t)a.B);
+  a.bonus_key = (unsigned long long *)p;
+  p += al(sizeof(unsigned long long) * (size_t)a.B);
   a.rres = (VRowRes *)p;
   p += al(sizeof(VRowRes) * rows);
   a.jobs = (VJob *)p;

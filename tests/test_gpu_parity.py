@@ -250,6 +250,31 @@ def test_verify_parity(case, with_lse):
     assert compare_verify(g, o) >= 0.9 * cfg.B
 
 
+@pytest.mark.parametrize("B,V", [(6, 40000), (5, 30000), (120, 64040)])
+def test_verify_bonus_draw_in_parts(B, V):
+    # the target rows of the verified positions are the draft's own rows, so every draft token
+    # is accepted and every request draws its bonus token; with few requests and several
+    # vocabulary slices per row the scan splits each bonus draw into parts over slice ranges
+    # (4, 3 and 2 parts here), whose winners merge in one packed maximum
+    cfg = wl.small_config("qwen", B=B, K_max=3, V=V)
+    inp = wl.draft_inputs(cfg, "cpu")
+    od = oracle_draft(inp, cfg.philox_seed)
+    ell = inp["K_r"].numpy().astype(np.int32)
+    tgt_dense = wl.target_dense(cfg, inp["U"], inp["K_r"])
+    D = torch.from_numpy(od["draft_logits"]).view(torch.bfloat16)
+    tgt_dense[:, : cfg.K_max] = D
+    flat, off = wl.flatten_targets(tgt_dense, torch.from_numpy(ell))
+    T = inp["temperature"].numpy()
+    lse = torch.from_numpy(oracle.row_lse(od["draft_logits"], np.repeat(T, cfg.K_max)).astype(np.float32)).to(DEV)
+    seed = 31
+    g = ds.verify_ragged(D.to(DEV), flat.to(DEV), off.to(DEV), torch.from_numpy(ell).to(DEV),
+                         torch.from_numpy(od["draft_tok"]).to(DEV), inp["temperature"].to(DEV), seed, draft_lse=lse)
+    assert ds.check(g["status"]) == "DSPARK_OK"
+    o = oracle.verify_ragged(host(D), host(flat), off.numpy(), ell, od["draft_tok"], T, seed)
+    assert (o["n_acc"] == ell).sum() >= B - 1        # (nearly) everything accepted
+    assert compare_verify(g, o) >= B - 1
+
+
 def test_verify_output_law_on_gpu():
     # two-token example: lossless output law (0.7, 0.3), acceptance 0.8
     N = 100000
