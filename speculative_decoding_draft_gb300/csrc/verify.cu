@@ -458,25 +458,33 @@ __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_co
   const int r = (int)(item / (K + 1)), j = (int)(item % (K + 1)) + 1;
   bool row = false;
   VRow w;
+  int rs = 0;
   if (r < B) {
+    // every value the row may need, loaded together before any of it is used (each index is
+    // in range whatever the lengths hold): one round trip to memory instead of a chain
     const int l = a.ell[r];
     const float T = a.temperature[r];
+    const int off = a.tgt_off[r];
+    const int drow = r * K + min(j, K) - 1;
+    const int x = a.draft_tok[drow];
+    const float zx_out = a.D_zx ? a.D_zx[drow] : 0.0f;
+    const float lse_q = a.D_lse ? a.D_lse[drow] : 0.0f;
+    rs = a.row_start[j];
     if (j == 1) {
-      const int err = request_error(K, r, l, T, a.tgt_off[r], a.tgt_off[r + 1], a.tgt_off[0]);
+      const int err = request_error(K, r, l, T, off, a.tgt_off[r + 1], a.tgt_off[0]);
       if (err) set_status(a.dev_status, err);
     }
     if (l >= 0 && l <= K && j <= l + 1) {
       const bool greedy = (T == 0.0f);
       const float invT = greedy ? 1.0f : 1.0f / T;
-      const int off = a.tgt_off[r];
       row = true;
       w.r = r;
       w.j = j;
       w.invT = invT;
       w.lqx = 0.0f;
       if (j <= l) {
-        w.drow = r * K + j - 1;
-        w.x = a.draft_tok[w.drow];
+        w.drow = drow;
+        w.x = x;
         w.trow = off + j - 1;
         if (w.x < 0 || w.x >= (int)a.V) {
           set_status(a.dev_status, DSPARK_ERR_TOKEN_RANGE);
@@ -486,8 +494,8 @@ __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_co
         } else if (a.D_lse != nullptr) {
           // log q(x_j) from the draft normaliser and the drawn token's logit (its own output,
           // or the stored row's element)
-          const float zx = a.D_zx ? a.D_zx[w.drow] : load1<DT>(a.D, (int64_t)w.drow * a.V + w.x);
-          w.lqx = zx * invT - a.D_lse[w.drow];
+          const float zx = a.D_zx ? zx_out : load1<DT>(a.D, (int64_t)w.drow * a.V + w.x);
+          w.lqx = zx * invT - lse_q;
           w.kind = 1;
         } else {
           w.kind = 3;
@@ -514,7 +522,7 @@ __global__ void __launch_bounds__(kFillThreads) verify_plan_fill(const __grid_co
   slot = __shfl_sync(peers, slot, leader) + np * __popc(peers & ((1u << lane) - 1u));
   for (int p = 0; p < np; ++p) {
     if (w.kind == 4) w.x = (np << 8) | p;
-    a.rows[bchk(a.row_start[j] + slot + p, (int64_t)B * (kMaxK + 1), a.dev_status)] = w;
+    a.rows[bchk(rs + slot + p, (int64_t)B * (kMaxK + 1), a.dev_status)] = w;
   }
 }
 
@@ -1015,31 +1023,50 @@ __global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant
   const int K = (int)a.K_max, B = (int)a.B, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kJobThreads + threadIdx.x;
   bool job = false;
-  int n = 0;
-  float T = 1.0f;
+  VJob jb;
   if (r < B) {
     if (a.key_out) {
       a.key_out[r] = 0ull;
       a.any_out[r] = 0;
     }
+    // the request's values, loaded together before any is used: its length, first rejection,
+    // temperature, bonus key, target offset, anchor and draft tokens (the loop is unrolled
+    // over kMaxK so that the tokens stay in registers)
     const int l = a.ell[r];
     const int dead = a.dead[r];
-    n = dead <= l ? dead - 1 : l;
-    T = a.temperature[r];
+    const float T = a.temperature[r];
+    const unsigned long long bk = a.bonus_key[r];
+    const int off = a.tgt_off[r];
+    const int anc = a.anchor ? a.anchor[r] : 0;
+    int tok[kMaxK];
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i) tok[i] = i < K ? a.draft_tok[(int64_t)r * K + i] : -1;
+    const int n = dead <= l ? dead - 1 : l;
     const bool greedy = (T == 0.0f);
     const int64_t rb = (int64_t)r * (K + 1);
+    // the deciding row's results (n <= l <= K_max: in range; for a T > 0 bonus not read)
+    const VRowRes rr = a.rres[rb + n];
+    const float lq = (a.D_lse && n < K) ? a.D_lse[(int64_t)r * K + n] : rr.lse_q;
     int last = -1;    // the token after the accepted ones: the correction, the bonus token
-    if (n < l) {
-      if (greedy) last = a.rres[rb + n].amax;
-    } else if (greedy) {
-      last = a.rres[rb + l].amax;
-    } else {
-      const unsigned long long bk = a.bonus_key[r];
-      last = bk ? key_index(bk) : -1;
-    }
-    for (int i = 0; i <= K; ++i) a.out_tok[rb + i] = i < n ? a.draft_tok[(int64_t)r * K + i] : (i == n ? last : -1);
+    if (greedy) last = rr.amax;                       // the rejecting row's or the bonus row's argmax
+    else if (n == l) last = bk ? key_index(bk) : -1;  // the bonus draw
+    int prev = anc;   // x_n, the token before position n + 1
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i)
+      if (i + 1 == n) prev = tok[i];
+#pragma unroll
+    for (int i = 0; i <= kMaxK; ++i)
+      if (i <= K) a.out_tok[rb + i] = i < n ? tok[i] : (i == n ? last : -1);
     a.n_acc[r] = n;
     job = n < l && !greedy;
+    jb.r = r;
+    jb.j = n + 1;
+    jb.prev = a.anchor ? prev : 0;
+    jb.urow = r * K + n;
+    jb.trow = off + n;
+    jb.lse_t = rr.lse_t;
+    jb.lse_q = lq;
+    jb.invT = 1.0f / T;
   }
   const uint32_t bal = __ballot_sync(0xffffffffu, job);
   if (bal == 0u) return;
@@ -1048,16 +1075,6 @@ __global__ void __launch_bounds__(kJobThreads) verify_jobs(const __grid_constant
   if (lane == leader) slot = atomicAdd(&a.jobs_nact[1], __popc(bal));
   slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(bal & ((1u << lane) - 1u));
   if (!job) return;
-  VJob jb;
-  jb.r = r;
-  jb.j = n + 1;
-  jb.prev = a.anchor ? ((n == 0) ? a.anchor[r] : a.draft_tok[(int64_t)r * K + n - 1]) : 0;
-  jb.urow = r * K + n;
-  jb.trow = a.tgt_off[r] + n;
-  const VRowRes rr = a.rres[(int64_t)r * (K + 1) + n];
-  jb.lse_t = rr.lse_t;
-  jb.lse_q = a.D_lse ? a.D_lse[(int64_t)r * K + n] : rr.lse_q;
-  jb.invT = 1.0f / T;
   a.jobs[bchk(slot, B, a.dev_status)] = jb;
 }
 
