@@ -47,20 +47,22 @@ constexpr int kAChunk = kTileM * 128;            // 16 KB: 128 rows x 64 rank va
 constexpr int kASize = 4 * kAChunk;              // rank <= 256
 constexpr int kPiece = kBlkN * 128;              // 8 KB: one packed block, 64 rank rows
 constexpr int kStageBytes = kMaxBlk * kPiece;    // 32 KB
-constexpr int kUDepth = 3;                       // U blocks each epilogue warp stages ahead
 constexpr int kUSlot = 32 * 64;                  // one 32-wide block of a warp's 32 rows (2 KB)
 constexpr int kOffA = 0;
 constexpr int kOffW = kOffA + kASize;
 
 // Per mode: epilogue warps (three per TMEM lane quadrant for the draft, which fits 128
-// registers a thread; two for the residual mode, which needs 168) and W2 stages (the draft's
-// extra U slots leave room for two; two stages measured as fast as three).
+// registers a thread; two for the residual mode, which needs 168), the U blocks each
+// epilogue warp stages ahead, and W2 stages: three in both (the draft's U ring of two blocks
+// per warp measured as fast as three and leaves room for the third stage, which took 2 % off
+// the draft at B = 64 and changed nothing at large batches).
 template <bool RESID>
 struct TcCfg {
   static constexpr int kEpiWarps = RESID ? 8 : 12;
   static constexpr int kWpq = kEpiWarps / 4;     // epilogue warps per TMEM lane quadrant
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
-  static constexpr int kStages = RESID ? 3 : 2;
+  static constexpr int kUDepth = RESID ? 3 : 2;
+  static constexpr int kStages = 3;
   static constexpr int kOffUr = kOffW + kStages * kStageBytes;
   static constexpr int kOffSh = kOffUr + kEpiWarps * kUDepth * kUSlot;
 };
@@ -226,6 +228,7 @@ __global__ void __launch_bounds__(TcCfg<RESID>::kThreads, 1) draft_tc_persistent
   constexpr int kOffUr = TcCfg<RESID>::kOffUr;
   constexpr int kOffSh = TcCfg<RESID>::kOffSh;
   using Shared = TcShared<kEpiWarps, kStages>;
+  constexpr int kUDepth = TcCfg<RESID>::kUDepth;
   constexpr int kLook = kUDepth;
   constexpr int kUpr = kRank / 8;                  // 16-byte units per W1 row
   extern __shared__ uint8_t smem_raw[];
