@@ -746,7 +746,11 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
   stats_init(rd);
   BRace rb;                // running bonus draw of the current row (kind 4)
   brace_init(rb);
-  int rows_done = 0;       // parity of the shared partials
+  // parity of the shared partials: it flips at the end of every row that has statistics (all
+  // such rows end at the named barrier), never at a skipped row, so a warp can write the
+  // partials of a row only after every warp passed the previous row's barrier -- that is,
+  // after warp 0 merged the row before that one, which used the same half
+  int rows_done = 0;
   for (int t = 0;; ++t) {
     const int s = t % kScanStages;
     const uint32_t use = (uint32_t)(t / kScanStages);
@@ -907,7 +911,7 @@ __global__ void __launch_bounds__(kScanThreads) verify_scan(const __grid_constan
     stats_init(rt);
     stats_init(rd);
     brace_init(rb);
-    ++rows_done;
+    if (m.kind) ++rows_done;
   }
   if (*abort && tid == 0) set_status(a.dev_status, DSPARK_ERR_DEVICE_TIMEOUT);
 }
