@@ -654,6 +654,8 @@ def main(argv=None):
             "roofline": roofline, "kernels": kernels, "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clk}
 
+    if rank == 0:
+        line["other_entry_points"] = next_rows_measure(cfg, w, step, dev, flush)
     if not args.no_e2e:
         line["e2e"] = e2e_measure(cfg, w, step, dev, args, alg)
     if rank == 0 and not args.no_cpu_baseline:
@@ -664,6 +666,76 @@ def main(argv=None):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def next_rows_measure(cfg, w, step, dev, flush, reps=10, warm=3):
+    """Device time of the other entry points on this workload's inputs (each call captured in
+    a CUDA graph and replayed, L2 flushed before each replay; median over reps): the step's
+    scheduler alone, the asynchronous scheduler's capacity and top-K admission, the static
+    threshold, and the draft with the confidence head's Markov term fused in (tensor-core
+    path) against the same draft without it. The schedulers are latency-bound single-CTA
+    calls; no roofline is claimed for any of these."""
+    import torch
+
+    ds = step.ds
+    conf, K_r, sps = w["conf"], w["inp"]["K_r"], w["sps"]
+    B, K = cfg.B, cfg.K_max
+
+    def timed(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warm):
+                fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(reps):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    st = step.status
+    res = {"schedule_survival_ms": timed(step.schedule)}
+    # one direct call each first: it allocates the outputs the captured calls then write into
+    oc = ds.schedule_capacity(conf, K_r, sps, workspace=step.ws_s, status=st)
+    res["schedule_capacity_ms"] = timed(lambda: ds.schedule_capacity(conf, K_r, sps, out=oc, workspace=step.ws_s,
+                                                                     status=st))
+    cap = oc["capacity"]
+    ot = ds.schedule_topk(conf, K_r, cap, workspace=step.ws_s, status=st)
+    res["schedule_topk_ms"] = timed(lambda: ds.schedule_topk(conf, K_r, cap, out=ot, workspace=step.ws_s, status=st))
+    oh = ds.schedule_threshold(conf, K_r, 0.5, status=st)
+    res["schedule_threshold_ms"] = timed(lambda: ds.schedule_threshold(conf, K_r, 0.5, out=oh, status=st))
+    if step.rnn is None:
+        inp = w["inp"]
+        gen = torch.Generator(device="cpu").manual_seed(5)
+        conf_h = torch.randn(B, K, generator=gen).to(dev)
+        conf_w = (torch.randn(cfg.rank, generator=gen) * 0.05).to(dev)
+
+        def draft_conf(out=None):
+            return ds.draft_markov_sample(inp["U"], inp["E"], step.W, inp["anchor"], K_r, inp["temperature"],
+                                          cfg.philox_seed, want_logits=not step.recompute, conf_h=conf_h,
+                                          conf_w=conf_w, out=out, workspace=step.ws_d, status=st,
+                                          spare_sm=step.spare_sm)
+        od = draft_conf()
+        res["draft_ms"] = timed(step.draft)
+        res["draft_confidence_ms"] = timed(lambda: draft_conf(od))
+    if ds.check(st) != "DSPARK_OK":
+        raise SystemExit("device status after the other entry points")
+    res["note"] = "cuda-graph replay of each call, L2 flushed before each, median of %d" % reps
+    return res
 
 
 def e2e_measure(cfg, w, step, dev, args, alg):
