@@ -250,15 +250,16 @@ def test_verify_parity(case, with_lse):
     assert compare_verify(g, o) >= 0.9 * cfg.B
 
 
-@pytest.mark.parametrize("B,V,greedy", [(6, 40000, False), (5, 30000, False), (120, 64040, False),
-                                         (8, 40000, True)])
-def test_verify_bonus_draw_in_parts(B, V, greedy):
+@pytest.mark.parametrize("B,K,V,greedy", [(6, 3, 40000, False), (5, 3, 30000, False), (120, 3, 64040, False),
+                                           (8, 3, 40000, True), (4, 15, 40000, False), (4, 16, 40000, False)])
+def test_verify_bonus_draw_in_parts(B, K, V, greedy):
     # the target rows of the verified positions are the draft's own rows, so every draft token
     # is accepted and every request draws its bonus token; with few requests and several
     # vocabulary slices per row the scan splits each T > 0 bonus draw into parts over slice
     # ranges (4, 3 and 2 parts here), whose winners merge in one packed maximum; with every
-    # other request greedy, the whole greedy bonus rows (argmax) share the list with the parts
-    cfg = wl.small_config("qwen", B=B, K_max=3, V=V)
+    # other request greedy, the whole greedy bonus rows (argmax) share the list with the parts;
+    # at K_max = 15 and 16 the row list's capacity B (K_max + 1) allows 2 parts and 1
+    cfg = wl.small_config("qwen", B=B, K_max=K, V=V)
     inp = wl.draft_inputs(cfg, "cpu")
     if greedy:
         inp["temperature"][::2] = 0.0
